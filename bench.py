@@ -1,0 +1,468 @@
+"""Benchmark of one wide-beam decode step (beam_select + beam_attn_decode).
+
+Default workload: 4 requests, prompts of 4096 tokens, 16 query / 8 kv heads of
+dim 128, bf16 KV, beam_width 512, top_k 512, vocabulary 151936 with SID codes
+3 x 8192, a 4M-item Zipf(1.1) catalog, fp32 logits N(0, 2) — the last of the
+three decode steps, reached by running the first two for real, so every
+request has 512 live beams at trie level 2 and 3 unshared tokens per beam.
+
+One JSON line on rank 0.  `value` is beam rows per second (rows = live beams
+processed per step, summed over requests and ranks) with inputs resident in
+HBM; `e2e` is the same metric through the C ABI from pinned host buffers with
+the step's inputs copied in and its outputs copied out inside the timed region.
+With --impl reference the CPU oracle is timed instead on a bounded sample.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "beam-decode step µs & beam-rows/s; attn+select HBM GB/s as fraction of peak"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# FP32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 flop x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _peak_value(d, *names):
+    for n in names:
+        for k, v in d.items():
+            if k == n and isinstance(v, (int, float)):
+                return float(v)
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    FIELDS = "index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active," \
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown," \
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, index):
+        self.index = index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                       "-i", str(self.index), "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------ GPU arm
+
+class Step:
+    """Resident inputs and state of the benchmarked decode step."""
+
+    def __init__(self, wl, dev):
+        from wide_beam_generative_gb300 import beamdec as bd
+        self.bd = bd
+        self.wl = wl
+        self.dev = dev
+        t0 = time.time()
+        self.items = synth.catalog(wl)
+        self.trie = bd.beam_trie_build(self.items, [wl.C] * wl.levels, wl.token_base(), wl.V) \
+            if wl.levels else None
+        self.t_setup_catalog = time.time() - t0
+        R, W, T = wl.R, wl.W, wl.T
+        self.step = T - 1
+        self.attn = synth.attention_inputs(wl, self.step, device=dev)
+        self.maxp = int(synth.prompt_lens(wl).max())
+        self.ws_sel = bd.workspace(bd.beam_select_workspace_size(R, W, wl.K, wl.V), dev)
+        self.ws_att = bd.workspace(bd.beam_attn_workspace_size(R, W, wl.Hq, wl.Hkv, wl.d, self.maxp,
+                                                               wl.kv_dtype), dev)
+        # reach the last step's state with the real chain (untimed)
+        st = dict(cum=torch.zeros((R, W), dtype=torch.float32, device=dev),
+                  node=torch.zeros((R, W), dtype=torch.int32, device=dev),
+                  n_live=torch.ones((R,), dtype=torch.int32, device=dev),
+                  slot=torch.full((R, W, T), -1, dtype=torch.int32, device=dev))
+        for t in range(self.step):
+            lg = synth.logits(wl, t, device=dev)
+            res = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], self.trie, t, t,
+                                 wl.K, ws=self.ws_sel)
+            st = dict(cum=res["cum_out"], node=res["node_out"], n_live=res["n_live_out"],
+                      slot=res["slot_out"])
+            del lg
+        self.state = st
+        self.logits = synth.logits(wl, self.step, device=dev)
+        self.out_sel = dict(tokens=torch.empty((R, W), dtype=torch.int32, device=dev),
+                            parents=torch.empty((R, W), dtype=torch.int32, device=dev),
+                            cum_out=torch.empty((R, W), dtype=torch.float32, device=dev),
+                            lse_out=None,
+                            node_out=torch.empty((R, W), dtype=torch.int32, device=dev),
+                            n_live_out=torch.empty((R,), dtype=torch.int32, device=dev),
+                            slot_out=torch.empty((R, W, T), dtype=torch.int32, device=dev))
+        self.out_att = torch.empty((R, W, wl.Hq, wl.d),
+                                   dtype=torch.float32 if wl.q_dtype == synth.F32 else torch.bfloat16,
+                                   device=dev)
+        torch.cuda.synchronize()
+
+    def run(self, logits=None, q=None, state=None):
+        wl, bd, s = self.wl, self.bd, self.state if state is None else state
+        lg = self.logits if logits is None else logits
+        o = bd.beam_select(lg, s["cum"], s["node"], s["n_live"], s["slot"], self.trie, self.step,
+                           self.step, wl.K, out=self.out_sel, ws=self.ws_sel)
+        a = self.attn
+        bd.beam_attn_decode(a["q"] if q is None else q, a["shared_k"], a["shared_v"], a["prompt_offsets"],
+                            self.maxp, a["unshared_k"], a["unshared_v"], o["slot_out"], o["n_live_out"],
+                            self.step, k_scale=a["k_scale"], v_scale=a["v_scale"], out=self.out_att,
+                            ws=self.ws_att)
+        return o
+
+    def rows(self):
+        return int(self.state["n_live"].sum().item())
+
+
+def algorithmic(wl, rows, kernel):
+    """Algorithmic bytes or flops of one launch of `kernel` at this step."""
+    G = wl.G
+    L = wl.T                                   # unshared tokens per beam at the last step
+    b_kv = 1 if wl.kv_dtype == synth.E4M3 else (4 if wl.kv_dtype == synth.F32 else 2)
+    b_q = 4 if wl.q_dtype == synth.F32 else 2
+    P = synth.prompt_lens(wl)
+    if kernel == "bd_expand_kernel":
+        # one read of every live logits row + per-request pool keys written
+        return rows * wl.V * 4, "bytes"
+    if kernel in ("bd_attn_shared_simt_kernel", "bd_attn_shared_tc_kernel"):
+        return float(4 * wl.Hkv * wl.W * G * P.sum() * wl.d), "flops"
+    if kernel == "bd_attn_merge_kernel":
+        unshared = rows * L * wl.Hkv * wl.d * 2 * b_kv
+        qo = 2 * rows * wl.Hq * wl.d * b_q
+        return unshared + qo, "bytes"
+    if kernel == "bd_global_kernel":
+        return rows * 12, "bytes"
+    return 0, "bytes"
+
+
+def read_traffic(kernel):
+    """dram bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current source of that kernel."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+    if not os.path.exists(path):
+        return None
+    src_for = {"bd_expand_kernel": "select.cu", "bd_global_kernel": "select.cu",
+               "bd_attn_shared_simt_kernel": "attn_simt.cu", "bd_attn_shared_tc_kernel": "attn_tc.cu",
+               "bd_attn_merge_kernel": "attn_merge.cu"}
+    src = os.path.join(ROOT, "wide_beam_generative_gb300", "csrc", src_for.get(kernel, ""))
+    if not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:12]
+    for line in open(path):
+        f = line.strip().strip("|").split("|")
+        f = [x.strip() for x in f]
+        if len(f) >= 4 and f[0] == kernel and f[2] == sha:
+            try:
+                return float(f[1])
+            except ValueError:
+                return None
+    return None
+
+
+def gpu_arm(args, ws, rank, local):
+    from wide_beam_generative_gb300 import beamdec as bd
+    dev = torch.device("cuda", local)
+    wl = synth.WORKLOADS[args.workload]
+    step = Step(wl, dev)
+    rows = step.rows()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.zero_()
+        step.run()
+    torch.cuda.synchronize()
+    assert bd.read_status(step.ws_sel) == 0 and bd.read_status(step.ws_att) == 0
+    clocks = Clocks(local)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks.start()
+    bd.profile_enable(True)
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step.run()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    bd.profile_enable(False)
+    barrier(ws)
+    clk = clocks.stop()
+    times = [a.elapsed_time(b) for a, b in ev]
+    prof = bd.profile_read()
+    total_ms = max_over_ranks(sum(times), ws)
+    ms_per_step = total_ms / args.steps
+    value = rows * ws / (ms_per_step / 1e3)
+    launches = sum(n for _, n in prof.values())
+
+    # roofline of the dominant kernel
+    dom = max(prof.items(), key=lambda kv: kv[1][0])
+    kname, (kms, kn) = dom
+    units, kind = algorithmic(wl, rows, kname)
+    pk, src = peaks()
+    if kind == "bytes":
+        achieved = units / (kms / kn / 1e3) / 1e9
+        peak = _peak_value(pk, "hbm_gbs", "hbm_GBs", "hbm") or FALLBACK_PEAKS["hbm_gbs"]
+        roof = {"bound": "hbm", "unit": "GB/s"}
+    elif kname == "bd_attn_shared_simt_kernel":
+        achieved = units / (kms / kn / 1e3) / 1e12
+        peak = FP32_ALU_TFLOPS
+        roof = {"bound": "alu", "unit": "TFLOP/s"}
+        src = "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz"
+    else:
+        achieved = units / (kms / kn / 1e3) / 1e12
+        peak = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
+        roof = {"bound": "tensor", "unit": "TFLOP/s"}
+    roof.update(kernel=kname, achieved=round(achieved, 2), peak=peak, frac=round(achieved / peak, 4),
+                traffic=read_traffic(kname), peak_source=src,
+                algorithmic_per_launch=units, launch_us=round(kms / kn * 1e3, 2))
+    kernels = {k: {"us_per_launch": round(ms / n * 1e3, 2), "launches": n,
+                   "share": round(ms / max(1e-9, sum(x for x, _ in prof.values())), 4)}
+               for k, (ms, n) in prof.items() if n}
+
+    # end-to-end through the C ABI from pinned host buffers
+    e2e = e2e_arm(step, args, ws, flush)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "beam-rows/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "step_us": round(ms_per_step * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp32 logits / bf16 KV", "data": "synthetic (seeded; see synth)",
+        "config": {"workload": f"{wl.name}: R{wl.R} P{int(synth.prompt_lens(wl).max())} Hq{wl.Hq} Hkv{wl.Hkv} "
+                               f"d{wl.d} W{wl.W} K{wl.K} V{wl.V} SID {wl.levels}x{wl.C} "
+                               f"catalog {wl.n_items} step {step.step + 1}/{wl.T}",
+                   "rows_per_step_per_gpu": rows, "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MB write) before each step",
+                   "parallelism": f"request-sharded replicas x{ws}"},
+        "roofline": roof, "kernels": kernels, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows or 512)
+    return line
+
+
+def e2e_arm(step, args, ws, flush):
+    wl, dev = step.wl, step.dev
+    s = step.state
+    host = {"logits": step.logits.cpu().pin_memory(), "q": step.attn["q"].cpu().pin_memory()}
+    for k in ("cum", "node", "n_live", "slot"):
+        host[k] = s[k].cpu().pin_memory()
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    outs = ["tokens", "parents", "cum_out", "node_out", "n_live_out", "slot_out"]
+    host_out = {k: torch.empty_like(step.out_sel[k], device="cpu").pin_memory() for k in outs}
+    host_att = torch.empty_like(step.out_att, device="cpu").pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values()) + host_att.numel() * host_att.element_size()
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        st = dict(cum=dev_in["cum"], node=dev_in["node"], n_live=dev_in["n_live"], slot=dev_in["slot"])
+        step.run(logits=dev_in["logits"], q=dev_in["q"], state=st)
+        for k in outs:
+            host_out[k].copy_(step.out_sel[k], non_blocking=True)
+        host_att.copy_(step.out_att, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        one()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 10))
+    times = []
+    for _ in range(n):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = max_over_ranks(sum(times) / n, ws)
+    rows = step.rows()
+    return {"value": round(rows * ws / (ms / 1e3), 1), "unit": "beam-rows/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 3)}
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+
+def cpu_sample(wl, rows):
+    """A bounded sample of the workload for the oracle: the first `rows` beams
+    of request 0 at the last step (their logits rows, queries and slot rows)."""
+    from oracle import trie as otrie
+    items = synth.catalog(wl)
+    tr = otrie.build_trie(items, wl.C) if wl.levels else None
+    step = wl.T - 1
+    lg = synth.logit_rows(wl, step, 0, 0, rows).numpy()[None]
+    rng = np.random.default_rng(1)
+    if tr is not None:
+        pick = items[rng.integers(0, len(items), rows)]
+        node = np.array([[tr.node_of_prefix(p[:step]) for p in pick]], np.int64)
+    else:
+        node = np.zeros((1, rows), np.int64)
+    cum = np.zeros((1, rows), np.float32)
+    slot = np.zeros((1, rows, wl.T), np.int32)
+    for t in range(step):
+        slot[0, :, t] = t * wl.W + rng.integers(0, wl.W, rows)
+    a = synth.attention_inputs(wl.scaled(R=1, prompt_lens=[int(synth.prompt_lens(wl)[0])], p_range=None), step)
+
+    def raw(t):
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16)
+        if t.dtype == torch.float8_e4m3fn:
+            return t.view(torch.uint8).numpy()
+        return t.numpy()
+    inp = dict(q=raw(a["q"][:, :rows]), shared_k=raw(a["shared_k"]), shared_v=raw(a["shared_v"]),
+               unshared_k=raw(a["unshared_k"]), unshared_v=raw(a["unshared_v"]),
+               k_scale=a["k_scale"].numpy(), v_scale=a["v_scale"].numpy(),
+               prompt_offsets=a["prompt_offsets"].numpy(), q_dtype=wl.q_dtype, kv_dtype=wl.kv_dtype)
+    return dict(lg=lg, node=node, cum=cum, slot=slot, tr=tr, inp=inp, step=step, rows=rows)
+
+
+def cpu_run(wl, s):
+    from oracle import attention as oatt
+    from oracle import select as osel
+    rows, step = s["rows"], s["step"]
+    sel = osel.beam_select(s["lg"], s["cum"], s["node"], np.array([rows]), s["slot"], s["tr"],
+                           wl.token_base(), step, step, rows, min(wl.K, rows))
+    oatt.attention_decode(s["inp"], sel["slot_out"], sel["n_live_out"], step)
+    return rows
+
+
+def cpu_baseline(wl, rows):
+    s = cpu_sample(wl, rows)
+    t0 = time.time()
+    done = cpu_run(wl, s)
+    dt = time.time() - t0
+    return {"value": round(done / dt, 2), "unit": "beam-rows/s", "cores": os.cpu_count(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"request 0, beams 0..{rows - 1} of the last step: float64 log-sum-exp + trie "
+                      f"children + full sorts, float64 attention over prompt + ancestry "
+                      f"(numpy; BLAS matmuls may use every core)"}
+
+
+def reference_arm(args, ws, rank):
+    wl = synth.WORKLOADS[args.workload]
+    if rank != 0:
+        return None
+    s = cpu_sample(wl, args.cpu_rows or 128)
+    for _ in range(args.warmup):
+        cpu_run(wl, s)
+    t0 = time.time()
+    for _ in range(args.steps):
+        cpu_run(wl, s)
+    dt = (time.time() - t0) / args.steps
+    v = round(s["rows"] / dt, 2)
+    return {"metric": METRIC, "value": v, "unit": "beam-rows/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; see synth)",
+            "impl": "reference",
+            "config": {"workload": f"{wl.name} (bounded sample of {s['rows']} beams per step)"},
+            "cpu_baseline": {"value": v, "unit": "beam-rows/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"request 0, beams 0..{s['rows'] - 1} of the last decode step"},
+            "e2e": {"value": v, "unit": "beam-rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="libbeamdec")
+    ap.add_argument("--workload", default="onerec17b", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--cpu-rows", type=int, default=None,
+                    help="beams in the oracle's sample (default 512 for cpu_baseline, 128 per reference step)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        line = reference_arm(args, ws, rank)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA GPU")
+        line = gpu_arm(args, ws, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

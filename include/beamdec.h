@@ -1,0 +1,274 @@
+/*
+ * libbeamdec — the wide-beam decode step of generative recommendation, as a
+ * C ABI over hand-written CUDA kernels for sm_103a (GB300).
+ *
+ * One decode step of request r (beam_width W, top_k K, decode step t):
+ *
+ *   beam_select       log-softmax of every live beam's logits over the whole
+ *                     vocabulary, the catalog-trie mask of valid next codes,
+ *                     per-beam top_k, global top-W over the W x top_k pool,
+ *                     cumulative scores, parents, child nodes and the next
+ *                     slot-table rows.
+ *                     ("Generative recommendation design", xLLM, §4.1.1 beam
+ *                     expansion, §4.3 early filtering, §6 beam search then
+ *                     cache select; FlashRec: fused SID trie, CSR.)
+ *   beam_attn_decode  split-KV beam attention: the shared stage over the
+ *                     prompt KV (stored once, read once for all beams), the
+ *                     unshared stage over each beam's decode-token KV reached
+ *                     through the slot table, and the online-softmax merge.
+ *                     ("Generative recommendation design" §4.2.1, §4.2.2.)
+ *   beam_trie_build   catalog of semantic ids -> canonical CSR trie.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor pointer is a DEVICE pointer owned by the caller, unless its
+ *   comment says host.  Tensors are dense, row-major, in the layout given.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Compute entry points only enqueue work: they never synchronise the host,
+ *   never allocate, and return as soon as the kernels are launched.
+ * - Return value: BEAMDEC_OK or a negative BEAMDEC_ERR_* code.  Argument
+ *   errors are detected on the host before anything is launched.  Errors a
+ *   kernel detects (a slot index out of range, a bounded wait that ran out)
+ *   are recorded in the status word at the start of the workspace and read
+ *   with beamdec_read_status.  Kernels never trap or print.
+ * - Workspace: caller-owned device memory of at least the size returned by
+ *   the matching *_workspace_size query, 256-byte aligned.  A workspace may
+ *   be reused across calls on one stream; calls that run concurrently need
+ *   separate workspaces.
+ */
+#ifndef BEAMDEC_H
+#define BEAMDEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define BEAMDEC_OK 0
+#define BEAMDEC_ERR_INVALID_ARG (-1)   /* NULL pointer, bad size, bad enum    */
+#define BEAMDEC_ERR_UNSUPPORTED (-2)   /* legal but outside supported limits  */
+#define BEAMDEC_ERR_WORKSPACE (-3)     /* workspace smaller than required     */
+#define BEAMDEC_ERR_CUDA (-4)          /* a CUDA runtime call failed          */
+#define BEAMDEC_ERR_TIMEOUT (-5)       /* a bounded device wait ran out       */
+#define BEAMDEC_ERR_DEVICE_CHECK (-6)  /* a kernel found an index out of range */
+#define BEAMDEC_ERR_ALLOC (-7)         /* beam_trie_build could not allocate  */
+
+/* ---- element types ----------------------------------------------------- */
+#define BEAMDEC_F32 0    /* IEEE binary32                                   */
+#define BEAMDEC_BF16 1   /* bfloat16                                         */
+#define BEAMDEC_E4M3 2   /* OCP fp8 E4M3FN, with a per-kv-head float scale   */
+
+/* ---- limits ------------------------------------------------------------ */
+#define BEAMDEC_MAX_BEAM_WIDTH 8192     /* W: beam index fits 13 bits        */
+#define BEAMDEC_MAX_VOCAB 262144        /* V: token fits 18 bits             */
+#define BEAMDEC_MAX_LEVELS 8            /* trie levels                        */
+#define BEAMDEC_MAX_CODES 65536         /* codes per level                    */
+
+/* Human-readable name of a status code (static string). */
+const char* beamdec_error_string(int status);
+
+/* Library version as "major.minor.patch" (static string). */
+const char* beamdec_version(void);
+
+/*
+ * Reads the device status word a kernel may have set in `workspace` (the
+ * first 4 bytes of a beam_select or beam_attn_decode workspace), writes it to
+ * *host_status (BEAMDEC_OK when clean) and clears it.  Synchronises `stream`.
+ */
+int beamdec_read_status(void* workspace, void* stream, int32_t* host_status);
+
+/*
+ * Per-kernel timing for benchmarks.  beamdec_profile_enable(1) clears the
+ * record and brackets every following kernel launch with a CUDA event pair
+ * on its stream (at most 8192 launches are kept); beamdec_profile_enable(0)
+ * stops recording.  beamdec_profile_read synchronises the recorded events and
+ * returns the total milliseconds and launch count of one kernel id:
+ * 0 bd_expand_kernel, 1 bd_global_kernel, 2 bd_attn_shared_simt_kernel,
+ * 3 bd_attn_shared_tc_kernel, 4 bd_attn_merge_kernel.  Host-side state is
+ * process-wide; use from one host thread.
+ */
+int beamdec_profile_enable(int on);
+int beamdec_profile_read(int kernel_id, float* total_ms, int* launches);
+const char* beamdec_kernel_name(int kernel_id);
+
+/* ======================================================================== *
+ * Catalog trie
+ * ======================================================================== */
+
+/*
+ * Opaque handle to a trie resident in device memory.
+ *
+ * Canonical form ("Generative recommendation design" §4.3 early filtering;
+ * FlashRec's fused SID trie in CSR form): items are de-duplicated; the nodes
+ * of level t are the distinct length-t prefixes numbered in lexicographic
+ * order (level 0 holds only the root, node 0); a node's children are its
+ * distinct next codes in ascending order; the child reached through edge e of
+ * level t is node e of level t+1 (edges enumerate the length-(t+1) prefixes
+ * in lexicographic order).  At the last level, edge e is item e of the
+ * de-duplicated, lexicographically sorted catalog.
+ */
+typedef struct beamdec_trie beamdec_trie;
+
+/*
+ * Builds the trie of a catalog.
+ *   items_host       HOST [n_items][levels] int32 codes, item-major.
+ *   n_items          >= 1.
+ *   levels           1..BEAMDEC_MAX_LEVELS.
+ *   codes_per_level  HOST [levels]; codes of level l lie in [0, C_l),
+ *                    1 <= C_l <= BEAMDEC_MAX_CODES.
+ *   token_base       HOST [levels]; the vocabulary id of code c at level l is
+ *                    token_base[l] + c ("Deploying FlashRec": each SID level
+ *                    is a contiguous token range); token_base[l] + C_l <= vocab.
+ *   vocab            vocabulary size V, <= BEAMDEC_MAX_VOCAB.
+ *   stream           stream for the uploads.
+ *   out              receives the handle; free it with beam_trie_free.
+ * Allocates device memory (the only entry point that does).  Synchronises
+ * `stream` before returning.  Errors: INVALID_ARG (a code outside [0, C_l),
+ * bad sizes), UNSUPPORTED, ALLOC, CUDA.
+ */
+int beam_trie_build(const int32_t* items_host, int64_t n_items, int levels,
+                    const int32_t* codes_per_level, const int32_t* token_base,
+                    int32_t vocab, void* stream, beamdec_trie** out);
+
+/* Frees the handle and its device memory (NULL is a no-op). */
+void beam_trie_free(beamdec_trie* trie);
+
+/*
+ * Shape of the trie: levels, vocab, number of distinct items, and per level
+ * (arrays of length >= levels, any may be NULL) the node count, the edge count
+ * and the largest child count of any node.
+ */
+int beam_trie_info(const beamdec_trie* trie, int* levels, int32_t* vocab,
+                   int64_t* n_distinct_items, int64_t* n_nodes, int64_t* n_edges,
+                   int32_t* max_children);
+
+/*
+ * Device pointers of one level's CSR arrays, owned by the handle:
+ *   off   [n_nodes + 1] int32 edge offsets (children of node n are edges
+ *         off[n] .. off[n+1]-1);
+ *   code  [n_edges] int32 codes, ascending within each node.
+ */
+int beam_trie_export(const beamdec_trie* trie, int level, const int32_t** off,
+                     const int32_t** code);
+
+/* ======================================================================== *
+ * Beam selection
+ * ======================================================================== */
+
+/*
+ * Workspace bytes for beam_select with R requests, beam width W, top_k K and
+ * vocab V (pool W x min(K, V) keys per request plus counters).
+ */
+int beam_select_workspace_size(int R, int W, int K, int V, size_t* bytes);
+
+/*
+ * One expansion step for R requests ("Generative recommendation design"
+ * §4.1.1: every beam expands top_k candidates, beam_width beams are kept from
+ * the beam_width x top_k pool; §4.3: invalid paths never become candidates;
+ * §6: cache selection after the reorder).
+ *
+ * Inputs (device):
+ *   logits      fp32; the row of beam b of request r starts at
+ *               logits + (r*W + b) * row_stride and holds V values.
+ *               Only rows b < n_live_in[r] are read.  Values must be finite.
+ *   row_stride  elements between consecutive beam rows (>= V).
+ *   lse_in      optional [R][W] fp32: when not NULL, the log-sum-exp of each
+ *               live row is taken from here instead of being computed (e.g.
+ *               when the producer of the logits already has it).
+ *   cum_in      [R][W] fp32 cumulative log-probability of each live beam.
+ *   node_in     [R][W] int32 trie node of each live beam at level `level`
+ *               (ignored when trie is NULL).
+ *   n_live_in   [R] int32 live beams per request, 0..W (beams 0..n-1 live).
+ *   slot_in     [R][W][T] int32 slot rows of the live beams; entries
+ *               0..step-1 are read.
+ *   trie        catalog trie, or NULL for open-vocabulary decoding (every
+ *               token is a candidate).
+ *   level       trie level the beams sit at (0 <= level < trie levels).
+ *   step        decode step t (0 <= step < T); the token chosen by output
+ *               beam j at this step is assigned slot step*W + j.
+ *   R, W, K, V, T  requests, beam width (<= 8192), top_k (>= 1), vocab
+ *               (<= 262144, must equal the trie's vocab), slots per beam row.
+ * Outputs (device, [R][W] unless noted), rank-ordered by
+ * (score desc, parent asc, token asc):
+ *   tokens      int32 chosen token, -1 for rows j >= n_live_out[r].
+ *   parents     int32 index of the parent beam in the input, -1 if dead.
+ *   cum_out     fp32 score s = fl32(cum_in[parent] + fl32(logit - lse)),
+ *               round-to-nearest-even, no FMA; -inf if dead.
+ *   lse_out     optional fp32 log-sum-exp of each live input row (NULL to skip).
+ *   node_out    int32 child node at level+1 (= edge index); at the last level
+ *               the item index; -1 for open vocabulary or dead rows.
+ *   n_live_out  [R] int32 = min(W, pool size).
+ *   slot_out    [R][W][T] int32: entries 0..step-1 copied from the parent's
+ *               row, entry step = step*W + j, later entries -1; dead rows -1.
+ *               Must not alias slot_in.
+ * Per beam, candidates are ranked by (score desc, token asc) and the first
+ * min(top_k, #candidates) enter the pool.
+ * Errors: INVALID_ARG, UNSUPPORTED (W, V, K limits; a trie node with more
+ * children than the supported maximum), WORKSPACE, CUDA.
+ */
+int beam_select(const float* logits, int64_t row_stride, const float* lse_in,
+                const float* cum_in, const int32_t* node_in, const int32_t* n_live_in,
+                const int32_t* slot_in, const beamdec_trie* trie, int level, int step,
+                int R, int W, int K, int V, int T,
+                int32_t* tokens, int32_t* parents, float* cum_out, float* lse_out,
+                int32_t* node_out, int32_t* n_live_out, int32_t* slot_out,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* ======================================================================== *
+ * Beam attention
+ * ======================================================================== */
+
+/*
+ * Workspace bytes for beam_attn_decode (partial (max, sum, output) triples of
+ * the shared stage, one per prompt split and query row).
+ */
+int beam_attn_workspace_size(int R, int W, int Hq, int Hkv, int d, int max_prompt_len,
+                             int kv_dtype, size_t* bytes);
+
+/*
+ * Split-KV attention for one decode step ("Generative recommendation design"
+ * §4.2.1: shared KV = the prompt's prefill KV stored once for all beams,
+ * unshared KV = one entry per decode token per beam; §4.2.2: shared stage,
+ * unshared stage, OnlineSoftmax merge).
+ *
+ * For request r, live beam j < n_live[r] and query head h (kv head
+ * g = h / (Hq/Hkv)):
+ *   out[r][j][h] = softmax(sm_scale * q . k_i) v_i over the prompt rows of r
+ *                  followed by the unshared slots slot_table[r][j][0..step];
+ * rows j >= n_live[r] are written as zeros.
+ *
+ *   q               [R][W][Hq][d]  q_dtype (F32 or BF16).
+ *   shared_k/v      [sum P][Hkv][d] kv_dtype; request r owns rows
+ *                   prompt_offsets[r] .. prompt_offsets[r+1]-1.
+ *   prompt_offsets  [R+1] int32, non-decreasing, prompt_offsets[0] = 0.
+ *   max_prompt_len  host int >= every P_r (sizes the launch).
+ *   unshared_k/v    [R][T*W][Hkv][d] kv_dtype: the per-request slot pool.
+ *   slot_table      [R][W][T] int32; entries 0..step of live rows must lie in
+ *                   [0, T*W) (checked in-kernel; a bad slot sets
+ *                   BEAMDEC_ERR_DEVICE_CHECK in the status word and is skipped).
+ *   n_live          [R] int32.
+ *   k_scale/v_scale [Hkv] fp32 dequantisation scales, required for E4M3 KV,
+ *                   ignored otherwise (may be NULL).
+ *   sm_scale        softmax scale (pass 0 for 1/sqrt(d)).
+ *   out             [R][W][Hq][d] out_dtype (F32 or BF16).
+ * Supported: d in {64, 128}; Hq % Hkv == 0; Hq/Hkv <= 16; q/kv/out dtypes
+ * F32/F32/F32, BF16/BF16/BF16, BF16/E4M3/BF16.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
+ */
+int beam_attn_decode(const void* q, const void* shared_k, const void* shared_v,
+                     const int32_t* prompt_offsets, int max_prompt_len,
+                     const void* unshared_k, const void* unshared_v,
+                     const int32_t* slot_table, const int32_t* n_live, int step,
+                     int R, int W, int Hq, int Hkv, int d, int T,
+                     int q_dtype, int kv_dtype, int out_dtype,
+                     const float* k_scale, const float* v_scale, float sm_scale,
+                     void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BEAMDEC_H */

@@ -1,0 +1,121 @@
+"""C ABI checks that need no GPU: the library loads, exports every entry
+point the header declares, validates arguments on the host and sizes its
+workspaces.  No call here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "beamdec.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from wide_beam_generative_gb300 import build as b
+    b.build()
+    from wide_beam_generative_gb300 import beamdec
+    return beamdec.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(beam\w*)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert {"beam_select", "beam_attn_decode", "beam_trie_build"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_error_strings(L):
+    from wide_beam_generative_gb300 import beamdec as bd
+    assert bd.error_string(0) == "ok"
+    for s in range(-7, 0):
+        assert bd.error_string(s) != "unknown status"
+    assert L.beamdec_version().decode().count(".") == 2
+
+
+FAKE = ctypes.c_void_p(0x1000)   # never dereferenced: validation fails first
+
+
+def _select(L, **kw):
+    args = dict(logits=FAKE, row_stride=512, lse_in=None, cum=FAKE, node=FAKE, n_live=FAKE,
+                slot_in=FAKE, trie=None, level=0, step=0, R=1, W=8, K=8, V=512, T=3,
+                tokens=FAKE, parents=FAKE, cum_out=FAKE, lse_out=None, node_out=FAKE,
+                n_live_out=FAKE, slot_out=ctypes.c_void_p(0x2000), ws=FAKE, ws_bytes=0, stream=None)
+    args.update(kw)
+    return L.beam_select(*args.values())
+
+
+def test_select_validation(L):
+    from wide_beam_generative_gb300 import beamdec as bd
+    assert _select(L, logits=None) == bd.ERR_INVALID_ARG
+    assert _select(L, W=0) == bd.ERR_INVALID_ARG
+    assert _select(L, step=3) == bd.ERR_INVALID_ARG
+    assert _select(L, row_stride=100) == bd.ERR_INVALID_ARG
+    assert _select(L, step=1, slot_in=None) == bd.ERR_INVALID_ARG
+    assert _select(L, slot_out=FAKE) == bd.ERR_INVALID_ARG          # aliasing slot_in
+    assert _select(L, W=9000) == bd.ERR_UNSUPPORTED
+    assert _select(L, V=300000, row_stride=300000) == bd.ERR_UNSUPPORTED
+    assert _select(L, ws=ctypes.c_void_p(0x1010)) == bd.ERR_INVALID_ARG   # not 256-aligned
+    assert _select(L, ws_bytes=16) == bd.ERR_WORKSPACE
+
+
+def test_select_workspace_size(L):
+    from wide_beam_generative_gb300 import beamdec as bd
+    small = bd.beam_select_workspace_size(1, 8, 8, 512)
+    big = bd.beam_select_workspace_size(4, 512, 512, 151936)
+    assert big >= 4 * 512 * 512 * 8 > small > 0
+    with pytest.raises(bd.BeamdecError):
+        bd.beam_select_workspace_size(1, 9000, 8, 512)
+
+
+def _attn(L, **kw):
+    args = dict(q=FAKE, sk=FAKE, sv=FAKE, off=FAKE, maxp=256, uk=FAKE, uv=FAKE, slot=FAKE,
+                n_live=FAKE, step=0, R=1, W=8, Hq=2, Hkv=1, d=64, T=3, qd=0, kvd=0, od=0,
+                ks=None, vs=None, sm=0.0, out=FAKE, ws=FAKE, ws_bytes=0, stream=None)
+    args.update(kw)
+    return L.beam_attn_decode(*args.values())
+
+
+def test_attention_validation(L):
+    from wide_beam_generative_gb300 import beamdec as bd
+    assert _attn(L, q=None) == bd.ERR_INVALID_ARG
+    assert _attn(L, Hq=3, Hkv=2) == bd.ERR_INVALID_ARG
+    assert _attn(L, d=96) == bd.ERR_UNSUPPORTED
+    assert _attn(L, Hq=34, Hkv=2) == bd.ERR_UNSUPPORTED                # group of 17
+    assert _attn(L, qd=1, kvd=0, od=1) == bd.ERR_UNSUPPORTED            # bf16 q with fp32 KV
+    assert _attn(L, qd=7) == bd.ERR_INVALID_ARG
+    assert _attn(L, qd=1, kvd=2, od=1) == bd.ERR_INVALID_ARG            # e4m3 without scales
+    assert _attn(L, step=3) == bd.ERR_INVALID_ARG
+    assert _attn(L, maxp=256, sk=None) == bd.ERR_INVALID_ARG
+    assert _attn(L) == bd.ERR_WORKSPACE
+    n = bd.beam_attn_workspace_size(4, 512, 16, 8, 128, 4096, bd.BF16)
+    assert n >= 4 * 512 * 16 * 128 * 4
+
+
+def test_trie_validation_before_any_device_call(L):
+    from wide_beam_generative_gb300 import beamdec as bd
+    import numpy as np
+    with pytest.raises(bd.BeamdecError) as e:
+        bd.beam_trie_build(np.array([[0, 1, 16]]), [16, 16, 16], [0, 16, 32], 512)
+    assert e.value.status == bd.ERR_INVALID_ARG                          # code 16 >= C
+    with pytest.raises(bd.BeamdecError) as e:
+        bd.beam_trie_build(np.array([[0, 1, 2]]), [16, 16, 16], [0, 16, 500], 512)
+    assert e.value.status == bd.ERR_INVALID_ARG                          # range past vocab
+    with pytest.raises(bd.BeamdecError) as e:
+        bd.beam_trie_build(np.zeros((1, 9), np.int32), [2] * 9, [0] * 9, 512)
+    assert e.value.status == bd.ERR_UNSUPPORTED                          # > 8 levels
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from wide_beam_generative_gb300 import beamdec as bd
+    monkeypatch.setattr(bd, "_lib", None)
+    monkeypatch.setattr(bd, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        bd.lib()

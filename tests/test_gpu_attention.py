@@ -1,0 +1,116 @@
+"""GPU parity of beam_attn_decode against the float64 oracle on the same
+quantised inputs.  Tolerances (absolute): fp32 2e-5 (float32 accumulation of
+O(1) terms over <= a few thousand keys), bf16 KV 1e-2, fp8 e4m3 KV 5e-2."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import attention as oatt
+from tests._helpers import ATOL_ATTN, oracle_attn_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _slots(wl, step, n_live, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    slot = torch.full((wl.R, wl.W, wl.T), -1, dtype=torch.int32)
+    for t in range(step + 1):
+        slot[:, :, t] = t * wl.W + torch.randint(0, wl.W, (wl.R, wl.W), generator=g, dtype=torch.int32)
+    return slot
+
+
+def _run(wl, step, n_live, beams=None, seed=0):
+    from wide_beam_generative_gb300 import beamdec as bd
+    a = synth.attention_inputs(wl, step, device=DEV)
+    slot = _slots(wl, step, n_live, seed)
+    nl = torch.tensor(n_live, dtype=torch.int32)
+    maxp = int(synth.prompt_lens(wl).max())
+    out = bd.beam_attn_decode(a["q"], a["shared_k"], a["shared_v"], a["prompt_offsets"], maxp,
+                              a["unshared_k"], a["unshared_v"], slot.to(DEV), nl.to(DEV), step,
+                              k_scale=a["k_scale"], v_scale=a["v_scale"])
+    torch.cuda.synchronize()
+    inp = oracle_attn_inputs(a, a["q"], wl)
+    want = oatt.attention_decode(inp, slot.numpy(), nl.numpy(), step, beams=beams)
+    got = out.double().cpu().numpy()
+    return got, want, out
+
+
+def _check(wl, got, want, beams=None):
+    tol = ATOL_ATTN[wl.kv_dtype]
+    if beams is None:
+        err = np.abs(got - want).max()
+    else:
+        err = max(np.abs(got[r, j] - want[r, j]).max() for r, j in beams)
+    assert err < tol, f"max abs error {err} >= {tol}"
+    return err
+
+
+@pytest.mark.parametrize("step", [0, 1, 2])
+def test_tiny_fp32(gpu_lib, step):
+    wl = synth.WORKLOADS["tiny"]
+    got, want, _ = _run(wl, step, [wl.W - 3])
+    _check(wl, got, want)
+    assert np.all(got[:, wl.W - 3:] == 0)                     # dead rows are zeros
+
+
+def test_qwen06b_bf16_full(gpu_lib):
+    wl = synth.WORKLOADS["qwen06b"]
+    got, want, _ = _run(wl, 2, [wl.W])
+    _check(wl, got, want)
+
+
+def test_ragged_prompts_and_tails(gpu_lib):
+    """Prompts that are not multiples of any tile, an empty prompt, partial
+    beam tiles, d = 64 with bf16 and e4m3."""
+    for kvd in (synth.BF16, synth.E4M3):
+        for d in (64, 128):
+            wl = synth.WORKLOADS["qwen06b"].scaled(name="ragged", R=3, prompt_lens=[1, 0, 333], d=d,
+                                                   W=19, T=3, kv_dtype=kvd)
+            got, want, _ = _run(wl, 1, [19, 7, 1])
+            _check(wl, got, want)
+
+
+def test_onerec17b_full_size_sampled(gpu_lib):
+    """The benchmarked shape: 4 requests x 512 beams x 16 heads, prompts 4096."""
+    wl = synth.WORKLOADS["onerec17b"]
+    beams = [(r, j) for r in range(wl.R) for j in (0, 1, 255, 510, 511)]
+    got, want, _ = _run(wl, 2, [wl.W] * wl.R, beams=beams)
+    _check(wl, got, want, beams)
+
+
+def test_fp8kv_full_size_sampled(gpu_lib):
+    wl = synth.WORKLOADS["fp8kv"]
+    beams = [(r, j) for r in range(wl.R) for j in (0, 333, 998)]
+    got, want, _ = _run(wl, 3, [wl.W, wl.W, 999, 500], beams=beams)
+    _check(wl, got, want, beams)
+    assert np.all(got[2, 999:] == 0) and np.all(got[3, 500:] == 0)
+
+
+def test_openvocab_full_size_sampled(gpu_lib):
+    """2 requests x 5000 beams, 32 unshared tokens per beam at the last step."""
+    wl = synth.WORKLOADS["openvocab"]
+    beams = [(r, j) for r in range(wl.R) for j in (0, 2500, 4999)]
+    got, want, _ = _run(wl, 31, [wl.W] * wl.R, beams=beams)
+    _check(wl, got, want, beams)
+
+
+def test_deterministic(gpu_lib):
+    wl = synth.WORKLOADS["qwen06b"]
+    _, _, a = _run(wl, 1, [wl.W])
+    _, _, b = _run(wl, 1, [wl.W])
+    assert torch.equal(a, b)
+
+
+def test_bad_slot_sets_device_check(gpu_lib):
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl = synth.WORKLOADS["tiny"]
+    a = synth.attention_inputs(wl, 0, device=DEV)
+    slot = _slots(wl, 1, [wl.W])
+    slot[0, 3, 1] = 10_000                                     # outside the T*W pool
+    ws = bd.workspace(bd.beam_attn_workspace_size(1, wl.W, wl.Hq, wl.Hkv, wl.d, 256, wl.kv_dtype))
+    bd.beam_attn_decode(a["q"], a["shared_k"], a["shared_v"], a["prompt_offsets"], 256,
+                        a["unshared_k"], a["unshared_v"], slot.to(DEV),
+                        torch.tensor([wl.W], dtype=torch.int32, device=DEV), 1, ws=ws)
+    assert bd.read_status(ws) == bd.ERR_DEVICE_CHECK

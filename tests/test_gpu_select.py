@@ -1,0 +1,275 @@
+"""GPU parity of beam_trie_build and beam_select against the CPU oracle.
+
+Selection is compared bit for bit (tokens, parents, scores, child nodes, slot
+rows, live counts) when both sides use the same float32 log-sum-exp (the
+oracle's float64 value rounded to float32, passed to the kernel through
+``lse_in``).  The kernel's own log-sum-exp is compared with the oracle's
+float64 value within 1e-5, and the full path (kernel computes its own
+normaliser) is compared with a tolerance only at exact near-ties.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import select as osel
+from tests._helpers import ATOL_LSE, build_tries, compare_select, oracle_lse32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _catalog(wl):
+    return synth.catalog(wl)
+
+
+def _init_state(R, W, T):
+    return dict(cum=torch.zeros((R, W), dtype=torch.float32, device=DEV),
+                node=torch.zeros((R, W), dtype=torch.int32, device=DEV),
+                n_live=torch.ones((R,), dtype=torch.int32, device=DEV),
+                slot=torch.full((R, W, T), -1, dtype=torch.int32, device=DEV))
+
+
+def run_chain(wl, items=None, steps=None, K=None, W=None, logit_fn=None, check=True):
+    """Decode `steps` steps on the GPU and in the oracle in lockstep."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    W = W or wl.W
+    K = K or wl.K
+    T = wl.T
+    steps = T if steps is None else steps
+    if wl.levels:
+        gtrie, otr = build_tries(wl, items)
+    else:
+        gtrie, otr = None, None
+    st = _init_state(wl.R, W, T)
+    o_cum = np.zeros((wl.R, W), np.float32)
+    o_node = np.zeros((wl.R, W), np.int64)
+    o_nl = np.ones(wl.R, np.int32)
+    o_slot = np.full((wl.R, W, T), -1, np.int32)
+    ws = bd.workspace(bd.beam_select_workspace_size(wl.R, W, K, wl.V))
+    outs = []
+    for t in range(steps):
+        lg = logit_fn(t) if logit_fn else synth.logits(wl.scaled(W=W), t, device=DEV)
+        lg_np = lg.cpu().numpy()
+        lse32 = oracle_lse32(lg_np, o_nl)
+        res = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], gtrie, t, t, K,
+                             lse_in=torch.from_numpy(np.nan_to_num(lse32)).to(DEV), ws=ws)
+        ref = osel.beam_select(lg_np, o_cum, o_node, o_nl, o_slot, otr, wl.token_base(), t, t, W, K,
+                               lse32=lse32)
+        if check:
+            compare_select(res, ref, t, f"{wl.name} step {t}")
+        assert bd.read_status(ws) == 0
+        outs.append((res, ref))
+        st = dict(cum=res["cum_out"], node=res["node_out"], n_live=res["n_live_out"], slot=res["slot_out"])
+        o_cum, o_node, o_nl, o_slot = ref["cum_out"], ref["node_out"], ref["n_live_out"], ref["slot_out"]
+    return outs
+
+
+# ---------------------------------------------------------------------------- trie
+
+@pytest.mark.parametrize("name,n_items", [("tiny", None), ("qwen06b", None), ("fp8kv", 200_000)])
+def test_trie_matches_oracle(gpu_lib, name, n_items):
+    wl = synth.WORKLOADS[name]
+    if n_items:
+        wl = wl.scaled(n_items=n_items)
+    items = _catalog(wl)
+    gtrie, otr = build_tries(wl, items)
+    info = gtrie.info()
+    assert info["n_items"] == len(otr.items)
+    for lv in range(wl.levels):
+        off, code = gtrie.export(lv)
+        assert np.array_equal(off.cpu().numpy(), otr.off[lv])
+        assert np.array_equal(code.cpu().numpy(), otr.code[lv])
+        # canonical numbering: the child reached by edge e is node e of the next level
+        assert np.array_equal(otr.child_node[lv], np.arange(len(otr.code[lv])))
+        assert info["max_children"][lv] == int(np.diff(otr.off[lv]).max())
+
+
+def test_trie_with_duplicates_and_unsorted_input(gpu_lib):
+    from tests.golden import read_kv
+    from oracle import trie as otrie
+    from wide_beam_generative_gb300 import beamdec as bd
+    g = read_kv("trie_small.txt")
+    items = np.array(g["items"], np.int32)
+    t = bd.beam_trie_build(items, [4, 4, 4], [0, 4, 8], 12)
+    for lv in range(3):
+        off, code = t.export(lv)
+        assert off.cpu().tolist() == [int(x) for x in g[f"off{lv}"]]
+        assert code.cpu().tolist() == [int(x) for x in g[f"code{lv}"]]
+    assert t.info()["n_items"] == 6
+
+
+# ---------------------------------------------------------------------------- lse
+
+def test_lse_matches_float64(gpu_lib):
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl = synth.WORKLOADS["qwen06b"].scaled(W=64, K=4, levels=0, n_items=0)
+    lg = synth.logits(wl, 0, device=DEV)                       # N(0, 2)
+    lg[0, 1] = 3.25                                            # constant row: lse = c + ln V
+    lg[0, 2] = synth.logits(synth.WORKLOADS["fp8kv"].scaled(W=64), 1, device=DEV)[0, 2]  # spikes
+    lg[0, 3, 5] = 60.0                                         # one dominant logit
+    R, W, V = 1, 64, wl.V
+    st = _init_state(R, W, 1)
+    st["n_live"][:] = W
+    res = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], None, 0, 0, 4)
+    got = res["lse_out"].cpu().numpy()[0].astype(np.float64)
+    lg_np = lg.cpu().numpy()
+    want = np.array([osel.lse64(lg_np[0, b]) for b in range(W)])
+    assert np.abs(got - want).max() < ATOL_LSE
+    assert abs(got[1] - (3.25 + np.log(V))) < ATOL_LSE
+
+
+# ---------------------------------------------------------------------------- selection, bit-exact
+
+def test_tiny_chain_bitexact(gpu_lib):
+    wl = synth.WORKLOADS["tiny"]
+    run_chain(wl, _catalog(wl))
+
+
+@pytest.mark.parametrize("K", [1, 3, 8, 20])
+@pytest.mark.parametrize("W", [1, 8, 37])
+def test_tiny_chain_widths(gpu_lib, K, W):
+    wl = synth.WORKLOADS["tiny"]
+    run_chain(wl.scaled(W=W), _catalog(wl), K=K, W=W)
+
+
+def test_tiny_open_vocab_with_ties(gpu_lib):
+    wl = synth.WORKLOADS["tiny"].scaled(name="tiny-open", levels=0, n_items=0, W=16)
+
+    def quantised(t):   # integer logits: many exact ties in score
+        return torch.round(synth.logits(wl, t, device=DEV))
+    run_chain(wl, None, K=5, W=16, logit_fn=quantised)
+
+
+def test_constant_logits_all_ties(gpu_lib):
+    wl = synth.WORKLOADS["tiny"].scaled(name="tiny-const", levels=0, n_items=0, W=12)
+    run_chain(wl, None, K=7, W=12, logit_fn=lambda t: torch.zeros((1, 12, wl.V), device=DEV))
+
+
+def test_qwen06b_chain_bitexact(gpu_lib):
+    wl = synth.WORKLOADS["qwen06b"]
+    run_chain(wl, _catalog(wl))
+
+
+def test_open_vocab_large_vocab(gpu_lib):
+    wl = synth.WORKLOADS["openvocab"].scaled(W=48, K=48, T=4)
+    run_chain(wl, None, steps=3)
+    run_chain(wl, None, steps=2, K=5)          # top_k < beam_width: per-beam cap binds
+
+
+def test_onerec17b_full_size_bitexact(gpu_lib):
+    """The benchmarked workload at full size: 4 requests x 512 beams, top_k 512,
+    4M-item Zipf catalog, vocab 151936, all three steps."""
+    wl = synth.WORKLOADS["onerec17b"]
+    outs = run_chain(wl, _catalog(wl))
+    assert int(outs[-1][0]["n_live_out"].min()) == wl.W
+
+
+def test_fp8kv_full_size_bitexact(gpu_lib):
+    """4 requests x 1000 beams, top_k 128 < W, 4 SID levels of 4096, 2M items,
+    logits N(0,3) with 1% spikes of +8."""
+    wl = synth.WORKLOADS["fp8kv"]
+    run_chain(wl, _catalog(wl))
+
+
+def test_openvocab_full_size_properties(gpu_lib):
+    """2 requests x 5000 beams, top_k 5000, open vocabulary 151936: 25M-candidate
+    pools.  Step 0 is compared bit for bit; step 1 is checked exactly without a
+    full sort: with top_k >= W the selection is the top-W of the whole pool, so
+    the count of candidates whose key is at or below the W-th selected key must
+    be exactly W, and every selected score must equal its recomputed value."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl = synth.WORKLOADS["openvocab"]
+    outs = run_chain(wl, None, steps=1)
+    res0 = outs[0][0]
+    R, W, V = wl.R, wl.W, wl.V
+    lg = synth.logits(wl, 1, device=DEV)
+    lse64 = torch.logsumexp(lg.double(), dim=-1)                      # float64 on device
+    lse32 = lse64.float()
+    res = bd.beam_select(lg, res0["cum_out"], res0["node_out"], res0["n_live_out"], res0["slot_out"],
+                         None, 1, 1, wl.K, lse_in=lse32)
+    assert int(res["n_live_out"].min()) == W
+    cum_in = res0["cum_out"]
+    for r in range(R):
+        par = res["parents"][r].long()
+        tok = res["tokens"][r].long()
+        s_sel = (cum_in[r, par] + (lg[r, par, tok] - lse32[r, par]))
+        assert torch.equal(s_sel, res["cum_out"][r])                  # fp32 round-to-nearest steps
+        # exact top-W check by counting (score desc, beam asc, token asc) <= W-th key
+        sW, bW, tW = res["cum_out"][r, W - 1], int(par[W - 1]), int(tok[W - 1])
+        count = 0
+        for b0 in range(0, W, 500):
+            s = cum_in[r, b0:b0 + 500, None] + (lg[r, b0:b0 + 500] - lse32[r, b0:b0 + 500, None])
+            bidx = torch.arange(b0, b0 + s.shape[0], device=DEV)[:, None]
+            tidx = torch.arange(V, device=DEV)[None, :]
+            better = (s > sW) | ((s == sW) & ((bidx < bW) | ((bidx == bW) & (tidx <= tW))))
+            count += int(better.sum())
+        assert count == W
+
+
+# ---------------------------------------------------------------------------- full path
+
+def test_full_path_own_lse(gpu_lib):
+    """Kernel computes its own normaliser: lse within 1e-5 of float64, and the
+    selection equals the oracle's except where scores tie within 2e-5."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    from oracle import trie as otrie
+    wl = synth.WORKLOADS["qwen06b"]
+    items = _catalog(wl)
+    gtrie, otr = build_tries(wl, items)
+    W, K, R = wl.W, wl.K, wl.R
+    st = _init_state(R, W, wl.T)
+    for t in range(wl.T):
+        lg = synth.logits(wl, t, device=DEV)
+        res = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], gtrie, t, t, K)
+        lg_np = lg.cpu().numpy()
+        n_in = st["n_live"].cpu().numpy()
+        ref = osel.beam_select(lg_np, st["cum"].cpu().numpy(), st["node"].cpu().numpy(),
+                               n_in, st["slot"].cpu().numpy(), otr, wl.token_base(), t, t, W, K)
+        got_lse = res["lse_out"].cpu().numpy()
+        for r in range(R):
+            nl = int(n_in[r])
+            assert np.abs(got_lse[r, :nl] - ref["lse64"][r, :nl]).max() < ATOL_LSE
+        n = int(ref["n_live_out"][0])
+        assert int(res["n_live_out"][0]) == n
+        g_s = res["cum_out"].cpu().numpy()[0, :n].astype(np.float64)
+        o_s = ref["cum_out"][0, :n].astype(np.float64)
+        assert np.abs(g_s - o_s).max() < 2e-5
+        g_set = set(zip(res["parents"].cpu().numpy()[0, :n], res["tokens"].cpu().numpy()[0, :n]))
+        o_set = set(zip(ref["parents"][0, :n], ref["tokens"][0, :n]))
+        if g_set != o_set:   # only candidates within the tie tolerance of the cut may differ
+            cut = o_s[-1]
+            diff = g_set ^ o_set
+            lookup = {(p, tk): s for p, tk, s in zip(ref["parents"][0, :n], ref["tokens"][0, :n], o_s)}
+            for key in diff:
+                if key in lookup:
+                    assert abs(lookup[key] - cut) < 4e-5
+        st = dict(cum=res["cum_out"], node=res["node_out"], n_live=res["n_live_out"], slot=res["slot_out"])
+
+
+def test_deterministic_repeat(gpu_lib):
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl = synth.WORKLOADS["qwen06b"]
+    items = _catalog(wl)
+    gtrie, _ = build_tries(wl, items)
+    st = _init_state(wl.R, wl.W, wl.T)
+    lg = synth.logits(wl, 0, device=DEV)
+    a = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], gtrie, 0, 0, wl.K)
+    b = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], gtrie, 0, 0, wl.K)
+    for k in a:
+        if a[k] is not None:
+            assert torch.equal(a[k], b[k]), k
+
+
+def test_bad_node_sets_device_check(gpu_lib):
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl = synth.WORKLOADS["tiny"]
+    gtrie, _ = build_tries(wl, _catalog(wl))
+    st = _init_state(1, wl.W, wl.T)
+    st["node"][0, 0] = 10_000                                 # no such node at level 0
+    ws = bd.workspace(bd.beam_select_workspace_size(1, wl.W, wl.K, wl.V))
+    lg = synth.logits(wl, 0, device=DEV)
+    res = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], gtrie, 0, 0, wl.K, ws=ws)
+    assert bd.read_status(ws) == bd.ERR_DEVICE_CHECK
+    assert int(res["n_live_out"][0]) == 0                       # the bad beam contributed nothing
+    assert bd.read_status(ws) == 0                              # reading clears the word

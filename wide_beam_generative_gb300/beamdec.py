@@ -1,0 +1,257 @@
+"""Python binding of libbeamdec: argument marshalling only.
+
+Every function here forwards torch tensors' device pointers and the current
+CUDA stream to the C ABI declared in ``include/beamdec.h``; all computation
+happens in the library's CUDA kernels.  There is no CPU or eager fallback: if
+the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbeamdec.so")
+
+OK = 0
+ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_CHECK, ERR_ALLOC = \
+    -1, -2, -3, -4, -5, -6, -7
+F32, BF16, E4M3 = 0, 1, 2
+_DT = {torch.float32: F32, torch.bfloat16: BF16, torch.float8_e4m3fn: E4M3}
+
+_lib = None
+
+c_int, c_i64, c_sz, c_f, c_p = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p
+c_i32p = ctypes.POINTER(ctypes.c_int32)
+
+_SIGS = {
+    "beamdec_error_string": (ctypes.c_char_p, [c_int]),
+    "beamdec_version": (ctypes.c_char_p, []),
+    "beamdec_read_status": (c_int, [c_p, c_p, c_i32p]),
+    "beamdec_profile_enable": (c_int, [c_int]),
+    "beamdec_profile_read": (c_int, [c_int, ctypes.POINTER(c_f), ctypes.POINTER(c_int)]),
+    "beamdec_kernel_name": (ctypes.c_char_p, [c_int]),
+    "beam_trie_build": (c_int, [c_p, c_i64, c_int, c_p, c_p, ctypes.c_int32, c_p, ctypes.POINTER(c_p)]),
+    "beam_trie_free": (None, [c_p]),
+    "beam_trie_info": (c_int, [c_p, ctypes.POINTER(c_int), c_i32p, ctypes.POINTER(c_i64),
+                               c_p, c_p, c_p]),
+    "beam_trie_export": (c_int, [c_p, c_int, ctypes.POINTER(c_p), ctypes.POINTER(c_p)]),
+    "beam_select_workspace_size": (c_int, [c_int, c_int, c_int, c_int, ctypes.POINTER(c_sz)]),
+    "beam_select": (c_int, [c_p, c_i64, c_p, c_p, c_p, c_p, c_p, c_p, c_int, c_int,
+                            c_int, c_int, c_int, c_int, c_int,
+                            c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]),
+    "beam_attn_workspace_size": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                         ctypes.POINTER(c_sz)]),
+    "beam_attn_decode": (c_int, [c_p, c_p, c_p, c_p, c_int, c_p, c_p, c_p, c_p, c_int,
+                                 c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                 c_p, c_p, c_f, c_p, c_p, c_sz, c_p]),
+}
+
+
+class BeamdecError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {error_string(status)} ({status})")
+
+
+def lib():
+    """Loads libbeamdec.so (built in-tree by ``build.py``); raises if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libbeamdec.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def error_string(status):
+    return lib().beamdec_error_string(int(status)).decode()
+
+
+def _check(status, where):
+    if status != OK:
+        raise BeamdecError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+class _DevArray:
+    """Zero-copy view of a device int32 array owned by the library."""
+
+    def __init__(self, ptr, n):
+        self.__cuda_array_interface__ = {"shape": (int(n),), "typestr": "<i4",
+                                         "data": (int(ptr), True), "version": 3}
+
+
+class Trie:
+    """Handle of a catalog trie in device memory (freed with the object)."""
+
+    def __init__(self, handle):
+        self._h = handle
+
+    @property
+    def handle(self):
+        return self._h
+
+    def info(self):
+        L = lib()
+        levels, vocab, n = c_int(), ctypes.c_int32(), c_i64()
+        nodes = (c_i64 * 8)()
+        edges = (c_i64 * 8)()
+        mc = (ctypes.c_int32 * 8)()
+        _check(L.beam_trie_info(self._h, ctypes.byref(levels), ctypes.byref(vocab), ctypes.byref(n),
+                                nodes, edges, mc), "beam_trie_info")
+        k = levels.value
+        return dict(levels=k, vocab=vocab.value, n_items=n.value, n_nodes=list(nodes[:k]),
+                    n_edges=list(edges[:k]), max_children=list(mc[:k]))
+
+    def export(self, level):
+        """(off, code) of one level as torch int32 CUDA tensors (copies)."""
+        info = self.info()
+        off, code = c_p(), c_p()
+        _check(lib().beam_trie_export(self._h, level, ctypes.byref(off), ctypes.byref(code)),
+               "beam_trie_export")
+        o = torch.as_tensor(_DevArray(off.value, info["n_nodes"][level] + 1), device="cuda").clone()
+        c = torch.as_tensor(_DevArray(code.value, info["n_edges"][level]), device="cuda").clone()
+        return o, c
+
+    def __del__(self):
+        if getattr(self, "_h", None) and _lib is not None:
+            _lib.beam_trie_free(self._h)
+            self._h = None
+
+
+def beam_trie_build(items, codes_per_level, token_base, vocab, stream=None) -> Trie:
+    """Canonical CSR trie of ``items`` [n, levels] (host int32 codes)."""
+    items = np.ascontiguousarray(np.asarray(items, dtype=np.int32))
+    cpl = np.ascontiguousarray(np.asarray(codes_per_level, dtype=np.int32))
+    tb = np.ascontiguousarray(np.asarray(token_base, dtype=np.int32))
+    h = c_p()
+    st = _stream(stream) if torch.cuda.is_available() else c_p(0)
+    _check(lib().beam_trie_build(items.ctypes.data, items.shape[0], items.shape[1], cpl.ctypes.data,
+                                 tb.ctypes.data, int(vocab), st, ctypes.byref(h)), "beam_trie_build")
+    return Trie(h)
+
+
+def workspace(nbytes, device="cuda"):
+    ws = torch.empty(int(nbytes) + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + int(nbytes)]
+
+
+def beam_select_workspace_size(R, W, K, V):
+    n = c_sz()
+    _check(lib().beam_select_workspace_size(R, W, K, V, ctypes.byref(n)), "beam_select_workspace_size")
+    return n.value
+
+
+def beam_attn_workspace_size(R, W, Hq, Hkv, d, max_prompt_len, kv_dtype):
+    n = c_sz()
+    _check(lib().beam_attn_workspace_size(R, W, Hq, Hkv, d, max_prompt_len, kv_dtype, ctypes.byref(n)),
+           "beam_attn_workspace_size")
+    return n.value
+
+
+KERNELS = ["bd_expand_kernel", "bd_global_kernel", "bd_attn_shared_simt_kernel",
+           "bd_attn_shared_tc_kernel", "bd_attn_merge_kernel"]
+
+
+def profile_enable(on=True):
+    _check(lib().beamdec_profile_enable(1 if on else 0), "beamdec_profile_enable")
+
+
+def profile_read():
+    """{kernel name: (total ms, launches)} of the launches recorded since enable."""
+    res = {}
+    for k, name in enumerate(KERNELS):
+        ms, n = c_f(), c_int()
+        _check(lib().beamdec_profile_read(k, ctypes.byref(ms), ctypes.byref(n)), "beamdec_profile_read")
+        res[name] = (ms.value, n.value)
+    return res
+
+
+def read_status(ws, stream=None):
+    v = ctypes.c_int32()
+    _check(lib().beamdec_read_status(_ptr(ws), _stream(stream), ctypes.byref(v)), "beamdec_read_status")
+    return v.value
+
+
+def beam_select(logits, cum, node, n_live, slot_in, trie, level, step, K, T=None,
+                lse_in=None, out=None, ws=None, stream=None, want_lse=True):
+    """One expansion step.  logits [R, W, V] fp32 (row b of request r at
+    logits[r, b]); cum [R, W] fp32; node [R, W] int32 (ignored without trie);
+    n_live [R] int32; slot_in [R, W, T] int32.  Returns a dict of output
+    tensors: tokens, parents, cum_out, lse_out, node_out, n_live_out, slot_out."""
+    R, W = cum.shape
+    V = logits.shape[-1]
+    if logits.dim() != 3 or logits.shape[0] != R or logits.shape[1] != W or logits.stride(2) != 1 \
+            or logits.stride(0) != W * logits.stride(1):
+        raise ValueError("logits must be [R, W, V] with unit stride in V and rows packed per request")
+    T = slot_in.shape[2] if T is None else T
+    _need_cuda(cum, node, n_live, slot_in, lse_in)
+    dev = cum.device
+    if out is None:
+        out = dict(tokens=torch.empty((R, W), dtype=torch.int32, device=dev),
+                   parents=torch.empty((R, W), dtype=torch.int32, device=dev),
+                   cum_out=torch.empty((R, W), dtype=torch.float32, device=dev),
+                   lse_out=torch.empty((R, W), dtype=torch.float32, device=dev) if want_lse else None,
+                   node_out=torch.empty((R, W), dtype=torch.int32, device=dev),
+                   n_live_out=torch.empty((R,), dtype=torch.int32, device=dev),
+                   slot_out=torch.empty((R, W, T), dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = workspace(beam_select_workspace_size(R, W, K, V), dev)
+    rc = lib().beam_select(_ptr(logits), logits.stride(1), _ptr(lse_in), _ptr(cum), _ptr(node),
+                           _ptr(n_live), _ptr(slot_in), trie.handle if trie is not None else None,
+                           level, step, R, W, K, V, T,
+                           _ptr(out["tokens"]), _ptr(out["parents"]), _ptr(out["cum_out"]),
+                           _ptr(out.get("lse_out")), _ptr(out["node_out"]), _ptr(out["n_live_out"]),
+                           _ptr(out["slot_out"]), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "beam_select")
+    return out
+
+
+def beam_attn_decode(q, shared_k, shared_v, prompt_offsets, max_prompt_len, unshared_k, unshared_v,
+                     slot_table, n_live, step, k_scale=None, v_scale=None, sm_scale=0.0,
+                     out=None, ws=None, stream=None):
+    """Split-KV beam attention for one decode step; returns ``out``
+    [R, W, Hq, d] (fp32 for fp32 q, else bf16)."""
+    R, W, Hq, d = q.shape
+    Hkv = unshared_k.shape[2]
+    T = slot_table.shape[2]
+    _need_cuda(q, shared_k, shared_v, prompt_offsets, unshared_k, unshared_v, slot_table, n_live,
+               k_scale, v_scale)
+    qd, kvd = _DT[q.dtype], _DT[unshared_k.dtype]
+    od = F32 if qd == F32 else BF16
+    if out is None:
+        out = torch.empty((R, W, Hq, d), dtype=torch.float32 if od == F32 else torch.bfloat16,
+                          device=q.device)
+    if ws is None:
+        ws = workspace(beam_attn_workspace_size(R, W, Hq, Hkv, d, max_prompt_len, kvd), q.device)
+    rc = lib().beam_attn_decode(_ptr(q), _ptr(shared_k), _ptr(shared_v), _ptr(prompt_offsets),
+                                int(max_prompt_len), _ptr(unshared_k), _ptr(unshared_v),
+                                _ptr(slot_table), _ptr(n_live), step, R, W, Hq, Hkv, d, T,
+                                qd, kvd, od, _ptr(k_scale), _ptr(v_scale), float(sm_scale),
+                                _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "beam_attn_decode")
+    return out

@@ -1,0 +1,219 @@
+// C ABI of libbeamdec: argument validation, workspace sizing and dispatch.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "internal.h"
+
+namespace bd {
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+AttnPlan attn_plan(int R, int W, int Hq, int Hkv, int d, int max_prompt_len, int q_dtype,
+                   int kv_dtype) {
+  AttnPlan p;
+  p.tensor_core = false;
+  const int G = Hq / Hkv;
+  const int rows = W * G;
+  const int tile_rows = 32;
+  const long long units = (long long)R * Hkv * ((rows + tile_rows - 1) / tile_rows);
+  const int sms = 148;   // planning constant; the split count only shapes the work
+  int n_split = 1;
+  if (max_prompt_len > 0) {
+    long long want = (2ll * sms + units - 1) / units;
+    const int max_split = (max_prompt_len + 255) / 256;
+    if (want > max_split) want = max_split;
+    if (want < 1) want = 1;
+    n_split = (int)want;
+  }
+  int split_len = max_prompt_len > 0 ? (max_prompt_len + n_split - 1) / n_split : 128;
+  split_len = ((split_len + 127) / 128) * 128;
+  p.split_len = split_len;
+  p.n_split = max_prompt_len > 0 ? (max_prompt_len + split_len - 1) / split_len : 1;
+  (void)q_dtype;
+  (void)kv_dtype;
+  (void)d;
+  return p;
+}
+
+size_t attn_workspace_bytes(int R, int W, int Hq, int Hkv, int d, const AttnPlan& p) {
+  const size_t rows = (size_t)R * Hkv * W * (Hq / Hkv) * p.n_split;
+  return kWsHeaderBytesHost + a256(rows * 4) * 2 + a256(rows * d * 4);
+}
+
+AttnPartials attn_partials(void* ws, int R, int W, int Hq, int Hkv, int d, int n_split) {
+  const size_t rows = (size_t)R * Hkv * W * (Hq / Hkv) * n_split;
+  char* p = static_cast<char*>(ws) + kWsHeaderBytesHost;
+  AttnPartials a;
+  a.m = reinterpret_cast<float*>(p);
+  p += a256(rows * 4);
+  a.l = reinterpret_cast<float*>(p);
+  p += a256(rows * 4);
+  a.o = reinterpret_cast<float*>(p);
+  (void)d;
+  return a;
+}
+
+}  // namespace bd
+
+using namespace bd;
+
+extern "C" const char* beamdec_error_string(int s) {
+  switch (s) {
+    case BEAMDEC_OK: return "ok";
+    case BEAMDEC_ERR_INVALID_ARG: return "invalid argument";
+    case BEAMDEC_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case BEAMDEC_ERR_WORKSPACE: return "workspace too small";
+    case BEAMDEC_ERR_CUDA: return "CUDA runtime error";
+    case BEAMDEC_ERR_TIMEOUT: return "bounded device wait timed out";
+    case BEAMDEC_ERR_DEVICE_CHECK: return "device-side index check failed";
+    case BEAMDEC_ERR_ALLOC: return "device allocation failed";
+    default: return "unknown status";
+  }
+}
+
+extern "C" const char* beamdec_version(void) { return "0.1.0"; }
+
+extern "C" int beamdec_read_status(void* workspace, void* stream_ptr, int32_t* host_status) {
+  if (workspace == nullptr || host_status == nullptr) return BEAMDEC_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess ||
+      cudaMemsetAsync(workspace, 0, sizeof(v), stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return BEAMDEC_ERR_CUDA;
+  *host_status = v;
+  return BEAMDEC_OK;
+}
+
+extern "C" int beam_select_workspace_size(int R, int W, int K, int V, size_t* bytes) {
+  if (bytes == nullptr || R < 1 || W < 1 || K < 1 || V < 1) return BEAMDEC_ERR_INVALID_ARG;
+  if (W > BEAMDEC_MAX_BEAM_WIDTH || V > BEAMDEC_MAX_VOCAB) return BEAMDEC_ERR_UNSUPPORTED;
+  *bytes = select_workspace_bytes(R, W, K, V);
+  return BEAMDEC_OK;
+}
+
+extern "C" int beam_select(const float* logits, int64_t row_stride, const float* lse_in,
+                           const float* cum_in, const int32_t* node_in,
+                           const int32_t* n_live_in, const int32_t* slot_in,
+                           const beamdec_trie* trie, int level, int step, int R, int W, int K,
+                           int V, int T, int32_t* tokens, int32_t* parents, float* cum_out,
+                           float* lse_out, int32_t* node_out, int32_t* n_live_out,
+                           int32_t* slot_out, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (logits == nullptr || cum_in == nullptr || n_live_in == nullptr || tokens == nullptr ||
+      parents == nullptr || cum_out == nullptr || node_out == nullptr ||
+      n_live_out == nullptr || slot_out == nullptr || workspace == nullptr)
+    return BEAMDEC_ERR_INVALID_ARG;
+  if (R < 1 || W < 1 || K < 1 || V < 1 || T < 1 || step < 0 || step >= T || row_stride < V)
+    return BEAMDEC_ERR_INVALID_ARG;
+  if (step > 0 && slot_in == nullptr) return BEAMDEC_ERR_INVALID_ARG;
+  if (slot_in != nullptr && slot_in == slot_out) return BEAMDEC_ERR_INVALID_ARG;
+  if (W > BEAMDEC_MAX_BEAM_WIDTH || V > BEAMDEC_MAX_VOCAB) return BEAMDEC_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BEAMDEC_ERR_INVALID_ARG;
+  SelectArgs a{};
+  a.has_trie = trie != nullptr;
+  if (a.has_trie) {
+    if (node_in == nullptr || level < 0 || level >= trie->levels) return BEAMDEC_ERR_INVALID_ARG;
+    if (trie->vocab != V) return BEAMDEC_ERR_INVALID_ARG;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev != trie->device) return BEAMDEC_ERR_INVALID_ARG;
+    a.lvl.off = trie->off[level];
+    a.lvl.code = trie->code[level];
+    a.lvl.n_nodes = (int32_t)trie->n_nodes[level];
+    a.lvl.token_base = trie->token_base[level];
+  }
+  if (workspace_bytes < select_workspace_bytes(R, W, K, V)) return BEAMDEC_ERR_WORKSPACE;
+  a.logits = logits; a.row_stride = row_stride; a.lse_in = lse_in;
+  a.cum_in = cum_in; a.node_in = node_in; a.n_live_in = n_live_in; a.slot_in = slot_in;
+  a.level = level; a.step = step; a.R = R; a.W = W; a.K = K; a.V = V; a.T = T;
+  a.Kp = K < V ? K : V;
+  a.tokens = tokens; a.parents = parents; a.cum_out = cum_out; a.lse_out = lse_out;
+  a.node_out = node_out; a.n_live_out = n_live_out; a.slot_out = slot_out;
+  a.ws = workspace;
+  return launch_select(a, static_cast<cudaStream_t>(stream));
+}
+
+static bool attn_types_ok(int q, int kv, int o) {
+  return (q == BEAMDEC_F32 && kv == BEAMDEC_F32 && o == BEAMDEC_F32) ||
+         (q == BEAMDEC_BF16 && kv == BEAMDEC_BF16 && o == BEAMDEC_BF16) ||
+         (q == BEAMDEC_BF16 && kv == BEAMDEC_E4M3 && o == BEAMDEC_BF16);
+}
+
+static int attn_shape_check(int R, int W, int Hq, int Hkv, int d, int max_prompt_len) {
+  if (R < 1 || W < 1 || Hq < 1 || Hkv < 1 || d < 1 || max_prompt_len < 0)
+    return BEAMDEC_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return BEAMDEC_ERR_INVALID_ARG;
+  if ((d != 64 && d != 128) || Hq / Hkv > 16 || W > BEAMDEC_MAX_BEAM_WIDTH)
+    return BEAMDEC_ERR_UNSUPPORTED;
+  return BEAMDEC_OK;
+}
+
+extern "C" int beam_attn_workspace_size(int R, int W, int Hq, int Hkv, int d, int max_prompt_len,
+                                        int kv_dtype, size_t* bytes) {
+  if (bytes == nullptr) return BEAMDEC_ERR_INVALID_ARG;
+  const int s = attn_shape_check(R, W, Hq, Hkv, d, max_prompt_len);
+  if (s != BEAMDEC_OK) return s;
+  if (kv_dtype < BEAMDEC_F32 || kv_dtype > BEAMDEC_E4M3) return BEAMDEC_ERR_INVALID_ARG;
+  const int q_dtype = kv_dtype == BEAMDEC_F32 ? BEAMDEC_F32 : BEAMDEC_BF16;
+  AttnPlan p = attn_plan(R, W, Hq, Hkv, d, max_prompt_len, q_dtype, kv_dtype);
+  *bytes = attn_workspace_bytes(R, W, Hq, Hkv, d, p);
+  return BEAMDEC_OK;
+}
+
+extern "C" int beam_attn_decode(const void* q, const void* shared_k, const void* shared_v,
+                                const int32_t* prompt_offsets, int max_prompt_len,
+                                const void* unshared_k, const void* unshared_v,
+                                const int32_t* slot_table, const int32_t* n_live, int step,
+                                int R, int W, int Hq, int Hkv, int d, int T, int q_dtype,
+                                int kv_dtype, int out_dtype, const float* k_scale,
+                                const float* v_scale, float sm_scale, void* out,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  if (q == nullptr || prompt_offsets == nullptr || unshared_k == nullptr ||
+      unshared_v == nullptr || slot_table == nullptr || n_live == nullptr || out == nullptr ||
+      workspace == nullptr)
+    return BEAMDEC_ERR_INVALID_ARG;
+  if (max_prompt_len > 0 && (shared_k == nullptr || shared_v == nullptr))
+    return BEAMDEC_ERR_INVALID_ARG;
+  const int s = attn_shape_check(R, W, Hq, Hkv, d, max_prompt_len);
+  if (s != BEAMDEC_OK) return s;
+  if (T < 1 || step < 0 || step >= T) return BEAMDEC_ERR_INVALID_ARG;
+  if (!attn_types_ok(q_dtype, kv_dtype, out_dtype)) {
+    const bool enums_ok = q_dtype >= 0 && q_dtype <= 2 && kv_dtype >= 0 && kv_dtype <= 2 &&
+                          out_dtype >= 0 && out_dtype <= 2;
+    return enums_ok ? BEAMDEC_ERR_UNSUPPORTED : BEAMDEC_ERR_INVALID_ARG;
+  }
+  if (kv_dtype == BEAMDEC_E4M3 && (k_scale == nullptr || v_scale == nullptr))
+    return BEAMDEC_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BEAMDEC_ERR_INVALID_ARG;
+  AttnPlan p = attn_plan(R, W, Hq, Hkv, d, max_prompt_len, q_dtype, kv_dtype);
+  if (workspace_bytes < attn_workspace_bytes(R, W, Hq, Hkv, d, p)) return BEAMDEC_ERR_WORKSPACE;
+  AttnArgs a{};
+  a.q = q; a.shared_k = shared_k; a.shared_v = shared_v;
+  a.prompt_offsets = prompt_offsets; a.max_prompt_len = max_prompt_len;
+  a.unshared_k = unshared_k; a.unshared_v = unshared_v;
+  a.slot_table = slot_table; a.n_live = n_live;
+  a.step = step; a.R = R; a.W = W; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.T = T;
+  a.q_dtype = q_dtype; a.kv_dtype = kv_dtype; a.out_dtype = out_dtype;
+  a.k_scale = k_scale; a.v_scale = v_scale;
+  a.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)d);
+  a.out = out; a.ws = workspace;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = p.tensor_core ? launch_attn_shared_tc(a, p, st) : launch_attn_shared_simt(a, p, st);
+  if (rc != BEAMDEC_OK) return rc;
+  return launch_attn_merge(a, p, st);
+}

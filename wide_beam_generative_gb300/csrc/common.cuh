@@ -1,0 +1,97 @@
+// Shared device helpers of libbeamdec (CUDA side only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/beamdec.h"
+
+namespace bd {
+
+constexpr int kWsHeaderBytes = 256;   // status word, grid-barrier counters
+
+// First 256 bytes of every compute workspace.
+struct WsHeader {
+  int32_t status;        // first device-detected error (BEAMDEC_ERR_*), 0 = clean
+  uint32_t bar_count;    // grid barrier arrivals (returns to 0 after each barrier)
+  uint32_t bar_gen;      // grid barrier generation
+  uint32_t pad[61];
+};
+static_assert(sizeof(WsHeader) == kWsHeaderBytes, "header size");
+
+__device__ __forceinline__ void set_status(WsHeader* h, int code) {
+  atomicCAS(&h->status, 0, code);
+}
+
+// ---- order-preserving float keys ------------------------------------------
+// desc_key(s): smaller key <=> larger s; -0 and +0 map to one key.
+__device__ __forceinline__ uint32_t desc_key(float s) {
+  uint32_t b = __float_as_uint(s);
+  if (b == 0x80000000u) b = 0u;
+  uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ~ord;
+}
+__device__ __forceinline__ float desc_key_value(uint32_t k) {
+  uint32_t ord = ~k;
+  uint32_t b = (ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord;
+  return __uint_as_float(b);
+}
+
+// Global pool key: ascending order = (score desc, beam asc, token asc).
+constexpr int kTokBits = 18;
+constexpr int kBeamBits = 13;
+__device__ __forceinline__ uint64_t pool_key(uint32_t k32, int beam, int tok) {
+  return ((uint64_t)k32 << 32) | ((uint64_t)beam << kTokBits) | (uint64_t)tok;
+}
+__device__ __forceinline__ int pool_key_beam(uint64_t k) {
+  return (int)((k >> kTokBits) & ((1u << kBeamBits) - 1));
+}
+__device__ __forceinline__ int pool_key_tok(uint64_t k) { return (int)(k & ((1u << kTokBits) - 1)); }
+
+// ---- fast base-2 exponential (the hardware instruction) -------------------
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---- warp / block reductions ----------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---- bounded grid barrier (cooperative launches only) ---------------------
+// Every block of the grid must call it the same number of times.  The wait is
+// bounded: after `limit` polls the block records BEAMDEC_ERR_TIMEOUT and goes
+// on, so a broken launch ends with an error instead of a hung GPU.
+__device__ __forceinline__ void grid_barrier(WsHeader* h, unsigned nblocks,
+                                             long long limit = (1ll << 26)) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile uint32_t* gen = &h->bar_gen;
+    uint32_t g = *gen;
+    __threadfence();
+    uint32_t arrived = atomicAdd(&h->bar_count, 1u) + 1u;
+    if (arrived == nblocks) {
+      atomicExch(&h->bar_count, 0u);
+      __threadfence();
+      atomicAdd(&h->bar_gen, 1u);
+    } else {
+      long long it = 0;
+      while (*gen == g) {
+        if (++it > limit) { set_status(h, BEAMDEC_ERR_TIMEOUT); break; }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+}  // namespace bd

@@ -1,0 +1,92 @@
+// Internal declarations shared by the translation units of libbeamdec.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/beamdec.h"
+
+struct beamdec_trie {
+  int levels;
+  int32_t vocab;
+  int64_t n_items;                        // distinct items
+  int32_t C[BEAMDEC_MAX_LEVELS];          // codes per level
+  int32_t token_base[BEAMDEC_MAX_LEVELS];
+  int64_t n_nodes[BEAMDEC_MAX_LEVELS];    // nodes at level t
+  int64_t n_edges[BEAMDEC_MAX_LEVELS];    // edges out of level t = nodes at t+1
+  int32_t max_children[BEAMDEC_MAX_LEVELS];
+  int32_t* off[BEAMDEC_MAX_LEVELS];       // device [n_nodes+1]
+  int32_t* code[BEAMDEC_MAX_LEVELS];      // device [n_edges]
+  int device;
+};
+
+namespace bd {
+
+constexpr size_t kWsHeaderBytesHost = 256;   // status word + grid-barrier counters
+
+// Device view of one trie level for kernels.
+struct TrieLevel {
+  const int32_t* off;
+  const int32_t* code;
+  int32_t n_nodes;
+  int32_t token_base;
+};
+
+// ---- select ----------------------------------------------------------------
+constexpr int kSelectCap = 8192;        // candidate keys sorted by one block
+size_t select_workspace_bytes(int R, int W, int K, int V);
+
+struct SelectArgs {
+  const float* logits; int64_t row_stride; const float* lse_in;
+  const float* cum_in; const int32_t* node_in; const int32_t* n_live_in;
+  const int32_t* slot_in;
+  bool has_trie; TrieLevel lvl;
+  int level, step, R, W, K, V, T, Kp;
+  int32_t* tokens; int32_t* parents; float* cum_out; float* lse_out;
+  int32_t* node_out; int32_t* n_live_out; int32_t* slot_out;
+  void* ws;
+};
+int launch_select(const SelectArgs& a, cudaStream_t stream);
+
+// ---- attention ---------------------------------------------------------------
+struct AttnArgs {
+  const void* q; const void* shared_k; const void* shared_v;
+  const int32_t* prompt_offsets; int max_prompt_len;
+  const void* unshared_k; const void* unshared_v;
+  const int32_t* slot_table; const int32_t* n_live;
+  int step, R, W, Hq, Hkv, d, T;
+  int q_dtype, kv_dtype, out_dtype;
+  const float* k_scale; const float* v_scale; float sm_scale;
+  void* out; void* ws;
+};
+// Split plan of the shared stage over the prompt.
+struct AttnPlan {
+  int n_split;      // prompt splits (partials per query row)
+  int split_len;    // keys per split (multiple of 128)
+  bool tensor_core; // tcgen05 shared stage
+};
+AttnPlan attn_plan(int R, int W, int Hq, int Hkv, int d, int max_prompt_len, int q_dtype,
+                   int kv_dtype);
+size_t attn_workspace_bytes(int R, int W, int Hq, int Hkv, int d, const AttnPlan& p);
+int launch_attn_shared_simt(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
+int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
+int launch_attn_merge(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
+
+// Partial-triple layout in the attention workspace (after the 256-byte header):
+//   m, l : [n_split][R][Hkv][W*G] fp32 (m in log2 units of the scaled score)
+//   o    : [n_split][R][Hkv][W*G][d] fp32, not normalised by l
+struct AttnPartials {
+  float* m; float* l; float* o;
+};
+AttnPartials attn_partials(void* ws, int R, int W, int Hq, int Hkv, int d, int n_split);
+
+int sm_count();
+
+// ---- per-kernel event timing (off unless beamdec_profile_enable(1)) ---------
+enum KernelId { kKExpand = 0, kKGlobal = 1, kKAttnSimt = 2, kKAttnTc = 3, kKAttnMerge = 4,
+                kKCount = 5 };
+void prof_begin(int kid, cudaStream_t s);
+void prof_end(int kid, cudaStream_t s);
+
+}  // namespace bd

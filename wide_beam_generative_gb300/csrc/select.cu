@@ -1,0 +1,548 @@
+// Beam expansion: log-softmax, catalog-trie mask, per-beam top_k and global
+// top-W selection with the slot-table update.
+//
+// "Generative recommendation design" (xLLM) §4.1.1: each of the beam_width
+// beams expands top_k candidates and beam_width beams are chosen from the
+// beam_width x top_k pool; §4.3: invalid item paths are filtered before they
+// become candidates, sorting stops early; §6: cache selection follows the
+// reorder.  FlashRec (SGLang PR 31626 thread): fused SID trie in CSR form.
+//
+// Two launches per step:
+//   bd_expand_kernel   one block per (beam, request): streams the beam's logits
+//                      row once to get its log-sum-exp, scores the trie
+//                      children (or the whole vocabulary), keeps the row's
+//                      top_k by a block radix select and appends them to the
+//                      request's pool as 64-bit keys.
+//   bd_global_kernel   cooperative grid: per request, radix select of the
+//                      beam_width smallest pool keys (12-bit digits, block-
+//                      private histograms merged in global memory), a bitonic
+//                      sort of the survivors in shared memory, then the outputs
+//                      and the parent-pointer slot rows.
+// The 64-bit key (desc(score) << 32 | beam << 18 | token) orders candidates
+// by (score desc, beam asc, token asc), so the selection is deterministic.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace bd {
+namespace {
+
+constexpr int kExpandThreads = 512;
+constexpr int kGlobalThreads = 512;
+constexpr int kDigitBits = 12;
+constexpr int kBins = 1 << kDigitBits;  // 4096
+
+struct SelState {
+  unsigned long long prefix;  // resolved high bits of the threshold key
+  int32_t total;              // pool size of the request
+  int32_t n_target;           // min(W, total)
+  int32_t need;               // keys still to take inside the current prefix
+  int32_t sure;               // keys strictly below the current prefix
+  int32_t shift;              // bits below the resolved prefix (64 = none resolved)
+  int32_t done;
+  int32_t ncand;
+  int32_t pad[7];
+};
+static_assert(sizeof(SelState) == 64, "state size");
+
+struct SelWs {
+  WsHeader* hdr;
+  SelState* state;        // [R]
+  uint32_t* hist;         // [R][kBins]
+  unsigned long long* pool;  // [R][W*Kp]
+  unsigned long long* cand;  // [R][kSelectCap]
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+__host__ __device__ inline SelWs carve(void* ws, int R, int W, int Kp) {
+  char* p = (char*)ws;
+  SelWs s;
+  s.hdr = (WsHeader*)p; p += kWsHeaderBytes;
+  s.state = (SelState*)p; p += align256((size_t)R * sizeof(SelState));
+  s.hist = (uint32_t*)p; p += align256((size_t)R * kBins * sizeof(uint32_t));
+  s.pool = (unsigned long long*)p; p += align256((size_t)R * W * Kp * 8);
+  s.cand = (unsigned long long*)p;
+  return s;
+}
+
+// One warp: find the digit bin D holding the `need`-th smallest key (1-based)
+// of a histogram; returns D and the count of keys in bins below D.
+__device__ void warp_find_digit(const volatile uint32_t* hist, int nbins, uint32_t need,
+                                uint32_t* D, uint32_t* below) {
+  const int lane = threadIdx.x & 31;
+  const int per = nbins / 32;
+  uint32_t sum = 0;
+  for (int i = 0; i < per; ++i) sum += hist[lane * per + i];
+  uint32_t incl = sum;
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  uint32_t excl = incl - sum;
+  unsigned hit = __ballot_sync(0xffffffffu, excl < need && need <= incl);
+  int src = __ffs(hit) - 1;   // exactly one lane holds the need-th key
+  if (lane == src) {
+    uint32_t c = excl;
+    int d = lane * per;
+    for (int i = 0; i < per; ++i) {
+      uint32_t h = hist[lane * per + i];
+      if (c + h >= need) { d = lane * per + i; break; }
+      c += h;
+    }
+    *D = (uint32_t)d;
+    *below = c;
+  }
+  __syncwarp();
+}
+
+// Block-wide exclusive rank of `flag` among the block's threads, and the total.
+__device__ __forceinline__ int block_rank(int flag, int* warp_cnt, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  unsigned bal = __ballot_sync(0xffffffffu, flag);
+  int r = __popc(bal & ((1u << lane) - 1u));
+  if (lane == 0) warp_cnt[warp] = __popc(bal);
+  __syncthreads();
+  int base = 0, tot = 0;
+  for (int w = 0; w < nw; ++w) {
+    int c = warp_cnt[w];
+    if (w < warp) base += c;
+    tot += c;
+  }
+  __syncthreads();
+  *total = tot;
+  return base + r;
+}
+
+struct ExpandShared {
+  uint32_t hist[2048];
+  float red_m[32];
+  float red_s[32];
+  int warp_cnt[32];
+  uint32_t digit, below;
+  int count;
+  int pool_base;
+  float lse;
+};
+
+__global__ void __launch_bounds__(kExpandThreads)
+bd_expand_kernel(SelectArgs a) {
+  __shared__ ExpandShared sh;
+  const int b = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
+  const int Kp = a.Kp;
+  SelWs ws = carve(a.ws, a.R, a.W, Kp);
+  if (b == 0 && r == 0 && tid == 0) ws.hdr->bar_count = 0u;
+  const int nl = a.n_live_in[r];
+  if (b >= nl) return;
+
+  const size_t rowi = (size_t)r * a.W + b;
+  const float* row = a.logits + rowi * (size_t)a.row_stride;
+
+  // ---- a1: log-sum-exp over the full vocabulary (one streaming pass) ------
+  float lse;
+  if (a.lse_in != nullptr) {
+    lse = a.lse_in[rowi];
+  } else {
+    float m = -INFINITY, s = 0.f;
+    const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15u) == 0);
+    const int nvec = vec ? (a.V >> 2) : 0;
+    const float4* row4 = reinterpret_cast<const float4*>(row);
+    int i = tid;
+    for (; i + 3 * kExpandThreads < nvec; i += 4 * kExpandThreads) {
+      float4 v0 = __ldg(row4 + i);
+      float4 v1 = __ldg(row4 + i + kExpandThreads);
+      float4 v2 = __ldg(row4 + i + 2 * kExpandThreads);
+      float4 v3 = __ldg(row4 + i + 3 * kExpandThreads);
+      float mx = fmaxf(fmaxf(fmaxf(v0.x, v0.y), fmaxf(v0.z, v0.w)),
+                       fmaxf(fmaxf(v1.x, v1.y), fmaxf(v1.z, v1.w)));
+      mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(v2.x, v2.y), fmaxf(v2.z, v2.w)),
+                           fmaxf(fmaxf(v3.x, v3.y), fmaxf(v3.z, v3.w))));
+      if (mx > m) { s *= ex2((m - mx) * kLog2e); m = mx; }
+      const float mL = m * kLog2e;
+      float t0 = ex2(fmaf(v0.x, kLog2e, -mL)) + ex2(fmaf(v0.y, kLog2e, -mL)) +
+                 ex2(fmaf(v0.z, kLog2e, -mL)) + ex2(fmaf(v0.w, kLog2e, -mL));
+      float t1 = ex2(fmaf(v1.x, kLog2e, -mL)) + ex2(fmaf(v1.y, kLog2e, -mL)) +
+                 ex2(fmaf(v1.z, kLog2e, -mL)) + ex2(fmaf(v1.w, kLog2e, -mL));
+      float t2 = ex2(fmaf(v2.x, kLog2e, -mL)) + ex2(fmaf(v2.y, kLog2e, -mL)) +
+                 ex2(fmaf(v2.z, kLog2e, -mL)) + ex2(fmaf(v2.w, kLog2e, -mL));
+      float t3 = ex2(fmaf(v3.x, kLog2e, -mL)) + ex2(fmaf(v3.y, kLog2e, -mL)) +
+                 ex2(fmaf(v3.z, kLog2e, -mL)) + ex2(fmaf(v3.w, kLog2e, -mL));
+      s += (t0 + t1) + (t2 + t3);
+    }
+    for (; i < nvec; i += kExpandThreads) {
+      float4 v = __ldg(row4 + i);
+      float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+      if (mx > m) { s *= ex2((m - mx) * kLog2e); m = mx; }
+      const float mL = m * kLog2e;
+      s += ex2(fmaf(v.x, kLog2e, -mL)) + ex2(fmaf(v.y, kLog2e, -mL)) +
+           ex2(fmaf(v.z, kLog2e, -mL)) + ex2(fmaf(v.w, kLog2e, -mL));
+    }
+    for (int j = nvec * 4 + tid; j < a.V; j += kExpandThreads) {
+      float x = __ldg(row + j);
+      if (x > m) { s *= ex2((m - x) * kLog2e); m = x; }
+      s += ex2((x - m) * kLog2e);
+    }
+    // block reduction of (m, s)
+    for (int o = 16; o; o >>= 1) {
+      float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      float M = fmaxf(m, m2);
+      float a1 = (s == 0.f) ? 0.f : s * ex2((m - M) * kLog2e);
+      float a2 = (s2 == 0.f) ? 0.f : s2 * ex2((m2 - M) * kLog2e);
+      m = M; s = a1 + a2;
+    }
+    const int lane = tid & 31, warp = tid >> 5;
+    if (lane == 0) { sh.red_m[warp] = m; sh.red_s[warp] = s; }
+    __syncthreads();
+    if (warp == 0) {
+      const int nw = kExpandThreads / 32;
+      m = lane < nw ? sh.red_m[lane] : -INFINITY;
+      s = lane < nw ? sh.red_s[lane] : 0.f;
+      for (int o = 16; o; o >>= 1) {
+        float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        float M = fmaxf(m, m2);
+        float a1 = (s == 0.f) ? 0.f : s * ex2((m - M) * kLog2e);
+        float a2 = (s2 == 0.f) ? 0.f : s2 * ex2((m2 - M) * kLog2e);
+        m = M; s = a1 + a2;
+      }
+      if (lane == 0) sh.lse = m + logf(s);
+    }
+    __syncthreads();
+    lse = sh.lse;
+  }
+  if (a.lse_out != nullptr && tid == 0) a.lse_out[rowi] = lse;
+  const float cum = a.cum_in[rowi];
+
+  // ---- a2: candidate range (trie children or the whole vocabulary) --------
+  int n = a.V;
+  const int32_t* code = nullptr;
+  int tb = 0;
+  if (a.has_trie) {
+    const int node = a.node_in[rowi];
+    if (node < 0 || node >= a.lvl.n_nodes) {
+      if (tid == 0) set_status(ws.hdr, BEAMDEC_ERR_DEVICE_CHECK);
+      return;
+    }
+    const int e0 = a.lvl.off[node];
+    n = a.lvl.off[node + 1] - e0;
+    code = a.lvl.code + e0;
+    tb = a.lvl.token_base;
+  }
+  auto tok_of = [&](int i) -> int { return code ? tb + __ldg(code + i) : i; };
+  auto key_of = [&](int tok) -> uint32_t {
+    const float x = __ldg(row + tok);
+    return desc_key(__fadd_rn(cum, __fsub_rn(x, lse)));
+  };
+
+  SelState* st = ws.state + r;
+  unsigned long long* pool = ws.pool + (size_t)r * a.W * Kp;
+
+  // ---- a3: per-beam top_k -------------------------------------------------
+  if (n <= a.K) {
+    if (tid == 0) sh.pool_base = n > 0 ? atomicAdd(&st->total, n) : 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kExpandThreads) {
+      const int tok = tok_of(i);
+      pool[sh.pool_base + i] = pool_key(key_of(tok), b, tok);
+    }
+    return;
+  }
+  // radix select of the K-th smallest 32-bit score key: digits of 11, 11, 10 bits
+  uint32_t prefix = 0, need = (uint32_t)a.K;
+  const int widths[3] = {11, 11, 10};
+  int shift = 32;
+  for (int pass = 0; pass < 3; ++pass) {
+    const int w = widths[pass];
+    const int nb = 1 << w;
+    const int sh_next = shift - w;
+    for (int i = tid; i < nb; i += kExpandThreads) sh.hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kExpandThreads) {
+      const uint32_t k = key_of(tok_of(i));
+      if (shift == 32 || (k >> shift) == (prefix >> shift))
+        atomicAdd(&sh.hist[(k >> sh_next) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    if (tid < 32) warp_find_digit(sh.hist, nb, need, &sh.digit, &sh.below);
+    __syncthreads();
+    prefix |= sh.digit << sh_next;
+    need -= sh.below;
+    shift = sh_next;
+    __syncthreads();
+  }
+  const uint32_t kth = prefix;   // exact K-th smallest key; `need` ties at kth are kept
+  if (tid == 0) { sh.count = 0; sh.pool_base = atomicAdd(&st->total, a.K); }
+  __syncthreads();
+  const int base = sh.pool_base;
+  for (int i = tid; i < n; i += kExpandThreads) {
+    const int tok = tok_of(i);
+    const uint32_t k = key_of(tok);
+    if (k < kth) pool[base + atomicAdd(&sh.count, 1)] = pool_key(k, b, tok);
+  }
+  __syncthreads();
+  const int n_less = sh.count;
+  int taken = 0;
+  for (int c0 = 0; c0 < n && taken < (int)need; c0 += kExpandThreads) {
+    const int i = c0 + tid;
+    int tok = 0;
+    int flag = 0;
+    if (i < n) { tok = tok_of(i); flag = key_of(tok) == kth; }
+    int tot;
+    const int rk = block_rank(flag, sh.warp_cnt, &tot);
+    if (flag && taken + rk < (int)need) pool[base + n_less + taken + rk] = pool_key(kth, b, tok);
+    taken += tot;
+  }
+}
+
+// ---------------------------------------------------------------------------
+struct GlobalSmem {
+  uint32_t hist[kBins];
+  int warp_cnt[32];
+  uint32_t digit, below;
+  int all_done;
+};
+
+constexpr size_t kGlobalKeysOffset = (sizeof(GlobalSmem) + 15) & ~(size_t)15;
+
+__device__ __forceinline__ int find_child_edge(const TrieLevel& L, int node, int code) {
+  int lo = L.off[node], hi = L.off[node + 1];
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (L.code[mid] < code) lo = mid + 1; else hi = mid;
+  }
+  return (lo < L.off[node + 1] && L.code[lo] == code) ? lo : -1;
+}
+
+__global__ void __launch_bounds__(kGlobalThreads)
+bd_global_kernel(SelectArgs a) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  GlobalSmem& sh = *reinterpret_cast<GlobalSmem*>(dyn);
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(dyn + kGlobalKeysOffset);
+  const int tid = threadIdx.x;
+  const unsigned G = gridDim.x;
+  SelWs ws = carve(a.ws, a.R, a.W, a.Kp);
+
+  // phase 0: targets
+  for (int r = blockIdx.x; r < a.R; r += G) {
+    if (tid == 0) {
+      volatile SelState* st = ws.state + r;
+      const int total = st->total;
+      const int nt = total < a.W ? total : a.W;
+      st->n_target = nt;
+      st->need = nt;
+      st->sure = 0;
+      st->prefix = 0ull;
+      st->shift = 64;
+      st->ncand = 0;
+      st->done = (total <= kSelectCap) ? 1 : 0;   // small pools skip straight to the sort
+    }
+  }
+  grid_barrier(ws.hdr, G);
+
+  // radix-select passes over 12-bit digits until every request has at most
+  // kSelectCap keys at or below its threshold prefix
+  for (int pass = 0; pass < 6; ++pass) {
+    if (tid == 0) {
+      int all = 1;
+      for (int r = 0; r < a.R; ++r) all &= ((volatile SelState*)(ws.state + r))->done;
+      sh.all_done = all;
+    }
+    __syncthreads();
+    if (sh.all_done) break;
+    const int width = pass < 5 ? kDigitBits : 4;
+    for (int r = 0; r < a.R; ++r) {
+      volatile SelState* st = ws.state + r;
+      if (st->done) continue;
+      const int shift = st->shift;
+      const unsigned long long prefix = st->prefix;
+      const int nshift = shift - width;
+      const int total = st->total;
+      for (int i = tid; i < (1 << width); i += kGlobalThreads) sh.hist[i] = 0;
+      __syncthreads();
+      const unsigned long long* pool = ws.pool + (size_t)r * a.W * a.Kp;
+      const int per = (total + G - 1) / G;
+      const int i0 = blockIdx.x * per, i1 = min(total, i0 + per);
+      for (int i = i0 + tid; i < i1; i += kGlobalThreads) {
+        const unsigned long long k = pool[i];
+        if (shift == 64 || (k >> shift) == prefix)
+          atomicAdd(&sh.hist[(uint32_t)(k >> nshift) & ((1u << width) - 1u)], 1u);
+      }
+      __syncthreads();
+      uint32_t* gh = ws.hist + (size_t)r * kBins;
+      for (int i = tid; i < (1 << width); i += kGlobalThreads)
+        if (sh.hist[i]) atomicAdd(gh + i, sh.hist[i]);
+      __syncthreads();
+    }
+    grid_barrier(ws.hdr, G);
+    for (int r = blockIdx.x; r < a.R; r += G) {
+      volatile SelState* st = ws.state + r;
+      if (st->done) continue;
+      volatile uint32_t* gh = ws.hist + (size_t)r * kBins;
+      if (tid < 32) warp_find_digit(gh, 1 << width, (uint32_t)st->need, &sh.digit, &sh.below);
+      __syncthreads();
+      if (tid == 0) {
+        const uint32_t D = sh.digit;
+        const uint32_t in_bin = gh[D];
+        st->sure += (int)sh.below;
+        st->need -= (int)sh.below;
+        st->prefix = (st->prefix << width) | D;
+        st->shift -= width;
+        if (st->sure + (int)in_bin <= kSelectCap || st->shift == 0) st->done = 1;
+      }
+      __syncthreads();
+      for (int i = tid; i < (1 << width); i += kGlobalThreads) gh[i] = 0;
+      __syncthreads();
+    }
+    grid_barrier(ws.hdr, G);
+  }
+
+  // gather every key at or below the threshold prefix
+  for (int r = 0; r < a.R; ++r) {
+    volatile SelState* st = ws.state + r;
+    const int shift = st->shift;
+    const unsigned long long prefix = st->prefix;
+    const int total = st->total;
+    const unsigned long long* pool = ws.pool + (size_t)r * a.W * a.Kp;
+    unsigned long long* cand = ws.cand + (size_t)r * kSelectCap;
+    const int per = (total + G - 1) / G;
+    const int i0 = blockIdx.x * per, i1 = min(total, i0 + per);
+    for (int c0 = i0; c0 < i1; c0 += kGlobalThreads) {
+      const int i = c0 + tid;
+      unsigned long long k = 0;
+      int flag = 0;
+      if (i < i1) {
+        k = pool[i];
+        flag = (shift == 64) || ((k >> shift) <= prefix);
+      }
+      int tot;
+      const int rk = block_rank(flag, sh.warp_cnt, &tot);
+      if (tid == 0 && tot) sh.below = (uint32_t)atomicAdd((int*)&st->ncand, tot);
+      __syncthreads();
+      const int pos = (int)sh.below + rk;
+      if (flag) {
+        if (pos < kSelectCap) cand[pos] = k;
+        else set_status(ws.hdr, BEAMDEC_ERR_DEVICE_CHECK);
+      }
+      __syncthreads();
+    }
+  }
+  grid_barrier(ws.hdr, G);
+
+  // per request: sort the survivors, emit outputs and slot rows
+  for (int r = blockIdx.x; r < a.R; r += G) {
+    const volatile SelState* st = ws.state + r;
+    const int nc = min((int)st->ncand, kSelectCap);
+    const int nt = st->n_target;
+    int np = 32;
+    while (np < nc) np <<= 1;
+    const unsigned long long* cand = ws.cand + (size_t)r * kSelectCap;
+    for (int i = tid; i < np; i += kGlobalThreads) keys[i] = i < nc ? __ldcg(cand + i) : ~0ull;
+    __syncthreads();
+    for (int k = 2; k <= np; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < np; i += kGlobalThreads) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const unsigned long long x = keys[i], y = keys[ixj];
+            const bool up = (i & k) == 0;
+            if ((x > y) == up) { keys[i] = y; keys[ixj] = x; }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    const size_t o = (size_t)r * a.W;
+    for (int j = tid; j < a.W; j += kGlobalThreads) {
+      if (j < nt) {
+        const unsigned long long k = keys[j];
+        const int parent = pool_key_beam(k), tok = pool_key_tok(k);
+        a.tokens[o + j] = tok;
+        a.parents[o + j] = parent;
+        a.cum_out[o + j] = desc_key_value((uint32_t)(k >> 32));
+        int node = -1;
+        if (a.has_trie) {
+          node = find_child_edge(a.lvl, a.node_in[o + parent], tok - a.lvl.token_base);
+          if (node < 0) set_status(ws.hdr, BEAMDEC_ERR_DEVICE_CHECK);
+        }
+        a.node_out[o + j] = node;
+      } else {
+        a.tokens[o + j] = -1;
+        a.parents[o + j] = -1;
+        a.cum_out[o + j] = -INFINITY;
+        a.node_out[o + j] = -1;
+      }
+    }
+    const int T = a.T;
+    for (int idx = tid; idx < a.W * T; idx += kGlobalThreads) {
+      const int j = idx / T, t = idx - j * T;
+      int v = -1;
+      if (j < nt) {
+        if (t < a.step) v = a.slot_in[(o + pool_key_beam(keys[j])) * T + t];
+        else if (t == a.step) v = a.step * a.W + j;
+      }
+      a.slot_out[(o + j) * T + t] = v;
+    }
+    if (tid == 0) a.n_live_out[r] = nt;
+    __syncthreads();
+  }
+}
+
+struct GlobalLaunchCfg {
+  int max_blocks = 0;
+  size_t smem = 0;
+};
+
+}  // namespace
+
+size_t select_workspace_bytes(int R, int W, int K, int V) {
+  const int Kp = K < V ? K : V;
+  return kWsHeaderBytes + align256((size_t)R * sizeof(SelState)) +
+         align256((size_t)R * kBins * sizeof(uint32_t)) + align256((size_t)R * W * Kp * 8) +
+         (size_t)R * kSelectCap * 8;
+}
+
+int launch_select(const SelectArgs& a, cudaStream_t stream) {
+  static GlobalLaunchCfg cfg[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BEAMDEC_ERR_CUDA;
+  const size_t smem = kGlobalKeysOffset + (size_t)kSelectCap * 8;
+  if (cfg[dev].max_blocks == 0) {
+    if (cudaFuncSetAttribute(bd_global_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return BEAMDEC_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bd_global_kernel, kGlobalThreads,
+                                                      smem) != cudaSuccess || per_sm < 1)
+      return BEAMDEC_ERR_CUDA;
+    cfg[dev].max_blocks = per_sm * sm_count();
+    cfg[dev].smem = smem;
+  }
+  SelWs ws = carve(a.ws, a.R, a.W, a.Kp);
+  const size_t zero_bytes = (char*)ws.pool - (char*)ws.state;
+  if (cudaMemsetAsync(ws.state, 0, zero_bytes, stream) != cudaSuccess) return BEAMDEC_ERR_CUDA;
+
+  dim3 g1(a.W, a.R);
+  prof_begin(kKExpand, stream);
+  bd_expand_kernel<<<g1, kExpandThreads, 0, stream>>>(a);
+  prof_end(kKExpand, stream);
+  if (cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
+
+  const long long pool_max = (long long)a.R * a.W * a.Kp;
+  long long want = (pool_max + 4095) / 4096;
+  if (want < a.R) want = a.R;
+  int grid = (int)(want < cfg[dev].max_blocks ? want : cfg[dev].max_blocks);
+  if (grid < 1) grid = 1;
+  SelectArgs copy = a;
+  void* params[] = {&copy};
+  prof_begin(kKGlobal, stream);
+  const cudaError_t e = cudaLaunchCooperativeKernel((const void*)bd_global_kernel, dim3(grid),
+                                                    dim3(kGlobalThreads), params, cfg[dev].smem,
+                                                    stream);
+  prof_end(kKGlobal, stream);
+  return e == cudaSuccess ? BEAMDEC_OK : BEAMDEC_ERR_CUDA;
+}
+
+}  // namespace bd

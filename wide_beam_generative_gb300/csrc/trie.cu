@@ -1,0 +1,183 @@
+// Catalog trie construction (canonical CSR, one level per decode step).
+//
+// "Generative recommendation design" (xLLM) §4.3: invalid item paths are
+// filtered before they become candidates; FlashRec (SGLang PR 31626 thread):
+// a fused SID trie in CSR form keeps the illegal-SID rate at 0.
+//
+// The catalog is preprocessed once, not per decode step: items are sorted
+// lexicographically (packed into 64-bit keys when the code widths fit), de-
+// duplicated, and each level's CSR is read off the sorted order: sorted item
+// i opens a new length-(t+1) prefix (an edge of level t) exactly when it
+// differs from item i-1 within its first t+1 codes.  The CSR arrays are then
+// uploaded to device memory owned by the handle.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <numeric>
+#include <vector>
+
+#include "internal.h"
+
+namespace {
+
+int bits_for(int32_t C) {
+  int b = 0;
+  while ((1ll << b) < (long long)C) ++b;
+  return b;
+}
+
+}  // namespace
+
+extern "C" int beam_trie_build(const int32_t* items, int64_t n_items, int levels,
+                               const int32_t* codes_per_level, const int32_t* token_base,
+                               int32_t vocab, void* stream_ptr, beamdec_trie** out) {
+  if (out == nullptr) return BEAMDEC_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (items == nullptr || codes_per_level == nullptr || token_base == nullptr || n_items < 1 ||
+      levels < 1 || vocab < 1)
+    return BEAMDEC_ERR_INVALID_ARG;
+  if (levels > BEAMDEC_MAX_LEVELS || vocab > BEAMDEC_MAX_VOCAB || n_items >= (1ll << 31))
+    return BEAMDEC_ERR_UNSUPPORTED;
+  int total_bits = 0;
+  for (int l = 0; l < levels; ++l) {
+    const int32_t C = codes_per_level[l];
+    if (C < 1 || token_base[l] < 0) return BEAMDEC_ERR_INVALID_ARG;
+    if (C > BEAMDEC_MAX_CODES) return BEAMDEC_ERR_UNSUPPORTED;
+    if ((int64_t)token_base[l] + C > vocab) return BEAMDEC_ERR_INVALID_ARG;
+    total_bits += bits_for(C);
+  }
+  for (int64_t i = 0; i < n_items * levels; ++i) {
+    const int l = (int)(i % levels);
+    if (items[i] < 0 || items[i] >= codes_per_level[l]) return BEAMDEC_ERR_INVALID_ARG;
+  }
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+  // lexicographic order of the items
+  std::vector<int64_t> order(n_items);
+  std::iota(order.begin(), order.end(), 0);
+  if (total_bits <= 64) {
+    std::vector<uint64_t> key(n_items);
+    for (int64_t i = 0; i < n_items; ++i) {
+      uint64_t k = 0;
+      for (int l = 0; l < levels; ++l)
+        k = (total_bits ? (k << bits_for(codes_per_level[l])) : 0) | (uint64_t)items[i * levels + l];
+      key[i] = k;
+    }
+    std::sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
+      return key[a] < key[b] || (key[a] == key[b] && a < b);
+    });
+  } else {
+    std::sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
+      const int32_t* x = items + a * levels;
+      const int32_t* y = items + b * levels;
+      for (int l = 0; l < levels; ++l)
+        if (x[l] != y[l]) return x[l] < y[l];
+      return a < b;
+    });
+  }
+  // first differing level of each sorted item against its predecessor
+  // (levels = identical, i.e. a duplicate)
+  std::vector<int64_t> uniq;
+  std::vector<int8_t> diff;
+  uniq.reserve(n_items);
+  diff.reserve(n_items);
+  for (int64_t k = 0; k < n_items; ++k) {
+    const int32_t* x = items + order[k] * levels;
+    int dl = 0;
+    if (k > 0) {
+      const int32_t* y = items + order[k - 1] * levels;
+      while (dl < levels && x[dl] == y[dl]) ++dl;
+      if (dl == levels) continue;   // duplicate
+    }
+    uniq.push_back(order[k]);
+    diff.push_back((int8_t)dl);
+  }
+  const int64_t n = (int64_t)uniq.size();
+
+  beamdec_trie* t = new (std::nothrow) beamdec_trie();
+  if (t == nullptr) return BEAMDEC_ERR_ALLOC;
+  std::memset(t, 0, sizeof(*t));
+  t->levels = levels;
+  t->vocab = vocab;
+  t->n_items = n;
+  cudaGetDevice(&t->device);
+  int status = BEAMDEC_OK;
+  std::vector<int32_t> off, code;
+  for (int lv = 0; lv < levels && status == BEAMDEC_OK; ++lv) {
+    t->C[lv] = codes_per_level[lv];
+    t->token_base[lv] = token_base[lv];
+    // nodes at level lv = items opening a new lv-prefix (diff < lv); the root for lv = 0
+    off.assign(1, 0);
+    code.clear();
+    int64_t node = -1;
+    for (int64_t k = 0; k < n; ++k) {
+      const int d = diff[k];
+      if (lv == 0 ? k == 0 : d < lv) {   // new node at this level
+        ++node;
+        off.push_back(off.back());
+      }
+      if (d <= lv) {                      // new edge (a new (lv+1)-prefix)
+        code.push_back(items[uniq[k] * levels + lv]);
+        off.back() += 1;
+      }
+    }
+    t->n_nodes[lv] = node + 1;
+    t->n_edges[lv] = (int64_t)code.size();
+    int32_t mx = 0;
+    for (size_t i = 0; i + 1 < off.size(); ++i) mx = std::max(mx, off[i + 1] - off[i]);
+    t->max_children[lv] = mx;
+    if (cudaMalloc(&t->off[lv], off.size() * sizeof(int32_t)) != cudaSuccess ||
+        cudaMalloc(&t->code[lv], code.size() * sizeof(int32_t)) != cudaSuccess) {
+      status = BEAMDEC_ERR_ALLOC;
+      break;
+    }
+    if (cudaMemcpyAsync(t->off[lv], off.data(), off.size() * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(t->code[lv], code.data(), code.size() * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+      status = BEAMDEC_ERR_CUDA;
+      break;
+    }
+  }
+  if (status != BEAMDEC_OK) {
+    beam_trie_free(t);
+    return status;
+  }
+  *out = t;
+  return BEAMDEC_OK;
+}
+
+extern "C" void beam_trie_free(beamdec_trie* t) {
+  if (t == nullptr) return;
+  for (int l = 0; l < BEAMDEC_MAX_LEVELS; ++l) {
+    if (t->off[l]) cudaFree(t->off[l]);
+    if (t->code[l]) cudaFree(t->code[l]);
+  }
+  delete t;
+}
+
+extern "C" int beam_trie_info(const beamdec_trie* t, int* levels, int32_t* vocab,
+                              int64_t* n_distinct, int64_t* n_nodes, int64_t* n_edges,
+                              int32_t* max_children) {
+  if (t == nullptr) return BEAMDEC_ERR_INVALID_ARG;
+  if (levels) *levels = t->levels;
+  if (vocab) *vocab = t->vocab;
+  if (n_distinct) *n_distinct = t->n_items;
+  for (int l = 0; l < t->levels; ++l) {
+    if (n_nodes) n_nodes[l] = t->n_nodes[l];
+    if (n_edges) n_edges[l] = t->n_edges[l];
+    if (max_children) max_children[l] = t->max_children[l];
+  }
+  return BEAMDEC_OK;
+}
+
+extern "C" int beam_trie_export(const beamdec_trie* t, int level, const int32_t** off,
+                                const int32_t** code) {
+  if (t == nullptr || level < 0 || level >= t->levels) return BEAMDEC_ERR_INVALID_ARG;
+  if (off) *off = t->off[level];
+  if (code) *code = t->code[level];
+  return BEAMDEC_OK;
+}
