@@ -32,9 +32,11 @@
  *   are recorded in the status word at the start of the workspace and read
  *   with beamdec_read_status.  Kernels never trap or print.
  * - Workspace: caller-owned device memory of at least the size returned by
- *   the matching *_workspace_size query, 256-byte aligned.  A workspace may
- *   be reused across calls on one stream; calls that run concurrently need
- *   separate workspaces.
+ *   the matching *_workspace_size query, 256-byte aligned, zero-filled
+ *   before its first use (its first 256 bytes hold the status word and
+ *   counters that must start at zero; the library keeps them consistent
+ *   afterwards).  A workspace may be reused across calls on one stream;
+ *   calls that run concurrently need separate workspaces.
  */
 #ifndef BEAMDEC_H
 #define BEAMDEC_H
@@ -245,6 +247,8 @@ int beam_attn_workspace_size(int R, int W, int Hq, int Hkv, int d, int max_promp
  *                   prompt_offsets[r] .. prompt_offsets[r+1]-1.
  *   prompt_offsets  [R+1] int32, non-decreasing, prompt_offsets[0] = 0.
  *   max_prompt_len  host int >= every P_r (sizes the launch).
+ *   shared_rows     host: rows allocated in shared_k / shared_v (>= sum P);
+ *                   no row at or beyond it is ever read.
  *   unshared_k/v    [R][T*W][Hkv][d] kv_dtype: the per-request slot pool.
  *   slot_table      [R][W][T] int32; entries 0..step of live rows must lie in
  *                   [0, T*W) (checked in-kernel; a bad slot sets
@@ -259,7 +263,7 @@ int beam_attn_workspace_size(int R, int W, int Hq, int Hkv, int d, int max_promp
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  */
 int beam_attn_decode(const void* q, const void* shared_k, const void* shared_v,
-                     const int32_t* prompt_offsets, int max_prompt_len,
+                     const int32_t* prompt_offsets, int max_prompt_len, int64_t shared_rows,
                      const void* unshared_k, const void* unshared_v,
                      const int32_t* slot_table, const int32_t* n_live, int step,
                      int R, int W, int Hq, int Hkv, int d, int T,

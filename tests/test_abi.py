@@ -76,7 +76,7 @@ def test_select_workspace_size(L):
 
 
 def _attn(L, **kw):
-    args = dict(q=FAKE, sk=FAKE, sv=FAKE, off=FAKE, maxp=256, uk=FAKE, uv=FAKE, slot=FAKE,
+    args = dict(q=FAKE, sk=FAKE, sv=FAKE, off=FAKE, maxp=256, rows=256, uk=FAKE, uv=FAKE, slot=FAKE,
                 n_live=FAKE, step=0, R=1, W=8, Hq=2, Hkv=1, d=64, T=3, qd=0, kvd=0, od=0,
                 ks=None, vs=None, sm=0.0, out=FAKE, ws=FAKE, ws_bytes=0, stream=None)
     args.update(kw)
@@ -94,6 +94,7 @@ def test_attention_validation(L):
     assert _attn(L, qd=1, kvd=2, od=1) == bd.ERR_INVALID_ARG            # e4m3 without scales
     assert _attn(L, step=3) == bd.ERR_INVALID_ARG
     assert _attn(L, maxp=256, sk=None) == bd.ERR_INVALID_ARG
+    assert _attn(L, rows=100) == bd.ERR_INVALID_ARG                     # fewer rows than a prompt
     assert _attn(L) == bd.ERR_WORKSPACE
     n = bd.beam_attn_workspace_size(4, 512, 16, 8, 128, 4096, bd.BF16)
     assert n >= 4 * 512 * 16 * 128 * 4

@@ -22,6 +22,7 @@ def _slots(wl, step, n_live, seed=0):
 
 
 def _run(wl, step, n_live, beams=None, seed=0):
+    """Runs the library and the oracle on the same inputs."""
     from wide_beam_generative_gb300 import beamdec as bd
     a = synth.attention_inputs(wl, step, device=DEV)
     slot = _slots(wl, step, n_live, seed)
@@ -114,3 +115,14 @@ def test_bad_slot_sets_device_check(gpu_lib):
                         a["unshared_k"], a["unshared_v"], slot.to(DEV),
                         torch.tensor([wl.W], dtype=torch.int32, device=DEV), 1, ws=ws)
     assert bd.read_status(ws) == bd.ERR_DEVICE_CHECK
+
+
+@pytest.mark.parametrize("G,W,plens", [(2, 70, [300, 129]), (1, 200, [128, 1000]), (4, 33, [77, 512]),
+                                       (8, 16, [2049, 5]), (16, 8, [640, 641])])
+def test_tensor_core_shapes(gpu_lib, G, W, plens):
+    """bf16, d = 128: the tcgen05 shared stage, with query tiles that end
+    mid-tile, prompts that end mid-chunk and several prompt splits."""
+    wl = synth.WORKLOADS["qwen06b"].scaled(name="tc", R=len(plens), prompt_lens=plens, Hq=2 * G, Hkv=2,
+                                           W=W, T=3)
+    got, want, _ = _run(wl, 1, [W, max(1, W - 5)])
+    _check(wl, got, want)

@@ -45,7 +45,7 @@ _SIGS = {
                             c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]),
     "beam_attn_workspace_size": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                          ctypes.POINTER(c_sz)]),
-    "beam_attn_decode": (c_int, [c_p, c_p, c_p, c_p, c_int, c_p, c_p, c_p, c_p, c_int,
+    "beam_attn_decode": (c_int, [c_p, c_p, c_p, c_p, c_int, c_i64, c_p, c_p, c_p, c_p, c_int,
                                  c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                  c_p, c_p, c_f, c_p, c_p, c_sz, c_p]),
 }
@@ -155,7 +155,8 @@ def beam_trie_build(items, codes_per_level, token_base, vocab, stream=None) -> T
 
 
 def workspace(nbytes, device="cuda"):
-    ws = torch.empty(int(nbytes) + 256, dtype=torch.uint8, device=device)
+    """Zero-filled, 256-byte aligned device workspace of ``nbytes``."""
+    ws = torch.zeros(int(nbytes) + 256, dtype=torch.uint8, device=device)
     off = (-ws.data_ptr()) % 256
     return ws[off:off + int(nbytes)]
 
@@ -248,8 +249,9 @@ def beam_attn_decode(q, shared_k, shared_v, prompt_offsets, max_prompt_len, unsh
                           device=q.device)
     if ws is None:
         ws = workspace(beam_attn_workspace_size(R, W, Hq, Hkv, d, max_prompt_len, kvd), q.device)
+    shared_rows = shared_k.shape[0] if shared_k is not None else 0
     rc = lib().beam_attn_decode(_ptr(q), _ptr(shared_k), _ptr(shared_v), _ptr(prompt_offsets),
-                                int(max_prompt_len), _ptr(unshared_k), _ptr(unshared_v),
+                                int(max_prompt_len), int(shared_rows), _ptr(unshared_k), _ptr(unshared_v),
                                 _ptr(slot_table), _ptr(n_live), step, R, W, Hq, Hkv, d, T,
                                 qd, kvd, od, _ptr(k_scale), _ptr(v_scale), float(sm_scale),
                                 _ptr(out), _ptr(ws), ws.numel(), _stream(stream))

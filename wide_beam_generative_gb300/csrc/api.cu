@@ -24,10 +24,10 @@ static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 AttnPlan attn_plan(int R, int W, int Hq, int Hkv, int d, int max_prompt_len, int q_dtype,
                    int kv_dtype) {
   AttnPlan p;
-  p.tensor_core = false;
   const int G = Hq / Hkv;
+  p.tensor_core = attn_tc_supported(q_dtype, kv_dtype, d, G);
   const int rows = W * G;
-  const int tile_rows = 32;
+  const int tile_rows = p.tensor_core ? 128 : 32;
   const long long units = (long long)R * Hkv * ((rows + tile_rows - 1) / tile_rows);
   const int sms = 148;   // planning constant; the split count only shapes the work
   int n_split = 1;
@@ -177,7 +177,7 @@ extern "C" int beam_attn_workspace_size(int R, int W, int Hq, int Hkv, int d, in
 
 extern "C" int beam_attn_decode(const void* q, const void* shared_k, const void* shared_v,
                                 const int32_t* prompt_offsets, int max_prompt_len,
-                                const void* unshared_k, const void* unshared_v,
+                                int64_t shared_rows, const void* unshared_k, const void* unshared_v,
                                 const int32_t* slot_table, const int32_t* n_live, int step,
                                 int R, int W, int Hq, int Hkv, int d, int T, int q_dtype,
                                 int kv_dtype, int out_dtype, const float* k_scale,
@@ -188,6 +188,8 @@ extern "C" int beam_attn_decode(const void* q, const void* shared_k, const void*
       workspace == nullptr)
     return BEAMDEC_ERR_INVALID_ARG;
   if (max_prompt_len > 0 && (shared_k == nullptr || shared_v == nullptr))
+    return BEAMDEC_ERR_INVALID_ARG;
+  if (shared_rows < 0 || (max_prompt_len > 0 && shared_rows < max_prompt_len))
     return BEAMDEC_ERR_INVALID_ARG;
   const int s = attn_shape_check(R, W, Hq, Hkv, d, max_prompt_len);
   if (s != BEAMDEC_OK) return s;
@@ -204,7 +206,7 @@ extern "C" int beam_attn_decode(const void* q, const void* shared_k, const void*
   if (workspace_bytes < attn_workspace_bytes(R, W, Hq, Hkv, d, p)) return BEAMDEC_ERR_WORKSPACE;
   AttnArgs a{};
   a.q = q; a.shared_k = shared_k; a.shared_v = shared_v;
-  a.prompt_offsets = prompt_offsets; a.max_prompt_len = max_prompt_len;
+  a.prompt_offsets = prompt_offsets; a.max_prompt_len = max_prompt_len; a.shared_rows = shared_rows;
   a.unshared_k = unshared_k; a.unshared_v = unshared_v;
   a.slot_table = slot_table; a.n_live = n_live;
   a.step = step; a.R = R; a.W = W; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.T = T;

@@ -52,7 +52,7 @@ int launch_select(const SelectArgs& a, cudaStream_t stream);
 // ---- attention ---------------------------------------------------------------
 struct AttnArgs {
   const void* q; const void* shared_k; const void* shared_v;
-  const int32_t* prompt_offsets; int max_prompt_len;
+  const int32_t* prompt_offsets; int max_prompt_len; int64_t shared_rows;
   const void* unshared_k; const void* unshared_v;
   const int32_t* slot_table; const int32_t* n_live;
   int step, R, W, Hq, Hkv, d, T;
@@ -71,6 +71,7 @@ AttnPlan attn_plan(int R, int W, int Hq, int Hkv, int d, int max_prompt_len, int
 size_t attn_workspace_bytes(int R, int W, int Hq, int Hkv, int d, const AttnPlan& p);
 int launch_attn_shared_simt(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
+bool attn_tc_supported(int q_dtype, int kv_dtype, int d, int G);
 int launch_attn_merge(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 
 // Partial-triple layout in the attention workspace (after the 256-byte header):
