@@ -274,6 +274,8 @@ def gpu_arm(args, ws, rank, local):
     launches = sum(n for _, n in prof.values())
 
     # roofline of the dominant kernel
+    if not any(n for _, n in prof.values()):
+        raise SystemExit("no kernel launches were recorded in the timed region")
     dom = max(prof.items(), key=lambda kv: kv[1][0])
     kname, (kms, kn) = dom
     units, kind = algorithmic(wl, rows, kname)

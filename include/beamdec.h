@@ -199,7 +199,8 @@ int beam_select_workspace_size(int R, int W, int K, int V, size_t* bytes);
  *   parents     int32 index of the parent beam in the input, -1 if dead.
  *   cum_out     fp32 score s = fl32(cum_in[parent] + fl32(logit - lse)),
  *               round-to-nearest-even, no FMA; -inf if dead.
- *   lse_out     optional fp32 log-sum-exp of each live input row (NULL to skip).
+ *   lse_out     optional fp32 log-sum-exp of each live input row (NULL to skip);
+ *               entries of rows b >= n_live_in[r] are left untouched.
  *   node_out    int32 child node at level+1 (= edge index); at the last level
  *               the item index; -1 for open vocabulary or dead rows.
  *   n_live_out  [R] int32 = min(W, pool size).

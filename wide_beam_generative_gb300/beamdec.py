@@ -101,7 +101,7 @@ class _DevArray:
 
     def __init__(self, ptr, n):
         self.__cuda_array_interface__ = {"shape": (int(n),), "typestr": "<i4",
-                                         "data": (int(ptr), True), "version": 3}
+                                         "data": (int(ptr), False), "version": 3}
 
 
 class Trie:

@@ -13,8 +13,8 @@
 //               (two 64-column SWIZZLE_128B boxes each) into a 2-stage ring;
 //   warp 1      allocates TMEM and issues the MMAs from one thread:
 //               S = Q K^T (M 128, N 128, K 128) into a double-buffered TMEM
-//               score tile, and O_c = P V (M 128, N 64 per half of d) into a
-//               double-buffered TMEM output tile;
+//               score tile, and O_c = P V (M 128, N 128, K 128; V read
+//               d-major) into a double-buffered TMEM output tile;
 //   warps 4-7   softmax: thread t owns query row t (TMEM lane t); reads its
 //               scores from TMEM, keeps the running max / sum in log2 units,
 //               writes P as bf16 into shared memory in the 128B-swizzled
@@ -46,9 +46,10 @@ constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;
 constexpr uint32_t kSmemBytes = kOffP + kTileBytes + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;  // S0 S1 O0 O1, 128 columns each
 
-// MN-major B operand (V): stride between 8-key groups and between 64-column
-// atoms along d.
-constexpr uint32_t kVLbo = 16384;
+// MN-major B operand (V, d contiguous): the leading byte offset is the stride
+// between 64-column swizzle atoms along d (the two 16 KB halves), the stride
+// byte offset the stride between groups of 8 keys (8 x 128 B).
+constexpr uint32_t kVLbo = kHalfBytes;
 constexpr uint32_t kVSbo = 1024;
 
 struct TcParams {
@@ -183,7 +184,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-    const uint32_t idO = idesc_bf16_f32(128, 64, false, true);
+    const uint32_t idO = idesc_bf16_f32(128, 128, false, true);
     const uint32_t qa = smem_u32(sm + kOffQ);
     bool ok = mbar_wait(&bars.q, 0);
     auto issue_s = [&](int c) -> bool {
@@ -216,7 +217,6 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         const uint64_t a = sdesc_sw128(pa + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
         const uint32_t vk = vb + k * 16 * 128;   // 16 keys per step
         mma_bf16(tmem + 256 + s * 128, a, sdesc_sw128(vk, kVLbo, kVSbo), idO, k > 0);
-        mma_bf16(tmem + 256 + s * 128 + 64, a, sdesc_sw128(vk + kHalfBytes, kVLbo, kVSbo), idO, k > 0);
       }
       mma_commit(&bars.empty_v[s]);
       mma_commit(&bars.pv_done);

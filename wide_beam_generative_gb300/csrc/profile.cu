@@ -54,9 +54,11 @@ extern "C" int beamdec_profile_enable(int on) {
         if (cudaEventCreate(&g_ev[i][k]) != cudaSuccess) return BEAMDEC_ERR_CUDA;
     g_created = true;
   }
+  if (on) {   // a new recording starts empty; disabling keeps it for reading
+    g_n = 0;
+    for (int k = 0; k < kKCount; ++k) g_open[k] = -1;
+  }
   g_on = on != 0;
-  g_n = 0;
-  for (int k = 0; k < kKCount; ++k) g_open[k] = -1;
   return BEAMDEC_OK;
 }
 
