@@ -220,6 +220,38 @@ int beam_select(const float* logits, int64_t row_stride, const float* lse_in,
                 int32_t* node_out, int32_t* n_live_out, int32_t* slot_out,
                 void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * beam_select_static — beam_select without a caller-provided workspace.
+ * The pages have no counterpart to this entry point; it serves callers of
+ * this library that cannot allocate device memory: a plugin interface that
+ * hands the library only its input and output buffers, or a process whose
+ * device memory belongs to another allocator, so that cudaMalloc may not be
+ * called on the calling path.
+ *
+ * Arguments, outputs, ordering and errors are those of beam_select, minus
+ * `workspace` / `workspace_bytes`.  The scratch is one file-scope device
+ * array of BEAMDEC_STATIC_SELECT_BYTES bytes, which every GPU that loads the
+ * library holds until the process exits; shapes whose
+ * beam_select_workspace_size exceeds it are rejected with
+ * BEAMDEC_ERR_UNSUPPORTED before anything is launched.  Nothing is allocated.
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it: make that first call before any stream
+ * capture.  All calls on a device share the array and it keeps the last
+ * call's contents; each call clears the status word and counters it needs on
+ * its own stream first, so calls in stream order are independent, but calls
+ * that overlap on the GPU (unordered streams) race on the array.  The status
+ * word in the array is cleared at the start of each call and is not readable
+ * through beamdec_read_status; use beam_select with an own workspace to
+ * observe device-side checks.
+ */
+#define BEAMDEC_STATIC_SELECT_BYTES ((size_t)16 << 20)
+int beam_select_static(const float* logits, int64_t row_stride, const float* lse_in,
+                       const float* cum_in, const int32_t* node_in, const int32_t* n_live_in,
+                       const int32_t* slot_in, const beamdec_trie* trie, int level, int step,
+                       int R, int W, int K, int V, int T,
+                       int32_t* tokens, int32_t* parents, float* cum_out, float* lse_out,
+                       int32_t* node_out, int32_t* n_live_out, int32_t* slot_out, void* stream);
+
 /* ======================================================================== *
  * Beam attention
  * ======================================================================== */

@@ -120,3 +120,12 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(bd, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         bd.lib()
+
+
+def test_static_select_rejects_oversized_shapes_on_host(L):
+    from wide_beam_generative_gb300 import beamdec as bd
+    fake = ctypes.c_void_p(0x1000)
+    rc = L.beam_select_static(fake, 151936, None, fake, fake, fake, fake, None, 0, 0,
+                              2, 5000, 5000, 151936, 2, fake, fake, fake, None, fake, fake,
+                              ctypes.c_void_p(0x2000), None)
+    assert rc == bd.ERR_UNSUPPORTED

@@ -43,6 +43,9 @@ _SIGS = {
     "beam_select": (c_int, [c_p, c_i64, c_p, c_p, c_p, c_p, c_p, c_p, c_int, c_int,
                             c_int, c_int, c_int, c_int, c_int,
                             c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]),
+    "beam_select_static": (c_int, [c_p, c_i64, c_p, c_p, c_p, c_p, c_p, c_p, c_int, c_int,
+                                   c_int, c_int, c_int, c_int, c_int,
+                                   c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p]),
     "beam_attn_workspace_size": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                          ctypes.POINTER(c_sz)]),
     "beam_attn_decode": (c_int, [c_p, c_p, c_p, c_p, c_int, c_i64, c_p, c_p, c_p, c_p, c_int,
@@ -229,6 +232,36 @@ def beam_select(logits, cum, node, n_live, slot_in, trie, level, step, K, T=None
                            _ptr(out.get("lse_out")), _ptr(out["node_out"]), _ptr(out["n_live_out"]),
                            _ptr(out["slot_out"]), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "beam_select")
+    return out
+
+
+def beam_select_static(logits, cum, node, n_live, slot_in, trie, level, step, K, T=None,
+                       lse_in=None, out=None, stream=None, want_lse=True):
+    """beam_select with the library's fixed static scratch instead of a
+    workspace (for callers that cannot allocate); same arguments and outputs."""
+    R, W = cum.shape
+    V = logits.shape[-1]
+    if logits.dim() != 3 or logits.shape[0] != R or logits.shape[1] != W or logits.stride(2) != 1 \
+            or logits.stride(0) != W * logits.stride(1):
+        raise ValueError("logits must be [R, W, V] with unit stride in V and rows packed per request")
+    T = slot_in.shape[2] if T is None else T
+    _need_cuda(cum, node, n_live, slot_in, lse_in)
+    dev = cum.device
+    if out is None:
+        out = dict(tokens=torch.empty((R, W), dtype=torch.int32, device=dev),
+                   parents=torch.empty((R, W), dtype=torch.int32, device=dev),
+                   cum_out=torch.empty((R, W), dtype=torch.float32, device=dev),
+                   lse_out=torch.empty((R, W), dtype=torch.float32, device=dev) if want_lse else None,
+                   node_out=torch.empty((R, W), dtype=torch.int32, device=dev),
+                   n_live_out=torch.empty((R,), dtype=torch.int32, device=dev),
+                   slot_out=torch.empty((R, W, T), dtype=torch.int32, device=dev))
+    rc = lib().beam_select_static(_ptr(logits), logits.stride(1), _ptr(lse_in), _ptr(cum), _ptr(node),
+                                  _ptr(n_live), _ptr(slot_in), trie.handle if trie is not None else None,
+                                  level, step, R, W, K, V, T,
+                                  _ptr(out["tokens"]), _ptr(out["parents"]), _ptr(out["cum_out"]),
+                                  _ptr(out.get("lse_out")), _ptr(out["node_out"]), _ptr(out["n_live_out"]),
+                                  _ptr(out["slot_out"]), _stream(stream))
+    _check(rc, "beam_select_static")
     return out
 
 
