@@ -241,6 +241,9 @@ def gpu_arm(args, ws, rank, local):
     from wide_beam_generative_gb300 import beamdec as bd
     dev = torch.device("cuda", local)
     wl = synth.WORKLOADS[args.workload]
+    if args.requests:
+        wl = wl.scaled(R=args.requests, prompt_lens=None if wl.prompt_lens is None else
+                       list(wl.prompt_lens[:1]) * args.requests)
     step = Step(wl, dev)
     rows = step.rows()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -301,7 +304,7 @@ def gpu_arm(args, ws, rank, local):
                for k, (ms, n) in prof.items() if n}
 
     # end-to-end through the C ABI from pinned host buffers
-    e2e = e2e_arm(step, args, ws, flush)
+    e2e = None if args.no_e2e else e2e_arm(step, args, ws, flush)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "beam-rows/s", "n_gpus": ws,
@@ -316,7 +319,7 @@ def gpu_arm(args, ws, rank, local):
         "roofline": roof, "kernels": kernels, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows or 512)
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows or 4 * wl.W)
     return line
 
 
@@ -365,46 +368,59 @@ def e2e_arm(step, args, ws, flush):
 # ------------------------------------------------------------------------------ CPU oracle
 
 def cpu_sample(wl, rows):
-    """A bounded sample of the workload for the oracle: the first `rows` beams
-    of request 0 at the last step (their logits rows, queries and slot rows)."""
+    """A bounded sample of the workload for the oracle: `rows` beams of the
+    last decode step, taken request by request (W beams each), with their
+    logits rows, queries and ancestry rows."""
     from oracle import trie as otrie
     items = synth.catalog(wl)
     tr = otrie.build_trie(items, wl.C) if wl.levels else None
     step = wl.T - 1
-    lg = synth.logit_rows(wl, step, 0, 0, rows).numpy()[None]
     rng = np.random.default_rng(1)
-    if tr is not None:
-        pick = items[rng.integers(0, len(items), rows)]
-        node = np.array([[tr.node_of_prefix(p[:step]) for p in pick]], np.int64)
-    else:
-        node = np.zeros((1, rows), np.int64)
-    cum = np.zeros((1, rows), np.float32)
-    slot = np.zeros((1, rows, wl.T), np.int32)
-    for t in range(step):
-        slot[0, :, t] = t * wl.W + rng.integers(0, wl.W, rows)
-    a = synth.attention_inputs(wl.scaled(R=1, prompt_lens=[int(synth.prompt_lens(wl)[0])], p_range=None), step)
+    parts = []
+    left = rows
+    for r in range(wl.R):
+        if left <= 0:
+            break
+        n = min(wl.W, left)
+        left -= n
+        lg = synth.logit_rows(wl, step, r, 0, n).numpy()[None]
+        if tr is not None:
+            pick = items[rng.integers(0, len(items), n)]
+            node = np.array([[tr.node_of_prefix(p[:step]) for p in pick]], np.int64)
+        else:
+            node = np.zeros((1, n), np.int64)
+        cum = np.zeros((1, n), np.float32)
+        slot = np.zeros((1, n, wl.T), np.int32)
+        for t in range(step):
+            slot[0, :, t] = t * wl.W + rng.integers(0, wl.W, n)
+        sub = wl.scaled(R=1, prompt_lens=[int(synth.prompt_lens(wl)[r])], p_range=None)
+        a = synth.attention_inputs(sub, step)
 
-    def raw(t):
-        if t.dtype == torch.bfloat16:
-            return t.view(torch.int16).numpy().view(np.uint16)
-        if t.dtype == torch.float8_e4m3fn:
-            return t.view(torch.uint8).numpy()
-        return t.numpy()
-    inp = dict(q=raw(a["q"][:, :rows]), shared_k=raw(a["shared_k"]), shared_v=raw(a["shared_v"]),
-               unshared_k=raw(a["unshared_k"]), unshared_v=raw(a["unshared_v"]),
-               k_scale=a["k_scale"].numpy(), v_scale=a["v_scale"].numpy(),
-               prompt_offsets=a["prompt_offsets"].numpy(), q_dtype=wl.q_dtype, kv_dtype=wl.kv_dtype)
-    return dict(lg=lg, node=node, cum=cum, slot=slot, tr=tr, inp=inp, step=step, rows=rows)
+        def raw(t):
+            if t.dtype == torch.bfloat16:
+                return t.view(torch.int16).numpy().view(np.uint16)
+            if t.dtype == torch.float8_e4m3fn:
+                return t.view(torch.uint8).numpy()
+            return t.numpy()
+        inp = dict(q=raw(a["q"][:, :n]), shared_k=raw(a["shared_k"]), shared_v=raw(a["shared_v"]),
+                   unshared_k=raw(a["unshared_k"]), unshared_v=raw(a["unshared_v"]),
+                   k_scale=a["k_scale"].numpy(), v_scale=a["v_scale"].numpy(),
+                   prompt_offsets=a["prompt_offsets"].numpy(), q_dtype=wl.q_dtype, kv_dtype=wl.kv_dtype)
+        parts.append(dict(lg=lg, node=node, cum=cum, slot=slot, inp=inp, rows=n))
+    return dict(parts=parts, tr=tr, step=step, rows=sum(p["rows"] for p in parts))
 
 
 def cpu_run(wl, s):
+    """The oracle's decode step (selection, then attention) on the sample."""
     from oracle import attention as oatt
     from oracle import select as osel
-    rows, step = s["rows"], s["step"]
-    sel = osel.beam_select(s["lg"], s["cum"], s["node"], np.array([rows]), s["slot"], s["tr"],
-                           wl.token_base(), step, step, rows, min(wl.K, rows))
-    oatt.attention_decode(s["inp"], sel["slot_out"], sel["n_live_out"], step)
-    return rows
+    step = s["step"]
+    for p in s["parts"]:
+        n = p["rows"]
+        sel = osel.beam_select(p["lg"], p["cum"], p["node"], np.array([n]), p["slot"], s["tr"],
+                               wl.token_base(), step, step, n, min(wl.K, n))
+        oatt.attention_decode(p["inp"], sel["slot_out"], sel["n_live_out"], step)
+    return s["rows"]
 
 
 def cpu_baseline(wl, rows):
@@ -414,9 +430,9 @@ def cpu_baseline(wl, rows):
     dt = time.time() - t0
     return {"value": round(done / dt, 2), "unit": "beam-rows/s", "cores": os.cpu_count(),
             "kind": "oracle", "seconds": round(dt, 2),
-            "sample": f"request 0, beams 0..{rows - 1} of the last step: float64 log-sum-exp + trie "
-                      f"children + full sorts, float64 attention over prompt + ancestry "
-                      f"(numpy; BLAS matmuls may use every core)"}
+            "sample": f"{done} beams ({min(wl.R, (rows + wl.W - 1) // wl.W)} requests x up to {wl.W}) of the "
+                      f"last decode step: float64 log-sum-exp + trie children + full sorts, float64 "
+                      f"attention over prompt + ancestry (numpy; BLAS matmuls may use every core)"}
 
 
 def reference_arm(args, ws, rank):
@@ -435,9 +451,10 @@ def reference_arm(args, ws, rank):
             "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; see synth)",
             "impl": "reference",
-            "config": {"workload": f"{wl.name} (bounded sample of {s['rows']} beams per step)"},
+            "config": {"workload": f"{wl.name} (bounded sample of {s['rows']} beams per step)",
+                       "requests": wl.R},
             "cpu_baseline": {"value": v, "unit": "beam-rows/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": f"request 0, beams 0..{s['rows'] - 1} of the last decode step"},
+                             "sample": f"{s['rows']} beams of the last decode step"},
             "e2e": {"value": v, "unit": "beam-rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -451,6 +468,9 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=None,
                     help="beams in the oracle's sample (default 512 for cpu_baseline, 128 per reference step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--requests", type=int, default=None,
+                    help="override the workload's request count (smaller cases for profiling)")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     if args.impl == "reference":
