@@ -12,7 +12,9 @@
 //
 // One warp per (request, beam, query head).  Lane l owns dims
 // [l*D/32, (l+1)*D/32).  The beam's slot row (<= 32 entries read per step) is
-// loaded once, one slot per lane, and broadcast with shuffles.
+// loaded once, one slot per lane, and broadcast with shuffles.  Loads that do
+// not depend on each other (query, the first splits' partials, a few tokens'
+// K and V) are issued together so a warp waits on few memory round trips.
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -37,9 +39,11 @@ __device__ __forceinline__ void load_lane(const void* base, size_t e, float (&x)
 }
 
 template <int DQ, int DKV, int D>
-__global__ void __launch_bounds__(512)
+__global__ void __launch_bounds__(512, 2)
 bd_attn_merge_kernel(AttnArgs a, int n_split, AttnPartials part) {
   constexpr int PL = D / 32;
+  constexpr int kPre = 2;          // prompt splits whose partials are prefetched
+  constexpr int kTok = PL == 4 ? 2 : 4;   // unshared tokens whose K/V loads are in flight together
   const int j = blockIdx.x, r = blockIdx.y;
   const int lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
@@ -74,61 +78,111 @@ bd_attn_merge_kernel(AttnArgs a, int n_split, AttnPartials part) {
       continue;
     }
     const int g = h / G, gi = h - g * G;
+    const int row = j * G + gi;
+    // independent loads first: query, and the first splits' partial triples
+    float q[PL];
+    load_lane<DQ, PL>(a.q, out_e, q);
+    float pm_l = -INFINITY, pl_l = 0.f;   // lane c holds split c's (m, l)
+    if (lane < n_split) {
+      const size_t pi = (((size_t)lane * a.R + r) * a.Hkv + g) * rows + row;
+      pm_l = part.m[pi];
+      pl_l = part.l[pi];
+    }
+    float oc[kPre][PL];
+#pragma unroll
+    for (int c = 0; c < kPre; ++c) {
+      if (c < n_split) {
+        const size_t pi = (((size_t)c * a.R + r) * a.Hkv + g) * rows + row;
+        const float* src = part.o + pi * D + lane * PL;
+        if constexpr (PL == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          oc[c][0] = v.x; oc[c][1] = v.y; oc[c][2] = v.z; oc[c][3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          oc[c][0] = v.x; oc[c][1] = v.y;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < PL; ++i) oc[c][i] = 0.f;
+      }
+    }
     const float ks = (DKV == 2 && a.k_scale) ? a.k_scale[g] : 1.f;
     const float vs = (DKV == 2 && a.v_scale) ? a.v_scale[g] : 1.f;
     const float scale2 = a.sm_scale * kLog2e * ks;
-    float q[PL];
-    load_lane<DQ, PL>(a.q, out_e, q);
 #pragma unroll
     for (int i = 0; i < PL; ++i) q[i] *= scale2;
-    // unshared stage over the beam's L decode tokens
+    // unshared stage over the beam's L decode tokens, kTok tokens per round
     float m = -INFINITY, l = 0.f, o[PL];
 #pragma unroll
     for (int i = 0; i < PL; ++i) o[i] = 0.f;
-    for (int t = 0; t < L; ++t) {
-      int slot = __shfl_sync(0xffffffffu, my_slot, t & 31);
-      if (t >= 32) {   // rows longer than a warp: read the entry directly
-        slot = a.slot_table[((size_t)r * a.W + j) * a.T + t];
-        if (slot < 0 || slot >= TW) {
-          if (lane == 0) set_status(hdr, BEAMDEC_ERR_DEVICE_CHECK);
-          slot = -1;
+    for (int t0 = 0; t0 < L; t0 += kTok) {
+      int slot[kTok];
+      float k[kTok][PL], v[kTok][PL];
+#pragma unroll
+      for (int u = 0; u < kTok; ++u) {
+        const int t = t0 + u;
+        int sl = __shfl_sync(0xffffffffu, my_slot, t & 31);
+        if (t >= L) sl = -1;
+        else if (t >= 32) {   // rows longer than a warp: read the entry directly
+          sl = a.slot_table[((size_t)r * a.W + j) * a.T + t];
+          if (sl < 0 || sl >= TW) {
+            if (lane == 0) set_status(hdr, BEAMDEC_ERR_DEVICE_CHECK);
+            sl = -1;
+          }
+        }
+        slot[u] = sl;
+        if (sl >= 0) {
+          const size_t e = (((size_t)r * TW + sl) * a.Hkv + g) * D + lane * PL;
+          load_lane<DKV, PL>(a.unshared_k, e, k[u]);
+          load_lane<DKV, PL>(a.unshared_v, e, v[u]);
         }
       }
-      if (slot < 0) continue;
-      const size_t e = (((size_t)r * TW + slot) * a.Hkv + g) * D + lane * PL;
-      float k[PL], v[PL];
-      load_lane<DKV, PL>(a.unshared_k, e, k);
-      load_lane<DKV, PL>(a.unshared_v, e, v);
-      float sdot = 0.f;
 #pragma unroll
-      for (int i = 0; i < PL; ++i) sdot = fmaf(q[i], k[i], sdot);
-      sdot = warp_sum(sdot);
-      const float mn = fmaxf(m, sdot);
-      const float alpha = ex2(m - mn), pt = ex2(sdot - mn);
-      l = l * alpha + pt;
+      for (int u = 0; u < kTok; ++u) {
+        if (slot[u] < 0) continue;
+        float sdot = 0.f;
 #pragma unroll
-      for (int i = 0; i < PL; ++i) o[i] = fmaf(pt, v[i], o[i] * alpha);
-      m = mn;
+        for (int i = 0; i < PL; ++i) sdot = fmaf(q[i], k[u][i], sdot);
+        sdot = warp_sum(sdot);
+        const float mn = fmaxf(m, sdot);
+        const float alpha = ex2(m - mn), pt = ex2(sdot - mn);
+        l = l * alpha + pt;
+#pragma unroll
+        for (int i = 0; i < PL; ++i) o[i] = fmaf(pt, v[u][i], o[i] * alpha);
+        m = mn;
+      }
     }
     // merge with the shared-stage partials of every prompt split
-    const int row = j * G + gi;
     float M = m;
-    for (int c = 0; c < n_split; ++c)
-      M = fmaxf(M, part.m[(((size_t)c * a.R + r) * a.Hkv + g) * rows + row]);
-    float Lsum = (l == 0.f) ? 0.f : l * ex2(m - M);
-    float O[PL];
+    for (int c = 0; c < n_split; ++c) {
+      const float mc = c < 32 ? __shfl_sync(0xffffffffu, pm_l, c)
+                              : part.m[(((size_t)c * a.R + r) * a.Hkv + g) * rows + row];
+      M = fmaxf(M, mc);
+    }
     const float wu = (l == 0.f) ? 0.f : ex2(m - M);
+    float Lsum = l * wu;
+    float O[PL];
 #pragma unroll
     for (int i = 0; i < PL; ++i) O[i] = o[i] * wu;
     for (int c = 0; c < n_split; ++c) {
       const size_t pi = (((size_t)c * a.R + r) * a.Hkv + g) * rows + row;
-      const float lc = part.l[pi];
+      const float mc = c < 32 ? __shfl_sync(0xffffffffu, pm_l, c) : part.m[pi];
+      const float lc = c < 32 ? __shfl_sync(0xffffffffu, pl_l, c) : part.l[pi];
       if (lc == 0.f) continue;
-      const float w = ex2(part.m[pi] - M);
+      const float w = ex2(mc - M);
       Lsum = fmaf(lc, w, Lsum);
-      const float* oc = part.o + pi * D + lane * PL;
+      if (c < kPre) {
 #pragma unroll
-      for (int i = 0; i < PL; ++i) O[i] = fmaf(oc[i], w, O[i]);
+        for (int cc = 0; cc < kPre; ++cc)
+          if (cc == c) {
+#pragma unroll
+            for (int i = 0; i < PL; ++i) O[i] = fmaf(oc[cc][i], w, O[i]);
+          }
+      } else {
+        const float* src = part.o + pi * D + lane * PL;
+#pragma unroll
+        for (int i = 0; i < PL; ++i) O[i] = fmaf(src[i], w, O[i]);
+      }
     }
     const float inv = vs / Lsum;
     if constexpr (PL == 4) {

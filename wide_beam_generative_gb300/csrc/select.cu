@@ -7,13 +7,18 @@
 // become candidates, sorting stops early; §6: cache selection follows the
 // reorder.  FlashRec (SGLang PR 31626 thread): fused SID trie in CSR form.
 //
-// Two launches per step:
+// One or two launches per step:
 //   bd_expand_kernel   one block per (beam, request): streams the beam's logits
 //                      row once to get its log-sum-exp, scores the trie
 //                      children (or the whole vocabulary), keeps the row's
 //                      top_k by a block radix select and appends them to the
-//                      request's pool as 64-bit keys.
-//   bd_global_kernel   cooperative grid: per request, radix select of the
+//                      request's pool as 64-bit keys.  When a request's pool
+//                      is at most 1M keys (W <= 4096), the last of its blocks
+//                      to finish then selects the request's top-W itself
+//                      (radix narrowing, shared-memory sort, outputs), so the
+//                      selection tail of one request overlaps the streaming
+//                      of the others and no second launch is needed.
+//   bd_global_kernel   larger pools: cooperative grid; per request, radix select of the
 //                      beam_width smallest pool keys (12-bit digits, block-
 //                      private histograms merged in global memory), a bitonic
 //                      sort of the survivors in shared memory, then the outputs
@@ -33,6 +38,7 @@ constexpr int kExpandThreads = 512;
 constexpr int kGlobalThreads = 512;
 constexpr int kDigitBits = 12;
 constexpr int kBins = 1 << kDigitBits;  // 4096
+constexpr int kTailCap = 4096;          // keys one expand block can select in shared memory
 
 struct SelState {
   unsigned long long prefix;  // resolved high bits of the threshold key
@@ -43,7 +49,8 @@ struct SelState {
   int32_t shift;              // bits below the resolved prefix (64 = none resolved)
   int32_t done;
   int32_t ncand;
-  int32_t pad[7];
+  int32_t tickets;            // expand blocks of the request that have finished
+  int32_t pad[6];
 };
 static_assert(sizeof(SelState) == 64, "state size");
 
@@ -127,16 +134,12 @@ struct ExpandShared {
   float lse;
 };
 
-__global__ void __launch_bounds__(kExpandThreads)
-bd_expand_kernel(SelectArgs a) {
-  __shared__ ExpandShared sh;
-  const int b = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
+// Rows a1-a3 for beam b of request r: log-sum-exp, trie children, per-beam
+// top_k appended to the request's pool.
+__device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
+                                               int r, int b) {
+  const int tid = threadIdx.x;
   const int Kp = a.Kp;
-  SelWs ws = carve(a.ws, a.R, a.W, Kp);
-  if (b == 0 && r == 0 && tid == 0) ws.hdr->bar_count = 0u;
-  const int nl = a.n_live_in[r];
-  if (b >= nl) return;
-
   const size_t rowi = (size_t)r * a.W + b;
   const float* row = a.logits + rowi * (size_t)a.row_stride;
 
@@ -239,6 +242,7 @@ bd_expand_kernel(SelectArgs a) {
 
   SelState* st = ws.state + r;
   unsigned long long* pool = ws.pool + (size_t)r * a.W * Kp;
+  (void)Kp;
 
   // ---- a3: per-beam top_k -------------------------------------------------
   if (n <= a.K) {
@@ -297,15 +301,22 @@ bd_expand_kernel(SelectArgs a) {
   }
 }
 
-// ---------------------------------------------------------------------------
-struct GlobalSmem {
-  uint32_t hist[kBins];
-  int warp_cnt[32];
-  uint32_t digit, below;
-  int all_done;
-};
-
-constexpr size_t kGlobalKeysOffset = (sizeof(GlobalSmem) + 15) & ~(size_t)15;
+// Ascending bitonic sort of np (a power of two) 64-bit keys in shared memory.
+__device__ void bitonic_sort(unsigned long long* keys, int np) {
+  for (int k = 2; k <= np; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < np; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long x = keys[i], y = keys[ixj];
+          const bool up = (i & k) == 0;
+          if ((x > y) == up) { keys[i] = y; keys[ixj] = x; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
 
 __device__ __forceinline__ int find_child_edge(const TrieLevel& L, int node, int code) {
   int lo = L.off[node], hi = L.off[node + 1];
@@ -315,6 +326,187 @@ __device__ __forceinline__ int find_child_edge(const TrieLevel& L, int node, int
   }
   return (lo < L.off[node + 1] && L.code[lo] == code) ? lo : -1;
 }
+
+// a4/a5 outputs of request r from its nt winners, sorted ascending in keys[]:
+// tokens, parents, scores, child nodes, live count and the slot rows
+// (parent's row up to step-1, then step*W + j).
+__device__ void emit_outputs(const SelectArgs& a, const SelWs& ws, int r,
+                             const unsigned long long* keys, int nt) {
+  const int tid = threadIdx.x;
+  const size_t o = (size_t)r * a.W;
+  for (int j = tid; j < a.W; j += blockDim.x) {
+    if (j < nt) {
+      const unsigned long long k = keys[j];
+      const int parent = pool_key_beam(k), tok = pool_key_tok(k);
+      a.tokens[o + j] = tok;
+      a.parents[o + j] = parent;
+      a.cum_out[o + j] = desc_key_value((uint32_t)(k >> 32));
+      int node = -1;
+      if (a.has_trie) {
+        node = find_child_edge(a.lvl, a.node_in[o + parent], tok - a.lvl.token_base);
+        if (node < 0) set_status(ws.hdr, BEAMDEC_ERR_DEVICE_CHECK);
+      }
+      a.node_out[o + j] = node;
+    } else {
+      a.tokens[o + j] = -1;
+      a.parents[o + j] = -1;
+      a.cum_out[o + j] = -INFINITY;
+      a.node_out[o + j] = -1;
+    }
+  }
+  const int T = a.T;
+  for (int idx = tid; idx < a.W * T; idx += blockDim.x) {
+    const int j = idx / T, t = idx - j * T;
+    int v = -1;
+    if (j < nt) {
+      if (t < a.step) v = a.slot_in[(o + pool_key_beam(keys[j])) * T + t];
+      else if (t == a.step) v = a.step * a.W + j;
+    }
+    a.slot_out[(o + j) * T + t] = v;
+  }
+  if (tid == 0) a.n_live_out[r] = nt;
+}
+
+// One radix-narrowing pass over `n` keys (shared or global memory): among the
+// keys whose bits above `shift` equal `prefix`, histogram the next `w` bits
+// and pick the digit holding the need-th smallest key.  Updates prefix,
+// shift, need and sure (keys strictly below the new prefix); returns the
+// count of keys inside the chosen digit.
+template <bool kGlobal>
+__device__ uint32_t narrow_pass(const unsigned long long* keys, int n, unsigned long long& prefix,
+                                int& shift, uint32_t& need, uint32_t& sure, ExpandShared& sh) {
+  const int w = shift < 11 ? shift : 11;
+  const int nshift = shift - w;
+  const uint32_t mask = (1u << w) - 1u;
+  const int nb = (1 << w) < 32 ? 32 : (1 << w);
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) sh.hist[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const unsigned long long k = kGlobal ? __ldcg(keys + i) : keys[i];
+    if (shift == 64 || (k >> shift) == prefix) atomicAdd(&sh.hist[(uint32_t)(k >> nshift) & mask], 1u);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) warp_find_digit(sh.hist, nb, need, &sh.digit, &sh.below);
+  __syncthreads();
+  const uint32_t D = sh.digit, below = sh.below, in_bin = sh.hist[D];
+  __syncthreads();
+  sure += below;
+  need -= below;
+  prefix = (shift == 64 ? 0ull : (prefix << w)) | D;
+  shift = nshift;
+  return in_bin;
+}
+
+// Fused a4 for one request, run by the last expand block of the request:
+// select the min(W, pool) smallest pool keys, sort them, emit outputs.
+__device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs& ws, int r,
+                             unsigned long long* keys) {
+  const volatile SelState* st = ws.state + r;
+  const int total = st->total;
+  const int nt = total < a.W ? total : a.W;
+  const unsigned long long* pool = ws.pool + (size_t)r * a.W * a.Kp;
+  int nc;
+  if (total <= kTailCap) {
+    for (int i = threadIdx.x; i < total; i += blockDim.x) keys[i] = __ldcg(pool + i);
+    nc = total;
+  } else {
+    unsigned long long prefix = 0;
+    int shift = 64;
+    uint32_t need = (uint32_t)nt, sure = 0, in_bin = 0;
+    while (true) {
+      in_bin = narrow_pass<true>(pool, total, prefix, shift, need, sure, sh);
+      if (sure + in_bin <= (uint32_t)kTailCap || shift == 0) break;
+    }
+    if (threadIdx.x == 0) sh.count = 0;
+    __syncthreads();
+    for (int c0 = 0; c0 < total; c0 += blockDim.x) {
+      const int i = c0 + threadIdx.x;
+      unsigned long long k = 0;
+      int flag = 0;
+      if (i < total) {
+        k = __ldcg(pool + i);
+        flag = (k >> shift) <= prefix;
+      }
+      int tot;
+      const int rk = block_rank(flag, sh.warp_cnt, &tot);
+      const int pos = sh.count + rk;
+      if (flag && pos < kTailCap) keys[pos] = k;
+      __syncthreads();
+      if (threadIdx.x == 0) sh.count += tot;
+      __syncthreads();
+    }
+    nc = sh.count < kTailCap ? sh.count : kTailCap;
+  }
+  __syncthreads();
+  if (nc > nt) {   // exact threshold: narrow until the keys at or below it number nt
+    unsigned long long prefix = 0;
+    int shift = 64;
+    uint32_t need = (uint32_t)nt, sure = 0;
+    while (true) {
+      const uint32_t in_bin = narrow_pass<false>(keys, nc, prefix, shift, need, sure, sh);
+      if (sure + in_bin == (uint32_t)nt || shift == 0) break;
+    }
+    // in-place compaction of the winners to keys[0..nt)
+    if (threadIdx.x == 0) sh.count = 0;
+    __syncthreads();
+    for (int c0 = 0; c0 < nc; c0 += blockDim.x) {
+      const int i = c0 + threadIdx.x;
+      unsigned long long k = 0;
+      int flag = 0;
+      if (i < nc) {
+        k = keys[i];
+        flag = (k >> shift) <= prefix;
+      }
+      int tot;
+      const int rk = block_rank(flag, sh.warp_cnt, &tot);   // all reads of the chunk precede writes
+      if (flag) keys[sh.count + rk] = k;
+      __syncthreads();
+      if (threadIdx.x == 0) sh.count += tot;
+      __syncthreads();
+    }
+  }
+  int np = 32;
+  while (np < nt) np <<= 1;
+  for (int i = nt + threadIdx.x; i < np; i += blockDim.x) keys[i] = ~0ull;
+  __syncthreads();
+  bitonic_sort(keys, np);
+  emit_outputs(a, ws, r, keys, nt);
+}
+
+template <bool kFused>
+__global__ void __launch_bounds__(kExpandThreads)
+bd_expand_kernel(SelectArgs a) {
+  __shared__ ExpandShared sh;
+  extern __shared__ __align__(16) unsigned char tail_smem[];
+  const int b = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
+  SelWs ws = carve(a.ws, a.R, a.W, a.Kp);
+  if (b == 0 && r == 0 && tid == 0) ws.hdr->bar_count = 0u;
+  const int nl = a.n_live_in[r];
+  if (b >= nl) return;
+  expand_candidates(a, sh, ws, r, b);
+  if constexpr (kFused) {
+    // the last block of the request to finish runs the request's global top-W
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      sh.count = atomicAdd(&ws.state[r].tickets, 1);
+    }
+    __syncthreads();
+    if (sh.count != nl - 1) return;
+    __threadfence();
+    request_tail(a, sh, ws, r, reinterpret_cast<unsigned long long*>(tail_smem));
+  }
+}
+
+// ---------------------------------------------------------------------------
+struct GlobalSmem {
+  uint32_t hist[kBins];
+  int warp_cnt[32];
+  uint32_t digit, below;
+  int all_done;
+};
+
+constexpr size_t kGlobalKeysOffset = (sizeof(GlobalSmem) + 15) & ~(size_t)15;
 
 __global__ void __launch_bounds__(kGlobalThreads)
 bd_global_kernel(SelectArgs a) {
@@ -436,56 +628,13 @@ bd_global_kernel(SelectArgs a) {
     const volatile SelState* st = ws.state + r;
     const int nc = min((int)st->ncand, kSelectCap);
     const int nt = st->n_target;
+    const unsigned long long* cand = ws.cand + (size_t)r * kSelectCap;
     int np = 32;
     while (np < nc) np <<= 1;
-    const unsigned long long* cand = ws.cand + (size_t)r * kSelectCap;
     for (int i = tid; i < np; i += kGlobalThreads) keys[i] = i < nc ? __ldcg(cand + i) : ~0ull;
     __syncthreads();
-    for (int k = 2; k <= np; k <<= 1) {
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int i = tid; i < np; i += kGlobalThreads) {
-          const int ixj = i ^ j;
-          if (ixj > i) {
-            const unsigned long long x = keys[i], y = keys[ixj];
-            const bool up = (i & k) == 0;
-            if ((x > y) == up) { keys[i] = y; keys[ixj] = x; }
-          }
-        }
-        __syncthreads();
-      }
-    }
-    const size_t o = (size_t)r * a.W;
-    for (int j = tid; j < a.W; j += kGlobalThreads) {
-      if (j < nt) {
-        const unsigned long long k = keys[j];
-        const int parent = pool_key_beam(k), tok = pool_key_tok(k);
-        a.tokens[o + j] = tok;
-        a.parents[o + j] = parent;
-        a.cum_out[o + j] = desc_key_value((uint32_t)(k >> 32));
-        int node = -1;
-        if (a.has_trie) {
-          node = find_child_edge(a.lvl, a.node_in[o + parent], tok - a.lvl.token_base);
-          if (node < 0) set_status(ws.hdr, BEAMDEC_ERR_DEVICE_CHECK);
-        }
-        a.node_out[o + j] = node;
-      } else {
-        a.tokens[o + j] = -1;
-        a.parents[o + j] = -1;
-        a.cum_out[o + j] = -INFINITY;
-        a.node_out[o + j] = -1;
-      }
-    }
-    const int T = a.T;
-    for (int idx = tid; idx < a.W * T; idx += kGlobalThreads) {
-      const int j = idx / T, t = idx - j * T;
-      int v = -1;
-      if (j < nt) {
-        if (t < a.step) v = a.slot_in[(o + pool_key_beam(keys[j])) * T + t];
-        else if (t == a.step) v = a.step * a.W + j;
-      }
-      a.slot_out[(o + j) * T + t] = v;
-    }
-    if (tid == 0) a.n_live_out[r] = nt;
+    bitonic_sort(keys, np);
+    emit_outputs(a, ws, r, keys, nt);
     __syncthreads();
   }
 }
@@ -525,10 +674,17 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
   if (cudaMemsetAsync(ws.state, 0, zero_bytes, stream) != cudaSuccess) return BEAMDEC_ERR_CUDA;
 
   dim3 g1(a.W, a.R);
+  // Pools of at most 1M keys per request (W <= 4096) are selected by the last
+  // expand block of each request; larger ones by the cooperative grid kernel.
+  const bool fused = a.W <= kTailCap && (long long)a.W * a.Kp <= (1ll << 20);
   prof_begin(kKExpand, stream);
-  bd_expand_kernel<<<g1, kExpandThreads, 0, stream>>>(a);
+  if (fused)
+    bd_expand_kernel<true><<<g1, kExpandThreads, kTailCap * sizeof(unsigned long long), stream>>>(a);
+  else
+    bd_expand_kernel<false><<<g1, kExpandThreads, 0, stream>>>(a);
   prof_end(kKExpand, stream);
   if (cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
+  if (fused) return BEAMDEC_OK;
 
   const long long pool_max = (long long)a.R * a.W * a.Kp;
   long long want = (pool_max + 4095) / 4096;
