@@ -23,27 +23,33 @@ static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 AttnPlan attn_plan(int R, int W, int Hq, int Hkv, int d, int max_prompt_len, int q_dtype,
                    int kv_dtype) {
+  // The plan depends on shapes only (never on the device), so the workspace
+  // size query and the call always agree.
   AttnPlan p;
   const int G = Hq / Hkv;
   p.tensor_core = attn_tc_supported(q_dtype, kv_dtype, d, G);
   const int rows = W * G;
-  const int tile_rows = p.tensor_core ? 128 : 32;
+  const int tile_rows = p.tensor_core ? 256 : 32;
   const long long units = (long long)R * Hkv * ((rows + tile_rows - 1) / tile_rows);
-  const int sms = 148;   // planning constant; the split count only shapes the work
-  int n_split = 1;
-  if (max_prompt_len > 0) {
-    long long want = (2ll * sms + units - 1) / units;
-    const int max_split = (max_prompt_len + 255) / 256;
-    if (want > max_split) want = max_split;
-    if (want < 1) want = 1;
-    n_split = (int)want;
+  const long long sms = 152;   // GB300 SM count, a planning constant
+  const int chunk = 128;
+  const int chunks = max_prompt_len > 0 ? (max_prompt_len + chunk - 1) / chunk : 1;
+  // split count from a small time model (microseconds): each wave of CTAs
+  // costs its chunks (about 1.1 us per 128 keys for a 256-row tile on the
+  // tensor cores) plus a 2 us prologue, and every split's partial triples are
+  // read back by the merge at about 6 TB/s.
+  const double chunk_us = p.tensor_core ? 1.1 : 4.0;
+  const double part_us = (double)R * Hkv * rows * (d + 2) * 4 / 6.0e6;
+  int best = 1;
+  double best_cost = 1e30;
+  for (int s = 1; s <= 16 && s <= chunks; ++s) {
+    const long long waves = (units * s + sms - 1) / sms;
+    const long long per = (chunks + s - 1) / s;
+    const double cost = (double)waves * (per * chunk_us + 2.0) + s * part_us;
+    if (cost < best_cost - 1e-9) { best_cost = cost; best = s; }
   }
-  int split_len = max_prompt_len > 0 ? (max_prompt_len + n_split - 1) / n_split : 128;
-  split_len = ((split_len + 127) / 128) * 128;
-  p.split_len = split_len;
-  p.n_split = max_prompt_len > 0 ? (max_prompt_len + split_len - 1) / split_len : 1;
-  (void)q_dtype;
-  (void)kv_dtype;
+  p.split_len = ((chunks + best - 1) / best) * chunk;
+  p.n_split = max_prompt_len > 0 ? (max_prompt_len + p.split_len - 1) / p.split_len : 1;
   (void)d;
   return p;
 }

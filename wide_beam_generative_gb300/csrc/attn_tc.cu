@@ -8,20 +8,28 @@
 // output is the partial (max, sum, unnormalised output) of every query row,
 // merged later with the unshared stage.
 //
-// One CTA owns 128 query rows of one (request, kv head, prompt split):
-//   warp 0      TMA producer: Q once, then K and V tiles of 128 keys
-//               (two 64-column SWIZZLE_128B boxes each) into a 2-stage ring;
-//   warp 1      allocates TMEM and issues the MMAs from one thread:
-//               S = Q K^T (M 128, N 128, K 128) into a double-buffered TMEM
-//               score tile, and O_c = P V (M 128, N 128, K 128; V read
-//               d-major) into a double-buffered TMEM output tile;
-//   warps 4-7   softmax: thread t owns query row t (TMEM lane t); reads its
-//               scores from TMEM, keeps the running max / sum in log2 units,
-//               writes P as bf16 into shared memory in the 128B-swizzled
-//               K-major layout the MMA reads, and folds each chunk's output
-//               O_c into a register accumulator one chunk behind the MMAs.
-// Every wait on an mbarrier is bounded; a timeout records
-// BEAMDEC_ERR_TIMEOUT, stops the loops and still frees TMEM.
+// One CTA owns 256 query rows (two 128-row tiles) of one (request, kv head,
+// prompt split), so every K/V tile it loads feeds two tiles of MMAs:
+//   warp 0       TMA producer: Q once, then K and V tiles of 128 keys (two
+//                64-column SWIZZLE_128B boxes each) through a 3-slot ring;
+//   warp 1       allocates TMEM and issues every MMA from one thread, in the
+//                order S0(c) S1(c) | PV0(c) S0(c+1) | PV1(c) S1(c+1) | ... so
+//                the tensor core works on one tile while the other tile's
+//                softmax runs;
+//   warps 4-7    softmax of tile 0, warps 8-11 softmax of tile 1: thread t
+//                owns row t (TMEM lane t); reads its 128 scores from TMEM
+//                twice (row max, then P), keeps max/sum in log2 units, writes
+//                P (bf16) into shared memory in the 128B-swizzled K-major
+//                layout the MMA reads.
+// The output O accumulates in TMEM across chunks (S0 O0 S1 O1, 128 columns
+// each).  The running max used for P only moves when a chunk's max exceeds
+// it by more than 2^8; then the warp rescales its O rows in TMEM before the
+// next PV.  That keeps P <= 2^8 and leaves the result exact.  The commit that
+// signals S_t(c+1) also covers PV_t(c) (a commit tracks every earlier MMA of
+// the issuing thread), so the softmax of chunk c+1 may overwrite P_t and
+// touch O_t once it has seen S_t(c+1).
+// Every mbarrier wait is bounded; a timeout records BEAMDEC_ERR_TIMEOUT, ends
+// the loops and still frees TMEM.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -36,19 +44,20 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 256;
-constexpr uint32_t kHalfBytes = 16384;          // 128 rows x 128 B
-constexpr uint32_t kTileBytes = 2 * kHalfBytes; // 128 x 128 bf16
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kTileBytes;                 // 2 stages
-constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;     // 2 stages
-constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;
-constexpr uint32_t kSmemBytes = kOffP + kTileBytes + 1024;  // + alignment slack
-constexpr uint32_t kTmemCols = 512;  // S0 S1 O0 O1, 128 columns each
+constexpr int kThreads = 384;
+constexpr uint32_t kHalfBytes = 16384;           // 128 rows x 128 B
+constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 128 x 128 bf16
+constexpr int kSlots = 3;                        // K/V ring
+constexpr uint32_t kOffQ = 0;                    // Q0, Q1
+constexpr uint32_t kOffKV = 2 * kTileBytes;      // kSlots tiles
+constexpr uint32_t kOffP = kOffKV + kSlots * kTileBytes;  // P0, P1
+constexpr uint32_t kSmemBytes = kOffP + 2 * kTileBytes + 1024;
+constexpr uint32_t kTmemCols = 512;              // S0 O0 S1 O1
+constexpr float kRescale = 8.f;                  // log2 headroom before O is rescaled
 
 // MN-major B operand (V, d contiguous): the leading byte offset is the stride
-// between 64-column swizzle atoms along d (the two 16 KB halves), the stride
-// byte offset the stride between groups of 8 keys (8 x 128 B).
+// between the two 64-column swizzle atoms along d (the two 16 KB halves), the
+// stride byte offset the stride between groups of 8 keys (8 x 128 B).
 constexpr uint32_t kVLbo = kHalfBytes;
 constexpr uint32_t kVSbo = 1024;
 
@@ -57,7 +66,6 @@ struct TcParams {
   float scale_log2;   // sm_scale * log2(e)
   const int32_t* prompt_offsets;
   const int32_t* n_live;
-  const float* k_scale;   // fp8 only (nullptr otherwise)
   float* pm;
   float* pl;
   float* po;
@@ -66,13 +74,13 @@ struct TcParams {
 
 struct Bars {
   uint64_t q;
-  uint64_t full_k[2], empty_k[2], full_v[2], empty_v[2];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, pv_done;
+  uint64_t kv_full[kSlots], kv_empty[kSlots];
+  uint64_t s_full[2], s_free[2], p_full[2];
+  uint64_t done;
 };
 
-// One lane polls (bounded), the warp agrees on the outcome, then every lane
-// observes the completed phase itself (acquire) before touching the data.
+// One lane polls (bounded), the warp agrees, then every lane observes the
+// completed phase itself before touching the data it guards.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   bool ok = false;
   if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity);
@@ -85,10 +93,25 @@ __device__ __forceinline__ bool warp_flag(volatile int* f) {
   return __shfl_sync(0xffffffffu, *f, 0) != 0;
 }
 
-__device__ __forceinline__ void write_empty_partials(const TcParams& p, size_t base, int row0, int nrows) {
-  for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+      "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+      "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
+      "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
+      "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void write_empty_partials(const TcParams& p, size_t base, int row0) {
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
     const int row = row0 + i;
-    if (row >= nrows) continue;
+    if (row >= p.rows) continue;
     p.pm[base + row] = -INFINITY;
     p.pl[base + row] = 0.f;
     float4* o = reinterpret_cast<float4*>(p.po + (base + row) * 128);
@@ -101,8 +124,8 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                          const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, TcParams p) {
   extern __shared__ __align__(1024) unsigned char dsm_raw[];
-  unsigned char* sm =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
   __shared__ Bars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
@@ -111,17 +134,16 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   const int g = blockIdx.y % p.Hkv;
   const int sp = blockIdx.y / p.Hkv;
   const int r = blockIdx.z;
-  const int row0 = mt * 128;
+  const int row0 = mt * 256;
   const int G = p.G;
-  if (row0 >= p.n_live[r] * G) return;   // every row of the tile is a dead beam
+  if (row0 >= p.n_live[r] * G) return;   // every row of the CTA is a dead beam
   const int pbase = p.prompt_offsets[r];
   const int P = p.prompt_offsets[r + 1] - pbase;
   const int k0 = sp * p.split_len;
   const int k1 = min(P, k0 + p.split_len);
-  const size_t pbase_rows = ((size_t)sp * p.R + r) * p.Hkv + g;
-  const size_t prow_base = pbase_rows * p.rows;
+  const size_t prow_base = (((size_t)sp * p.R + r) * p.Hkv + g) * p.rows;
   if (k1 <= k0) {   // this split holds no key of the request
-    write_empty_partials(p, prow_base, row0, p.rows);
+    write_empty_partials(p, prow_base, row0);
     return;
   }
   const int nchunks = (k1 - k0 + 127) / 128;
@@ -130,16 +152,16 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   if (threadIdx.x == 0) {
     abort_sh = 0;
     mbar_init(&bars.q, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars.full_k[s], 1);
-      mbar_init(&bars.empty_k[s], 1);
-      mbar_init(&bars.full_v[s], 1);
-      mbar_init(&bars.empty_v[s], 1);
-      mbar_init(&bars.s_full[s], 1);
-      mbar_init(&bars.s_free[s], 128);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
     }
-    mbar_init(&bars.p_full, 128);
-    mbar_init(&bars.pv_done, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars.s_full[t], 1);
+      mbar_init(&bars.s_free[t], 128);
+      mbar_init(&bars.p_full[t], 128);
+    }
+    mbar_init(&bars.done, 1);
     mbar_fence_init();
   }
   if (warp == 1) tmem_alloc(&tmem_base_sh, kTmemCols);
@@ -153,176 +175,192 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     prefetch_tmap(&qmap);
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
-    const int j0 = row0 / G;
-    mbar_expect_tx(&bars.q, kTileBytes);
+    const int j0 = row0 / G, jt = 128 / G;
+    mbar_expect_tx(&bars.q, 2 * kTileBytes);
     tma_load_4d(sm + kOffQ, &qmap, &bars.q, 0, g * G, j0, r);
     tma_load_4d(sm + kOffQ + kHalfBytes, &qmap, &bars.q, 64, g * G, j0, r);
+    tma_load_4d(sm + kOffQ + kTileBytes, &qmap, &bars.q, 0, g * G, j0 + jt, r);
+    tma_load_4d(sm + kOffQ + kTileBytes + kHalfBytes, &qmap, &bars.q, 64, g * G, j0 + jt, r);
     int issued = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      const int s = c & 1;
-      const uint32_t ph = (c >> 1) & 1;
-      const int key = pbase + k0 + c * 128;
-      if (!mbar_wait(&bars.empty_k[s], ph ^ 1)) { abort_sh = 1; break; }
-      mbar_expect_tx(&bars.full_k[s], kTileBytes);
-      tma_load_3d(sm + kOffK + s * kTileBytes, &kmap, &bars.full_k[s], 0, g, key);
-      tma_load_3d(sm + kOffK + s * kTileBytes + kHalfBytes, &kmap, &bars.full_k[s], 64, g, key);
-      if (!mbar_wait(&bars.empty_v[s], ph ^ 1)) { abort_sh = 1; issued = c * 2 + 1; break; }
-      mbar_expect_tx(&bars.full_v[s], kTileBytes);
-      tma_load_3d(sm + kOffV + s * kTileBytes, &vmap, &bars.full_v[s], 0, g, key);
-      tma_load_3d(sm + kOffV + s * kTileBytes + kHalfBytes, &vmap, &bars.full_v[s], 64, g, key);
-      issued = c * 2 + 2;
+    for (int i = 0; i < 2 * nchunks; ++i) {   // K0 V0 K1 V1 ...
+      const int s = i % kSlots;
+      const uint32_t u = (uint32_t)(i / kSlots);
+      if (!mbar_wait(&bars.kv_empty[s], (u & 1) ^ 1)) { abort_sh = 1; break; }
+      const int key = pbase + k0 + (i >> 1) * 128;
+      const CUtensorMap* map = (i & 1) ? &vmap : &kmap;
+      unsigned char* dst = sm + kOffKV + s * kTileBytes;
+      mbar_expect_tx(&bars.kv_full[s], kTileBytes);
+      tma_load_3d(dst, map, &bars.kv_full[s], 0, g, key);
+      tma_load_3d(dst + kHalfBytes, map, &bars.kv_full[s], 64, g, key);
+      issued = i + 1;
       if (abort_sh) break;
     }
-    if (abort_sh) {
-      // let every copy this thread started land before the CTA exits
+    if (abort_sh) {   // let every copy this thread started land before exiting
       mbar_wait(&bars.q, 0);
-      for (int u = 0; u < issued; ++u) {
-        const int c = u >> 1, s = c & 1;
-        mbar_wait((u & 1) ? &bars.full_v[s] : &bars.full_k[s], (c >> 1) & 1);
-      }
+      for (int i = (issued > kSlots ? issued - kSlots : 0); i < issued; ++i)
+        mbar_wait(&bars.kv_full[i % kSlots], (uint32_t)(i / kSlots) & 1);
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
     const uint32_t idO = idesc_bf16_f32(128, 128, false, true);
     const uint32_t qa = smem_u32(sm + kOffQ);
-    bool ok = mbar_wait(&bars.q, 0);
-    auto issue_s = [&](int c) -> bool {
-      const int s = c & 1;
-      if (!mbar_wait(&bars.full_k[s], (c >> 1) & 1)) return false;
-      if (!mbar_wait(&bars.s_free[s], ((c >> 1) & 1) ^ 1)) return false;
-      fence_after_sync();
-      const uint32_t kb = smem_u32(sm + kOffK + s * kTileBytes);
+    const uint32_t pa = smem_u32(sm + kOffP);
+    const uint32_t kvb = smem_u32(sm + kOffKV);
+    auto wait_kv = [&](int i) -> bool {
+      return mbar_wait(&bars.kv_full[i % kSlots], (uint32_t)(i / kSlots) & 1);
+    };
+    auto issue_s = [&](int t, int c) {   // S_t = Q_t K(c)^T
+      const uint32_t kb = kvb + ((2 * c) % kSlots) * kTileBytes;
+      const uint32_t qt = qa + t * kTileBytes;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-        mma_bf16(tmem + s * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idS,
-                 k > 0);
+        mma_bf16(tmem + t * 256, sdesc_sw128(qt + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                 idS, k > 0);
       }
-      mma_commit(&bars.empty_k[s]);
-      mma_commit(&bars.s_full[s]);
-      return true;
+      mma_commit(&bars.s_full[t]);
     };
-    if (ok) ok = issue_s(0);
-    for (int c = 0; ok && c < nchunks; ++c) {
-      if (c + 1 < nchunks && !issue_s(c + 1)) { ok = false; break; }
-      const int s = c & 1;
-      if (!mbar_wait(&bars.p_full, c & 1)) { ok = false; break; }
-      if (!mbar_wait(&bars.full_v[s], (c >> 1) & 1)) { ok = false; break; }
-      fence_after_sync();
-      const uint32_t pa = smem_u32(sm + kOffP);
-      const uint32_t vb = smem_u32(sm + kOffV + s * kTileBytes);
+    auto issue_pv = [&](int t, int c) {   // O_t += P_t V(c)
+      const uint32_t vb = kvb + ((2 * c + 1) % kSlots) * kTileBytes;
+      const uint32_t pt = pa + t * kTileBytes;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const uint64_t a = sdesc_sw128(pa + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
-        const uint32_t vk = vb + k * 16 * 128;   // 16 keys per step
-        mma_bf16(tmem + 256 + s * 128, a, sdesc_sw128(vk, kVLbo, kVSbo), idO, k > 0);
+        const uint64_t a = sdesc_sw128(pt + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
+        mma_bf16(tmem + t * 256 + 128, a, sdesc_sw128(vb + k * 16 * 128, kVLbo, kVSbo), idO,
+                 (c > 0 || k > 0) ? 1u : 0u);
       }
-      mma_commit(&bars.empty_v[s]);
-      mma_commit(&bars.pv_done);
+    };
+    bool ok = mbar_wait(&bars.q, 0) && wait_kv(0);
+    if (ok) {
+      fence_after_sync();
+      issue_s(0, 0);
+      issue_s(1, 0);
+      mma_commit(&bars.kv_empty[0]);
+    }
+    for (int c = 0; ok && c < nchunks; ++c) {
+      const bool more = c + 1 < nchunks;
+      if (!wait_kv(2 * c + 1)) { ok = false; break; }                 // V(c)
+      if (!mbar_wait(&bars.p_full[0], c & 1)) { ok = false; break; }
+      fence_after_sync();
+      issue_pv(0, c);
+      if (more) {
+        if (!wait_kv(2 * c + 2)) { ok = false; break; }               // K(c+1)
+        if (!mbar_wait(&bars.s_free[0], c & 1)) { ok = false; break; }
+        fence_after_sync();
+        issue_s(0, c + 1);
+      }
+      if (!mbar_wait(&bars.p_full[1], c & 1)) { ok = false; break; }
+      fence_after_sync();
+      issue_pv(1, c);
+      mma_commit(&bars.kv_empty[(2 * c + 1) % kSlots]);               // V(c) consumed
+      if (more) {
+        if (!mbar_wait(&bars.s_free[1], c & 1)) { ok = false; break; }
+        fence_after_sync();
+        issue_s(1, c + 1);
+        mma_commit(&bars.kv_empty[(2 * c + 2) % kSlots]);             // K(c+1) consumed
+      }
       if (abort_sh) { ok = false; break; }
     }
-    if (!ok) abort_sh = 1;
+    if (ok) mma_commit(&bars.done);
+    else abort_sh = 1;
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax rows
-    const int t = threadIdx.x - 128;           // query row within the tile = TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-    const float ks = p.k_scale ? p.k_scale[g] : 1.f;
-    const float sc = p.scale_log2 * ks;
-    float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
-    float O[128];
-#pragma unroll
-    for (int i = 0; i < 128; ++i) O[i] = 0.f;
-    unsigned char* Ps = sm + kOffP;
+    const int t = (warp - 4) >> 2;                 // tile
+    const int row_in_tile = threadIdx.x - 128 - t * 128;
+    const uint32_t lane_off = (uint32_t)(((warp - 4) & 3) * 32) << 16;
+    const uint32_t tS = tmem + t * 256 + lane_off;
+    const uint32_t tO = tS + 128;
+    const float sc = p.scale_log2;
+    unsigned char* Ps = sm + kOffP + t * kTileBytes;
+    float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int c = 0; c < nchunks; ++c) {
-      const int s = c & 1;
-      if (!warp_wait(&bars.s_full[s], (c >> 1) & 1)) { ok = false; break; }
+      if (!warp_wait(&bars.s_full[t], c & 1)) { ok = false; break; }
       fence_after_sync();
+      // pass 1: the chunk's row max (scores stay in TMEM)
       const int nvalid = min(128, k1 - (k0 + c * 128));
       float mx = -INFINITY;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         float v[32];
-        tmem_ld32(tmem + s * 128 + lane_off + q * 32, v);
+        tmem_ld32(tS + q * 32, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           if (q * 32 + i < nvalid) mx = fmaxf(mx, v[i]);
       }
-      const float m_new = fmaxf(m, mx * sc);
-      const float alpha = ex2(m - m_new);
-      if (c > 0) {
-        if (!warp_wait(&bars.pv_done, (c - 1) & 1)) { ok = false; break; }
-        fence_after_sync();
+      mx *= sc;
+      const bool need = mx > m_used + kRescale;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? mx : m_used;
+        const float factor = ex2(m_used - m_new);   // 0 on the first chunk, 1 for rows that keep m
+        l *= factor;
+        if (c > 0) {   // O_t holds chunks < c (their PV completed before S_t(c) was signalled)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float v[32];
+            tmem_ld32(tO + q * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= factor;
+            tmem_st32(tO + q * 32, v);
+          }
+          tmem_wait_st();
+        }
+        m_used = m_new;
       }
+      // pass 2: P = 2^(s - m) as bf16 into the swizzled K-major tile
       float sum = 0.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         float v[32];
-        tmem_ld32(tmem + s * 128 + lane_off + q * 32, v);
+        tmem_ld32(tS + q * 32, v);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int k2 = q * 32 + 2 * i;
-          const float p0 = (k2 < nvalid) ? ex2(fmaf(v[2 * i], sc, -m_new)) : 0.f;
-          const float p1 = (k2 + 1 < nvalid) ? ex2(fmaf(v[2 * i + 1], sc, -m_new)) : 0.f;
+          const float p0 = (k2 < nvalid) ? ex2(fmaf(v[2 * i], sc, -m_used)) : 0.f;
+          const float p1 = (k2 + 1 < nvalid) ? ex2(fmaf(v[2 * i + 1], sc, -m_used)) : 0.f;
+          sum += p0 + p1;
           const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
-          const float2 bf = __bfloat1622float2(b);
-          sum += bf.x + bf.y;
           pk[i] = *reinterpret_cast<const uint32_t*>(&b);
         }
         const int half = q >> 1;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int chunk = (q & 1) * 4 + k;
-          uint4* dst = reinterpret_cast<uint4*>(Ps + half * kHalfBytes + t * 128 +
-                                                ((chunk ^ (t & 7)) << 4));
+          uint4* dst = reinterpret_cast<uint4*>(Ps + half * kHalfBytes + row_in_tile * 128 +
+                                                ((chunk ^ (row_in_tile & 7)) << 4));
           *dst = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
       }
+      l += sum;
       fence_before_sync();
-      mbar_arrive(&bars.s_free[s]);
+      mbar_arrive(&bars.s_free[t]);
       fence_proxy_async_smem();
-      mbar_arrive(&bars.p_full);
-      l = l * alpha + sum;
-      if (c > 0) {   // fold O of the previous chunk (its PV is complete)
-        const int so = (c - 1) & 1;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float v[32];
-          tmem_ld32(tmem + 256 + so * 128 + lane_off + q * 32, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) O[q * 32 + i] = fmaf(O[q * 32 + i], alpha_prev, v[i]);
-        }
-      }
-      alpha_prev = alpha;
-      m = m_new;
+      mbar_arrive(&bars.p_full[t]);
       if (warp_flag(&abort_sh)) { ok = false; break; }
     }
-    if (ok) {
-      if (warp_wait(&bars.pv_done, (nchunks - 1) & 1)) {
-        fence_after_sync();
-        const int so = (nchunks - 1) & 1;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float v[32];
-          tmem_ld32(tmem + 256 + so * 128 + lane_off + q * 32, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) O[q * 32 + i] = fmaf(O[q * 32 + i], alpha_prev, v[i]);
-        }
-      } else {
-        ok = false;
-      }
-    }
+    if (ok && !warp_wait(&bars.done, 0)) ok = false;
     if (!ok) abort_sh = 1;
-    const int row = row0 + t;
-    if (ok && row < p.rows) {
+    const int row = row0 + t * 128 + row_in_tile;
+    if (ok) {
+      fence_after_sync();
       const size_t pi = prow_base + row;
-      p.pm[pi] = m;
-      p.pl[pi] = l;
       float4* o = reinterpret_cast<float4*>(p.po + pi * 128);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] = make_float4(O[4 * i], O[4 * i + 1], O[4 * i + 2], O[4 * i + 3]);
+      for (int q = 0; q < 4; ++q) {
+        float v[32];
+        tmem_ld32(tO + q * 32, v);
+        if (row < p.rows) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            o[q * 8 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+      }
+      if (row < p.rows) {
+        p.pm[pi] = m_used;
+        p.pl[pi] = l;
+      }
     }
   }
   fence_before_sync();
@@ -408,11 +446,10 @@ int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t st
   p.scale_log2 = a.sm_scale * kLog2e;
   p.prompt_offsets = a.prompt_offsets;
   p.n_live = a.n_live;
-  p.k_scale = nullptr;
   AttnPartials part = attn_partials(a.ws, a.R, a.W, a.Hq, a.Hkv, a.d, pl.n_split);
   p.pm = part.m; p.pl = part.l; p.po = part.o;
   p.hdr = reinterpret_cast<WsHeader*>(a.ws);
-  dim3 grid((p.rows + 127) / 128, a.Hkv * pl.n_split, a.R);
+  dim3 grid((p.rows + 255) / 256, a.Hkv * pl.n_split, a.R);
   prof_begin(kKAttnTc, stream);
   bd_attn_shared_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qm, km, vm, p);
   prof_end(kKAttnTc, stream);

@@ -123,6 +123,18 @@ __device__ __forceinline__ int block_rank(int flag, int* warp_cnt, int* total) {
   return base + r;
 }
 
+// Coarse bin of a candidate score relative to a per-request reference score
+// (the score of the request's rank-0 beam): floor((ref - s) * 64), clamped to
+// [0, 4095].  It is monotone (a higher score never gets a higher bin), so a
+// request-wide histogram of bins brackets the W-th best score from one count.
+constexpr int kTailBins = 4096;
+__device__ __forceinline__ int score_bin(float ref, float s) {
+  const float u = __fmul_rn(__fsub_rn(ref, s), 64.f);
+  if (!(u > 0.f)) return 0;
+  if (u >= (float)(kTailBins - 1)) return kTailBins - 1;
+  return (int)u;
+}
+
 struct ExpandShared {
   uint32_t hist[2048];
   float red_m[32];
@@ -137,7 +149,7 @@ struct ExpandShared {
 // Rows a1-a3 for beam b of request r: log-sum-exp, trie children, per-beam
 // top_k appended to the request's pool.
 __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
-                                               int r, int b) {
+                                                 int r, int b, uint32_t* bins) {
   const int tid = threadIdx.x;
   const int Kp = a.Kp;
   const size_t rowi = (size_t)r * a.W + b;
@@ -242,7 +254,7 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
 
   SelState* st = ws.state + r;
   unsigned long long* pool = ws.pool + (size_t)r * a.W * Kp;
-  (void)Kp;
+  const float ref = a.cum_in[(size_t)r * a.W];   // bin reference: the rank-0 beam's score
 
   // ---- a3: per-beam top_k -------------------------------------------------
   if (n <= a.K) {
@@ -250,7 +262,9 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
     __syncthreads();
     for (int i = tid; i < n; i += kExpandThreads) {
       const int tok = tok_of(i);
-      pool[sh.pool_base + i] = pool_key(key_of(tok), b, tok);
+      const uint32_t k = key_of(tok);
+      pool[sh.pool_base + i] = pool_key(k, b, tok);
+      if (bins) atomicAdd(&bins[score_bin(ref, desc_key_value(k))], 1u);
     }
     return;
   }
@@ -284,7 +298,10 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
   for (int i = tid; i < n; i += kExpandThreads) {
     const int tok = tok_of(i);
     const uint32_t k = key_of(tok);
-    if (k < kth) pool[base + atomicAdd(&sh.count, 1)] = pool_key(k, b, tok);
+    if (k < kth) {
+      pool[base + atomicAdd(&sh.count, 1)] = pool_key(k, b, tok);
+      if (bins) atomicAdd(&bins[score_bin(ref, desc_key_value(k))], 1u);
+    }
   }
   __syncthreads();
   const int n_less = sh.count;
@@ -296,7 +313,10 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
     if (i < n) { tok = tok_of(i); flag = key_of(tok) == kth; }
     int tot;
     const int rk = block_rank(flag, sh.warp_cnt, &tot);
-    if (flag && taken + rk < (int)need) pool[base + n_less + taken + rk] = pool_key(kth, b, tok);
+    if (flag && taken + rk < (int)need) {
+      pool[base + n_less + taken + rk] = pool_key(kth, b, tok);
+      if (bins) atomicAdd(&bins[score_bin(ref, desc_key_value(kth))], 1u);
+    }
     taken += tot;
   }
 }
@@ -410,6 +430,39 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
     for (int i = threadIdx.x; i < total; i += blockDim.x) keys[i] = __ldcg(pool + i);
     nc = total;
   } else {
+    // the request's score-bin histogram (complete: every block flushed it
+    // before taking its ticket) brackets the nt-th best score
+    const volatile uint32_t* gh = ws.hist + (size_t)r * kBins;
+    if (threadIdx.x < 32) warp_find_digit(gh, kTailBins, (uint32_t)nt, &sh.digit, &sh.below);
+    __syncthreads();
+    const int Dbin = (int)sh.digit;
+    const uint32_t c_le = sh.below + gh[Dbin];
+    __syncthreads();
+    if (c_le <= (uint32_t)kTailCap) {
+      const float ref = a.cum_in[(size_t)r * a.W];
+      if (threadIdx.x == 0) sh.count = 0;
+      __syncthreads();
+      for (int c0 = 0; c0 < total; c0 += blockDim.x) {
+        const int i = c0 + threadIdx.x;
+        unsigned long long k = 0;
+        int flag = 0;
+        if (i < total) {
+          k = __ldcg(pool + i);
+          flag = score_bin(ref, desc_key_value((uint32_t)(k >> 32))) <= Dbin;
+        }
+        int tot;
+        const int rk = block_rank(flag, sh.warp_cnt, &tot);
+        const int pos = sh.count + rk;
+        if (flag && pos < kTailCap) keys[pos] = k;
+        __syncthreads();
+        if (threadIdx.x == 0) sh.count += tot;
+        __syncthreads();
+      }
+      nc = sh.count < kTailCap ? sh.count : kTailCap;
+      goto selected;
+    }
+  }
+  if (total > kTailCap) {
     unsigned long long prefix = 0;
     int shift = 64;
     uint32_t need = (uint32_t)nt, sure = 0, in_bin = 0;
@@ -437,6 +490,7 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
     }
     nc = sh.count < kTailCap ? sh.count : kTailCap;
   }
+selected:
   __syncthreads();
   if (nc > nt) {   // exact threshold: narrow until the keys at or below it number nt
     unsigned long long prefix = 0;
@@ -483,8 +537,18 @@ bd_expand_kernel(SelectArgs a) {
   if (b == 0 && r == 0 && tid == 0) ws.hdr->bar_count = 0u;
   const int nl = a.n_live_in[r];
   if (b >= nl) return;
-  expand_candidates(a, sh, ws, r, b);
+  uint32_t* bins = nullptr;
+  if constexpr (kFused) {   // the tail buffer holds this block's score-bin histogram until the ticket
+    bins = reinterpret_cast<uint32_t*>(tail_smem);
+    for (int i = tid; i < kTailBins; i += kExpandThreads) bins[i] = 0;
+    __syncthreads();
+  }
+  expand_candidates(a, sh, ws, r, b, bins);
   if constexpr (kFused) {
+    __syncthreads();
+    uint32_t* gh = ws.hist + (size_t)r * kBins;
+    for (int i = tid; i < kTailBins; i += kExpandThreads)
+      if (bins[i]) atomicAdd(gh + i, bins[i]);
     // the last block of the request to finish runs the request's global top-W
     __syncthreads();
     if (tid == 0) {
