@@ -89,7 +89,8 @@ int beamdec_read_status(void* workspace, void* stream, int32_t* host_status);
  * stops recording.  beamdec_profile_read synchronises the recorded events and
  * returns the total milliseconds and launch count of one kernel id:
  * 0 bd_expand_kernel, 1 bd_global_kernel, 2 bd_attn_shared_simt_kernel,
- * 3 bd_attn_shared_tc_kernel, 4 bd_attn_merge_kernel.  Host-side state is
+ * 3 bd_attn_shared_tc_kernel, 4 bd_attn_merge_kernel, 5 bd_kv_e4m3_to_bf16_kernel.
+ * Host-side state is
  * process-wide; use from one host thread.
  */
 int beamdec_profile_enable(int on);
@@ -280,8 +281,10 @@ int beam_attn_workspace_size(int R, int W, int Hq, int Hkv, int d, int max_promp
  *                   prompt_offsets[r] .. prompt_offsets[r+1]-1.
  *   prompt_offsets  [R+1] int32, non-decreasing, prompt_offsets[0] = 0.
  *   max_prompt_len  host int >= every P_r (sizes the launch).
- *   shared_rows     host: rows allocated in shared_k / shared_v (>= sum P);
- *                   no row at or beyond it is ever read.
+ *   shared_rows     host copy of prompt_offsets[R]: the rows of shared_k /
+ *                   shared_v (<= R * max_prompt_len).  No row at or beyond it
+ *                   is read; a device-side mismatch with prompt_offsets[R]
+ *                   sets BEAMDEC_ERR_DEVICE_CHECK.
  *   unshared_k/v    [R][T*W][Hkv][d] kv_dtype: the per-request slot pool.
  *   slot_table      [R][W][T] int32; entries 0..step of live rows must lie in
  *                   [0, T*W) (checked in-kernel; a bad slot sets
@@ -292,7 +295,10 @@ int beam_attn_workspace_size(int R, int W, int Hq, int Hkv, int d, int max_promp
  *   sm_scale        softmax scale (pass 0 for 1/sqrt(d)).
  *   out             [R][W][Hq][d] out_dtype (F32 or BF16).
  * Supported: d in {64, 128}; Hq % Hkv == 0; Hq/Hkv <= 16; q/kv/out dtypes
- * F32/F32/F32, BF16/BF16/BF16, BF16/E4M3/BF16.
+ * F32/F32/F32, BF16/BF16/BF16, BF16/E4M3/BF16.  BF16 queries with d = 128
+ * and a group size dividing 128 take the tensor-core shared stage (fp8 KV is
+ * first dequantised to bf16 in the workspace); other shapes run it on CUDA
+ * cores.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  */
 int beam_attn_decode(const void* q, const void* shared_k, const void* shared_v,

@@ -2,6 +2,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <cuda_bf16.h>
+
 #include "internal.h"
 
 namespace bd {
@@ -49,6 +51,8 @@ AttnPlan attn_plan(int R, int W, int Hq, int Hkv, int d, int max_prompt_len, int
     if (cost < best_cost - 1e-9) { best_cost = cost; best = s; }
   }
   p.split_len = ((chunks + best - 1) / best) * chunk;
+  p.convert_kv = p.tensor_core && kv_dtype == BEAMDEC_E4M3;
+  p.max_prompt_len = max_prompt_len;
   p.n_split = max_prompt_len > 0 ? (max_prompt_len + p.split_len - 1) / p.split_len : 1;
   (void)d;
   return p;
@@ -56,7 +60,14 @@ AttnPlan attn_plan(int R, int W, int Hq, int Hkv, int d, int max_prompt_len, int
 
 size_t attn_workspace_bytes(int R, int W, int Hq, int Hkv, int d, const AttnPlan& p) {
   const size_t rows = (size_t)R * Hkv * W * (Hq / Hkv) * p.n_split;
-  return kWsHeaderBytesHost + a256(rows * 4) * 2 + a256(rows * d * 4);
+  const size_t kv16 = p.convert_kv ? a256((size_t)2 * R * p.max_prompt_len * Hkv * d * 2) : 0;
+  return kWsHeaderBytesHost + a256(rows * 4) * 2 + a256(rows * d * 4) + kv16;
+}
+
+__nv_bfloat16* attn_kv16(void* ws, int R, int W, int Hq, int Hkv, int d, int n_split) {
+  const size_t rows = (size_t)R * Hkv * W * (Hq / Hkv) * n_split;
+  char* p = static_cast<char*>(ws) + kWsHeaderBytesHost + a256(rows * 4) * 2 + a256(rows * d * 4);
+  return reinterpret_cast<__nv_bfloat16*>(p);
 }
 
 AttnPartials attn_partials(void* ws, int R, int W, int Hq, int Hkv, int d, int n_split) {
@@ -195,7 +206,8 @@ extern "C" int beam_attn_decode(const void* q, const void* shared_k, const void*
     return BEAMDEC_ERR_INVALID_ARG;
   if (max_prompt_len > 0 && (shared_k == nullptr || shared_v == nullptr))
     return BEAMDEC_ERR_INVALID_ARG;
-  if (shared_rows < 0 || (max_prompt_len > 0 && shared_rows < max_prompt_len))
+  if (shared_rows < 0 || (max_prompt_len > 0 && shared_rows < max_prompt_len) ||
+      shared_rows > (int64_t)R * max_prompt_len)
     return BEAMDEC_ERR_INVALID_ARG;
   const int s = attn_shape_check(R, W, Hq, Hkv, d, max_prompt_len);
   if (s != BEAMDEC_OK) return s;

@@ -73,8 +73,12 @@ bd_attn_merge_kernel(AttnArgs a, int n_split, AttnPartials part) {
   const int g = (int)(wid % a.Hkv);
   const int j = (int)((wid / a.Hkv) % a.W);
   const int r = (int)(wid / ((long long)a.Hkv * a.W));
-  const bool live = j < a.n_live[r];
   const size_t head0 = ((size_t)r * a.W + j) * a.Hq + (size_t)g * G;
+  // first round of independent loads: live count, slot row, and below the
+  // queries and partials of the first head group
+  const int nl = a.n_live[r];
+  int my_slot = lane < L ? a.slot_table[((size_t)r * a.W + j) * a.T + lane] : -1;
+  const bool live = j < nl;
   if (!live) {
     float z[PL];
 #pragma unroll
@@ -82,13 +86,9 @@ bd_attn_merge_kernel(AttnArgs a, int n_split, AttnPartials part) {
     for (int gi = 0; gi < G; ++gi) store_lane<DQ, DKV, D>(a.out, (head0 + gi) * D + lane * PL, z, a.out_dtype);
     return;
   }
-  int my_slot = -1;
-  if (lane < L) {
-    my_slot = a.slot_table[((size_t)r * a.W + j) * a.T + lane];
-    if (my_slot < 0 || my_slot >= TW) {
-      set_status(hdr, BEAMDEC_ERR_DEVICE_CHECK);
-      my_slot = -1;
-    }
+  if (lane < L && (my_slot < 0 || my_slot >= TW)) {
+    set_status(hdr, BEAMDEC_ERR_DEVICE_CHECK);
+    my_slot = -1;
   }
   const float ks = (DKV == 2 && a.k_scale) ? a.k_scale[g] : 1.f;
   const float vs = (DKV == 2 && a.v_scale) ? a.v_scale[g] : 1.f;
@@ -96,7 +96,7 @@ bd_attn_merge_kernel(AttnArgs a, int n_split, AttnPartials part) {
   for (int g0 = 0; g0 < G; g0 += kGq) {
     const int ng = G - g0 < kGq ? G - g0 : kGq;
     // independent loads: queries and the shared-stage partials of these heads
-    float q[kGq][PL], o[kGq][PL], m[kGq], l[kGq];
+    float q[kGq][PL], o[kGq][PL], m[kGq], l[kGq], o0[kGq][PL];
     float pm[kGq], pl[kGq];   // lane c < n_split holds split c
 #pragma unroll
     for (int u = 0; u < kGq; ++u) {
@@ -105,9 +105,20 @@ bd_attn_merge_kernel(AttnArgs a, int n_split, AttnPartials part) {
       pm[u] = -INFINITY;
       pl[u] = 0.f;
 #pragma unroll
-      for (int i = 0; i < PL; ++i) { q[u][i] = 0.f; o[u][i] = 0.f; }
+      for (int i = 0; i < PL; ++i) { q[u][i] = 0.f; o[u][i] = 0.f; o0[u][i] = 0.f; }
       if (u < ng) {
         load_lane<DQ, PL>(a.q, (head0 + g0 + u) * D + lane * PL, q[u]);
+        if (n_split > 0) {   // split 0's partial output, prefetched
+          const size_t p0 = (((size_t)r) * a.Hkv + g) * rows + (size_t)j * G + g0 + u;
+          const float* src = part.o + p0 * D + lane * PL;
+          if constexpr (PL == 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src);
+            o0[u][0] = x.x; o0[u][1] = x.y; o0[u][2] = x.z; o0[u][3] = x.w;
+          } else {
+            const float2 x = *reinterpret_cast<const float2*>(src);
+            o0[u][0] = x.x; o0[u][1] = x.y;
+          }
+        }
 #pragma unroll
         for (int i = 0; i < PL; ++i) q[u][i] *= scale2;
         if (lane < n_split) {
@@ -183,13 +194,18 @@ bd_attn_merge_kernel(AttnArgs a, int n_split, AttnPartials part) {
         const float w = ex2(mc - M);
         Lsum = fmaf(lc, w, Lsum);
         float oc[PL];
-        const float* src = part.o + pi * D + lane * PL;
-        if constexpr (PL == 4) {
-          const float4 x = *reinterpret_cast<const float4*>(src);
-          oc[0] = x.x; oc[1] = x.y; oc[2] = x.z; oc[3] = x.w;
+        if (c == 0) {
+#pragma unroll
+          for (int i = 0; i < PL; ++i) oc[i] = o0[u][i];
         } else {
-          const float2 x = *reinterpret_cast<const float2*>(src);
-          oc[0] = x.x; oc[1] = x.y;
+          const float* src = part.o + pi * D + lane * PL;
+          if constexpr (PL == 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src);
+            oc[0] = x.x; oc[1] = x.y; oc[2] = x.z; oc[3] = x.w;
+          } else {
+            const float2 x = *reinterpret_cast<const float2*>(src);
+            oc[0] = x.x; oc[1] = x.y;
+          }
         }
 #pragma unroll
         for (int i = 0; i < PL; ++i) O[i] = fmaf(oc[i], w, O[i]);

@@ -32,6 +32,8 @@
 // the loops and still frees TMEM.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -64,6 +66,8 @@ constexpr uint32_t kVSbo = 1024;
 struct TcParams {
   int R, W, Hq, Hkv, G, rows, split_len;
   float scale_log2;   // sm_scale * log2(e)
+  const float* k_scale;   // per kv head; fp8 KV only (nullptr otherwise)
+  int64_t shared_rows;
   const int32_t* prompt_offsets;
   const int32_t* n_live;
   float* pm;
@@ -136,6 +140,9 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   const int r = blockIdx.z;
   const int row0 = mt * 256;
   const int G = p.G;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 &&
+      (int64_t)p.prompt_offsets[p.R] != p.shared_rows)
+    set_status(p.hdr, BEAMDEC_ERR_DEVICE_CHECK);   // the K/V maps end at shared_rows
   if (row0 >= p.n_live[r] * G) return;   // every row of the CTA is a dead beam
   const int pbase = p.prompt_offsets[r];
   const int P = p.prompt_offsets[r + 1] - pbase;
@@ -271,7 +278,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     const uint32_t lane_off = (uint32_t)(((warp - 4) & 3) * 32) << 16;
     const uint32_t tS = tmem + t * 256 + lane_off;
     const uint32_t tO = tS + 128;
-    const float sc = p.scale_log2;
+    const float sc = p.scale_log2 * (p.k_scale ? p.k_scale[g] : 1.f);
     unsigned char* Ps = sm + kOffP + t * kTileBytes;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
@@ -372,6 +379,38 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   }
 }
 
+// fp8 e4m3 K/V of the prompt -> bf16 (exact: every e4m3 value is a bf16
+// value), rows [0, prompt_offsets[R]), for the tensor-core shared stage.  The
+// per-head scales are not applied here: K's scale multiplies the softmax
+// scale and V's scale the merged output.
+__global__ void __launch_bounds__(256)
+bd_kv_e4m3_to_bf16_kernel(const uint8_t* __restrict__ k8, const uint8_t* __restrict__ v8,
+                          __nv_bfloat16* __restrict__ k16, __nv_bfloat16* __restrict__ v16,
+                          const int32_t* prompt_offsets, int R, int64_t row_elems) {
+  const int64_t n16 = (int64_t)prompt_offsets[R] * row_elems / 16;   // 16-element groups
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n16;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const bool isv = i >= n16;
+    const int64_t e = (isv ? i - n16 : i) * 16;
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>((isv ? v8 : k8) + e));
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((w[q] >> (16 * h)) & 0xffffu);
+        const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3)));
+        const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+        o[2 * q + h] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+    }
+    uint4* dst = reinterpret_cast<uint4*>((isv ? v16 : k16) + e);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 // ---- host side ------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -404,8 +443,8 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
 }  // namespace
 
 bool attn_tc_supported(int q_dtype, int kv_dtype, int d, int G) {
-  return q_dtype == BEAMDEC_BF16 && kv_dtype == BEAMDEC_BF16 && d == 128 && G >= 1 && G <= 16 &&
-         (128 % G) == 0;
+  return q_dtype == BEAMDEC_BF16 && (kv_dtype == BEAMDEC_BF16 || kv_dtype == BEAMDEC_E4M3) &&
+         d == 128 && G >= 1 && G <= 16 && (128 % G) == 0;
 }
 
 int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t stream) {
@@ -423,6 +462,25 @@ int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t st
       return BEAMDEC_ERR_CUDA;
     attr_set[dev] = true;
   }
+  const void* kbase = a.shared_k;
+  const void* vbase = a.shared_v;
+  if (a.kv_dtype == BEAMDEC_E4M3 && a.shared_rows > 0) {
+    // dequantise the prompt KV once into the workspace (bf16, same layout)
+    __nv_bfloat16* k16 = attn_kv16(a.ws, a.R, a.W, a.Hq, a.Hkv, a.d, pl.n_split);
+    __nv_bfloat16* v16 = k16 + (size_t)a.R * a.max_prompt_len * a.Hkv * a.d;
+    const int64_t groups = a.shared_rows * a.Hkv * a.d / 16 * 2;
+    int blocks = (int)((groups + 255) / 256);
+    if (blocks > 8 * sm_count()) blocks = 8 * sm_count();
+    if (blocks < 1) blocks = 1;
+    prof_begin(kKKvConvert, stream);
+    bd_kv_e4m3_to_bf16_kernel<<<blocks, 256, 0, stream>>>(
+        static_cast<const uint8_t*>(a.shared_k), static_cast<const uint8_t*>(a.shared_v), k16, v16,
+        a.prompt_offsets, a.R, (int64_t)a.Hkv * a.d);
+    prof_end(kKKvConvert, stream);
+    if (cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
+    kbase = k16;
+    vbase = v16;
+  }
   CUtensorMap qm, km, vm;
   {
     const cuuint64_t dims[4] = {(cuuint64_t)a.d, (cuuint64_t)a.Hq, (cuuint64_t)a.W, (cuuint64_t)a.R};
@@ -436,14 +494,16 @@ int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t st
     const cuuint64_t dims[3] = {(cuuint64_t)a.d, (cuuint64_t)a.Hkv, total > 0 ? total : 1};
     const cuuint64_t st[2] = {(cuuint64_t)a.d * 2, (cuuint64_t)a.Hkv * a.d * 2};
     const cuuint32_t box[3] = {64, 1, 128};
-    if (!make_map(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.shared_k, dims, st, box) ||
-        !make_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.shared_v, dims, st, box))
+    if (!make_map(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kbase, dims, st, box) ||
+        !make_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, vbase, dims, st, box))
       return BEAMDEC_ERR_CUDA;
   }
   TcParams p;
   p.R = a.R; p.W = a.W; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.rows = a.W * G;
   p.split_len = pl.split_len;
   p.scale_log2 = a.sm_scale * kLog2e;
+  p.k_scale = a.kv_dtype == BEAMDEC_E4M3 ? a.k_scale : nullptr;
+  p.shared_rows = a.shared_rows;
   p.prompt_offsets = a.prompt_offsets;
   p.n_live = a.n_live;
   AttnPartials part = attn_partials(a.ws, a.R, a.W, a.Hq, a.Hkv, a.d, pl.n_split);

@@ -37,7 +37,11 @@ __device__ __forceinline__ float desc_key_value(uint32_t k) {
   return __uint_as_float(b);
 }
 
-// Global pool key: ascending order = (score desc, beam asc, token asc).
+// Global pool key: desc(score) << 32 | beam << 18 | index, where index is the
+// candidate's position among its beam's candidates (the child position within
+// the trie node, whose codes ascend, or the token itself with no trie).  Within
+// one beam the index order is the token order, so ascending keys order
+// candidates by (score desc, beam asc, token asc).
 constexpr int kTokBits = 18;
 constexpr int kBeamBits = 13;
 __device__ __forceinline__ uint64_t pool_key(uint32_t k32, int beam, int tok) {

@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libbeamdec.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -65,6 +66,8 @@ struct AttnPlan {
   int n_split;      // prompt splits (partials per query row)
   int split_len;    // keys per split (multiple of 128)
   bool tensor_core; // tcgen05 shared stage
+  bool convert_kv;  // fp8 prompt KV dequantised to bf16 in the workspace first
+  int max_prompt_len;
 };
 AttnPlan attn_plan(int R, int W, int Hq, int Hkv, int d, int max_prompt_len, int q_dtype,
                    int kv_dtype);
@@ -81,12 +84,14 @@ struct AttnPartials {
   float* m; float* l; float* o;
 };
 AttnPartials attn_partials(void* ws, int R, int W, int Hq, int Hkv, int d, int n_split);
+// bf16 copies of fp8 prompt K then V (R * max_prompt_len rows each), after the partials.
+__nv_bfloat16* attn_kv16(void* ws, int R, int W, int Hq, int Hkv, int d, int n_split);
 
 int sm_count();
 
 // ---- per-kernel event timing (off unless beamdec_profile_enable(1)) ---------
 enum KernelId { kKExpand = 0, kKGlobal = 1, kKAttnSimt = 2, kKAttnTc = 3, kKAttnMerge = 4,
-                kKCount = 5 };
+                kKKvConvert = 5, kKCount = 6 };
 void prof_begin(int kid, cudaStream_t s);
 void prof_end(int kid, cudaStream_t s);
 

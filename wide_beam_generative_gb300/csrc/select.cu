@@ -261,9 +261,8 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
     if (tid == 0) sh.pool_base = n > 0 ? atomicAdd(&st->total, n) : 0;
     __syncthreads();
     for (int i = tid; i < n; i += kExpandThreads) {
-      const int tok = tok_of(i);
-      const uint32_t k = key_of(tok);
-      pool[sh.pool_base + i] = pool_key(k, b, tok);
+      const uint32_t k = key_of(tok_of(i));
+      pool[sh.pool_base + i] = pool_key(k, b, i);
       if (bins) atomicAdd(&bins[score_bin(ref, desc_key_value(k))], 1u);
     }
     return;
@@ -296,10 +295,9 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
   __syncthreads();
   const int base = sh.pool_base;
   for (int i = tid; i < n; i += kExpandThreads) {
-    const int tok = tok_of(i);
-    const uint32_t k = key_of(tok);
+    const uint32_t k = key_of(tok_of(i));
     if (k < kth) {
-      pool[base + atomicAdd(&sh.count, 1)] = pool_key(k, b, tok);
+      pool[base + atomicAdd(&sh.count, 1)] = pool_key(k, b, i);
       if (bins) atomicAdd(&bins[score_bin(ref, desc_key_value(k))], 1u);
     }
   }
@@ -308,13 +306,12 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
   int taken = 0;
   for (int c0 = 0; c0 < n && taken < (int)need; c0 += kExpandThreads) {
     const int i = c0 + tid;
-    int tok = 0;
     int flag = 0;
-    if (i < n) { tok = tok_of(i); flag = key_of(tok) == kth; }
+    if (i < n) flag = key_of(tok_of(i)) == kth;
     int tot;
     const int rk = block_rank(flag, sh.warp_cnt, &tot);
     if (flag && taken + rk < (int)need) {
-      pool[base + n_less + taken + rk] = pool_key(kth, b, tok);
+      pool[base + n_less + taken + rk] = pool_key(kth, b, i);
       if (bins) atomicAdd(&bins[score_bin(ref, desc_key_value(kth))], 1u);
     }
     taken += tot;
@@ -338,15 +335,6 @@ __device__ void bitonic_sort(unsigned long long* keys, int np) {
   }
 }
 
-__device__ __forceinline__ int find_child_edge(const TrieLevel& L, int node, int code) {
-  int lo = L.off[node], hi = L.off[node + 1];
-  while (lo < hi) {
-    int mid = (lo + hi) >> 1;
-    if (L.code[mid] < code) lo = mid + 1; else hi = mid;
-  }
-  return (lo < L.off[node + 1] && L.code[lo] == code) ? lo : -1;
-}
-
 // a4/a5 outputs of request r from its nt winners, sorted ascending in keys[]:
 // tokens, parents, scores, child nodes, live count and the slot rows
 // (parent's row up to step-1, then step*W + j).
@@ -357,15 +345,16 @@ __device__ void emit_outputs(const SelectArgs& a, const SelWs& ws, int r,
   for (int j = tid; j < a.W; j += blockDim.x) {
     if (j < nt) {
       const unsigned long long k = keys[j];
-      const int parent = pool_key_beam(k), tok = pool_key_tok(k);
+      const int parent = pool_key_beam(k), idx = pool_key_tok(k);
+      int tok = idx, node = -1;
+      if (a.has_trie) {
+        const int nd = a.node_in[o + parent];
+        node = a.lvl.off[nd] + idx;           // edge index = child node at the next level
+        tok = a.lvl.token_base + a.lvl.code[node];
+      }
       a.tokens[o + j] = tok;
       a.parents[o + j] = parent;
       a.cum_out[o + j] = desc_key_value((uint32_t)(k >> 32));
-      int node = -1;
-      if (a.has_trie) {
-        node = find_child_edge(a.lvl, a.node_in[o + parent], tok - a.lvl.token_base);
-        if (node < 0) set_status(ws.hdr, BEAMDEC_ERR_DEVICE_CHECK);
-      }
       a.node_out[o + j] = node;
     } else {
       a.tokens[o + j] = -1;
@@ -417,6 +406,104 @@ __device__ uint32_t narrow_pass(const unsigned long long* keys, int n, unsigned 
   return in_bin;
 }
 
+// Block-wide exclusive prefix sum of one int per thread; *total = block sum.
+__device__ __forceinline__ int block_excl_scan(int x, int* warp_tmp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = x;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tmp[warp] = incl;
+  __syncthreads();
+  int base = 0, tot = 0;
+  for (int w = 0; w < nw; ++w) {
+    const int c = warp_tmp[w];
+    if (w < warp) base += c;
+    tot += c;
+  }
+  __syncthreads();
+  *total = tot;
+  return base + incl - x;
+}
+
+// Appends to keys[] (up to cap) every pool key for which pred(key) holds,
+// 8 keys per thread per round so the loads of a round are all in flight.
+// Returns the number of keys that satisfied pred (may exceed cap).
+template <class Pred>
+__device__ int block_gather(const unsigned long long* pool, int total, Pred pred,
+                            unsigned long long* keys, int cap, ExpandShared& sh) {
+  constexpr int kPer = 8;
+  int count = 0;
+  for (int base = 0; base < total; base += kPer * (int)blockDim.x) {
+    unsigned long long v[kPer];
+    int c = 0;
+    uint32_t fl = 0;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = base + u * (int)blockDim.x + (int)threadIdx.x;
+      v[u] = i < total ? __ldcg(pool + i) : 0ull;
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = base + u * (int)blockDim.x + (int)threadIdx.x;
+      if (i < total && pred(v[u])) { fl |= 1u << u; ++c; }
+    }
+    int tot;
+    int pos = count + block_excl_scan(c, sh.warp_cnt, &tot);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u)
+      if (fl & (1u << u)) {
+        if (pos < cap) keys[pos] = v[u];
+        ++pos;
+      }
+    count += tot;
+  }
+  __syncthreads();
+  return count;
+}
+
+// Writes the nt smallest of the n distinct keys src[0..n) to dst[0..nt) in
+// ascending order: each key's rank is the count of smaller keys.
+__device__ void rank_sort(const unsigned long long* src, int n, int nt, unsigned long long* dst) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const unsigned long long k = src[i];
+    int rank = 0;
+    for (int m = 0; m < n; ++m) rank += src[m] < k;
+    if (rank < nt) dst[rank] = k;
+  }
+  __syncthreads();
+}
+
+// Block-wide: the bin holding the need-th key (1-based) of a global
+// histogram of nbins (a multiple of blockDim.x); *below = keys in lower bins.
+__device__ void block_find_bin(const uint32_t* gh, int nbins, uint32_t need, ExpandShared& sh,
+                               int* bin, uint32_t* below) {
+  const int per = nbins / blockDim.x;
+  uint32_t c[16];
+  int sum = 0;
+  for (int i = 0; i < per && i < 16; ++i) {
+    c[i] = __ldcg(gh + threadIdx.x * per + i);
+    sum += (int)c[i];
+  }
+  int tot;
+  const int excl = block_excl_scan(sum, sh.warp_cnt, &tot);
+  if ((uint32_t)excl < need && need <= (uint32_t)(excl + sum)) {
+    uint32_t acc = (uint32_t)excl;
+    int d = threadIdx.x * per;
+    for (int i = 0; i < per && i < 16; ++i) {
+      if (acc + c[i] >= need) { d = threadIdx.x * per + i; break; }
+      acc += c[i];
+    }
+    sh.digit = (uint32_t)d;
+    sh.below = acc;
+  }
+  __syncthreads();
+  *bin = (int)sh.digit;
+  *below = sh.below;
+  __syncthreads();
+}
+
 // Fused a4 for one request, run by the last expand block of the request:
 // select the min(W, pool) smallest pool keys, sort them, emit outputs.
 __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs& ws, int r,
@@ -425,74 +512,47 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
   const int total = st->total;
   const int nt = total < a.W ? total : a.W;
   const unsigned long long* pool = ws.pool + (size_t)r * a.W * a.Kp;
-  int nc;
+  int nc = -1;
   if (total <= kTailCap) {
     for (int i = threadIdx.x; i < total; i += blockDim.x) keys[i] = __ldcg(pool + i);
     nc = total;
   } else {
     // the request's score-bin histogram (complete: every block flushed it
     // before taking its ticket) brackets the nt-th best score
-    const volatile uint32_t* gh = ws.hist + (size_t)r * kBins;
-    if (threadIdx.x < 32) warp_find_digit(gh, kTailBins, (uint32_t)nt, &sh.digit, &sh.below);
-    __syncthreads();
-    const int Dbin = (int)sh.digit;
-    const uint32_t c_le = sh.below + gh[Dbin];
-    __syncthreads();
+    int dbin;
+    uint32_t below;
+    block_find_bin(ws.hist + (size_t)r * kBins, kTailBins, (uint32_t)nt, sh, &dbin, &below);
+    const uint32_t c_le = below + __ldcg(ws.hist + (size_t)r * kBins + dbin);
     if (c_le <= (uint32_t)kTailCap) {
       const float ref = a.cum_in[(size_t)r * a.W];
-      if (threadIdx.x == 0) sh.count = 0;
-      __syncthreads();
-      for (int c0 = 0; c0 < total; c0 += blockDim.x) {
-        const int i = c0 + threadIdx.x;
-        unsigned long long k = 0;
-        int flag = 0;
-        if (i < total) {
-          k = __ldcg(pool + i);
-          flag = score_bin(ref, desc_key_value((uint32_t)(k >> 32))) <= Dbin;
-        }
-        int tot;
-        const int rk = block_rank(flag, sh.warp_cnt, &tot);
-        const int pos = sh.count + rk;
-        if (flag && pos < kTailCap) keys[pos] = k;
-        __syncthreads();
-        if (threadIdx.x == 0) sh.count += tot;
-        __syncthreads();
+      const int got = block_gather(pool, total, [&](unsigned long long k) {
+        return score_bin(ref, desc_key_value((uint32_t)(k >> 32))) <= dbin;
+      }, keys, kTailCap, sh);
+      nc = got < kTailCap ? got : kTailCap;
+    } else {
+      // many equal-looking scores: radix narrowing over the pool
+      unsigned long long prefix = 0;
+      int shift = 64;
+      uint32_t need = (uint32_t)nt, sure = 0, in_bin = 0;
+      while (true) {
+        in_bin = narrow_pass<true>(pool, total, prefix, shift, need, sure, sh);
+        if (sure + in_bin <= (uint32_t)kTailCap || shift == 0) break;
       }
-      nc = sh.count < kTailCap ? sh.count : kTailCap;
-      goto selected;
+      const int got = block_gather(pool, total, [&](unsigned long long k) {
+        return (k >> shift) <= prefix;
+      }, keys, kTailCap, sh);
+      nc = got < kTailCap ? got : kTailCap;
     }
   }
-  if (total > kTailCap) {
-    unsigned long long prefix = 0;
-    int shift = 64;
-    uint32_t need = (uint32_t)nt, sure = 0, in_bin = 0;
-    while (true) {
-      in_bin = narrow_pass<true>(pool, total, prefix, shift, need, sure, sh);
-      if (sure + in_bin <= (uint32_t)kTailCap || shift == 0) break;
-    }
-    if (threadIdx.x == 0) sh.count = 0;
-    __syncthreads();
-    for (int c0 = 0; c0 < total; c0 += blockDim.x) {
-      const int i = c0 + threadIdx.x;
-      unsigned long long k = 0;
-      int flag = 0;
-      if (i < total) {
-        k = __ldcg(pool + i);
-        flag = (k >> shift) <= prefix;
-      }
-      int tot;
-      const int rk = block_rank(flag, sh.warp_cnt, &tot);
-      const int pos = sh.count + rk;
-      if (flag && pos < kTailCap) keys[pos] = k;
-      __syncthreads();
-      if (threadIdx.x == 0) sh.count += tot;
-      __syncthreads();
-    }
-    nc = sh.count < kTailCap ? sh.count : kTailCap;
-  }
-selected:
   __syncthreads();
-  if (nc > nt) {   // exact threshold: narrow until the keys at or below it number nt
+  constexpr int kRankMax = kTailCap / 4;   // 1024
+  unsigned long long* sorted = keys + kTailCap / 2;
+  if (nc <= kRankMax) {   // small candidate sets: rank directly
+    rank_sort(keys, nc, nt, sorted);
+    emit_outputs(a, ws, r, sorted, nt);
+    return;
+  }
+  {   // exact threshold: narrow until the keys at or below it number nt
     unsigned long long prefix = 0;
     int shift = 64;
     uint32_t need = (uint32_t)nt, sure = 0;
@@ -519,6 +579,11 @@ selected:
       __syncthreads();
     }
   }
+  if (nt <= kRankMax) {
+    rank_sort(keys, nt, nt, sorted);
+    emit_outputs(a, ws, r, sorted, nt);
+    return;
+  }
   int np = 32;
   while (np < nt) np <<= 1;
   for (int i = nt + threadIdx.x; i < np; i += blockDim.x) keys[i] = ~0ull;
@@ -528,7 +593,7 @@ selected:
 }
 
 template <bool kFused>
-__global__ void __launch_bounds__(kExpandThreads)
+__global__ void __launch_bounds__(kExpandThreads, 4)
 bd_expand_kernel(SelectArgs a) {
   __shared__ ExpandShared sh;
   extern __shared__ __align__(16) unsigned char tail_smem[];
