@@ -10,17 +10,17 @@
 //
 // One CTA owns 256 query rows (two 128-row tiles) of one (request, kv head,
 // prompt split), so every K/V tile it loads feeds two tiles of MMAs:
-//   warp 0       TMA producer: Q once, then K and V tiles of 128 keys (two
+//   warp 8       TMA producer: Q once, then K and V tiles of 128 keys (two
 //                64-column SWIZZLE_128B boxes each) through a 3-slot ring;
-//   warp 1       allocates TMEM and issues every MMA from one thread, in the
+//   warp 9       allocates TMEM and issues every MMA from one thread, in the
 //                order S0(c) S1(c) | PV0(c) S0(c+1) | PV1(c) S1(c+1) | ... so
 //                the tensor core works on one tile while the other tile's
 //                softmax runs;
-//   warps 4-7    softmax of tile 0, warps 8-11 softmax of tile 1: thread t
+//   warps 0-3    softmax of tile 0, warps 4-7 softmax of tile 1: thread t
 //                owns row t (TMEM lane t); reads its 128 scores from TMEM
-//                twice (row max, then P), keeps max/sum in log2 units, writes
-//                P (bf16) into shared memory in the 128B-swizzled K-major
-//                layout the MMA reads.
+//                twice (row max, then P; one 128-column load each), keeps
+//                max/sum in log2 units, writes P (bf16) into shared memory in
+//                the 128B-swizzled K-major layout the MMA reads.
 // The output O accumulates in TMEM across chunks (S0 O0 S1 O1, 128 columns
 // each).  The running max used for P only moves when a chunk's max exceeds
 // it by more than 2^8; then the warp rescales its O rows in TMEM before the
@@ -46,7 +46,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 320;   // warps 0-7 softmax, 8 TMA, 9 MMA
 constexpr uint32_t kHalfBytes = 16384;           // 128 rows x 128 B
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 128 x 128 bf16
 constexpr int kSlots = 3;                        // K/V ring
@@ -171,13 +171,13 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     mbar_init(&bars.done, 1);
     mbar_fence_init();
   }
-  if (warp == 1) tmem_alloc(&tmem_base_sh, kTmemCols);
+  if (warp == 9) tmem_alloc(&tmem_base_sh, kTmemCols);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     prefetch_tmap(&qmap);
     prefetch_tmap(&kmap);
@@ -207,7 +207,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       for (int i = (issued > kSlots ? issued - kSlots : 0); i < issued; ++i)
         mbar_wait(&bars.kv_full[i % kSlots], (uint32_t)(i / kSlots) & 1);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 9 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
     const uint32_t idO = idesc_bf16_f32(128, 128, false, true);
@@ -271,11 +271,11 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     }
     if (ok) mma_commit(&bars.done);
     else abort_sh = 1;
-  } else if (warp >= 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax rows
-    const int t = (warp - 4) >> 2;                 // tile
-    const int row_in_tile = threadIdx.x - 128 - t * 128;
-    const uint32_t lane_off = (uint32_t)(((warp - 4) & 3) * 32) << 16;
+    const int t = warp >> 2;                       // tile
+    const int row_in_tile = threadIdx.x - t * 128;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + t * 256 + lane_off;
     const uint32_t tO = tS + 128;
     const float sc = p.scale_log2 * (p.k_scale ? p.k_scale[g] : 1.f);
@@ -285,16 +285,15 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     for (int c = 0; c < nchunks; ++c) {
       if (!warp_wait(&bars.s_full[t], c & 1)) { ok = false; break; }
       fence_after_sync();
-      // pass 1: the chunk's row max (scores stay in TMEM)
+      // pass 1: the chunk's row max (one 128-column TMEM load)
       const int nvalid = min(128, k1 - (k0 + c * 128));
       float mx = -INFINITY;
+      {
+        float sv[128];
+        tmem_ld128(tS, sv);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float v[32];
-        tmem_ld32(tS + q * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (q * 32 + i < nvalid) mx = fmaxf(mx, v[i]);
+        for (int i = 0; i < 128; ++i)
+          if (i < nvalid) mx = fmaxf(mx, sv[i]);
       }
       mx *= sc;
       const bool need = mx > m_used + kRescale;
@@ -317,16 +316,16 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       }
       // pass 2: P = 2^(s - m) as bf16 into the swizzled K-major tile
       float sum = 0.f;
+      float sv[128];
+      tmem_ld128(tS, sv);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        float v[32];
-        tmem_ld32(tS + q * 32, v);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int k2 = q * 32 + 2 * i;
-          const float p0 = (k2 < nvalid) ? ex2(fmaf(v[2 * i], sc, -m_used)) : 0.f;
-          const float p1 = (k2 + 1 < nvalid) ? ex2(fmaf(v[2 * i + 1], sc, -m_used)) : 0.f;
+          const float p0 = (k2 < nvalid) ? ex2(fmaf(sv[k2], sc, -m_used)) : 0.f;
+          const float p1 = (k2 + 1 < nvalid) ? ex2(fmaf(sv[k2 + 1], sc, -m_used)) : 0.f;
           sum += p0 + p1;
           const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
           pk[i] = *reinterpret_cast<const uint32_t*>(&b);
@@ -373,7 +372,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   fence_before_sync();
   __syncthreads();
   if (abort_sh && threadIdx.x == 0) set_status(p.hdr, BEAMDEC_ERR_TIMEOUT);
-  if (warp == 1) {
+  if (warp == 9) {
     fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }

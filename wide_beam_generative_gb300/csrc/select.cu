@@ -53,6 +53,7 @@ struct SelState {
   int32_t pad[6];
 };
 static_assert(sizeof(SelState) == 64, "state size");
+static_assert(4096 % 512 == 0, "tail bins per thread");
 
 struct SelWs {
   WsHeader* hdr;
@@ -427,27 +428,33 @@ __device__ __forceinline__ int block_excl_scan(int x, int* warp_tmp, int* total)
   return base + incl - x;
 }
 
-// Appends to keys[] (up to cap) every pool key for which pred(key) holds,
+// Appends to keys[] (up to cap) every pool key that passes the predicate:
+// by_bin: score_bin(ref, score) <= dbin; otherwise (key >> shift) <= prefix.
 // 8 keys per thread per round so the loads of a round are all in flight.
-// Returns the number of keys that satisfied pred (may exceed cap).
-template <class Pred>
-__device__ int block_gather(const unsigned long long* pool, int total, Pred pred,
+// Returns the number of keys that passed (may exceed cap).
+__device__ int block_gather(const unsigned long long* pool, int total, bool by_bin, float ref,
+                            int dbin, int shift, unsigned long long prefix,
                             unsigned long long* keys, int cap, ExpandShared& sh) {
   constexpr int kPer = 8;
   int count = 0;
   for (int base = 0; base < total; base += kPer * (int)blockDim.x) {
     unsigned long long v[kPer];
-    int c = 0;
-    uint32_t fl = 0;
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int i = base + u * (int)blockDim.x + (int)threadIdx.x;
       v[u] = i < total ? __ldcg(pool + i) : 0ull;
     }
+    int c = 0;
+    uint32_t fl = 0;
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int i = base + u * (int)blockDim.x + (int)threadIdx.x;
-      if (i < total && pred(v[u])) { fl |= 1u << u; ++c; }
+      bool pass = false;
+      if (i < total) {
+        if (by_bin) pass = score_bin(ref, desc_key_value((uint32_t)(v[u] >> 32))) <= dbin;
+        else pass = (v[u] >> shift) <= prefix;
+      }
+      if (pass) { fl |= 1u << u; ++c; }
     }
     int tot;
     int pos = count + block_excl_scan(c, sh.warp_cnt, &tot);
@@ -475,25 +482,30 @@ __device__ void rank_sort(const unsigned long long* src, int n, int nt, unsigned
   __syncthreads();
 }
 
-// Block-wide: the bin holding the need-th key (1-based) of a global
-// histogram of nbins (a multiple of blockDim.x); *below = keys in lower bins.
-__device__ void block_find_bin(const uint32_t* gh, int nbins, uint32_t need, ExpandShared& sh,
-                               int* bin, uint32_t* below) {
-  const int per = nbins / blockDim.x;
-  uint32_t c[16];
+// Block-wide: the bin holding the need-th key (1-based) of the request's
+// kTailBins-bin global histogram; *below = keys in lower bins.
+__device__ void block_find_bin(const uint32_t* gh, uint32_t need, ExpandShared& sh, int* bin,
+                               uint32_t* below) {
+  constexpr int kPer = kTailBins / kExpandThreads;   // 8 bins per thread
+  uint32_t c[kPer];
   int sum = 0;
-  for (int i = 0; i < per && i < 16; ++i) {
-    c[i] = __ldcg(gh + threadIdx.x * per + i);
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    c[i] = __ldcg(gh + threadIdx.x * kPer + i);
     sum += (int)c[i];
   }
   int tot;
   const int excl = block_excl_scan(sum, sh.warp_cnt, &tot);
   if ((uint32_t)excl < need && need <= (uint32_t)(excl + sum)) {
     uint32_t acc = (uint32_t)excl;
-    int d = threadIdx.x * per;
-    for (int i = 0; i < per && i < 16; ++i) {
-      if (acc + c[i] >= need) { d = threadIdx.x * per + i; break; }
-      acc += c[i];
+    int d = threadIdx.x * kPer + kPer - 1;
+    bool found = false;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      if (!found) {
+        if (acc + c[i] >= need) { d = threadIdx.x * kPer + i; found = true; }
+        else acc += c[i];
+      }
     }
     sh.digit = (uint32_t)d;
     sh.below = acc;
@@ -512,6 +524,10 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
   const int total = st->total;
   const int nt = total < a.W ? total : a.W;
   const unsigned long long* pool = ws.pool + (size_t)r * a.W * a.Kp;
+  if ((reinterpret_cast<uintptr_t>(keys) & 15u) || (reinterpret_cast<uintptr_t>(pool) & 7u)) {
+    if (threadIdx.x == 0) set_status(ws.hdr, BEAMDEC_ERR_DEVICE_CHECK);   // never expected
+    return;
+  }
   int nc = -1;
   if (total <= kTailCap) {
     for (int i = threadIdx.x; i < total; i += blockDim.x) keys[i] = __ldcg(pool + i);
@@ -521,13 +537,11 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
     // before taking its ticket) brackets the nt-th best score
     int dbin;
     uint32_t below;
-    block_find_bin(ws.hist + (size_t)r * kBins, kTailBins, (uint32_t)nt, sh, &dbin, &below);
+    block_find_bin(ws.hist + (size_t)r * kBins, (uint32_t)nt, sh, &dbin, &below);
     const uint32_t c_le = below + __ldcg(ws.hist + (size_t)r * kBins + dbin);
     if (c_le <= (uint32_t)kTailCap) {
       const float ref = a.cum_in[(size_t)r * a.W];
-      const int got = block_gather(pool, total, [&](unsigned long long k) {
-        return score_bin(ref, desc_key_value((uint32_t)(k >> 32))) <= dbin;
-      }, keys, kTailCap, sh);
+      const int got = block_gather(pool, total, true, ref, dbin, 0, 0ull, keys, kTailCap, sh);
       nc = got < kTailCap ? got : kTailCap;
     } else {
       // many equal-looking scores: radix narrowing over the pool
@@ -538,9 +552,7 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
         in_bin = narrow_pass<true>(pool, total, prefix, shift, need, sure, sh);
         if (sure + in_bin <= (uint32_t)kTailCap || shift == 0) break;
       }
-      const int got = block_gather(pool, total, [&](unsigned long long k) {
-        return (k >> shift) <= prefix;
-      }, keys, kTailCap, sh);
+      const int got = block_gather(pool, total, false, 0.f, 0, shift, prefix, keys, kTailCap, sh);
       nc = got < kTailCap ? got : kTailCap;
     }
   }
