@@ -53,7 +53,6 @@ struct SelState {
   int32_t pad[6];
 };
 static_assert(sizeof(SelState) == 64, "state size");
-static_assert(4096 % 512 == 0, "tail bins per thread");
 
 struct SelWs {
   WsHeader* hdr;
@@ -407,115 +406,6 @@ __device__ uint32_t narrow_pass(const unsigned long long* keys, int n, unsigned 
   return in_bin;
 }
 
-// Block-wide exclusive prefix sum of one int per thread; *total = block sum.
-__device__ __forceinline__ int block_excl_scan(int x, int* warp_tmp, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int incl = x;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_tmp[warp] = incl;
-  __syncthreads();
-  int base = 0, tot = 0;
-  for (int w = 0; w < nw; ++w) {
-    const int c = warp_tmp[w];
-    if (w < warp) base += c;
-    tot += c;
-  }
-  __syncthreads();
-  *total = tot;
-  return base + incl - x;
-}
-
-// Appends to keys[] (up to cap) every pool key that passes the predicate:
-// by_bin: score_bin(ref, score) <= dbin; otherwise (key >> shift) <= prefix.
-// 8 keys per thread per round so the loads of a round are all in flight.
-// Returns the number of keys that passed (may exceed cap).
-__device__ int block_gather(const unsigned long long* pool, int total, bool by_bin, float ref,
-                            int dbin, int shift, unsigned long long prefix,
-                            unsigned long long* keys, int cap, ExpandShared& sh) {
-  constexpr int kPer = 8;
-  int count = 0;
-  for (int base = 0; base < total; base += kPer * (int)blockDim.x) {
-    unsigned long long v[kPer];
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int i = base + u * (int)blockDim.x + (int)threadIdx.x;
-      v[u] = i < total ? __ldcg(pool + i) : 0ull;
-    }
-    int c = 0;
-    uint32_t fl = 0;
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int i = base + u * (int)blockDim.x + (int)threadIdx.x;
-      bool pass = false;
-      if (i < total) {
-        if (by_bin) pass = score_bin(ref, desc_key_value((uint32_t)(v[u] >> 32))) <= dbin;
-        else pass = (v[u] >> shift) <= prefix;
-      }
-      if (pass) { fl |= 1u << u; ++c; }
-    }
-    int tot;
-    int pos = count + block_excl_scan(c, sh.warp_cnt, &tot);
-#pragma unroll
-    for (int u = 0; u < kPer; ++u)
-      if (fl & (1u << u)) {
-        if (pos < cap) keys[pos] = v[u];
-        ++pos;
-      }
-    count += tot;
-  }
-  __syncthreads();
-  return count;
-}
-
-// Writes the nt smallest of the n distinct keys src[0..n) to dst[0..nt) in
-// ascending order: each key's rank is the count of smaller keys.
-__device__ void rank_sort(const unsigned long long* src, int n, int nt, unsigned long long* dst) {
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const unsigned long long k = src[i];
-    int rank = 0;
-    for (int m = 0; m < n; ++m) rank += src[m] < k;
-    if (rank < nt) dst[rank] = k;
-  }
-  __syncthreads();
-}
-
-// Block-wide: the bin holding the need-th key (1-based) of the request's
-// kTailBins-bin global histogram; *below = keys in lower bins.
-__device__ void block_find_bin(const uint32_t* gh, uint32_t need, ExpandShared& sh, int* bin,
-                               uint32_t* below) {
-  constexpr int kPer = kTailBins / kExpandThreads;   // 8 bins per thread
-  uint32_t c[kPer];
-  int sum = 0;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    c[i] = __ldcg(gh + threadIdx.x * kPer + i);
-    sum += (int)c[i];
-  }
-  int tot;
-  const int excl = block_excl_scan(sum, sh.warp_cnt, &tot);
-  if ((uint32_t)excl < need && need <= (uint32_t)(excl + sum)) {
-    uint32_t acc = (uint32_t)excl;
-    int d = threadIdx.x * kPer + kPer - 1;
-    bool found = false;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      if (!found) {
-        if (acc + c[i] >= need) { d = threadIdx.x * kPer + i; found = true; }
-        else acc += c[i];
-      }
-    }
-    sh.digit = (uint32_t)d;
-    sh.below = acc;
-  }
-  __syncthreads();
-  *bin = (int)sh.digit;
-  *below = sh.below;
-  __syncthreads();
-}
-
 // Fused a4 for one request, run by the last expand block of the request:
 // select the min(W, pool) smallest pool keys, sort them, emit outputs.
 __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs& ws, int r,
@@ -524,47 +414,74 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
   const int total = st->total;
   const int nt = total < a.W ? total : a.W;
   const unsigned long long* pool = ws.pool + (size_t)r * a.W * a.Kp;
-  if ((reinterpret_cast<uintptr_t>(keys) & 15u) || (reinterpret_cast<uintptr_t>(pool) & 7u)) {
-    if (threadIdx.x == 0) set_status(ws.hdr, BEAMDEC_ERR_DEVICE_CHECK);   // never expected
-    return;
-  }
-  int nc = -1;
+  int nc;
   if (total <= kTailCap) {
     for (int i = threadIdx.x; i < total; i += blockDim.x) keys[i] = __ldcg(pool + i);
     nc = total;
   } else {
     // the request's score-bin histogram (complete: every block flushed it
     // before taking its ticket) brackets the nt-th best score
-    int dbin;
-    uint32_t below;
-    block_find_bin(ws.hist + (size_t)r * kBins, (uint32_t)nt, sh, &dbin, &below);
-    const uint32_t c_le = below + __ldcg(ws.hist + (size_t)r * kBins + dbin);
+    const volatile uint32_t* gh = ws.hist + (size_t)r * kBins;
+    if (threadIdx.x < 32) warp_find_digit(gh, kTailBins, (uint32_t)nt, &sh.digit, &sh.below);
+    __syncthreads();
+    const int Dbin = (int)sh.digit;
+    const uint32_t c_le = sh.below + gh[Dbin];
+    __syncthreads();
     if (c_le <= (uint32_t)kTailCap) {
       const float ref = a.cum_in[(size_t)r * a.W];
-      const int got = block_gather(pool, total, true, ref, dbin, 0, 0ull, keys, kTailCap, sh);
-      nc = got < kTailCap ? got : kTailCap;
-    } else {
-      // many equal-looking scores: radix narrowing over the pool
-      unsigned long long prefix = 0;
-      int shift = 64;
-      uint32_t need = (uint32_t)nt, sure = 0, in_bin = 0;
-      while (true) {
-        in_bin = narrow_pass<true>(pool, total, prefix, shift, need, sure, sh);
-        if (sure + in_bin <= (uint32_t)kTailCap || shift == 0) break;
+      if (threadIdx.x == 0) sh.count = 0;
+      __syncthreads();
+      for (int c0 = 0; c0 < total; c0 += blockDim.x) {
+        const int i = c0 + threadIdx.x;
+        unsigned long long k = 0;
+        int flag = 0;
+        if (i < total) {
+          k = __ldcg(pool + i);
+          flag = score_bin(ref, desc_key_value((uint32_t)(k >> 32))) <= Dbin;
+        }
+        int tot;
+        const int rk = block_rank(flag, sh.warp_cnt, &tot);
+        const int pos = sh.count + rk;
+        if (flag && pos < kTailCap) keys[pos] = k;
+        __syncthreads();
+        if (threadIdx.x == 0) sh.count += tot;
+        __syncthreads();
       }
-      const int got = block_gather(pool, total, false, 0.f, 0, shift, prefix, keys, kTailCap, sh);
-      nc = got < kTailCap ? got : kTailCap;
+      nc = sh.count < kTailCap ? sh.count : kTailCap;
+      goto selected;
     }
   }
-  __syncthreads();
-  constexpr int kRankMax = kTailCap / 4;   // 1024
-  unsigned long long* sorted = keys + kTailCap / 2;
-  if (nc <= kRankMax) {   // small candidate sets: rank directly
-    rank_sort(keys, nc, nt, sorted);
-    emit_outputs(a, ws, r, sorted, nt);
-    return;
+  if (total > kTailCap) {
+    unsigned long long prefix = 0;
+    int shift = 64;
+    uint32_t need = (uint32_t)nt, sure = 0, in_bin = 0;
+    while (true) {
+      in_bin = narrow_pass<true>(pool, total, prefix, shift, need, sure, sh);
+      if (sure + in_bin <= (uint32_t)kTailCap || shift == 0) break;
+    }
+    if (threadIdx.x == 0) sh.count = 0;
+    __syncthreads();
+    for (int c0 = 0; c0 < total; c0 += blockDim.x) {
+      const int i = c0 + threadIdx.x;
+      unsigned long long k = 0;
+      int flag = 0;
+      if (i < total) {
+        k = __ldcg(pool + i);
+        flag = (k >> shift) <= prefix;
+      }
+      int tot;
+      const int rk = block_rank(flag, sh.warp_cnt, &tot);
+      const int pos = sh.count + rk;
+      if (flag && pos < kTailCap) keys[pos] = k;
+      __syncthreads();
+      if (threadIdx.x == 0) sh.count += tot;
+      __syncthreads();
+    }
+    nc = sh.count < kTailCap ? sh.count : kTailCap;
   }
-  {   // exact threshold: narrow until the keys at or below it number nt
+selected:
+  __syncthreads();
+  if (nc > nt) {   // exact threshold: narrow until the keys at or below it number nt
     unsigned long long prefix = 0;
     int shift = 64;
     uint32_t need = (uint32_t)nt, sure = 0;
@@ -591,11 +508,6 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
       __syncthreads();
     }
   }
-  if (nt <= kRankMax) {
-    rank_sort(keys, nt, nt, sorted);
-    emit_outputs(a, ws, r, sorted, nt);
-    return;
-  }
   int np = 32;
   while (np < nt) np <<= 1;
   for (int i = nt + threadIdx.x; i < np; i += blockDim.x) keys[i] = ~0ull;
@@ -605,7 +517,7 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
 }
 
 template <bool kFused>
-__global__ void __launch_bounds__(kExpandThreads, 4)
+__global__ void __launch_bounds__(kExpandThreads)
 bd_expand_kernel(SelectArgs a) {
   __shared__ ExpandShared sh;
   extern __shared__ __align__(16) unsigned char tail_smem[];
