@@ -19,6 +19,9 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "attn_common.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -38,6 +41,60 @@ __device__ __forceinline__ void load_lane(const void* base, size_t e, float (&x)
     if (e == e4) { x[0] = v.x; x[1] = v.y; } else { x[0] = v.z; x[1] = v.w; }
   }
 }
+
+
+// Raw storage of PL consecutive K/V elements of one lane, kept packed in
+// 32-bit words until use (bf16: 2 per word, e4m3: 4 per word, fp32: 1).
+template <int DT, int PL>
+struct KvRaw {
+  static constexpr int kWords = DT == 0 ? PL : (DT == 1 ? (PL + 1) / 2 : 1);
+  uint32_t w[kWords];
+  __device__ __forceinline__ void load(const void* base, size_t e) {
+    if constexpr (DT == 0) {
+      if constexpr (PL == 4) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + e));
+        w[0] = __float_as_uint(v.x); w[1] = __float_as_uint(v.y);
+        w[2] = __float_as_uint(v.z); w[3] = __float_as_uint(v.w);
+      } else {
+        const float2 v = __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(base) + e));
+        w[0] = __float_as_uint(v.x); w[1] = __float_as_uint(v.y);
+      }
+    } else if constexpr (DT == 1) {
+      if constexpr (PL == 4) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + e));
+        w[0] = v.x; w[1] = v.y;
+      } else {
+        w[0] = __ldg(reinterpret_cast<const unsigned int*>(static_cast<const __nv_bfloat16*>(base) + e));
+      }
+    } else {
+      if constexpr (PL == 4) {
+        w[0] = __ldg(reinterpret_cast<const unsigned int*>(static_cast<const uint8_t*>(base) + e));
+      } else {
+        w[0] = __ldg(reinterpret_cast<const unsigned short*>(static_cast<const uint8_t*>(base) + e));
+      }
+    }
+  }
+  __device__ __forceinline__ void to_float(float (&x)[PL]) const {
+    if constexpr (DT == 0) {
+#pragma unroll
+      for (int i = 0; i < PL; ++i) x[i] = __uint_as_float(w[i]);
+    } else if constexpr (DT == 1) {
+#pragma unroll
+      for (int i = 0; i < PL / 2; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < PL / 2; ++i) {
+        const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((w[0] >> (16 * i)) & 0xffffu);
+        const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3)));
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+      }
+    }
+  }
+};
 
 template <int DQ, int DKV, int D>
 __device__ __forceinline__ void store_lane(void* out, size_t e, const float (&v)[D / 32], int out_dtype) {
@@ -61,7 +118,7 @@ __global__ void __launch_bounds__(256, 3)
 bd_attn_merge_kernel(AttnArgs a, int n_split, AttnPartials part) {
   constexpr int PL = D / 32;
   constexpr int kGq = 2;           // query heads per pass
-  constexpr int kTok = PL == 4 ? 2 : 4;   // unshared tokens whose K/V loads are in flight together
+  constexpr int kTok = 4;          // unshared tokens whose K/V loads are in flight together
   const int lane = threadIdx.x & 31;
   const int G = a.Hq / a.Hkv;
   const int rows = a.W * G;
@@ -131,7 +188,7 @@ bd_attn_merge_kernel(AttnArgs a, int n_split, AttnPartials part) {
     // unshared stage
     for (int t0 = 0; t0 < L; t0 += kTok) {
       int slot[kTok];
-      float k[kTok][PL], v[kTok][PL];
+      KvRaw<DKV, PL> kr[kTok], vr[kTok];
 #pragma unroll
       for (int w = 0; w < kTok; ++w) {
         const int t = t0 + w;
@@ -147,25 +204,28 @@ bd_attn_merge_kernel(AttnArgs a, int n_split, AttnPartials part) {
         slot[w] = sl;
         if (sl >= 0) {
           const size_t e = (((size_t)r * TW + sl) * a.Hkv + g) * D + lane * PL;
-          load_lane<DKV, PL>(a.unshared_k, e, k[w]);
-          load_lane<DKV, PL>(a.unshared_v, e, v[w]);
+          kr[w].load(a.unshared_k, e);
+          vr[w].load(a.unshared_v, e);
         }
       }
 #pragma unroll
       for (int w = 0; w < kTok; ++w) {
         if (slot[w] < 0) continue;
+        float k[PL], v[PL];
+        kr[w].to_float(k);
+        vr[w].to_float(v);
 #pragma unroll
         for (int u = 0; u < kGq; ++u) {
           if (u >= ng) continue;
           float sdot = 0.f;
 #pragma unroll
-          for (int i = 0; i < PL; ++i) sdot = fmaf(q[u][i], k[w][i], sdot);
+          for (int i = 0; i < PL; ++i) sdot = fmaf(q[u][i], k[i], sdot);
           sdot = warp_sum(sdot);
           const float mn = fmaxf(m[u], sdot);
           const float alpha = ex2(m[u] - mn), pt = ex2(sdot - mn);
           l[u] = l[u] * alpha + pt;
 #pragma unroll
-          for (int i = 0; i < PL; ++i) o[u][i] = fmaf(pt, v[w][i], o[u][i] * alpha);
+          for (int i = 0; i < PL; ++i) o[u][i] = fmaf(pt, v[i], o[u][i] * alpha);
           m[u] = mn;
         }
       }

@@ -291,9 +291,14 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       {
         float sv[128];
         tmem_ld128(tS, sv);
+        float mq[8];   // eight independent max chains
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mq[u] = -INFINITY;
 #pragma unroll
         for (int i = 0; i < 128; ++i)
-          if (i < nvalid) mx = fmaxf(mx, sv[i]);
+          if (i < nvalid) mq[i & 7] = fmaxf(mq[i & 7], sv[i]);
+        mx = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
+                   fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
       }
       mx *= sc;
       const bool need = mx > m_used + kRescale;
@@ -315,7 +320,9 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         m_used = m_new;
       }
       // pass 2: P = 2^(s - m) as bf16 into the swizzled K-major tile
-      float sum = 0.f;
+      float sq[8];   // eight independent sum chains
+#pragma unroll
+      for (int u = 0; u < 8; ++u) sq[u] = 0.f;
       float sv[128];
       tmem_ld128(tS, sv);
 #pragma unroll
@@ -326,7 +333,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
           const int k2 = q * 32 + 2 * i;
           const float p0 = (k2 < nvalid) ? ex2(fmaf(sv[k2], sc, -m_used)) : 0.f;
           const float p1 = (k2 + 1 < nvalid) ? ex2(fmaf(sv[k2 + 1], sc, -m_used)) : 0.f;
-          sum += p0 + p1;
+          sq[i & 7] += p0 + p1;
           const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
           pk[i] = *reinterpret_cast<const uint32_t*>(&b);
         }
@@ -339,7 +346,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
           *dst = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
       }
-      l += sum;
+      l += ((sq[0] + sq[1]) + (sq[2] + sq[3])) + ((sq[4] + sq[5]) + (sq[6] + sq[7]));
       fence_before_sync();
       mbar_arrive(&bars.s_free[t]);
       fence_proxy_async_smem();

@@ -165,26 +165,22 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
     const int nvec = vec ? (a.V >> 2) : 0;
     const float4* row4 = reinterpret_cast<const float4*>(row);
     int i = tid;
-    for (; i + 3 * kExpandThreads < nvec; i += 4 * kExpandThreads) {
-      float4 v0 = __ldg(row4 + i);
-      float4 v1 = __ldg(row4 + i + kExpandThreads);
-      float4 v2 = __ldg(row4 + i + 2 * kExpandThreads);
-      float4 v3 = __ldg(row4 + i + 3 * kExpandThreads);
-      float mx = fmaxf(fmaxf(fmaxf(v0.x, v0.y), fmaxf(v0.z, v0.w)),
-                       fmaxf(fmaxf(v1.x, v1.y), fmaxf(v1.z, v1.w)));
-      mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(v2.x, v2.y), fmaxf(v2.z, v2.w)),
-                           fmaxf(fmaxf(v3.x, v3.y), fmaxf(v3.z, v3.w))));
+    for (; i + 7 * kExpandThreads < nvec; i += 8 * kExpandThreads) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldg(row4 + i + u * kExpandThreads);
+      float mx = m;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        mx = fmaxf(mx, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
       if (mx > m) { s *= ex2((m - mx) * kLog2e); m = mx; }
       const float mL = m * kLog2e;
-      float t0 = ex2(fmaf(v0.x, kLog2e, -mL)) + ex2(fmaf(v0.y, kLog2e, -mL)) +
-                 ex2(fmaf(v0.z, kLog2e, -mL)) + ex2(fmaf(v0.w, kLog2e, -mL));
-      float t1 = ex2(fmaf(v1.x, kLog2e, -mL)) + ex2(fmaf(v1.y, kLog2e, -mL)) +
-                 ex2(fmaf(v1.z, kLog2e, -mL)) + ex2(fmaf(v1.w, kLog2e, -mL));
-      float t2 = ex2(fmaf(v2.x, kLog2e, -mL)) + ex2(fmaf(v2.y, kLog2e, -mL)) +
-                 ex2(fmaf(v2.z, kLog2e, -mL)) + ex2(fmaf(v2.w, kLog2e, -mL));
-      float t3 = ex2(fmaf(v3.x, kLog2e, -mL)) + ex2(fmaf(v3.y, kLog2e, -mL)) +
-                 ex2(fmaf(v3.z, kLog2e, -mL)) + ex2(fmaf(v3.w, kLog2e, -mL));
-      s += (t0 + t1) + (t2 + t3);
+      float t[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        t[u] = (ex2(fmaf(v[u].x, kLog2e, -mL)) + ex2(fmaf(v[u].y, kLog2e, -mL))) +
+               (ex2(fmaf(v[u].z, kLog2e, -mL)) + ex2(fmaf(v[u].w, kLog2e, -mL)));
+      s += ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
     }
     for (; i < nvec; i += kExpandThreads) {
       float4 v = __ldg(row4 + i);
@@ -376,6 +372,18 @@ __device__ void emit_outputs(const SelectArgs& a, const SelWs& ws, int r,
   if (tid == 0) a.n_live_out[r] = nt;
 }
 
+// Writes the nt smallest of the n distinct keys src[0..n) to dst[0..nt) in
+// ascending order: each key's rank is the count of smaller keys.
+__device__ void rank_sort(const unsigned long long* src, int n, int nt, unsigned long long* dst) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const unsigned long long k = src[i];
+    int rank = 0;
+    for (int m = 0; m < n; ++m) rank += src[m] < k ? 1 : 0;
+    if (rank < nt) dst[rank] = k;
+  }
+  __syncthreads();
+}
+
 // One radix-narrowing pass over `n` keys (shared or global memory): among the
 // keys whose bits above `shift` equal `prefix`, histogram the next `w` bits
 // and pick the digit holding the need-th smallest key.  Updates prefix,
@@ -481,6 +489,12 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
   }
 selected:
   __syncthreads();
+  unsigned long long* sorted = keys + kTailCap / 2;   // disjoint from keys[0..1024)
+  if (nc <= kTailCap / 4) {   // small candidate sets: rank directly
+    rank_sort(keys, nc, nt, sorted);
+    emit_outputs(a, ws, r, sorted, nt);
+    return;
+  }
   if (nc > nt) {   // exact threshold: narrow until the keys at or below it number nt
     unsigned long long prefix = 0;
     int shift = 64;
@@ -508,6 +522,11 @@ selected:
       __syncthreads();
     }
   }
+  if (nt <= kTailCap / 4) {   // winners now in keys[0..nt)
+    rank_sort(keys, nt, nt, sorted);
+    emit_outputs(a, ws, r, sorted, nt);
+    return;
+  }
   int np = 32;
   while (np < nt) np <<= 1;
   for (int i = nt + threadIdx.x; i < np; i += blockDim.x) keys[i] = ~0ull;
@@ -517,7 +536,7 @@ selected:
 }
 
 template <bool kFused>
-__global__ void __launch_bounds__(kExpandThreads)
+__global__ void __launch_bounds__(kExpandThreads, 3)
 bd_expand_kernel(SelectArgs a) {
   __shared__ ExpandShared sh;
   extern __shared__ __align__(16) unsigned char tail_smem[];
