@@ -285,20 +285,27 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     for (int c = 0; c < nchunks; ++c) {
       if (!warp_wait(&bars.s_full[t], c & 1)) { ok = false; break; }
       fence_after_sync();
-      // pass 1: the chunk's row max (one 128-column TMEM load)
+      // pass 1: the chunk's row max (one 128-column TMEM load); only the last
+      // chunk of a split can hold fewer than 128 keys, so the full case runs
+      // without per-element masks
       const int nvalid = min(128, k1 - (k0 + c * 128));
+      const bool full = nvalid == 128;
       float mx = -INFINITY;
       {
         float sv[128];
         tmem_ld128(tS, sv);
-        float mq[8];   // eight independent max chains
+        if (full) {   // pairwise tree: depth 7 instead of a 128-long chain
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mq[u] = -INFINITY;
+          for (int w = 64; w >= 1; w >>= 1) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i < nvalid) mq[i & 7] = fmaxf(mq[i & 7], sv[i]);
-        mx = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
-                   fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
+            for (int i = 0; i < w; ++i) sv[i] = fmaxf(sv[i], sv[i + w]);
+          }
+          mx = sv[0];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i < nvalid) mx = fmaxf(mx, sv[i]);
+        }
       }
       mx *= sc;
       const bool need = mx > m_used + kRescale;
@@ -320,20 +327,26 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         m_used = m_new;
       }
       // pass 2: P = 2^(s - m) as bf16 into the swizzled K-major tile
-      float sq[8];   // eight independent sum chains
-#pragma unroll
-      for (int u = 0; u < 8; ++u) sq[u] = 0.f;
+      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;   // four independent chains
       float sv[128];
       tmem_ld128(tS, sv);
+      if (!full) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= nvalid) sv[i] = -INFINITY;
+      }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int k2 = q * 32 + 2 * i;
-          const float p0 = (k2 < nvalid) ? ex2(fmaf(sv[k2], sc, -m_used)) : 0.f;
-          const float p1 = (k2 + 1 < nvalid) ? ex2(fmaf(sv[k2 + 1], sc, -m_used)) : 0.f;
-          sq[i & 7] += p0 + p1;
+          const float p0 = ex2(fmaf(sv[k2], sc, -m_used));
+          const float p1 = ex2(fmaf(sv[k2 + 1], sc, -m_used));
+          if ((i & 3) == 0) sum0 += p0 + p1;
+          else if ((i & 3) == 1) sum1 += p0 + p1;
+          else if ((i & 3) == 2) sum2 += p0 + p1;
+          else sum3 += p0 + p1;
           const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
           pk[i] = *reinterpret_cast<const uint32_t*>(&b);
         }
@@ -346,7 +359,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
           *dst = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
       }
-      l += ((sq[0] + sq[1]) + (sq[2] + sq[3])) + ((sq[4] + sq[5]) + (sq[6] + sq[7]));
+      l += (sum0 + sum1) + (sum2 + sum3);
       fence_before_sync();
       mbar_arrive(&bars.s_free[t]);
       fence_proxy_async_smem();

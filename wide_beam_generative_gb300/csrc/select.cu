@@ -128,6 +128,7 @@ __device__ __forceinline__ int block_rank(int flag, int* warp_cnt, int* total) {
 // [0, 4095].  It is monotone (a higher score never gets a higher bin), so a
 // request-wide histogram of bins brackets the W-th best score from one count.
 constexpr int kTailBins = 4096;
+constexpr int kKeyCache = 4096;   // children whose 32-bit keys a block caches in shared memory
 __device__ __forceinline__ int score_bin(float ref, float s) {
   const float u = __fmul_rn(__fsub_rn(ref, s), 64.f);
   if (!(u > 0.f)) return 0;
@@ -149,7 +150,7 @@ struct ExpandShared {
 // Rows a1-a3 for beam b of request r: log-sum-exp, trie children, per-beam
 // top_k appended to the request's pool.
 __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
-                                                 int r, int b, uint32_t* bins) {
+                                                 int r, int b, uint32_t* bins, uint32_t* kcache) {
   const int tid = threadIdx.x;
   const int Kp = a.Kp;
   const size_t rowi = (size_t)r * a.W + b;
@@ -165,22 +166,26 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
     const int nvec = vec ? (a.V >> 2) : 0;
     const float4* row4 = reinterpret_cast<const float4*>(row);
     int i = tid;
-    for (; i + 7 * kExpandThreads < nvec; i += 8 * kExpandThreads) {
-      float4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = __ldg(row4 + i + u * kExpandThreads);
-      float mx = m;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        mx = fmaxf(mx, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
+    for (; i + 3 * kExpandThreads < nvec; i += 4 * kExpandThreads) {
+      float4 v0 = __ldg(row4 + i);
+      float4 v1 = __ldg(row4 + i + kExpandThreads);
+      float4 v2 = __ldg(row4 + i + 2 * kExpandThreads);
+      float4 v3 = __ldg(row4 + i + 3 * kExpandThreads);
+      float mx = fmaxf(fmaxf(fmaxf(v0.x, v0.y), fmaxf(v0.z, v0.w)),
+                       fmaxf(fmaxf(v1.x, v1.y), fmaxf(v1.z, v1.w)));
+      mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(v2.x, v2.y), fmaxf(v2.z, v2.w)),
+                           fmaxf(fmaxf(v3.x, v3.y), fmaxf(v3.z, v3.w))));
       if (mx > m) { s *= ex2((m - mx) * kLog2e); m = mx; }
       const float mL = m * kLog2e;
-      float t[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        t[u] = (ex2(fmaf(v[u].x, kLog2e, -mL)) + ex2(fmaf(v[u].y, kLog2e, -mL))) +
-               (ex2(fmaf(v[u].z, kLog2e, -mL)) + ex2(fmaf(v[u].w, kLog2e, -mL)));
-      s += ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+      float t0 = ex2(fmaf(v0.x, kLog2e, -mL)) + ex2(fmaf(v0.y, kLog2e, -mL)) +
+                 ex2(fmaf(v0.z, kLog2e, -mL)) + ex2(fmaf(v0.w, kLog2e, -mL));
+      float t1 = ex2(fmaf(v1.x, kLog2e, -mL)) + ex2(fmaf(v1.y, kLog2e, -mL)) +
+                 ex2(fmaf(v1.z, kLog2e, -mL)) + ex2(fmaf(v1.w, kLog2e, -mL));
+      float t2 = ex2(fmaf(v2.x, kLog2e, -mL)) + ex2(fmaf(v2.y, kLog2e, -mL)) +
+                 ex2(fmaf(v2.z, kLog2e, -mL)) + ex2(fmaf(v2.w, kLog2e, -mL));
+      float t3 = ex2(fmaf(v3.x, kLog2e, -mL)) + ex2(fmaf(v3.y, kLog2e, -mL)) +
+                 ex2(fmaf(v3.z, kLog2e, -mL)) + ex2(fmaf(v3.w, kLog2e, -mL));
+      s += (t0 + t1) + (t2 + t3);
     }
     for (; i < nvec; i += kExpandThreads) {
       float4 v = __ldg(row4 + i);
@@ -263,6 +268,14 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
     }
     return;
   }
+  // the row's candidate keys, computed once into shared memory when they fit
+  // (the radix passes below then read shared memory instead of re-gathering)
+  const bool cached = kcache != nullptr && n <= kKeyCache;
+  if (cached) {
+    for (int i = tid; i < n; i += kExpandThreads) kcache[i] = key_of(tok_of(i));
+    __syncthreads();
+  }
+  auto kc = [&](int i) -> uint32_t { return cached ? kcache[i] : key_of(tok_of(i)); };
   // radix select of the K-th smallest 32-bit score key: digits of 11, 11, 10 bits
   uint32_t prefix = 0, need = (uint32_t)a.K;
   const int widths[3] = {11, 11, 10};
@@ -274,7 +287,7 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
     for (int i = tid; i < nb; i += kExpandThreads) sh.hist[i] = 0;
     __syncthreads();
     for (int i = tid; i < n; i += kExpandThreads) {
-      const uint32_t k = key_of(tok_of(i));
+      const uint32_t k = kc(i);
       if (shift == 32 || (k >> shift) == (prefix >> shift))
         atomicAdd(&sh.hist[(k >> sh_next) & (nb - 1)], 1u);
     }
@@ -291,7 +304,7 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
   __syncthreads();
   const int base = sh.pool_base;
   for (int i = tid; i < n; i += kExpandThreads) {
-    const uint32_t k = key_of(tok_of(i));
+    const uint32_t k = kc(i);
     if (k < kth) {
       pool[base + atomicAdd(&sh.count, 1)] = pool_key(k, b, i);
       if (bins) atomicAdd(&bins[score_bin(ref, desc_key_value(k))], 1u);
@@ -303,7 +316,7 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
   for (int c0 = 0; c0 < n && taken < (int)need; c0 += kExpandThreads) {
     const int i = c0 + tid;
     int flag = 0;
-    if (i < n) flag = key_of(tok_of(i)) == kth;
+    if (i < n) flag = kc(i) == kth;
     int tot;
     const int rk = block_rank(flag, sh.warp_cnt, &tot);
     if (flag && taken + rk < (int)need) {
@@ -439,21 +452,27 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
       const float ref = a.cum_in[(size_t)r * a.W];
       if (threadIdx.x == 0) sh.count = 0;
       __syncthreads();
-      for (int c0 = 0; c0 < total; c0 += blockDim.x) {
-        const int i = c0 + threadIdx.x;
-        unsigned long long k = 0;
-        int flag = 0;
-        if (i < total) {
-          k = __ldcg(pool + i);
-          flag = score_bin(ref, desc_key_value((uint32_t)(k >> 32))) <= Dbin;
+      constexpr int kPer = 4;   // rounds of kPer x blockDim keys: the loads of a round overlap
+      for (int c0 = 0; c0 < total; c0 += kPer * blockDim.x) {
+        unsigned long long kv[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int i = c0 + u * blockDim.x + threadIdx.x;
+          kv[u] = i < total ? __ldcg(pool + i) : 0ull;
         }
-        int tot;
-        const int rk = block_rank(flag, sh.warp_cnt, &tot);
-        const int pos = sh.count + rk;
-        if (flag && pos < kTailCap) keys[pos] = k;
-        __syncthreads();
-        if (threadIdx.x == 0) sh.count += tot;
-        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int i = c0 + u * blockDim.x + threadIdx.x;
+          const int flag =
+              (i < total) && score_bin(ref, desc_key_value((uint32_t)(kv[u] >> 32))) <= Dbin;
+          int tot;
+          const int rk = block_rank(flag, sh.warp_cnt, &tot);
+          const int pos = sh.count + rk;
+          if (flag && pos < kTailCap) keys[pos] = kv[u];
+          __syncthreads();
+          if (threadIdx.x == 0) sh.count += tot;
+          __syncthreads();
+        }
       }
       nc = sh.count < kTailCap ? sh.count : kTailCap;
       goto selected;
@@ -545,13 +564,16 @@ bd_expand_kernel(SelectArgs a) {
   if (b == 0 && r == 0 && tid == 0) ws.hdr->bar_count = 0u;
   const int nl = a.n_live_in[r];
   if (b >= nl) return;
+  // dynamic shared memory: [key cache 16 KB][score-bin histogram 16 KB, fused only];
+  // the fused tail reuses all of it for candidate keys after the ticket
+  uint32_t* kcache = reinterpret_cast<uint32_t*>(tail_smem);
   uint32_t* bins = nullptr;
-  if constexpr (kFused) {   // the tail buffer holds this block's score-bin histogram until the ticket
-    bins = reinterpret_cast<uint32_t*>(tail_smem);
+  if constexpr (kFused) {
+    bins = kcache + kKeyCache;
     for (int i = tid; i < kTailBins; i += kExpandThreads) bins[i] = 0;
     __syncthreads();
   }
-  expand_candidates(a, sh, ws, r, b, bins);
+  expand_candidates(a, sh, ws, r, b, bins, kcache);
   if constexpr (kFused) {
     __syncthreads();
     uint32_t* gh = ws.hist + (size_t)r * kBins;
@@ -750,10 +772,11 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
   // expand block of each request; larger ones by the cooperative grid kernel.
   const bool fused = a.W <= kTailCap && (long long)a.W * a.Kp <= (1ll << 20);
   prof_begin(kKExpand, stream);
+  static_assert(kKeyCache * 4 + kTailBins * 4 <= kTailCap * 8, "fused dynamic shared memory");
   if (fused)
     bd_expand_kernel<true><<<g1, kExpandThreads, kTailCap * sizeof(unsigned long long), stream>>>(a);
   else
-    bd_expand_kernel<false><<<g1, kExpandThreads, 0, stream>>>(a);
+    bd_expand_kernel<false><<<g1, kExpandThreads, kKeyCache * sizeof(uint32_t), stream>>>(a);
   prof_end(kKExpand, stream);
   if (cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
   if (fused) return BEAMDEC_OK;
