@@ -44,6 +44,7 @@ struct SelectArgs {
   const int32_t* slot_in;
   bool has_trie; TrieLevel lvl;
   int level, step, R, W, K, V, T, Kp;
+  int row_splits, row_chunk;   // blocks per logits row and logits per block
   int32_t* tokens; int32_t* parents; float* cum_out; float* lse_out;
   int32_t* node_out; int32_t* n_live_out; int32_t* slot_out;
   void* ws;

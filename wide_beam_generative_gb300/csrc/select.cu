@@ -38,6 +38,7 @@ constexpr int kExpandThreads = 512;
 constexpr int kGlobalThreads = 512;
 constexpr int kDigitBits = 12;
 constexpr int kBins = 1 << kDigitBits;  // 4096
+constexpr int kMaxRowSplits = 8;         // blocks that stream one logits row together
 constexpr int kTailCap = 4096;          // keys one expand block can select in shared memory
 
 struct SelState {
@@ -57,9 +58,11 @@ static_assert(sizeof(SelState) == 64, "state size");
 struct SelWs {
   WsHeader* hdr;
   SelState* state;        // [R]
+  int32_t* rowtick;       // [R][W] finished chunk blocks per row
   uint32_t* hist;         // [R][kBins]
   unsigned long long* pool;  // [R][W*Kp]
   unsigned long long* cand;  // [R][kSelectCap]
+  float2* rowpart;        // [R][W][kMaxRowSplits] per-chunk (max, sum of exp)
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -69,9 +72,11 @@ __host__ __device__ inline SelWs carve(void* ws, int R, int W, int Kp) {
   SelWs s;
   s.hdr = (WsHeader*)p; p += kWsHeaderBytes;
   s.state = (SelState*)p; p += align256((size_t)R * sizeof(SelState));
+  s.rowtick = (int32_t*)p; p += align256((size_t)R * W * sizeof(int32_t));
   s.hist = (uint32_t*)p; p += align256((size_t)R * kBins * sizeof(uint32_t));
   s.pool = (unsigned long long*)p; p += align256((size_t)R * W * Kp * 8);
-  s.cand = (unsigned long long*)p;
+  s.cand = (unsigned long long*)p; p += align256((size_t)R * kSelectCap * 8);
+  s.rowpart = (float2*)p;
   return s;
 }
 
@@ -147,60 +152,68 @@ struct ExpandShared {
   float lse;
 };
 
-// Rows a1-a3 for beam b of request r: log-sum-exp, trie children, per-beam
-// top_k appended to the request's pool.
-__device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
-                                                 int r, int b, uint32_t* bins, uint32_t* kcache) {
+// Running (max, sum of exp(x - max)) of row[c0..c1) for the whole block,
+// returned to every thread.  One streaming pass: four 16-byte loads in
+// flight per thread, the exponentials with the ex2 instruction.
+__device__ __forceinline__ float2 stream_max_sum(const float* row, int c0, int c1, ExpandShared& sh) {
   const int tid = threadIdx.x;
-  const int Kp = a.Kp;
-  const size_t rowi = (size_t)r * a.W + b;
-  const float* row = a.logits + rowi * (size_t)a.row_stride;
-
-  // ---- a1: log-sum-exp over the full vocabulary (one streaming pass) ------
-  float lse;
-  if (a.lse_in != nullptr) {
-    lse = a.lse_in[rowi];
-  } else {
-    float m = -INFINITY, s = 0.f;
-    const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15u) == 0);
-    const int nvec = vec ? (a.V >> 2) : 0;
-    const float4* row4 = reinterpret_cast<const float4*>(row);
-    int i = tid;
-    for (; i + 3 * kExpandThreads < nvec; i += 4 * kExpandThreads) {
-      float4 v0 = __ldg(row4 + i);
-      float4 v1 = __ldg(row4 + i + kExpandThreads);
-      float4 v2 = __ldg(row4 + i + 2 * kExpandThreads);
-      float4 v3 = __ldg(row4 + i + 3 * kExpandThreads);
-      float mx = fmaxf(fmaxf(fmaxf(v0.x, v0.y), fmaxf(v0.z, v0.w)),
-                       fmaxf(fmaxf(v1.x, v1.y), fmaxf(v1.z, v1.w)));
-      mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(v2.x, v2.y), fmaxf(v2.z, v2.w)),
-                           fmaxf(fmaxf(v3.x, v3.y), fmaxf(v3.z, v3.w))));
-      if (mx > m) { s *= ex2((m - mx) * kLog2e); m = mx; }
-      const float mL = m * kLog2e;
-      float t0 = ex2(fmaf(v0.x, kLog2e, -mL)) + ex2(fmaf(v0.y, kLog2e, -mL)) +
-                 ex2(fmaf(v0.z, kLog2e, -mL)) + ex2(fmaf(v0.w, kLog2e, -mL));
-      float t1 = ex2(fmaf(v1.x, kLog2e, -mL)) + ex2(fmaf(v1.y, kLog2e, -mL)) +
-                 ex2(fmaf(v1.z, kLog2e, -mL)) + ex2(fmaf(v1.w, kLog2e, -mL));
-      float t2 = ex2(fmaf(v2.x, kLog2e, -mL)) + ex2(fmaf(v2.y, kLog2e, -mL)) +
-                 ex2(fmaf(v2.z, kLog2e, -mL)) + ex2(fmaf(v2.w, kLog2e, -mL));
-      float t3 = ex2(fmaf(v3.x, kLog2e, -mL)) + ex2(fmaf(v3.y, kLog2e, -mL)) +
-                 ex2(fmaf(v3.z, kLog2e, -mL)) + ex2(fmaf(v3.w, kLog2e, -mL));
-      s += (t0 + t1) + (t2 + t3);
-    }
-    for (; i < nvec; i += kExpandThreads) {
-      float4 v = __ldg(row4 + i);
-      float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-      if (mx > m) { s *= ex2((m - mx) * kLog2e); m = mx; }
-      const float mL = m * kLog2e;
-      s += ex2(fmaf(v.x, kLog2e, -mL)) + ex2(fmaf(v.y, kLog2e, -mL)) +
-           ex2(fmaf(v.z, kLog2e, -mL)) + ex2(fmaf(v.w, kLog2e, -mL));
-    }
-    for (int j = nvec * 4 + tid; j < a.V; j += kExpandThreads) {
-      float x = __ldg(row + j);
-      if (x > m) { s *= ex2((m - x) * kLog2e); m = x; }
-      s += ex2((x - m) * kLog2e);
-    }
-    // block reduction of (m, s)
+  float m = -INFINITY, s = 0.f;
+  const float* base = row + c0;
+  const int len = c1 - c0;
+  const bool vec = ((reinterpret_cast<uintptr_t>(base) & 15u) == 0);
+  const int nvec = vec ? (len >> 2) : 0;
+  const float4* row4 = reinterpret_cast<const float4*>(base);
+  int i = tid;
+  for (; i + 3 * kExpandThreads < nvec; i += 4 * kExpandThreads) {
+    float4 v0 = __ldg(row4 + i);
+    float4 v1 = __ldg(row4 + i + kExpandThreads);
+    float4 v2 = __ldg(row4 + i + 2 * kExpandThreads);
+    float4 v3 = __ldg(row4 + i + 3 * kExpandThreads);
+    float mx = fmaxf(fmaxf(fmaxf(v0.x, v0.y), fmaxf(v0.z, v0.w)),
+                     fmaxf(fmaxf(v1.x, v1.y), fmaxf(v1.z, v1.w)));
+    mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(v2.x, v2.y), fmaxf(v2.z, v2.w)),
+                         fmaxf(fmaxf(v3.x, v3.y), fmaxf(v3.z, v3.w))));
+    if (mx > m) { s *= ex2((m - mx) * kLog2e); m = mx; }
+    const float mL = m * kLog2e;
+    float t0 = ex2(fmaf(v0.x, kLog2e, -mL)) + ex2(fmaf(v0.y, kLog2e, -mL)) +
+               ex2(fmaf(v0.z, kLog2e, -mL)) + ex2(fmaf(v0.w, kLog2e, -mL));
+    float t1 = ex2(fmaf(v1.x, kLog2e, -mL)) + ex2(fmaf(v1.y, kLog2e, -mL)) +
+               ex2(fmaf(v1.z, kLog2e, -mL)) + ex2(fmaf(v1.w, kLog2e, -mL));
+    float t2 = ex2(fmaf(v2.x, kLog2e, -mL)) + ex2(fmaf(v2.y, kLog2e, -mL)) +
+               ex2(fmaf(v2.z, kLog2e, -mL)) + ex2(fmaf(v2.w, kLog2e, -mL));
+    float t3 = ex2(fmaf(v3.x, kLog2e, -mL)) + ex2(fmaf(v3.y, kLog2e, -mL)) +
+               ex2(fmaf(v3.z, kLog2e, -mL)) + ex2(fmaf(v3.w, kLog2e, -mL));
+    s += (t0 + t1) + (t2 + t3);
+  }
+  for (; i < nvec; i += kExpandThreads) {
+    float4 v = __ldg(row4 + i);
+    float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    if (mx > m) { s *= ex2((m - mx) * kLog2e); m = mx; }
+    const float mL = m * kLog2e;
+    s += ex2(fmaf(v.x, kLog2e, -mL)) + ex2(fmaf(v.y, kLog2e, -mL)) +
+         ex2(fmaf(v.z, kLog2e, -mL)) + ex2(fmaf(v.w, kLog2e, -mL));
+  }
+  for (int j = nvec * 4 + tid; j < len; j += kExpandThreads) {
+    float x = __ldg(base + j);
+    if (x > m) { s *= ex2((m - x) * kLog2e); m = x; }
+    s += ex2((x - m) * kLog2e);
+  }
+  // block reduction of (m, s)
+  for (int o = 16; o; o >>= 1) {
+    float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    float M = fmaxf(m, m2);
+    float a1 = (s == 0.f) ? 0.f : s * ex2((m - M) * kLog2e);
+    float a2 = (s2 == 0.f) ? 0.f : s2 * ex2((m2 - M) * kLog2e);
+    m = M; s = a1 + a2;
+  }
+  const int lane = tid & 31, warp = tid >> 5;
+  if (lane == 0) { sh.red_m[warp] = m; sh.red_s[warp] = s; }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = kExpandThreads / 32;
+    m = lane < nw ? sh.red_m[lane] : -INFINITY;
+    s = lane < nw ? sh.red_s[lane] : 0.f;
     for (int o = 16; o; o >>= 1) {
       float m2 = __shfl_xor_sync(0xffffffffu, m, o);
       float s2 = __shfl_xor_sync(0xffffffffu, s, o);
@@ -209,26 +222,24 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
       float a2 = (s2 == 0.f) ? 0.f : s2 * ex2((m2 - M) * kLog2e);
       m = M; s = a1 + a2;
     }
-    const int lane = tid & 31, warp = tid >> 5;
-    if (lane == 0) { sh.red_m[warp] = m; sh.red_s[warp] = s; }
-    __syncthreads();
-    if (warp == 0) {
-      const int nw = kExpandThreads / 32;
-      m = lane < nw ? sh.red_m[lane] : -INFINITY;
-      s = lane < nw ? sh.red_s[lane] : 0.f;
-      for (int o = 16; o; o >>= 1) {
-        float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-        float M = fmaxf(m, m2);
-        float a1 = (s == 0.f) ? 0.f : s * ex2((m - M) * kLog2e);
-        float a2 = (s2 == 0.f) ? 0.f : s2 * ex2((m2 - M) * kLog2e);
-        m = M; s = a1 + a2;
-      }
-      if (lane == 0) sh.lse = m + logf(s);
-    }
-    __syncthreads();
-    lse = sh.lse;
+    if (lane == 0) { sh.red_m[0] = m; sh.red_s[0] = s; }
   }
+  __syncthreads();
+  const float2 res = make_float2(sh.red_m[0], sh.red_s[0]);
+  __syncthreads();
+  return res;
+}
+
+// Rows a2-a3 for beam b of request r: log-sum-exp, trie children, per-beam
+// top_k appended to the request's pool.
+__device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
+                                                 int r, int b, uint32_t* bins, uint32_t* kcache,
+                                                 float lse) {
+  const int tid = threadIdx.x;
+  const int Kp = a.Kp;
+  const size_t rowi = (size_t)r * a.W + b;
+  const float* row = a.logits + rowi * (size_t)a.row_stride;
+
   if (a.lse_out != nullptr && tid == 0) a.lse_out[rowi] = lse;
   const float cum = a.cum_in[rowi];
 
@@ -559,11 +570,50 @@ __global__ void __launch_bounds__(kExpandThreads, 3)
 bd_expand_kernel(SelectArgs a) {
   __shared__ ExpandShared sh;
   extern __shared__ __align__(16) unsigned char tail_smem[];
-  const int b = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
+  const int S = a.row_splits;
+  const int b = blockIdx.x / S, sidx = blockIdx.x - b * S, r = blockIdx.y, tid = threadIdx.x;
   SelWs ws = carve(a.ws, a.R, a.W, a.Kp);
-  if (b == 0 && r == 0 && tid == 0) ws.hdr->bar_count = 0u;
+  if (blockIdx.x == 0 && r == 0 && tid == 0) ws.hdr->bar_count = 0u;
   const int nl = a.n_live_in[r];
   if (b >= nl) return;
+  const size_t rowi = (size_t)r * a.W + b;
+  // ---- a1: log-sum-exp over the full vocabulary.  S blocks stream one
+  // chunk of the row each; the last of them to finish combines the chunks'
+  // (max, sum) and carries on with the row.
+  float lse;
+  if (a.lse_in != nullptr) {
+    if (sidx != 0) return;
+    lse = a.lse_in[rowi];
+  } else {
+    const float* row = a.logits + rowi * (size_t)a.row_stride;
+    const int chunk = a.row_chunk;
+    const int c0 = sidx * chunk;
+    const int c1 = min(a.V, c0 + chunk);
+    const float2 ms = stream_max_sum(row, c0, c1, sh);
+    if (S == 1) {
+      lse = ms.x + logf(ms.y);
+    } else {
+      if (tid == 0) {
+        ws.rowpart[rowi * kMaxRowSplits + sidx] = ms;
+        __threadfence();
+        sh.count = atomicAdd(ws.rowtick + rowi, 1);
+      }
+      __syncthreads();
+      if (sh.count != S - 1) return;
+      __threadfence();
+      if (tid < 32) {   // one warp: lane k holds chunk k's (max, sum)
+        const float2 p = tid < S ? __ldcg(ws.rowpart + rowi * kMaxRowSplits + tid)
+                                 : make_float2(-INFINITY, 0.f);
+        float M = p.x;
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float tot = (p.y > 0.f) ? p.y * ex2((p.x - M) * kLog2e) : 0.f;
+        for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        if (tid == 0) sh.lse = M + logf(tot);
+      }
+      __syncthreads();
+      lse = sh.lse;
+    }
+  }
   // dynamic shared memory: [key cache 16 KB][score-bin histogram 16 KB, fused only];
   // the fused tail reuses all of it for candidate keys after the ticket
   uint32_t* kcache = reinterpret_cast<uint32_t*>(tail_smem);
@@ -573,7 +623,7 @@ bd_expand_kernel(SelectArgs a) {
     for (int i = tid; i < kTailBins; i += kExpandThreads) bins[i] = 0;
     __syncthreads();
   }
-  expand_candidates(a, sh, ws, r, b, bins, kcache);
+  expand_candidates(a, sh, ws, r, b, bins, kcache, lse);
   if constexpr (kFused) {
     __syncthreads();
     uint32_t* gh = ws.hist + (size_t)r * kBins;
@@ -743,8 +793,9 @@ struct GlobalLaunchCfg {
 size_t select_workspace_bytes(int R, int W, int K, int V) {
   const int Kp = K < V ? K : V;
   return kWsHeaderBytes + align256((size_t)R * sizeof(SelState)) +
+         align256((size_t)R * W * sizeof(int32_t)) +
          align256((size_t)R * kBins * sizeof(uint32_t)) + align256((size_t)R * W * Kp * 8) +
-         (size_t)R * kSelectCap * 8;
+         align256((size_t)R * kSelectCap * 8) + (size_t)R * W * kMaxRowSplits * sizeof(float2);
 }
 
 int launch_select(const SelectArgs& a, cudaStream_t stream) {
@@ -763,20 +814,30 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
     cfg[dev].max_blocks = per_sm * sm_count();
     cfg[dev].smem = smem;
   }
+  SelectArgs a2 = a;
+  // blocks per logits row: about 32K logits each (the row's tail of partial
+  // waves shrinks with the work unit), at most kMaxRowSplits
+  int S = a.V / 32768;
+  if (S < 1) S = 1;
+  if (S > kMaxRowSplits) S = kMaxRowSplits;
+  int chunk = ((a.V + S - 1) / S + 3) & ~3;
+  S = (a.V + chunk - 1) / chunk;
+  a2.row_splits = S;
+  a2.row_chunk = chunk;
   SelWs ws = carve(a.ws, a.R, a.W, a.Kp);
   const size_t zero_bytes = (char*)ws.pool - (char*)ws.state;
   if (cudaMemsetAsync(ws.state, 0, zero_bytes, stream) != cudaSuccess) return BEAMDEC_ERR_CUDA;
 
-  dim3 g1(a.W, a.R);
+  dim3 g1(a.W * S, a.R);
   // Pools of at most 1M keys per request (W <= 4096) are selected by the last
   // expand block of each request; larger ones by the cooperative grid kernel.
   const bool fused = a.W <= kTailCap && (long long)a.W * a.Kp <= (1ll << 20);
   prof_begin(kKExpand, stream);
   static_assert(kKeyCache * 4 + kTailBins * 4 <= kTailCap * 8, "fused dynamic shared memory");
   if (fused)
-    bd_expand_kernel<true><<<g1, kExpandThreads, kTailCap * sizeof(unsigned long long), stream>>>(a);
+    bd_expand_kernel<true><<<g1, kExpandThreads, kTailCap * sizeof(unsigned long long), stream>>>(a2);
   else
-    bd_expand_kernel<false><<<g1, kExpandThreads, kKeyCache * sizeof(uint32_t), stream>>>(a);
+    bd_expand_kernel<false><<<g1, kExpandThreads, kKeyCache * sizeof(uint32_t), stream>>>(a2);
   prof_end(kKExpand, stream);
   if (cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
   if (fused) return BEAMDEC_OK;
@@ -786,7 +847,7 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
   if (want < a.R) want = a.R;
   int grid = (int)(want < cfg[dev].max_blocks ? want : cfg[dev].max_blocks);
   if (grid < 1) grid = 1;
-  SelectArgs copy = a;
+  SelectArgs copy = a2;
   void* params[] = {&copy};
   prof_begin(kKGlobal, stream);
   const cudaError_t e = cudaLaunchCooperativeKernel((const void*)bd_global_kernel, dim3(grid),
