@@ -453,11 +453,16 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
   } else {
     // the request's score-bin histogram (complete: every block flushed it
     // before taking its ticket) brackets the nt-th best score
-    const volatile uint32_t* gh = ws.hist + (size_t)r * kBins;
-    if (threadIdx.x < 32) warp_find_digit(gh, kTailBins, (uint32_t)nt, &sh.digit, &sh.below);
+    // copied to shared memory first (the upper half of the key buffer, free
+    // until the gather below), so the bin search reads shared memory
+    uint32_t* hs = reinterpret_cast<uint32_t*>(keys + kTailCap / 2);
+    const uint32_t* gh = ws.hist + (size_t)r * kBins;
+    for (int i = threadIdx.x; i < kTailBins; i += blockDim.x) hs[i] = __ldcg(gh + i);
+    __syncthreads();
+    if (threadIdx.x < 32) warp_find_digit(hs, kTailBins, (uint32_t)nt, &sh.digit, &sh.below);
     __syncthreads();
     const int Dbin = (int)sh.digit;
-    const uint32_t c_le = sh.below + gh[Dbin];
+    const uint32_t c_le = sh.below + hs[Dbin];
     __syncthreads();
     if (c_le <= (uint32_t)kTailCap) {
       const float ref = a.cum_in[(size_t)r * a.W];
@@ -717,11 +722,13 @@ bd_global_kernel(SelectArgs a) {
       volatile SelState* st = ws.state + r;
       if (st->done) continue;
       volatile uint32_t* gh = ws.hist + (size_t)r * kBins;
-      if (tid < 32) warp_find_digit(gh, 1 << width, (uint32_t)st->need, &sh.digit, &sh.below);
+      for (int i = tid; i < (1 << width); i += kGlobalThreads) sh.hist[i] = gh[i];   // to shared memory
+      __syncthreads();
+      if (tid < 32) warp_find_digit(sh.hist, 1 << width, (uint32_t)st->need, &sh.digit, &sh.below);
       __syncthreads();
       if (tid == 0) {
         const uint32_t D = sh.digit;
-        const uint32_t in_bin = gh[D];
+        const uint32_t in_bin = sh.hist[D];
         st->sure += (int)sh.below;
         st->need -= (int)sh.below;
         st->prefix = (st->prefix << width) | D;
