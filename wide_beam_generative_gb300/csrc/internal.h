@@ -76,6 +76,9 @@ size_t attn_workspace_bytes(int R, int W, int Hq, int Hkv, int d, const AttnPlan
 int launch_attn_shared_simt(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 bool attn_tc_supported(int q_dtype, int kv_dtype, int d, int G);
+// The tensor-core kernel also runs the unshared stage and the merge (one
+// prompt split and at most 8 decode tokens): no partials, no merge kernel.
+bool attn_tc_fuses(const AttnPlan& pl, int step);
 int launch_attn_merge(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 
 // Partial-triple layout in the attention workspace (after the 256-byte header):

@@ -30,6 +30,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace bd {
 namespace {
@@ -141,7 +142,12 @@ __device__ __forceinline__ int score_bin(float ref, float s) {
   return (int)u;
 }
 
+constexpr int kStreamStages = 8;           // bulk-copy ring of the logits stream
+constexpr int kStageFloats = 2048;         // 8 KB per stage (4 floats per thread)
+
 struct ExpandShared {
+  unsigned long long stage_bar[kStreamStages];
+  int stream_fail;
   uint32_t hist[2048];
   float red_m[32];
   float red_s[32];
@@ -151,6 +157,41 @@ struct ExpandShared {
   int pool_base;
   float lse;
 };
+
+// Block-wide combine of per-thread (max, sum of exp(x - max)); every thread
+// gets the result.
+__device__ float2 block_reduce_ms(float m, float s, ExpandShared& sh) {
+  const int tid = threadIdx.x;
+  for (int o = 16; o; o >>= 1) {
+    float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    float M = fmaxf(m, m2);
+    float a1 = (s == 0.f) ? 0.f : s * ex2((m - M) * kLog2e);
+    float a2 = (s2 == 0.f) ? 0.f : s2 * ex2((m2 - M) * kLog2e);
+    m = M; s = a1 + a2;
+  }
+  const int lane = tid & 31, warp = tid >> 5;
+  if (lane == 0) { sh.red_m[warp] = m; sh.red_s[warp] = s; }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = kExpandThreads / 32;
+    m = lane < nw ? sh.red_m[lane] : -INFINITY;
+    s = lane < nw ? sh.red_s[lane] : 0.f;
+    for (int o = 16; o; o >>= 1) {
+      float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      float M = fmaxf(m, m2);
+      float a1 = (s == 0.f) ? 0.f : s * ex2((m - M) * kLog2e);
+      float a2 = (s2 == 0.f) ? 0.f : s2 * ex2((m2 - M) * kLog2e);
+      m = M; s = a1 + a2;
+    }
+    if (lane == 0) { sh.red_m[0] = m; sh.red_s[0] = s; }
+  }
+  __syncthreads();
+  const float2 res = make_float2(sh.red_m[0], sh.red_s[0]);
+  __syncthreads();
+  return res;
+}
 
 // Running (max, sum of exp(x - max)) of row[c0..c1) for the whole block,
 // returned to every thread.  One streaming pass: four 16-byte loads in
@@ -198,36 +239,82 @@ __device__ __forceinline__ float2 stream_max_sum(const float* row, int c0, int c
     if (x > m) { s *= ex2((m - x) * kLog2e); m = x; }
     s += ex2((x - m) * kLog2e);
   }
-  // block reduction of (m, s)
-  for (int o = 16; o; o >>= 1) {
-    float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    float M = fmaxf(m, m2);
-    float a1 = (s == 0.f) ? 0.f : s * ex2((m - M) * kLog2e);
-    float a2 = (s2 == 0.f) ? 0.f : s2 * ex2((m2 - M) * kLog2e);
-    m = M; s = a1 + a2;
+  return block_reduce_ms(m, s, sh);
+}
+
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          tc::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+
+// (max, sum of exp(x - max)) of row[c0..c1) through a ring of bulk copies:
+// thread 0 keeps up to kStreamStages 8 KB copies in flight (no registers
+// hold in-flight data), every thread folds one float4 per stage from shared
+// memory.  The row chunk must start 16-byte aligned; a tail shorter than a
+// stage is read directly.  Waits are bounded: on a timeout the block records
+// BEAMDEC_ERR_TIMEOUT, waits for the copies it started and returns NaN.
+__device__ float2 stream_max_sum_bulk(const float* base, int len, ExpandShared& sh, float* ring,
+                                      WsHeader* hdr) {
+  const int tid = threadIdx.x;
+  const int nfull = len / kStageFloats;
+  float m = -INFINITY, s = 0.f;
+  if (tid == 0) {
+    sh.stream_fail = 0;
+    for (int k = 0; k < kStreamStages; ++k) tc::mbar_init(reinterpret_cast<uint64_t*>(&sh.stage_bar[k]), 1);
+    tc::mbar_fence_init();
   }
-  const int lane = tid & 31, warp = tid >> 5;
-  if (lane == 0) { sh.red_m[warp] = m; sh.red_s[warp] = s; }
   __syncthreads();
-  if (warp == 0) {
-    const int nw = kExpandThreads / 32;
-    m = lane < nw ? sh.red_m[lane] : -INFINITY;
-    s = lane < nw ? sh.red_s[lane] : 0.f;
-    for (int o = 16; o; o >>= 1) {
-      float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-      float M = fmaxf(m, m2);
-      float a1 = (s == 0.f) ? 0.f : s * ex2((m - M) * kLog2e);
-      float a2 = (s2 == 0.f) ? 0.f : s2 * ex2((m2 - M) * kLog2e);
-      m = M; s = a1 + a2;
+  if (tid == 0) {
+    const int pre = nfull < kStreamStages ? nfull : kStreamStages;
+    for (int k = 0; k < pre; ++k) {
+      uint64_t* bar = reinterpret_cast<uint64_t*>(&sh.stage_bar[k]);
+      tc::mbar_expect_tx(bar, kStageFloats * 4);
+      bulk_load(ring + k * kStageFloats, base + (size_t)k * kStageFloats, kStageFloats * 4, bar);
     }
-    if (lane == 0) { sh.red_m[0] = m; sh.red_s[0] = s; }
   }
-  __syncthreads();
-  const float2 res = make_float2(sh.red_m[0], sh.red_s[0]);
-  __syncthreads();
-  return res;
+  int issued_hi = nfull < kStreamStages ? nfull : kStreamStages;   // thread 0's view
+  for (int k = 0; k < nfull; ++k) {
+    const int slot = k % kStreamStages;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(&sh.stage_bar[slot]);
+    const uint32_t parity = (uint32_t)(k / kStreamStages) & 1u;
+    if (!tc::mbar_wait(bar, parity)) sh.stream_fail = 1;
+    __syncthreads();
+    if (sh.stream_fail) break;
+    const float4 v = reinterpret_cast<const float4*>(ring + slot * kStageFloats)[tid];
+    const float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    if (mx > m) { s *= ex2((m - mx) * kLog2e); m = mx; }
+    const float mL = m * kLog2e;
+    s += (ex2(fmaf(v.x, kLog2e, -mL)) + ex2(fmaf(v.y, kLog2e, -mL))) +
+         (ex2(fmaf(v.z, kLog2e, -mL)) + ex2(fmaf(v.w, kLog2e, -mL)));
+    __syncthreads();   // the slot is consumed by every thread
+    if (tid == 0 && k + kStreamStages < nfull) {
+      tc::mbar_expect_tx(bar, kStageFloats * 4);
+      bulk_load(ring + slot * kStageFloats, base + (size_t)(k + kStreamStages) * kStageFloats,
+                kStageFloats * 4, bar);
+      issued_hi = k + kStreamStages + 1;
+    }
+  }
+  if (sh.stream_fail) {
+    if (tid == 0) {
+      set_status(hdr, BEAMDEC_ERR_TIMEOUT);
+      for (int k = 0; k < issued_hi; ++k)   // let started copies land before the block moves on
+        tc::mbar_wait(reinterpret_cast<uint64_t*>(&sh.stage_bar[k % kStreamStages]),
+                      (uint32_t)(k / kStreamStages) & 1u);
+    }
+    __syncthreads();
+    return make_float2(NAN, NAN);
+  }
+  // tail shorter than one stage
+  for (int j = nfull * kStageFloats + tid; j < len; j += kExpandThreads) {
+    const float x = __ldg(base + j);
+    if (x > m) { s *= ex2((m - x) * kLog2e); m = x; }
+    s += ex2((x - m) * kLog2e);
+  }
+  return block_reduce_ms(m, s, sh);
 }
 
 // Rows a2-a3 for beam b of request r: log-sum-exp, trie children, per-beam
@@ -594,7 +681,11 @@ bd_expand_kernel(SelectArgs a) {
     const int chunk = a.row_chunk;
     const int c0 = sidx * chunk;
     const int c1 = min(a.V, c0 + chunk);
-    const float2 ms = stream_max_sum(row, c0, c1, sh);
+    const float* base = row + c0;
+    const float2 ms = ((reinterpret_cast<uintptr_t>(base) & 15u) == 0)
+                          ? stream_max_sum_bulk(base, c1 - c0, sh,
+                                                reinterpret_cast<float*>(tail_smem), ws.hdr)
+                          : stream_max_sum(row, c0, c1, sh);
     if (S == 1) {
       lse = ms.x + logf(ms.y);
     } else {
@@ -807,8 +898,18 @@ size_t select_workspace_bytes(int R, int W, int K, int V) {
 
 int launch_select(const SelectArgs& a, cudaStream_t stream) {
   static GlobalLaunchCfg cfg[64];
+  static bool expand_attr[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BEAMDEC_ERR_CUDA;
+  if (!expand_attr[dev]) {
+    const int dyn = kStreamStages * kStageFloats * 4;
+    if (cudaFuncSetAttribute(bd_expand_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dyn) != cudaSuccess ||
+        cudaFuncSetAttribute(bd_expand_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dyn) != cudaSuccess)
+      return BEAMDEC_ERR_CUDA;
+    expand_attr[dev] = true;
+  }
   const size_t smem = kGlobalKeysOffset + (size_t)kSelectCap * 8;
   if (cfg[dev].max_blocks == 0) {
     if (cudaFuncSetAttribute(bd_global_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -841,10 +942,12 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
   const bool fused = a.W <= kTailCap && (long long)a.W * a.Kp <= (1ll << 20);
   prof_begin(kKExpand, stream);
   static_assert(kKeyCache * 4 + kTailBins * 4 <= kTailCap * 8, "fused dynamic shared memory");
+  static_assert(kStreamStages * kStageFloats * 4 >= kTailCap * 8, "ring covers the tail buffer");
+  const size_t dyn = (size_t)kStreamStages * kStageFloats * 4;   // 64 KB, reused after the stream
   if (fused)
-    bd_expand_kernel<true><<<g1, kExpandThreads, kTailCap * sizeof(unsigned long long), stream>>>(a2);
+    bd_expand_kernel<true><<<g1, kExpandThreads, dyn, stream>>>(a2);
   else
-    bd_expand_kernel<false><<<g1, kExpandThreads, kKeyCache * sizeof(uint32_t), stream>>>(a2);
+    bd_expand_kernel<false><<<g1, kExpandThreads, dyn, stream>>>(a2);
   prof_end(kKExpand, stream);
   if (cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
   if (fused) return BEAMDEC_OK;
