@@ -89,7 +89,8 @@ int beamdec_read_status(void* workspace, void* stream, int32_t* host_status);
  * stops recording.  beamdec_profile_read synchronises the recorded events and
  * returns the total milliseconds and launch count of one kernel id:
  * 0 bd_expand_kernel, 1 bd_global_kernel, 2 bd_attn_shared_simt_kernel,
- * 3 bd_attn_shared_tc_kernel, 4 bd_attn_merge_kernel, 5 bd_kv_e4m3_to_bf16_kernel.
+ * 3 bd_attn_shared_tc_kernel, 4 bd_attn_merge_kernel, 5 bd_kv_e4m3_to_bf16_kernel,
+ * 6 bd_lse_kernel.
  * Host-side state is
  * process-wide; use from one host thread.
  */

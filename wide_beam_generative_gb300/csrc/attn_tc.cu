@@ -74,15 +74,6 @@ struct TcParams {
   float* pl;
   float* po;
   WsHeader* hdr;
-  // unshared stage + merge in the epilogue (one prompt split, few decode tokens)
-  int fuse;                 // 1: write the final output instead of partials
-  int kv8;                  // unshared KV stored as e4m3
-  const void* uk;
-  const void* uv;
-  const int32_t* slot;
-  int step, T;
-  const float* v_scale;
-  __nv_bfloat16* out;
 };
 
 struct Bars {
@@ -132,123 +123,6 @@ __device__ __forceinline__ void write_empty_partials(const TcParams& p, size_t b
   }
 }
 
-// Eight consecutive K/V elements of one unshared row as fp32 (bf16 or e4m3
-// storage; e4m3 unscaled).
-__device__ __forceinline__ void load8(const void* base, size_t e, int kv8, float (&x)[8]) {
-  if (kv8) {
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(base) + e));
-    const uint32_t w[2] = {u.x, u.y};
-#pragma unroll
-    for (int q = 0; q < 2; ++q)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w[q] >> (16 * h)) & 0xffffu);
-        const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
-        x[4 * q + 2 * h] = f.x;
-        x[4 * q + 2 * h + 1] = f.y;
-      }
-  } else {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + e));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      x[2 * q] = __uint_as_float(w[q] << 16);
-      x[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
-    }
-  }
-}
-
-constexpr int kFuseMaxTokens = 8;
-
-// Unshared stage and merge for one query row, done by the thread that owns
-// the row after its shared-stage O is complete in TMEM: scores of the beam's
-// decode tokens (slots from the parent-pointer table), the online-softmax
-// merge with the shared (m, l, O), and the final bf16 output row.
-__device__ __noinline__ void fused_epilogue(const TcParams& p, const unsigned char* qtile,
-                                            int row_in_tile, int row, int r, int g, float sc,
-                                            float m_sh, float l_sh, uint32_t tO) {
-  const bool in_range = row < p.rows;
-  const int G = p.G;
-  const int j = in_range ? row / G : 0;
-  const int h = g * G + (in_range ? row - j * G : 0);
-  const bool live = in_range && j < p.n_live[r];
-  const int L = p.step + 1;
-  const int TW = p.T * p.W;
-  // scores of the unshared tokens (log2 units)
-  float su[kFuseMaxTokens];
-  size_t ue[kFuseMaxTokens];
-  float M = m_sh;
-#pragma unroll
-  for (int u = 0; u < kFuseMaxTokens; ++u) {
-    su[u] = -INFINITY;
-    ue[u] = 0;
-    if (!live || u >= L) continue;
-    const int sl = p.slot[((size_t)r * p.W + j) * p.T + u];
-    if (sl < 0 || sl >= TW) {
-      set_status(p.hdr, BEAMDEC_ERR_DEVICE_CHECK);
-      continue;
-    }
-    ue[u] = (((size_t)r * TW + sl) * p.Hkv + g) * 128;
-    float acc = 0.f;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const uint4 qw = *reinterpret_cast<const uint4*>(
-          qtile + (c >> 3) * kHalfBytes + row_in_tile * 128 + (((c & 7) ^ (row_in_tile & 7)) << 4));
-      const uint32_t w[4] = {qw.x, qw.y, qw.z, qw.w};
-      float kx[8];
-      load8(p.uk, ue[u] + c * 8, p.kv8, kx);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(__uint_as_float(w[e] << 16), kx[2 * e], acc);
-        acc = fmaf(__uint_as_float(w[e] & 0xffff0000u), kx[2 * e + 1], acc);
-      }
-    }
-    su[u] = acc * sc;
-    M = fmaxf(M, su[u]);
-  }
-  const float alpha = (l_sh > 0.f) ? ex2(m_sh - M) : 0.f;
-  float lsum = l_sh * alpha;
-  float pu[kFuseMaxTokens];
-#pragma unroll
-  for (int u = 0; u < kFuseMaxTokens; ++u) {
-    pu[u] = (su[u] == -INFINITY) ? 0.f : ex2(su[u] - M);
-    lsum += pu[u];
-  }
-  const float vs = p.kv8 && p.v_scale ? p.v_scale[g] : 1.f;
-  const float inv = live && lsum > 0.f ? vs / lsum : 0.f;
-  uint4* dst = reinterpret_cast<uint4*>(p.out + (((size_t)r * p.W + j) * p.Hq + h) * 128);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    float o[32];
-    tmem_ld32(tO + q * 32, o);   // warp-collective: every lane takes part
-#pragma unroll
-    for (int i = 0; i < 32; ++i) o[i] *= alpha;
-#pragma unroll
-    for (int u = 0; u < kFuseMaxTokens; ++u) {
-      if (pu[u] == 0.f) continue;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float vx[8];
-        load8(p.uv, ue[u] + q * 32 + c * 8, p.kv8, vx);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[c * 8 + e] = fmaf(pu[u], vx[e], o[c * 8 + e]);
-      }
-    }
-    if (in_range) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __nv_bfloat162 b = __floats2bfloat162_rn(o[c * 8 + 2 * e] * inv, o[c * 8 + 2 * e + 1] * inv);
-          pk[e] = *reinterpret_cast<const uint32_t*>(&b);
-        }
-        dst[q * 4 + c] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      }
-    }
-  }
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
 bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                          const __grid_constant__ CUtensorMap kmap,
@@ -269,18 +143,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 &&
       (int64_t)p.prompt_offsets[p.R] != p.shared_rows)
     set_status(p.hdr, BEAMDEC_ERR_DEVICE_CHECK);   // the K/V maps end at shared_rows
-  if (row0 >= p.n_live[r] * G) {   // every row of the CTA is a dead beam
-    if (p.fuse) {
-      for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
-        const int row = row0 + (i >> 4);
-        if (row >= p.rows) continue;
-        const int j = row / G, h = g * G + (row - (row / G) * G);
-        reinterpret_cast<uint4*>(p.out + (((size_t)r * p.W + j) * p.Hq + h) * 128)[i & 15] =
-            make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    return;
-  }
+  if (row0 >= p.n_live[r] * G) return;   // every row of the CTA is a dead beam
   const int pbase = p.prompt_offsets[r];
   const int P = p.prompt_offsets[r + 1] - pbase;
   const int k0 = sp * p.split_len;
@@ -506,10 +369,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     if (ok && !warp_wait(&bars.done, 0)) ok = false;
     if (!ok) abort_sh = 1;
     const int row = row0 + t * 128 + row_in_tile;
-    if (ok && p.fuse) {
-      fence_after_sync();
-      fused_epilogue(p, sm + kOffQ + t * kTileBytes, row_in_tile, row, r, g, sc, m_used, l, tO);
-    } else if (ok) {
+    if (ok) {
       fence_after_sync();
       const size_t pi = prow_base + row;
       float4* o = reinterpret_cast<float4*>(p.po + pi * 128);
@@ -601,10 +461,6 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
 
 }  // namespace
 
-bool attn_tc_fuses(const AttnPlan& pl, int step) {
-  return pl.tensor_core && pl.n_split == 1 && step + 1 <= kFuseMaxTokens;
-}
-
 bool attn_tc_supported(int q_dtype, int kv_dtype, int d, int G) {
   return q_dtype == BEAMDEC_BF16 && (kv_dtype == BEAMDEC_BF16 || kv_dtype == BEAMDEC_E4M3) &&
          d == 128 && G >= 1 && G <= 16 && (128 % G) == 0;
@@ -672,15 +528,6 @@ int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t st
   AttnPartials part = attn_partials(a.ws, a.R, a.W, a.Hq, a.Hkv, a.d, pl.n_split);
   p.pm = part.m; p.pl = part.l; p.po = part.o;
   p.hdr = reinterpret_cast<WsHeader*>(a.ws);
-  p.fuse = attn_tc_fuses(pl, a.step) ? 1 : 0;
-  p.kv8 = a.kv_dtype == BEAMDEC_E4M3 ? 1 : 0;
-  p.uk = a.unshared_k;
-  p.uv = a.unshared_v;
-  p.slot = a.slot_table;
-  p.step = a.step;
-  p.T = a.T;
-  p.v_scale = a.kv_dtype == BEAMDEC_E4M3 ? a.v_scale : nullptr;
-  p.out = static_cast<__nv_bfloat16*>(a.out);
   dim3 grid((p.rows + 255) / 256, a.Hkv * pl.n_split, a.R);
   prof_begin(kKAttnTc, stream);
   bd_attn_shared_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qm, km, vm, p);

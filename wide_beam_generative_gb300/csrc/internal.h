@@ -76,9 +76,6 @@ size_t attn_workspace_bytes(int R, int W, int Hq, int Hkv, int d, const AttnPlan
 int launch_attn_shared_simt(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 bool attn_tc_supported(int q_dtype, int kv_dtype, int d, int G);
-// The tensor-core kernel also runs the unshared stage and the merge (one
-// prompt split and at most 8 decode tokens): no partials, no merge kernel.
-bool attn_tc_fuses(const AttnPlan& pl, int step);
 int launch_attn_merge(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 
 // Partial-triple layout in the attention workspace (after the 256-byte header):
@@ -95,7 +92,7 @@ int sm_count();
 
 // ---- per-kernel event timing (off unless beamdec_profile_enable(1)) ---------
 enum KernelId { kKExpand = 0, kKGlobal = 1, kKAttnSimt = 2, kKAttnTc = 3, kKAttnMerge = 4,
-                kKKvConvert = 5, kKCount = 6 };
+                kKKvConvert = 5, kKLse = 6, kKCount = 7 };
 void prof_begin(int kid, cudaStream_t s);
 void prof_end(int kid, cudaStream_t s);
 

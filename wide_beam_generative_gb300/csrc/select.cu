@@ -30,7 +30,6 @@
 
 #include "common.cuh"
 #include "internal.h"
-#include "tc_ptx.cuh"
 
 namespace bd {
 namespace {
@@ -64,6 +63,7 @@ struct SelWs {
   unsigned long long* pool;  // [R][W*Kp]
   unsigned long long* cand;  // [R][kSelectCap]
   float2* rowpart;        // [R][W][kMaxRowSplits] per-chunk (max, sum of exp)
+  float* rowlse;          // [R][W] log-sum-exp of each live row
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -77,7 +77,8 @@ __host__ __device__ inline SelWs carve(void* ws, int R, int W, int Kp) {
   s.hist = (uint32_t*)p; p += align256((size_t)R * kBins * sizeof(uint32_t));
   s.pool = (unsigned long long*)p; p += align256((size_t)R * W * Kp * 8);
   s.cand = (unsigned long long*)p; p += align256((size_t)R * kSelectCap * 8);
-  s.rowpart = (float2*)p;
+  s.rowpart = (float2*)p; p += align256((size_t)R * W * kMaxRowSplits * sizeof(float2));
+  s.rowlse = (float*)p;
   return s;
 }
 
@@ -142,12 +143,7 @@ __device__ __forceinline__ int score_bin(float ref, float s) {
   return (int)u;
 }
 
-constexpr int kStreamStages = 8;           // bulk-copy ring of the logits stream
-constexpr int kStageFloats = 2048;         // 8 KB per stage (4 floats per thread)
-
 struct ExpandShared {
-  unsigned long long stage_bar[kStreamStages];
-  int stream_fail;
   uint32_t hist[2048];
   float red_m[32];
   float red_s[32];
@@ -157,41 +153,6 @@ struct ExpandShared {
   int pool_base;
   float lse;
 };
-
-// Block-wide combine of per-thread (max, sum of exp(x - max)); every thread
-// gets the result.
-__device__ float2 block_reduce_ms(float m, float s, ExpandShared& sh) {
-  const int tid = threadIdx.x;
-  for (int o = 16; o; o >>= 1) {
-    float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    float M = fmaxf(m, m2);
-    float a1 = (s == 0.f) ? 0.f : s * ex2((m - M) * kLog2e);
-    float a2 = (s2 == 0.f) ? 0.f : s2 * ex2((m2 - M) * kLog2e);
-    m = M; s = a1 + a2;
-  }
-  const int lane = tid & 31, warp = tid >> 5;
-  if (lane == 0) { sh.red_m[warp] = m; sh.red_s[warp] = s; }
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = kExpandThreads / 32;
-    m = lane < nw ? sh.red_m[lane] : -INFINITY;
-    s = lane < nw ? sh.red_s[lane] : 0.f;
-    for (int o = 16; o; o >>= 1) {
-      float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-      float M = fmaxf(m, m2);
-      float a1 = (s == 0.f) ? 0.f : s * ex2((m - M) * kLog2e);
-      float a2 = (s2 == 0.f) ? 0.f : s2 * ex2((m2 - M) * kLog2e);
-      m = M; s = a1 + a2;
-    }
-    if (lane == 0) { sh.red_m[0] = m; sh.red_s[0] = s; }
-  }
-  __syncthreads();
-  const float2 res = make_float2(sh.red_m[0], sh.red_s[0]);
-  __syncthreads();
-  return res;
-}
 
 // Running (max, sum of exp(x - max)) of row[c0..c1) for the whole block,
 // returned to every thread.  One streaming pass: four 16-byte loads in
@@ -239,82 +200,83 @@ __device__ __forceinline__ float2 stream_max_sum(const float* row, int c0, int c
     if (x > m) { s *= ex2((m - x) * kLog2e); m = x; }
     s += ex2((x - m) * kLog2e);
   }
-  return block_reduce_ms(m, s, sh);
-}
-
-
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          tc::smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
-      : "memory");
-}
-
-// (max, sum of exp(x - max)) of row[c0..c1) through a ring of bulk copies:
-// thread 0 keeps up to kStreamStages 8 KB copies in flight (no registers
-// hold in-flight data), every thread folds one float4 per stage from shared
-// memory.  The row chunk must start 16-byte aligned; a tail shorter than a
-// stage is read directly.  Waits are bounded: on a timeout the block records
-// BEAMDEC_ERR_TIMEOUT, waits for the copies it started and returns NaN.
-__device__ float2 stream_max_sum_bulk(const float* base, int len, ExpandShared& sh, float* ring,
-                                      WsHeader* hdr) {
-  const int tid = threadIdx.x;
-  const int nfull = len / kStageFloats;
-  float m = -INFINITY, s = 0.f;
-  if (tid == 0) {
-    sh.stream_fail = 0;
-    for (int k = 0; k < kStreamStages; ++k) tc::mbar_init(reinterpret_cast<uint64_t*>(&sh.stage_bar[k]), 1);
-    tc::mbar_fence_init();
+  // block reduction of (m, s)
+  for (int o = 16; o; o >>= 1) {
+    float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    float M = fmaxf(m, m2);
+    float a1 = (s == 0.f) ? 0.f : s * ex2((m - M) * kLog2e);
+    float a2 = (s2 == 0.f) ? 0.f : s2 * ex2((m2 - M) * kLog2e);
+    m = M; s = a1 + a2;
+  }
+  const int lane = tid & 31, warp = tid >> 5;
+  if (lane == 0) { sh.red_m[warp] = m; sh.red_s[warp] = s; }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = kExpandThreads / 32;
+    m = lane < nw ? sh.red_m[lane] : -INFINITY;
+    s = lane < nw ? sh.red_s[lane] : 0.f;
+    for (int o = 16; o; o >>= 1) {
+      float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      float M = fmaxf(m, m2);
+      float a1 = (s == 0.f) ? 0.f : s * ex2((m - M) * kLog2e);
+      float a2 = (s2 == 0.f) ? 0.f : s2 * ex2((m2 - M) * kLog2e);
+      m = M; s = a1 + a2;
+    }
+    if (lane == 0) { sh.red_m[0] = m; sh.red_s[0] = s; }
   }
   __syncthreads();
-  if (tid == 0) {
-    const int pre = nfull < kStreamStages ? nfull : kStreamStages;
-    for (int k = 0; k < pre; ++k) {
-      uint64_t* bar = reinterpret_cast<uint64_t*>(&sh.stage_bar[k]);
-      tc::mbar_expect_tx(bar, kStageFloats * 4);
-      bulk_load(ring + k * kStageFloats, base + (size_t)k * kStageFloats, kStageFloats * 4, bar);
-    }
-  }
-  int issued_hi = nfull < kStreamStages ? nfull : kStreamStages;   // thread 0's view
-  for (int k = 0; k < nfull; ++k) {
-    const int slot = k % kStreamStages;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(&sh.stage_bar[slot]);
-    const uint32_t parity = (uint32_t)(k / kStreamStages) & 1u;
-    if (!tc::mbar_wait(bar, parity)) sh.stream_fail = 1;
-    __syncthreads();
-    if (sh.stream_fail) break;
-    const float4 v = reinterpret_cast<const float4*>(ring + slot * kStageFloats)[tid];
-    const float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-    if (mx > m) { s *= ex2((m - mx) * kLog2e); m = mx; }
-    const float mL = m * kLog2e;
-    s += (ex2(fmaf(v.x, kLog2e, -mL)) + ex2(fmaf(v.y, kLog2e, -mL))) +
-         (ex2(fmaf(v.z, kLog2e, -mL)) + ex2(fmaf(v.w, kLog2e, -mL)));
-    __syncthreads();   // the slot is consumed by every thread
-    if (tid == 0 && k + kStreamStages < nfull) {
-      tc::mbar_expect_tx(bar, kStageFloats * 4);
-      bulk_load(ring + slot * kStageFloats, base + (size_t)(k + kStreamStages) * kStageFloats,
-                kStageFloats * 4, bar);
-      issued_hi = k + kStreamStages + 1;
-    }
-  }
-  if (sh.stream_fail) {
+  const float2 res = make_float2(sh.red_m[0], sh.red_s[0]);
+  __syncthreads();
+  return res;
+}
+
+
+// a1 on its own: S blocks per live logits row each fold (max, sum of exp) of
+// one chunk; the last of them (a per-row ticket) combines the chunks into the
+// row's log-sum-exp.  Kept free of the selection code so that it stays at 32
+// registers and four 512-thread blocks per SM keep enough loads in flight.
+__global__ void __launch_bounds__(kExpandThreads, 4)
+bd_lse_kernel(SelectArgs a) {
+  __shared__ ExpandShared sh;
+  const int S = a.row_splits;
+  const int b = blockIdx.x / S, sidx = blockIdx.x - b * S, r = blockIdx.y, tid = threadIdx.x;
+  if (b >= a.n_live_in[r]) return;
+  SelWs ws = carve(a.ws, a.R, a.W, a.Kp);
+  const size_t rowi = (size_t)r * a.W + b;
+  const float* row = a.logits + rowi * (size_t)a.row_stride;
+  const int c0 = sidx * a.row_chunk;
+  const int c1 = min(a.V, c0 + a.row_chunk);
+  const float2 ms = stream_max_sum(row, c0, c1, sh);
+  float lse;
+  if (S == 1) {
+    lse = ms.x + logf(ms.y);
+  } else {
     if (tid == 0) {
-      set_status(hdr, BEAMDEC_ERR_TIMEOUT);
-      for (int k = 0; k < issued_hi; ++k)   // let started copies land before the block moves on
-        tc::mbar_wait(reinterpret_cast<uint64_t*>(&sh.stage_bar[k % kStreamStages]),
-                      (uint32_t)(k / kStreamStages) & 1u);
+      ws.rowpart[rowi * kMaxRowSplits + sidx] = ms;
+      __threadfence();
+      sh.count = atomicAdd(ws.rowtick + rowi, 1);
     }
     __syncthreads();
-    return make_float2(NAN, NAN);
+    if (sh.count != S - 1) return;
+    __threadfence();
+    if (tid < 32) {   // one warp: lane k holds chunk k's (max, sum)
+      const float2 p = tid < S ? __ldcg(ws.rowpart + rowi * kMaxRowSplits + tid)
+                               : make_float2(-INFINITY, 0.f);
+      float M = p.x;
+      for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float tot = (p.y > 0.f) ? p.y * ex2((p.x - M) * kLog2e) : 0.f;
+      for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      if (tid == 0) sh.lse = M + logf(tot);
+    }
+    __syncthreads();
+    lse = sh.lse;
   }
-  // tail shorter than one stage
-  for (int j = nfull * kStageFloats + tid; j < len; j += kExpandThreads) {
-    const float x = __ldg(base + j);
-    if (x > m) { s *= ex2((m - x) * kLog2e); m = x; }
-    s += ex2((x - m) * kLog2e);
+  if (tid == 0) {
+    ws.rowlse[rowi] = lse;
+    if (a.lse_out != nullptr) a.lse_out[rowi] = lse;
   }
-  return block_reduce_ms(m, s, sh);
 }
 
 // Rows a2-a3 for beam b of request r: log-sum-exp, trie children, per-beam
@@ -327,7 +289,7 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
   const size_t rowi = (size_t)r * a.W + b;
   const float* row = a.logits + rowi * (size_t)a.row_stride;
 
-  if (a.lse_out != nullptr && tid == 0) a.lse_out[rowi] = lse;
+  if (a.lse_in != nullptr && a.lse_out != nullptr && tid == 0) a.lse_out[rowi] = lse;
   const float cum = a.cum_in[rowi];
 
   // ---- a2: candidate range (trie children or the whole vocabulary) --------
@@ -658,58 +620,17 @@ selected:
 }
 
 template <bool kFused>
-__global__ void __launch_bounds__(kExpandThreads, 3)
+__global__ void __launch_bounds__(kExpandThreads)
 bd_expand_kernel(SelectArgs a) {
   __shared__ ExpandShared sh;
   extern __shared__ __align__(16) unsigned char tail_smem[];
-  const int S = a.row_splits;
-  const int b = blockIdx.x / S, sidx = blockIdx.x - b * S, r = blockIdx.y, tid = threadIdx.x;
+  const int b = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
   SelWs ws = carve(a.ws, a.R, a.W, a.Kp);
-  if (blockIdx.x == 0 && r == 0 && tid == 0) ws.hdr->bar_count = 0u;
+  if (b == 0 && r == 0 && tid == 0) ws.hdr->bar_count = 0u;
   const int nl = a.n_live_in[r];
   if (b >= nl) return;
   const size_t rowi = (size_t)r * a.W + b;
-  // ---- a1: log-sum-exp over the full vocabulary.  S blocks stream one
-  // chunk of the row each; the last of them to finish combines the chunks'
-  // (max, sum) and carries on with the row.
-  float lse;
-  if (a.lse_in != nullptr) {
-    if (sidx != 0) return;
-    lse = a.lse_in[rowi];
-  } else {
-    const float* row = a.logits + rowi * (size_t)a.row_stride;
-    const int chunk = a.row_chunk;
-    const int c0 = sidx * chunk;
-    const int c1 = min(a.V, c0 + chunk);
-    const float* base = row + c0;
-    const float2 ms = ((reinterpret_cast<uintptr_t>(base) & 15u) == 0)
-                          ? stream_max_sum_bulk(base, c1 - c0, sh,
-                                                reinterpret_cast<float*>(tail_smem), ws.hdr)
-                          : stream_max_sum(row, c0, c1, sh);
-    if (S == 1) {
-      lse = ms.x + logf(ms.y);
-    } else {
-      if (tid == 0) {
-        ws.rowpart[rowi * kMaxRowSplits + sidx] = ms;
-        __threadfence();
-        sh.count = atomicAdd(ws.rowtick + rowi, 1);
-      }
-      __syncthreads();
-      if (sh.count != S - 1) return;
-      __threadfence();
-      if (tid < 32) {   // one warp: lane k holds chunk k's (max, sum)
-        const float2 p = tid < S ? __ldcg(ws.rowpart + rowi * kMaxRowSplits + tid)
-                                 : make_float2(-INFINITY, 0.f);
-        float M = p.x;
-        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float tot = (p.y > 0.f) ? p.y * ex2((p.x - M) * kLog2e) : 0.f;
-        for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-        if (tid == 0) sh.lse = M + logf(tot);
-      }
-      __syncthreads();
-      lse = sh.lse;
-    }
-  }
+  const float lse = a.lse_in != nullptr ? a.lse_in[rowi] : __ldcg(ws.rowlse + rowi);
   // dynamic shared memory: [key cache 16 KB][score-bin histogram 16 KB, fused only];
   // the fused tail reuses all of it for candidate keys after the ticket
   uint32_t* kcache = reinterpret_cast<uint32_t*>(tail_smem);
@@ -893,23 +814,14 @@ size_t select_workspace_bytes(int R, int W, int K, int V) {
   return kWsHeaderBytes + align256((size_t)R * sizeof(SelState)) +
          align256((size_t)R * W * sizeof(int32_t)) +
          align256((size_t)R * kBins * sizeof(uint32_t)) + align256((size_t)R * W * Kp * 8) +
-         align256((size_t)R * kSelectCap * 8) + (size_t)R * W * kMaxRowSplits * sizeof(float2);
+         align256((size_t)R * kSelectCap * 8) +
+         align256((size_t)R * W * kMaxRowSplits * sizeof(float2)) + (size_t)R * W * sizeof(float);
 }
 
 int launch_select(const SelectArgs& a, cudaStream_t stream) {
   static GlobalLaunchCfg cfg[64];
-  static bool expand_attr[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BEAMDEC_ERR_CUDA;
-  if (!expand_attr[dev]) {
-    const int dyn = kStreamStages * kStageFloats * 4;
-    if (cudaFuncSetAttribute(bd_expand_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             dyn) != cudaSuccess ||
-        cudaFuncSetAttribute(bd_expand_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             dyn) != cudaSuccess)
-      return BEAMDEC_ERR_CUDA;
-    expand_attr[dev] = true;
-  }
   const size_t smem = kGlobalKeysOffset + (size_t)kSelectCap * 8;
   if (cfg[dev].max_blocks == 0) {
     if (cudaFuncSetAttribute(bd_global_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -936,18 +848,23 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
   const size_t zero_bytes = (char*)ws.pool - (char*)ws.state;
   if (cudaMemsetAsync(ws.state, 0, zero_bytes, stream) != cudaSuccess) return BEAMDEC_ERR_CUDA;
 
-  dim3 g1(a.W * S, a.R);
+  if (a.lse_in == nullptr) {
+    dim3 g0(a.W * S, a.R);
+    prof_begin(kKLse, stream);
+    bd_lse_kernel<<<g0, kExpandThreads, 0, stream>>>(a2);
+    prof_end(kKLse, stream);
+    if (cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
+  }
+  dim3 g1(a.W, a.R);
   // Pools of at most 1M keys per request (W <= 4096) are selected by the last
   // expand block of each request; larger ones by the cooperative grid kernel.
   const bool fused = a.W <= kTailCap && (long long)a.W * a.Kp <= (1ll << 20);
   prof_begin(kKExpand, stream);
   static_assert(kKeyCache * 4 + kTailBins * 4 <= kTailCap * 8, "fused dynamic shared memory");
-  static_assert(kStreamStages * kStageFloats * 4 >= kTailCap * 8, "ring covers the tail buffer");
-  const size_t dyn = (size_t)kStreamStages * kStageFloats * 4;   // 64 KB, reused after the stream
   if (fused)
-    bd_expand_kernel<true><<<g1, kExpandThreads, dyn, stream>>>(a2);
+    bd_expand_kernel<true><<<g1, kExpandThreads, kTailCap * sizeof(unsigned long long), stream>>>(a2);
   else
-    bd_expand_kernel<false><<<g1, kExpandThreads, dyn, stream>>>(a2);
+    bd_expand_kernel<false><<<g1, kExpandThreads, kKeyCache * sizeof(uint32_t), stream>>>(a2);
   prof_end(kKExpand, stream);
   if (cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
   if (fused) return BEAMDEC_OK;
