@@ -10,17 +10,19 @@
 //
 // One CTA owns 256 query rows (two 128-row tiles) of one (request, kv head,
 // prompt split), so every K/V tile it loads feeds two tiles of MMAs:
-//   warp 8       TMA producer: Q once, then K and V tiles of 128 keys (two
+//   warp 16      TMA producer: Q once, then K and V tiles of 128 keys (two
 //                64-column SWIZZLE_128B boxes each) through a 3-slot ring;
-//   warp 9       allocates TMEM and issues every MMA from one thread, in the
+//   warp 17      allocates TMEM and issues every MMA from one thread, in the
 //                order S0(c) S1(c) | PV0(c) S0(c+1) | PV1(c) S1(c+1) | ... so
 //                the tensor core works on one tile while the other tile's
 //                softmax runs;
-//   warps 0-3    softmax of tile 0, warps 4-7 softmax of tile 1: thread t
-//                owns row t (TMEM lane t); reads its 128 scores from TMEM
-//                twice (row max, then P; one 128-column load each), keeps
-//                max/sum in log2 units, writes P (bf16) into shared memory in
-//                the 128B-swizzled K-major layout the MMA reads.
+//   warps 0-7    softmax of tile 0, warps 8-15 softmax of tile 1: two
+//                threads per row (TMEM lane), each owning 64 of the 128 score
+//                columns; they read their scores from TMEM twice (row max,
+//                then P), trade partial maxima through shared memory, keep
+//                max/sum in log2 units and write their half of P (bf16) in the
+//                128B-swizzled K-major layout the MMA reads.  Four softmax
+//                warps per SM sub-partition hide each other's latencies.
 // The output O accumulates in TMEM across chunks (S0 O0 S1 O1, 128 columns
 // each).  The running max used for P only moves when a chunk's max exceeds
 // it by more than 2^8; then the warp rescales its O rows in TMEM before the
@@ -46,7 +48,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 320;   // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr int kThreads = 576;   // warps 0-15 softmax, 16 TMA, 17 MMA
 constexpr uint32_t kHalfBytes = 16384;           // 128 rows x 128 B
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 128 x 128 bf16
 constexpr int kSlots = 3;                        // K/V ring
@@ -81,6 +83,7 @@ struct Bars {
   uint64_t kv_full[kSlots], kv_empty[kSlots];
   uint64_t s_full[2], s_free[2], p_full[2];
   uint64_t done;
+  uint64_t xchg[2][4];   // per (tile, row group): both column halves have left their partial
 };
 
 // One lane polls (bounded), the warp agrees, then every lane observes the
@@ -165,19 +168,21 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars.s_full[t], 1);
-      mbar_init(&bars.s_free[t], 128);
-      mbar_init(&bars.p_full[t], 128);
+      mbar_init(&bars.s_free[t], 256);
+      mbar_init(&bars.p_full[t], 256);
     }
     mbar_init(&bars.done, 1);
+    for (int tt = 0; tt < 2; ++tt)
+      for (int q = 0; q < 4; ++q) mbar_init(&bars.xchg[tt][q], 64);
     mbar_fence_init();
   }
-  if (warp == 9) tmem_alloc(&tmem_base_sh, kTmemCols);
+  if (warp == 17) tmem_alloc(&tmem_base_sh, kTmemCols);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp == 8 && lane == 0) {
+  if (warp == 16 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     prefetch_tmap(&qmap);
     prefetch_tmap(&kmap);
@@ -207,7 +212,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       for (int i = (issued > kSlots ? issued - kSlots : 0); i < issued; ++i)
         mbar_wait(&bars.kv_full[i % kSlots], (uint32_t)(i / kSlots) & 1);
     }
-  } else if (warp == 9 && lane == 0) {
+  } else if (warp == 17 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
     const uint32_t idO = idesc_bf16_f32(128, 128, false, true);
@@ -271,51 +276,65 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     }
     if (ok) mma_commit(&bars.done);
     else abort_sh = 1;
-  } else if (warp < 8) {
+  } else if (warp < 16) {
     // ------------------------------------------------------------ softmax rows
-    const int t = warp >> 2;                       // tile
-    const int row_in_tile = threadIdx.x - t * 128;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + t * 256 + lane_off;
-    const uint32_t tO = tS + 128;
+    // warp w: tile t = w / 8, column half hf = (w / 4) % 2, TMEM lanes of
+    // row group w % 4; thread (t, hf, row) owns columns [64 hf, 64 hf + 64)
+    // of that row.  The two halves of a row exchange their partial max
+    // through shared memory, paired by one mbarrier per row group (bounded
+    // waits, so a broken partner cannot hang the other half).
+    const int t = warp >> 3;
+    const int hf = (warp >> 2) & 1;
+    const int lg = warp & 3;
+    const int row_in_tile = lg * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+    const uint32_t tS = tmem + t * 256 + lane_off + hf * 64;
+    const uint32_t tO = tmem + t * 256 + 128 + lane_off + hf * 64;
     const float sc = p.scale_log2 * (p.k_scale ? p.k_scale[g] : 1.f);
-    unsigned char* Ps = sm + kOffP + t * kTileBytes;
+    unsigned char* Ph = sm + kOffP + t * kTileBytes + hf * kHalfBytes;
+    // partial-max exchange: a thread leaves its value in the partner's half of
+    // the P tile (row line), reads the partner's value from its own half, and
+    // only then overwrites its own half with P; the tile is free here because
+    // the commit that signalled S_t(c) covers PV_t(c-1)
+    float* x_mine = reinterpret_cast<float*>(sm + kOffP + t * kTileBytes + hf * kHalfBytes +
+                                             row_in_tile * 128);
+    float* x_partner = reinterpret_cast<float*>(sm + kOffP + t * kTileBytes + (hf ^ 1) * kHalfBytes +
+                                                row_in_tile * 128);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int c = 0; c < nchunks; ++c) {
       if (!warp_wait(&bars.s_full[t], c & 1)) { ok = false; break; }
       fence_after_sync();
-      // pass 1: the chunk's row max (one 128-column TMEM load); only the last
-      // chunk of a split can hold fewer than 128 keys, so the full case runs
-      // without per-element masks
-      const int nvalid = min(128, k1 - (k0 + c * 128));
-      const bool full = nvalid == 128;
+      const int nvalid = min(128, k1 - (k0 + c * 128)) - hf * 64;   // valid columns of this half
       float mx = -INFINITY;
       {
-        float sv[128];
-        tmem_ld128(tS, sv);
-        if (full) {   // pairwise tree: depth 7 instead of a 128-long chain
+        float sv[64];
+        tmem_ld64(tS, sv);
+        if (nvalid >= 64) {   // pairwise tree: depth 6
 #pragma unroll
-          for (int w = 64; w >= 1; w >>= 1) {
+          for (int w = 32; w >= 1; w >>= 1) {
 #pragma unroll
             for (int i = 0; i < w; ++i) sv[i] = fmaxf(sv[i], sv[i + w]);
           }
           mx = sv[0];
         } else {
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
+          for (int i = 0; i < 64; ++i)
             if (i < nvalid) mx = fmaxf(mx, sv[i]);
         }
       }
-      mx *= sc;
+      *x_partner = mx;
+      mbar_arrive(&bars.xchg[t][lg]);
+      if (!warp_wait(&bars.xchg[t][lg], c & 1)) { ok = false; break; }
+      mx = fmaxf(mx, *x_mine) * sc;
       const bool need = mx > m_used + kRescale;
-      if (__any_sync(0xffffffffu, need)) {
+      if (__any_sync(0xffffffffu, need)) {   // the partner warp holds the same rows: same outcome
         const float m_new = need ? mx : m_used;
         const float factor = ex2(m_used - m_new);   // 0 on the first chunk, 1 for rows that keep m
         l *= factor;
         if (c > 0) {   // O_t holds chunks < c (their PV completed before S_t(c) was signalled)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < 2; ++q) {
             float v[32];
             tmem_ld32(tO + q * 32, v);
 #pragma unroll
@@ -326,17 +345,17 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         }
         m_used = m_new;
       }
-      // pass 2: P = 2^(s - m) as bf16 into the swizzled K-major tile
-      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;   // four independent chains
-      float sv[128];
-      tmem_ld128(tS, sv);
-      if (!full) {
+      // P = 2^(s - m) as bf16 into this half of the swizzled K-major tile
+      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+      float sv[64];
+      tmem_ld64(tS, sv);
+      if (nvalid < 64) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
+        for (int i = 0; i < 64; ++i)
           if (i >= nvalid) sv[i] = -INFINITY;
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -350,11 +369,10 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
           const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
           pk[i] = *reinterpret_cast<const uint32_t*>(&b);
         }
-        const int half = q >> 1;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const int chunk = (q & 1) * 4 + k;
-          uint4* dst = reinterpret_cast<uint4*>(Ps + half * kHalfBytes + row_in_tile * 128 +
+          const int chunk = q * 4 + k;
+          uint4* dst = reinterpret_cast<uint4*>(Ph + row_in_tile * 128 +
                                                 ((chunk ^ (row_in_tile & 7)) << 4));
           *dst = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
@@ -369,12 +387,23 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     if (ok && !warp_wait(&bars.done, 0)) ok = false;
     if (!ok) abort_sh = 1;
     const int row = row0 + t * 128 + row_in_tile;
+    // the row's sum is the sum of both halves' partial sums (the P tile is
+    // free once the last PV has completed)
+    bool xok = false;
+    if (ok) {
+      *x_partner = l;
+      mbar_arrive(&bars.xchg[t][lg]);
+      xok = warp_wait(&bars.xchg[t][lg], nchunks & 1);
+      if (!xok) abort_sh = 1;
+    }
+    const float l_row = xok ? l + *x_mine : l;
+    ok = ok && xok;
     if (ok) {
       fence_after_sync();
       const size_t pi = prow_base + row;
-      float4* o = reinterpret_cast<float4*>(p.po + pi * 128);
+      float4* o = reinterpret_cast<float4*>(p.po + pi * 128 + hf * 64);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         float v[32];
         tmem_ld32(tO + q * 32, v);
         if (row < p.rows) {
@@ -383,16 +412,16 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
             o[q * 8 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
       }
-      if (row < p.rows) {
+      if (row < p.rows && hf == 0) {
         p.pm[pi] = m_used;
-        p.pl[pi] = l;
+        p.pl[pi] = l_row;
       }
     }
   }
   fence_before_sync();
   __syncthreads();
   if (abort_sh && threadIdx.x == 0) set_status(p.hdr, BEAMDEC_ERR_TIMEOUT);
-  if (warp == 9) {
+  if (warp == 17) {
     fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
