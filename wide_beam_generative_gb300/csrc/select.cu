@@ -87,9 +87,11 @@ __host__ __device__ inline SelWs carve(void* ws, int R, int W, int Kp) {
 __device__ void warp_find_digit(const volatile uint32_t* hist, int nbins, uint32_t need,
                                 uint32_t* D, uint32_t* below) {
   const int lane = threadIdx.x & 31;
-  const int per = nbins / 32;
+  const int per = nbins / 32;   // a power of two
   uint32_t sum = 0;
-  for (int i = 0; i < per; ++i) sum += hist[lane * per + i];
+  // lane l sums bins [l*per, (l+1)*per) starting at offset l: when per is a
+  // multiple of 32 the 32 lanes of one load hit 32 different banks
+  for (int i = 0; i < per; ++i) sum += hist[lane * per + ((i + lane) & (per - 1))];
   uint32_t incl = sum;
   for (int o = 1; o < 32; o <<= 1) {
     uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
@@ -130,6 +132,49 @@ __device__ __forceinline__ int block_rank(int flag, int* warp_cnt, int* total) {
   return base + r;
 }
 
+// Adds one to hist[bin] for every lane with `on`: lanes that share a bin add
+// their count once, so a histogram whose keys crowd into a few bins costs one
+// atomic per bin and warp instead of one per key.  Every lane of the warp
+// calls it (shared or global memory).
+__device__ __forceinline__ void warp_hist_add(uint32_t* hist, uint32_t bin, bool on) {
+  const unsigned act = __ballot_sync(0xffffffffu, on);
+  if (on) {
+    const unsigned peers = __match_any_sync(act, bin);
+    if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(hist + bin, (uint32_t)__popc(peers));
+  }
+}
+
+// Reserves one slot of *counter for every lane with `on` (one atomic per
+// warp) and returns this lane's slot (unordered across warps).  Every lane of
+// the warp calls it.
+__device__ __forceinline__ int warp_reserve(int* counter, bool on) {
+  const unsigned act = __ballot_sync(0xffffffffu, on);
+  const int lane = threadIdx.x & 31;
+  const int leader = act ? __ffs(act) - 1 : 0;
+  int base = 0;
+  if (act && lane == leader) base = atomicAdd(counter, __popc(act));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return base + __popc(act & ((1u << lane) - 1u));
+}
+
+// Reserves one slot of cursor[bin] for every lane with `on`; lanes that share
+// a bin take consecutive slots with one atomic.  Every lane of the warp calls
+// it; lanes without `on` get 0.
+__device__ __forceinline__ uint32_t warp_bin_reserve(uint32_t* cursor, uint32_t bin, bool on) {
+  const unsigned act = __ballot_sync(0xffffffffu, on);
+  const int lane = threadIdx.x & 31;
+  uint32_t base = 0;
+  int leader = 0;
+  unsigned peers = 0;
+  if (on) {
+    peers = __match_any_sync(act, bin);
+    leader = __ffs(peers) - 1;
+    if (lane == leader) base = atomicAdd(cursor + bin, (uint32_t)__popc(peers));
+  }
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return on ? base + (uint32_t)__popc(peers & ((1u << lane) - 1u)) : 0u;
+}
+
 // Coarse bin of a candidate score relative to a per-request reference score
 // (the score of the request's rank-0 beam): floor((ref - s) * 64), clamped to
 // [0, 4095].  It is monotone (a higher score never gets a higher bin), so a
@@ -152,6 +197,7 @@ struct ExpandShared {
   int count;
   int pool_base;
   float lse;
+  uint32_t c_le;
 };
 
 // Running (max, sum of exp(x - max)) of row[c0..c1) for the whole block,
@@ -281,7 +327,11 @@ bd_lse_kernel(SelectArgs a) {
 
 // Rows a2-a3 for beam b of request r: log-sum-exp, trie children, per-beam
 // top_k appended to the request's pool.
-__device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
+// `bins` (shared memory, fused launches only) collects the score bins of a
+// row that goes through the radix select; rows whose children all enter the
+// pool add theirs straight to the request's histogram in global memory.
+// Returns true when `bins` holds counts the caller must flush.
+__device__ __forceinline__ bool expand_candidates(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
                                                  int r, int b, uint32_t* bins, uint32_t* kcache,
                                                  float lse) {
   const int tid = threadIdx.x;
@@ -300,7 +350,7 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
     const int node = a.node_in[rowi];
     if (node < 0 || node >= a.lvl.n_nodes) {
       if (tid == 0) set_status(ws.hdr, BEAMDEC_ERR_DEVICE_CHECK);
-      return;
+      return false;
     }
     const int e0 = a.lvl.off[node];
     n = a.lvl.off[node + 1] - e0;
@@ -319,14 +369,23 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
 
   // ---- a3: per-beam top_k -------------------------------------------------
   if (n <= a.K) {
+    // the first round's gathers are in flight while the pool slots are reserved
+    const uint32_t k_first = tid < n ? key_of(tok_of(tid)) : 0u;
     if (tid == 0) sh.pool_base = n > 0 ? atomicAdd(&st->total, n) : 0;
     __syncthreads();
-    for (int i = tid; i < n; i += kExpandThreads) {
-      const uint32_t k = key_of(tok_of(i));
-      pool[sh.pool_base + i] = pool_key(k, b, i);
-      if (bins) atomicAdd(&bins[score_bin(ref, desc_key_value(k))], 1u);
+    const int base = sh.pool_base;
+    uint32_t* gh = bins ? ws.hist + (size_t)r * kBins : nullptr;
+    for (int c0 = 0; c0 < n; c0 += kExpandThreads) {   // block-uniform trip count
+      const int i = c0 + tid;
+      const bool on = i < n;
+      const uint32_t k = c0 == 0 ? k_first : (on ? key_of(tok_of(i)) : 0u);
+      if (on) pool[base + i] = pool_key(k, b, i);
+      if (gh) warp_hist_add(gh, (uint32_t)score_bin(ref, desc_key_value(k)), on);
     }
-    return;
+    return false;
+  }
+  if (bins) {
+    for (int i = tid; i < kTailBins; i += kExpandThreads) bins[i] = 0;   // ordered by the passes' barriers
   }
   // the row's candidate keys, computed once into shared memory when they fit
   // (the radix passes below then read shared memory instead of re-gathering)
@@ -346,10 +405,11 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
     const int sh_next = shift - w;
     for (int i = tid; i < nb; i += kExpandThreads) sh.hist[i] = 0;
     __syncthreads();
-    for (int i = tid; i < n; i += kExpandThreads) {
-      const uint32_t k = kc(i);
-      if (shift == 32 || (k >> shift) == (prefix >> shift))
-        atomicAdd(&sh.hist[(k >> sh_next) & (nb - 1)], 1u);
+    for (int c0 = 0; c0 < n; c0 += kExpandThreads) {   // block-uniform trip count
+      const int i = c0 + tid;
+      const uint32_t k = i < n ? kc(i) : 0u;
+      const bool on = i < n && (shift == 32 || (k >> shift) == (prefix >> shift));
+      warp_hist_add(sh.hist, (k >> sh_next) & (nb - 1), on);
     }
     __syncthreads();
     if (tid < 32) warp_find_digit(sh.hist, nb, need, &sh.digit, &sh.below);
@@ -363,12 +423,13 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
   if (tid == 0) { sh.count = 0; sh.pool_base = atomicAdd(&st->total, a.K); }
   __syncthreads();
   const int base = sh.pool_base;
-  for (int i = tid; i < n; i += kExpandThreads) {
-    const uint32_t k = kc(i);
-    if (k < kth) {
-      pool[base + atomicAdd(&sh.count, 1)] = pool_key(k, b, i);
-      if (bins) atomicAdd(&bins[score_bin(ref, desc_key_value(k))], 1u);
-    }
+  for (int c0 = 0; c0 < n; c0 += kExpandThreads) {   // block-uniform trip count
+    const int i = c0 + tid;
+    const uint32_t k = i < n ? kc(i) : 0u;
+    const bool on = i < n && k < kth;
+    const int pos = warp_reserve(&sh.count, on);
+    if (on) pool[base + pos] = pool_key(k, b, i);
+    if (bins) warp_hist_add(bins, (uint32_t)score_bin(ref, desc_key_value(k)), on);
   }
   __syncthreads();
   const int n_less = sh.count;
@@ -379,12 +440,12 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
     if (i < n) flag = kc(i) == kth;
     int tot;
     const int rk = block_rank(flag, sh.warp_cnt, &tot);
-    if (flag && taken + rk < (int)need) {
-      pool[base + n_less + taken + rk] = pool_key(kth, b, i);
-      if (bins) atomicAdd(&bins[score_bin(ref, desc_key_value(kth))], 1u);
-    }
+    const bool on = flag && taken + rk < (int)need;
+    if (on) pool[base + n_less + taken + rk] = pool_key(kth, b, i);
+    if (bins) warp_hist_add(bins, (uint32_t)score_bin(ref, desc_key_value(kth)), on);
     taken += tot;
   }
+  return bins != nullptr;
 }
 
 // Ascending bitonic sort of np (a power of two) 64-bit keys in shared memory.
@@ -445,15 +506,48 @@ __device__ void emit_outputs(const SelectArgs& a, const SelWs& ws, int r,
   if (tid == 0) a.n_live_out[r] = nt;
 }
 
-// Writes the nt smallest of the n distinct keys src[0..n) to dst[0..nt) in
-// ascending order: each key's rank is the count of smaller keys.
-__device__ void rank_sort(const unsigned long long* src, int n, int nt, unsigned long long* dst) {
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const unsigned long long k = src[i];
-    int rank = 0;
-    for (int m = 0; m < n; ++m) rank += src[m] < k ? 1 : 0;
-    if (rank < nt) dst[rank] = k;
+// Sorts keys[0..n) ascending in place, n <= 2 * kExpandThreads, called by
+// every thread of a kExpandThreads-thread block.  A bitonic network over
+// 2 * kExpandThreads slots held in registers, slots t and t + kExpandThreads
+// by thread t: partners closer than 32 slots are exchanged by warp shuffles,
+// farther ones through keys[] itself.  Pad slots hold ~0, above every pool
+// key (bit 31 of a pool key is always 0), so they sort last.
+__device__ void block_sort_small(unsigned long long* keys, int n) {
+  constexpr int kH = kExpandThreads;
+  const int t = threadIdx.x;
+  unsigned long long x0 = t < n ? keys[t] : ~0ull;
+  unsigned long long x1 = t + kH < n ? keys[t + kH] : ~0ull;
+  __syncthreads();   // every read above precedes the exchange writes below
+  for (int k = 2; k <= 2 * kH; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j == kH) {   // k == 2 kH: both slots of the thread, ascending
+        const unsigned long long lo = x0 < x1 ? x0 : x1, hi = x0 < x1 ? x1 : x0;
+        x0 = lo;
+        x1 = hi;
+        continue;
+      }
+      unsigned long long y0, y1;
+      if (j >= 32) {
+        keys[t] = x0;
+        keys[t + kH] = x1;
+        __syncthreads();
+        y0 = keys[t ^ j];
+        y1 = keys[(t + kH) ^ j];   // == keys[(t ^ j) + kH]: j < kH leaves that bit alone
+        __syncthreads();
+      } else {
+        y0 = __shfl_xor_sync(0xffffffffu, x0, j);
+        y1 = __shfl_xor_sync(0xffffffffu, x1, j);
+      }
+      // slot s keeps the smaller of its pair when it is the lower slot of an
+      // ascending run or the upper slot of a descending one
+      const bool min0 = ((t & j) == 0) == ((t & k) == 0);
+      const bool min1 = (((t + kH) & j) == 0) == (((t + kH) & k) == 0);
+      x0 = min0 ? (x0 < y0 ? x0 : y0) : (x0 < y0 ? y0 : x0);
+      x1 = min1 ? (x1 < y1 ? x1 : y1) : (x1 < y1 ? y1 : x1);
+    }
   }
+  keys[t] = x0;
+  keys[t + kH] = x1;
   __syncthreads();
 }
 
@@ -471,9 +565,11 @@ __device__ uint32_t narrow_pass(const unsigned long long* keys, int n, unsigned 
   const int nb = (1 << w) < 32 ? 32 : (1 << w);
   for (int i = threadIdx.x; i < nb; i += blockDim.x) sh.hist[i] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const unsigned long long k = kGlobal ? __ldcg(keys + i) : keys[i];
-    if (shift == 64 || (k >> shift) == prefix) atomicAdd(&sh.hist[(uint32_t)(k >> nshift) & mask], 1u);
+  for (int c0 = 0; c0 < n; c0 += blockDim.x) {   // block-uniform trip count
+    const int i = c0 + threadIdx.x;
+    const unsigned long long k = i < n ? (kGlobal ? __ldcg(keys + i) : keys[i]) : 0ull;
+    const bool on = i < n && (shift == 64 || (k >> shift) == prefix);
+    warp_hist_add(sh.hist, (uint32_t)(k >> nshift) & mask, on);
   }
   __syncthreads();
   if (threadIdx.x < 32) warp_find_digit(sh.hist, nb, need, &sh.digit, &sh.below);
@@ -487,6 +583,46 @@ __device__ uint32_t narrow_pass(const unsigned long long* keys, int n, unsigned 
   return in_bin;
 }
 
+// In-place exclusive prefix sum of the kTailBins bins of hs (kExpandThreads
+// threads, 8 bins each), and the bin holding the need-th key (1-based,
+// need <= sum of all bins): sh.digit = that bin, sh.below = keys in lower
+// bins, sh.c_le = keys in it and below.
+__device__ void block_scan_bins(uint32_t* hs, uint32_t need, ExpandShared& sh) {
+  constexpr int kPer = kTailBins / kExpandThreads;
+  static_assert(kPer * kExpandThreads == kTailBins, "bins per thread");
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  if (t == 0) { sh.digit = kTailBins - 1; sh.below = 0; sh.c_le = 0; }
+  uint32_t v[kPer];
+  uint32_t sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    v[i] = hs[t * kPer + i];
+    sum += v[i];
+  }
+  uint32_t inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) sh.warp_cnt[warp] = (int)inc;
+  __syncthreads();
+  uint32_t run = inc - sum;
+  for (int w = 0; w < warp; ++w) run += (uint32_t)sh.warp_cnt[w];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const uint32_t c = v[j];
+    if (run < need && need <= run + c) {
+      sh.digit = (uint32_t)(t * kPer + j);
+      sh.below = run;
+      sh.c_le = run + c;
+    }
+    hs[t * kPer + j] = run;
+    run += c;
+  }
+  __syncthreads();
+}
+
 // Fused a4 for one request, run by the last expand block of the request:
 // select the min(W, pool) smallest pool keys, sort them, emit outputs.
 __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs& ws, int r,
@@ -495,55 +631,86 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
   const int total = st->total;
   const int nt = total < a.W ? total : a.W;
   const unsigned long long* pool = ws.pool + (size_t)r * a.W * a.Kp;
-  int nc;
-  if (total <= kTailCap) {
-    for (int i = threadIdx.x; i < total; i += blockDim.x) keys[i] = __ldcg(pool + i);
-    nc = total;
-  } else {
-    // the request's score-bin histogram (complete: every block flushed it
-    // before taking its ticket) brackets the nt-th best score
-    // copied to shared memory first (the upper half of the key buffer, free
-    // until the gather below), so the bin search reads shared memory
-    uint32_t* hs = reinterpret_cast<uint32_t*>(keys + kTailCap / 2);
+  if (total == 0) {
+    emit_outputs(a, ws, r, keys, 0);
+    return;
+  }
+  // the request's score-bin histogram (complete: every block added its
+  // candidates before taking its ticket), prefix-summed in shared memory (the
+  // upper half of the key buffer); it brackets the nt-th best score
+  uint32_t* hs = reinterpret_cast<uint32_t*>(keys + kTailCap / 2);
+  {
     const uint32_t* gh = ws.hist + (size_t)r * kBins;
     for (int i = threadIdx.x; i < kTailBins; i += blockDim.x) hs[i] = __ldcg(gh + i);
     __syncthreads();
-    if (threadIdx.x < 32) warp_find_digit(hs, kTailBins, (uint32_t)nt, &sh.digit, &sh.below);
-    __syncthreads();
-    const int Dbin = (int)sh.digit;
-    const uint32_t c_le = sh.below + hs[Dbin];
-    __syncthreads();
-    if (c_le <= (uint32_t)kTailCap) {
-      const float ref = a.cum_in[(size_t)r * a.W];
-      if (threadIdx.x == 0) sh.count = 0;
-      __syncthreads();
-      constexpr int kPer = 4;   // rounds of kPer x blockDim keys: the loads of a round overlap
-      for (int c0 = 0; c0 < total; c0 += kPer * blockDim.x) {
-        unsigned long long kv[kPer];
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-          const int i = c0 + u * blockDim.x + threadIdx.x;
-          kv[u] = i < total ? __ldcg(pool + i) : 0ull;
-        }
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-          const int i = c0 + u * blockDim.x + threadIdx.x;
-          const int flag =
-              (i < total) && score_bin(ref, desc_key_value((uint32_t)(kv[u] >> 32))) <= Dbin;
-          int tot;
-          const int rk = block_rank(flag, sh.warp_cnt, &tot);
-          const int pos = sh.count + rk;
-          if (flag && pos < kTailCap) keys[pos] = kv[u];
-          __syncthreads();
-          if (threadIdx.x == 0) sh.count += tot;
-          __syncthreads();
-        }
-      }
-      nc = sh.count < kTailCap ? sh.count : kTailCap;
-      goto selected;
-    }
+    block_scan_bins(hs, (uint32_t)nt, sh);
   }
-  if (total > kTailCap) {
+  const int Dbin = (int)sh.digit;
+  const uint32_t c_le = sh.c_le;
+  const float ref = a.cum_in[(size_t)r * a.W];
+  constexpr int kPer = 4;   // rounds of kPer x blockDim keys: the loads of a round overlap
+  if (c_le <= (uint32_t)(2 * kExpandThreads)) {
+    // bucket sort: the candidates of bins <= Dbin go to their bin's slots
+    // (hs[b] = first slot of bin b, advanced as slots fill), then each one's
+    // rank inside its bin settles its final place
+    unsigned long long* tmp = keys;
+    unsigned long long* sorted = keys + 2 * kExpandThreads;
+    for (int c0 = 0; c0 < total; c0 += kPer * kExpandThreads) {
+      unsigned long long kv[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int i = c0 + u * kExpandThreads + threadIdx.x;
+        kv[u] = i < total ? __ldcg(pool + i) : 0ull;
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int i = c0 + u * kExpandThreads + threadIdx.x;
+        const int bin = score_bin(ref, desc_key_value((uint32_t)(kv[u] >> 32)));
+        const bool on = i < total && bin <= Dbin;
+        const uint32_t slot = warp_bin_reserve(hs, (uint32_t)bin, on);
+        if (on && slot < c_le) tmp[slot] = kv[u];
+      }
+    }
+    __syncthreads();
+    // after the fill hs[b] is the end of bin b and hs[b - 1] its start
+    for (int j = threadIdx.x; j < (int)c_le; j += kExpandThreads) {
+      const unsigned long long k = tmp[j];
+      const int bin = score_bin(ref, desc_key_value((uint32_t)(k >> 32)));
+      const uint32_t end = min(hs[bin], c_le);
+      const uint32_t start = bin > 0 ? min(hs[bin - 1], end) : 0u;
+      uint32_t rank = start;
+      for (uint32_t m = start; m < end; ++m) rank += tmp[m] < k ? 1u : 0u;
+      if (rank < (uint32_t)nt) sorted[rank] = k;
+    }
+    __syncthreads();
+    emit_outputs(a, ws, r, sorted, nt);
+    return;
+  }
+  int nc = 0;
+  if (c_le <= (uint32_t)kTailCap) {
+    if (threadIdx.x == 0) sh.count = 0;
+    __syncthreads();
+    for (int c0 = 0; c0 < total; c0 += kPer * kExpandThreads) {
+      unsigned long long kv[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int i = c0 + u * kExpandThreads + threadIdx.x;
+        kv[u] = i < total ? __ldcg(pool + i) : 0ull;
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {   // the sort below orders them: slots are unordered
+        const int i = c0 + u * kExpandThreads + threadIdx.x;
+        const bool flag =
+            (i < total) && score_bin(ref, desc_key_value((uint32_t)(kv[u] >> 32))) <= Dbin;
+        const int pos = warp_reserve(&sh.count, flag);
+        if (flag && pos < kTailCap) keys[pos] = kv[u];
+      }
+    }
+    __syncthreads();
+    nc = sh.count < kTailCap ? sh.count : kTailCap;
+    goto selected;
+  }
+  {   // many candidates at about the same score: radix narrowing over the pool
     unsigned long long prefix = 0;
     int shift = 64;
     uint32_t need = (uint32_t)nt, sure = 0, in_bin = 0;
@@ -553,30 +720,21 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
     }
     if (threadIdx.x == 0) sh.count = 0;
     __syncthreads();
-    for (int c0 = 0; c0 < total; c0 += blockDim.x) {
+    for (int c0 = 0; c0 < total; c0 += blockDim.x) {   // block-uniform trip count
       const int i = c0 + threadIdx.x;
-      unsigned long long k = 0;
-      int flag = 0;
-      if (i < total) {
-        k = __ldcg(pool + i);
-        flag = (k >> shift) <= prefix;
-      }
-      int tot;
-      const int rk = block_rank(flag, sh.warp_cnt, &tot);
-      const int pos = sh.count + rk;
+      const unsigned long long k = i < total ? __ldcg(pool + i) : 0ull;
+      const bool flag = i < total && (k >> shift) <= prefix;
+      const int pos = warp_reserve(&sh.count, flag);
       if (flag && pos < kTailCap) keys[pos] = k;
-      __syncthreads();
-      if (threadIdx.x == 0) sh.count += tot;
-      __syncthreads();
     }
+    __syncthreads();
     nc = sh.count < kTailCap ? sh.count : kTailCap;
   }
 selected:
   __syncthreads();
-  unsigned long long* sorted = keys + kTailCap / 2;   // disjoint from keys[0..1024)
-  if (nc <= kTailCap / 4) {   // small candidate sets: rank directly
-    rank_sort(keys, nc, nt, sorted);
-    emit_outputs(a, ws, r, sorted, nt);
+  if (nc <= 2 * kExpandThreads) {   // small candidate sets: sort them all, keep the first nt
+    block_sort_small(keys, nc);
+    emit_outputs(a, ws, r, keys, nt);
     return;
   }
   if (nc > nt) {   // exact threshold: narrow until the keys at or below it number nt
@@ -606,9 +764,9 @@ selected:
       __syncthreads();
     }
   }
-  if (nt <= kTailCap / 4) {   // winners now in keys[0..nt)
-    rank_sort(keys, nt, nt, sorted);
-    emit_outputs(a, ws, r, sorted, nt);
+  if (nt <= 2 * kExpandThreads) {   // winners now in keys[0..nt)
+    block_sort_small(keys, nt);
+    emit_outputs(a, ws, r, keys, nt);
     return;
   }
   int np = 32;
@@ -634,18 +792,15 @@ bd_expand_kernel(SelectArgs a) {
   // dynamic shared memory: [key cache 16 KB][score-bin histogram 16 KB, fused only];
   // the fused tail reuses all of it for candidate keys after the ticket
   uint32_t* kcache = reinterpret_cast<uint32_t*>(tail_smem);
-  uint32_t* bins = nullptr;
-  if constexpr (kFused) {
-    bins = kcache + kKeyCache;
-    for (int i = tid; i < kTailBins; i += kExpandThreads) bins[i] = 0;
-    __syncthreads();
-  }
-  expand_candidates(a, sh, ws, r, b, bins, kcache, lse);
+  uint32_t* bins = kFused ? kcache + kKeyCache : nullptr;
+  const bool flush = expand_candidates(a, sh, ws, r, b, bins, kcache, lse);
   if constexpr (kFused) {
     __syncthreads();
-    uint32_t* gh = ws.hist + (size_t)r * kBins;
-    for (int i = tid; i < kTailBins; i += kExpandThreads)
-      if (bins[i]) atomicAdd(gh + i, bins[i]);
+    if (flush) {
+      uint32_t* gh = ws.hist + (size_t)r * kBins;
+      for (int i = tid; i < kTailBins; i += kExpandThreads)
+        if (bins[i]) atomicAdd(gh + i, bins[i]);
+    }
     // the last block of the request to finish runs the request's global top-W
     __syncthreads();
     if (tid == 0) {
