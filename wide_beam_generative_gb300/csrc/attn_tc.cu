@@ -10,26 +10,29 @@
 //
 // One CTA owns 256 query rows (two 128-row tiles) of one (request, kv head,
 // prompt split), so every K/V tile it loads feeds two tiles of MMAs:
-//   warp 16      TMA producer: Q once, then K and V tiles of 128 keys (two
-//                64-column SWIZZLE_128B boxes each) through a 3-slot ring;
-//   warp 17      allocates TMEM and issues every MMA from one thread, in the
+//   warp 8       TMA producer: Q once, then K and V tiles of 128 keys (two
+//                64-column SWIZZLE_128B boxes each) through a 5-slot ring
+//                (two and a half chunks ahead of the MMAs);
+//   warp 9       allocates TMEM and issues every MMA from one thread, in the
 //                order S0(c) S1(c) | PV0(c) S0(c+1) | PV1(c) S1(c+1) | ... so
 //                the tensor core works on one tile while the other tile's
 //                softmax runs;
-//   warps 0-7    softmax of tile 0, warps 8-15 softmax of tile 1: two
-//                threads per row (TMEM lane), each owning 64 of the 128 score
-//                columns; they read their scores from TMEM twice (row max,
-//                then P), trade partial maxima through shared memory, keep
-//                max/sum in log2 units and write their half of P (bf16) in the
-//                128B-swizzled K-major layout the MMA reads.  Four softmax
-//                warps per SM sub-partition hide each other's latencies.
+//   warps 0-3    softmax of tile 0, warps 4-7 softmax of tile 1: thread t
+//                owns row t (TMEM lane t); reads its 128 scores from TMEM
+//                twice (row max, then P; one 128-column load each), keeps
+//                max/sum in log2 units and writes P (bf16, two per column)
+//                back into TMEM over the first 64 columns of its S tile,
+//                where the PV MMA reads it as its A operand.
 // The output O accumulates in TMEM across chunks (S0 O0 S1 O1, 128 columns
-// each).  The running max used for P only moves when a chunk's max exceeds
+// each).  P_t(c) overwrites S_t(c) only after the softmax has read all of it,
+// and S_t(c+1) is issued after PV_t(c) by the same thread, so the tensor core
+// reads P before the next S lands on it.  The running max used for P only moves when a chunk's max exceeds
 // it by more than 2^8; then the warp rescales its O rows in TMEM before the
 // next PV.  That keeps P <= 2^8 and leaves the result exact.  The commit that
 // signals S_t(c+1) also covers PV_t(c) (a commit tracks every earlier MMA of
 // the issuing thread), so the softmax of chunk c+1 may overwrite P_t and
-// touch O_t once it has seen S_t(c+1).
+// touch O_t once it has seen S_t(c+1).  Keeping P out of shared memory frees
+// the ring's extra slots and the shared-memory bandwidth P would take.
 // Every mbarrier wait is bounded; a timeout records BEAMDEC_ERR_TIMEOUT, ends
 // the loops and still frees TMEM.
 #include <cuda.h>
@@ -48,14 +51,13 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 576;   // warps 0-15 softmax, 16 TMA, 17 MMA
+constexpr int kThreads = 320;   // warps 0-7 softmax, 8 TMA, 9 MMA
 constexpr uint32_t kHalfBytes = 16384;           // 128 rows x 128 B
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 128 x 128 bf16
-constexpr int kSlots = 3;                        // K/V ring
+constexpr int kSlots = 5;                        // K/V ring
 constexpr uint32_t kOffQ = 0;                    // Q0, Q1
 constexpr uint32_t kOffKV = 2 * kTileBytes;      // kSlots tiles
-constexpr uint32_t kOffP = kOffKV + kSlots * kTileBytes;  // P0, P1
-constexpr uint32_t kSmemBytes = kOffP + 2 * kTileBytes + 1024;
+constexpr uint32_t kSmemBytes = kOffKV + kSlots * kTileBytes + 1024;
 constexpr uint32_t kTmemCols = 512;              // S0 O0 S1 O1
 constexpr float kRescale = 8.f;                  // log2 headroom before O is rescaled
 
@@ -81,9 +83,8 @@ struct TcParams {
 struct Bars {
   uint64_t q;
   uint64_t kv_full[kSlots], kv_empty[kSlots];
-  uint64_t s_full[2], s_free[2], p_full[2];
+  uint64_t s_full[2], p_full[2];
   uint64_t done;
-  uint64_t xchg[2][4];   // per (tile, row group): both column halves have left their partial
 };
 
 // One lane polls (bounded), the warp agrees, then every lane observes the
@@ -113,6 +114,98 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---- packed fp32 pairs: one f32x2 instruction does two lanes' worth --------
+using f2 = unsigned long long;
+__device__ __forceinline__ f2 f2_pack(float a, float b) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(f2 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+  f2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
+  f2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2 f2_sub(f2 a, f2 b) {
+  f2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 2^x for a pair on the FMA pipe, to take part of the exponentials off the
+// MUFU unit whose ex2 rate bounds the softmax.  Cody and Waite's additive
+// range reduction x = n + f, n = round(x), f in [-1/2, 1/2] (adding 1.5 * 2^23
+// rounds x and leaves n in the low mantissa bits); 2^f from a cubic fitted to
+// 2^f in relative error on [-1/2, 1/2] (largest error 7.5e-5, far below the
+// 2^-9 of the bf16 P it feeds); n then goes into the exponent field: shifted
+// left by 23, the sum's bits are n << 23 (the magic number's bits vanish).  x
+// is clamped at -125 so the exponent stays normal; 2^-125 stands for 0 next
+// to a row sum of at least 1.
+__device__ __forceinline__ f2 exp2_poly2(f2 x) {
+  constexpr float kMagic = 12582912.f;   // 1.5 * 2^23
+  constexpr float c0 = 9.999280572e-01f, c1 = 6.932609677e-01f, c2 = 2.426111251e-01f,
+                  c3 = 5.517165363e-02f;
+  float2 xv = f2_unpack(x);
+  xv.x = fmaxf(xv.x, -125.f);
+  xv.y = fmaxf(xv.y, -125.f);
+  const f2 xc = f2_pack(xv.x, xv.y);
+  const f2 mg = f2_pack(kMagic, kMagic);
+  const f2 t = f2_add(xc, mg);
+  const f2 f = f2_sub(xc, f2_sub(t, mg));
+  f2 q = f2_fma(f2_pack(c3, c3), f, f2_pack(c2, c2));
+  q = f2_fma(q, f, f2_pack(c1, c1));
+  q = f2_fma(q, f, f2_pack(c0, c0));
+  const float2 tv = f2_unpack(t), qv = f2_unpack(q);
+  return f2_pack(__int_as_float(__float_as_int(qv.x) + (__float_as_int(tv.x) << 23)),
+                 __int_as_float(__float_as_int(qv.y) + (__float_as_int(tv.y) << 23)));
+}
+
+// P = 2^(s * sc - m) for the 128 scores of one row as bf16 pairs into TMEM
+// columns 0-63 of the row's S tile, and its sum (two f32x2 chains).  With
+// kPoly three of every eight pairs take the polynomial exponential.
+template <bool kPoly>
+__device__ __forceinline__ void softmax_row(const float (&sv)[128], float sc, float m_used,
+                                            uint32_t tS, f2& acc0, f2& acc1) {
+  const f2 scv = f2_pack(sc, sc), nm = f2_pack(-m_used, -m_used);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {   // keys 32q .. 32q+31 -> columns 16q .. 16q+15
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int k2 = q * 32 + 2 * i;
+      const f2 x = f2_fma(f2_pack(sv[k2], sv[k2 + 1]), scv, nm);
+      f2 pp;
+      if (kPoly && (i & 7) >= 5) {
+        pp = exp2_poly2(x);
+      } else {
+        const float2 xv = f2_unpack(x);
+        pp = f2_pack(ex2(xv.x), ex2(xv.y));
+      }
+      if (i & 1) acc1 = f2_add(acc1, pp);
+      else acc0 = f2_add(acc0, pp);
+      const float2 pv = f2_unpack(pp);
+      const __nv_bfloat162 b = __floats2bfloat162_rn(pv.x, pv.y);
+      pk[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    tmem_st16u(tS + 16 * q, pk);
+  }
 }
 
 __device__ __forceinline__ void write_empty_partials(const TcParams& p, size_t base, int row0) {
@@ -168,21 +261,18 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars.s_full[t], 1);
-      mbar_init(&bars.s_free[t], 256);
-      mbar_init(&bars.p_full[t], 256);
+      mbar_init(&bars.p_full[t], 128);
     }
     mbar_init(&bars.done, 1);
-    for (int tt = 0; tt < 2; ++tt)
-      for (int q = 0; q < 4; ++q) mbar_init(&bars.xchg[tt][q], 64);
     mbar_fence_init();
   }
-  if (warp == 17) tmem_alloc(&tmem_base_sh, kTmemCols);
+  if (warp == 9) tmem_alloc(&tmem_base_sh, kTmemCols);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp == 16 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     prefetch_tmap(&qmap);
     prefetch_tmap(&kmap);
@@ -212,12 +302,11 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       for (int i = (issued > kSlots ? issued - kSlots : 0); i < issued; ++i)
         mbar_wait(&bars.kv_full[i % kSlots], (uint32_t)(i / kSlots) & 1);
     }
-  } else if (warp == 17 && lane == 0) {
+  } else if (warp == 9 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
     const uint32_t idO = idesc_bf16_f32(128, 128, false, true);
     const uint32_t qa = smem_u32(sm + kOffQ);
-    const uint32_t pa = smem_u32(sm + kOffP);
     const uint32_t kvb = smem_u32(sm + kOffKV);
     auto wait_kv = [&](int i) -> bool {
       return mbar_wait(&bars.kv_full[i % kSlots], (uint32_t)(i / kSlots) & 1);
@@ -233,15 +322,12 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       }
       mma_commit(&bars.s_full[t]);
     };
-    auto issue_pv = [&](int t, int c) {   // O_t += P_t V(c)
+    auto issue_pv = [&](int t, int c) {   // O_t += P_t V(c), P_t read from TMEM
       const uint32_t vb = kvb + ((2 * c + 1) % kSlots) * kTileBytes;
-      const uint32_t pt = pa + t * kTileBytes;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint64_t a = sdesc_sw128(pt + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
-        mma_bf16(tmem + t * 256 + 128, a, sdesc_sw128(vb + k * 16 * 128, kVLbo, kVSbo), idO,
-                 (c > 0 || k > 0) ? 1u : 0u);
-      }
+      for (int k = 0; k < 8; ++k)   // 16 keys = 8 columns of packed bf16 pairs per step
+        mma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + k * 8,
+                    sdesc_sw128(vb + k * 16 * 128, kVLbo, kVSbo), idO, (c > 0 || k > 0) ? 1u : 0u);
     };
     bool ok = mbar_wait(&bars.q, 0) && wait_kv(0);
     if (ok) {
@@ -256,10 +342,8 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       if (!mbar_wait(&bars.p_full[0], c & 1)) { ok = false; break; }
       fence_after_sync();
       issue_pv(0, c);
-      if (more) {
+      if (more) {   // p_full also says S_0(c) has been read
         if (!wait_kv(2 * c + 2)) { ok = false; break; }               // K(c+1)
-        if (!mbar_wait(&bars.s_free[0], c & 1)) { ok = false; break; }
-        fence_after_sync();
         issue_s(0, c + 1);
       }
       if (!mbar_wait(&bars.p_full[1], c & 1)) { ok = false; break; }
@@ -267,8 +351,6 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       issue_pv(1, c);
       mma_commit(&bars.kv_empty[(2 * c + 1) % kSlots]);               // V(c) consumed
       if (more) {
-        if (!mbar_wait(&bars.s_free[1], c & 1)) { ok = false; break; }
-        fence_after_sync();
         issue_s(1, c + 1);
         mma_commit(&bars.kv_empty[(2 * c + 2) % kSlots]);             // K(c+1) consumed
       }
@@ -276,65 +358,53 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     }
     if (ok) mma_commit(&bars.done);
     else abort_sh = 1;
-  } else if (warp < 16) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax rows
-    // warp w: tile t = w / 8, column half hf = (w / 4) % 2, TMEM lanes of
-    // row group w % 4; thread (t, hf, row) owns columns [64 hf, 64 hf + 64)
-    // of that row.  The two halves of a row exchange their partial max
-    // through shared memory, paired by one mbarrier per row group (bounded
-    // waits, so a broken partner cannot hang the other half).
-    const int t = warp >> 3;
-    const int hf = (warp >> 2) & 1;
-    const int lg = warp & 3;
-    const int row_in_tile = lg * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
-    const uint32_t tS = tmem + t * 256 + lane_off + hf * 64;
-    const uint32_t tO = tmem + t * 256 + 128 + lane_off + hf * 64;
+    const int t = warp >> 2;                       // tile
+    const int row_in_tile = threadIdx.x - t * 128;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + t * 256 + lane_off;
+    const uint32_t tO = tS + 128;
     const float sc = p.scale_log2 * (p.k_scale ? p.k_scale[g] : 1.f);
-    unsigned char* Ph = sm + kOffP + t * kTileBytes + hf * kHalfBytes;
-    // partial-max exchange: a thread leaves its value in the partner's half of
-    // the P tile (row line), reads the partner's value from its own half, and
-    // only then overwrites its own half with P; the tile is free here because
-    // the commit that signalled S_t(c) covers PV_t(c-1)
-    float* x_mine = reinterpret_cast<float*>(sm + kOffP + t * kTileBytes + hf * kHalfBytes +
-                                             row_in_tile * 128);
-    float* x_partner = reinterpret_cast<float*>(sm + kOffP + t * kTileBytes + (hf ^ 1) * kHalfBytes +
-                                                row_in_tile * 128);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int c = 0; c < nchunks; ++c) {
       if (!warp_wait(&bars.s_full[t], c & 1)) { ok = false; break; }
       fence_after_sync();
-      const int nvalid = min(128, k1 - (k0 + c * 128)) - hf * 64;   // valid columns of this half
+      // pass 1: the chunk's row max (one 128-column TMEM load); only the last
+      // chunk of a split can hold fewer than 128 keys, so the full case runs
+      // without per-element masks
+      const int nvalid = min(128, k1 - (k0 + c * 128));
+      const bool full = nvalid == 128;
       float mx = -INFINITY;
       {
-        float sv[64];
-        tmem_ld64(tS, sv);
-        if (nvalid >= 64) {   // pairwise tree: depth 6
+        float sv[128];
+        tmem_ld128(tS, sv);
+        if (full) {   // tree of three-input maxima: 128 -> 43 -> 15 -> 5 -> 1
 #pragma unroll
-          for (int w = 32; w >= 1; w >>= 1) {
+          for (int i = 0; i < 42; ++i) sv[i] = max3f(sv[3 * i], sv[3 * i + 1], sv[3 * i + 2]);
+          sv[42] = fmaxf(sv[126], sv[127]);
 #pragma unroll
-            for (int i = 0; i < w; ++i) sv[i] = fmaxf(sv[i], sv[i + w]);
-          }
-          mx = sv[0];
+          for (int i = 0; i < 14; ++i) sv[i] = max3f(sv[3 * i], sv[3 * i + 1], sv[3 * i + 2]);
+          sv[14] = sv[42];
+#pragma unroll
+          for (int i = 0; i < 5; ++i) sv[i] = max3f(sv[3 * i], sv[3 * i + 1], sv[3 * i + 2]);
+          mx = max3f(sv[0], sv[1], max3f(sv[2], sv[3], sv[4]));
         } else {
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
+          for (int i = 0; i < 128; ++i)
             if (i < nvalid) mx = fmaxf(mx, sv[i]);
         }
       }
-      *x_partner = mx;
-      mbar_arrive(&bars.xchg[t][lg]);
-      if (!warp_wait(&bars.xchg[t][lg], c & 1)) { ok = false; break; }
-      mx = fmaxf(mx, *x_mine) * sc;
+      mx *= sc;
       const bool need = mx > m_used + kRescale;
-      if (__any_sync(0xffffffffu, need)) {   // the partner warp holds the same rows: same outcome
+      if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? mx : m_used;
         const float factor = ex2(m_used - m_new);   // 0 on the first chunk, 1 for rows that keep m
         l *= factor;
         if (c > 0) {   // O_t holds chunks < c (their PV completed before S_t(c) was signalled)
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
+          for (int q = 0; q < 4; ++q) {
             float v[32];
             tmem_ld32(tO + q * 32, v);
 #pragma unroll
@@ -345,83 +415,71 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         }
         m_used = m_new;
       }
-      // P = 2^(s - m) as bf16 into this half of the swizzled K-major tile
-      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
-      float sv[64];
-      tmem_ld64(tS, sv);
-      if (nvalid < 64) {
+      // pass 2: P = 2^(s - m) as bf16 pairs into TMEM columns 0-63 of S_t
+      // (the last, partial chunk masks its missing keys and stays on ex2,
+      // which gives exact zeros there)
+      f2 acc0 = f2_pack(0.f, 0.f), acc1 = f2_pack(0.f, 0.f);
+      {
+        float sv[128];
+        tmem_ld128(tS, sv);
+        if (full) {
+          softmax_row<true>(sv, sc, m_used, tS, acc0, acc1);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (i >= nvalid) sv[i] = -INFINITY;
-      }
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int k2 = q * 32 + 2 * i;
-          const float p0 = ex2(fmaf(sv[k2], sc, -m_used));
-          const float p1 = ex2(fmaf(sv[k2 + 1], sc, -m_used));
-          if ((i & 3) == 0) sum0 += p0 + p1;
-          else if ((i & 3) == 1) sum1 += p0 + p1;
-          else if ((i & 3) == 2) sum2 += p0 + p1;
-          else sum3 += p0 + p1;
-          const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
-          pk[i] = *reinterpret_cast<const uint32_t*>(&b);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int chunk = q * 4 + k;
-          uint4* dst = reinterpret_cast<uint4*>(Ph + row_in_tile * 128 +
-                                                ((chunk ^ (row_in_tile & 7)) << 4));
-          *dst = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          for (int i = 0; i < 128; ++i)
+            if (i >= nvalid) sv[i] = -INFINITY;
+          softmax_row<false>(sv, sc, m_used, tS, acc0, acc1);
         }
       }
-      l += (sum0 + sum1) + (sum2 + sum3);
+      {
+        const float2 a0 = f2_unpack(acc0), a1 = f2_unpack(acc1);
+        l += (a0.x + a0.y) + (a1.x + a1.y);
+      }
+      tmem_wait_st();
       fence_before_sync();
-      mbar_arrive(&bars.s_free[t]);
-      fence_proxy_async_smem();
       mbar_arrive(&bars.p_full[t]);
       if (warp_flag(&abort_sh)) { ok = false; break; }
     }
     if (ok && !warp_wait(&bars.done, 0)) ok = false;
     if (!ok) abort_sh = 1;
     const int row = row0 + t * 128 + row_in_tile;
-    // the row's sum is the sum of both halves' partial sums (the P tile is
-    // free once the last PV has completed)
-    bool xok = false;
-    if (ok) {
-      *x_partner = l;
-      mbar_arrive(&bars.xchg[t][lg]);
-      xok = warp_wait(&bars.xchg[t][lg], nchunks & 1);
-      if (!xok) abort_sh = 1;
-    }
-    const float l_row = xok ? l + *x_mine : l;
-    ok = ok && xok;
+    // O_t leaves through shared memory (the K/V ring is idle once every MMA
+    // is done): each thread puts its row there, 16-byte chunks swizzled by
+    // the row, then each warp stores whole 512-byte rows, coalesced
+    unsigned char* stage = sm + kOffKV + (uint32_t)t * (128u * 512u);
     if (ok) {
       fence_after_sync();
-      const size_t pi = prow_base + row;
-      float4* o = reinterpret_cast<float4*>(p.po + pi * 128 + hf * 64);
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
+      for (int q = 0; q < 4; ++q) {
         float v[32];
         tmem_ld32(tO + q * 32, v);
-        if (row < p.rows) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            o[q * 8 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        for (int i = 0; i < 8; ++i) {
+          const int chunk = q * 8 + i;
+          *reinterpret_cast<float4*>(stage + row_in_tile * 512 + ((chunk ^ (row_in_tile & 7)) << 4)) =
+              make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
       }
-      if (row < p.rows && hf == 0) {
-        p.pm[pi] = m_used;
-        p.pl[pi] = l_row;
+    }
+    named_bar(1 + t, 128);   // the tile's four warps; every one of them arrives, ok or not
+    if (ok) {
+      for (int rr = warp & 3; rr < 128; rr += 4) {
+        const int grow = row0 + t * 128 + rr;
+        if (grow < p.rows) {
+          const float4 v = *reinterpret_cast<const float4*>(stage + rr * 512 + ((lane ^ (rr & 7)) << 4));
+          reinterpret_cast<float4*>(p.po + (prow_base + grow) * 128)[lane] = v;
+        }
+      }
+      if (row < p.rows) {
+        p.pm[prow_base + row] = m_used;
+        p.pl[prow_base + row] = l;
       }
     }
   }
   fence_before_sync();
   __syncthreads();
   if (abort_sh && threadIdx.x == 0) set_status(p.hdr, BEAMDEC_ERR_TIMEOUT);
-  if (warp == 17) {
+  if (warp == 9) {
     fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -390,8 +390,24 @@ __device__ __forceinline__ bool expand_candidates(const SelectArgs& a, ExpandSha
   // the row's candidate keys, computed once into shared memory when they fit
   // (the radix passes below then read shared memory instead of re-gathering)
   const bool cached = kcache != nullptr && n <= kKeyCache;
-  if (cached) {
-    for (int i = tid; i < n; i += kExpandThreads) kcache[i] = key_of(tok_of(i));
+  if (cached) {   // four children per thread in flight: codes first, then their logits
+    constexpr int kU = 4;
+    for (int c0 = 0; c0 < n; c0 += kU * kExpandThreads) {
+      int tk[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = c0 + u * kExpandThreads + tid;
+        tk[u] = i < n ? tok_of(i) : 0;
+      }
+      float x[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) x[u] = __ldg(row + tk[u]);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = c0 + u * kExpandThreads + tid;
+        if (i < n) kcache[i] = desc_key(__fadd_rn(cum, __fsub_rn(x[u], lse)));
+      }
+    }
     __syncthreads();
   }
   auto kc = [&](int i) -> uint32_t { return cached ? kcache[i] : key_of(tok_of(i)); };
