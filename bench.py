@@ -198,8 +198,8 @@ def algorithmic(wl, rows, kernel):
     b_kv = 1 if wl.kv_dtype == synth.E4M3 else (4 if wl.kv_dtype == synth.F32 else 2)
     b_q = 4 if wl.q_dtype == synth.F32 else 2
     P = synth.prompt_lens(wl)
-    if kernel == "bd_lse_kernel":
-        # one read of every live logits row
+    if kernel == "bd_stream_select_kernel":
+        # one read of every live logits row (the children gathers hit L2)
         return rows * wl.V * 4, "bytes"
     if kernel in ("bd_attn_shared_simt_kernel", "bd_attn_shared_tc_kernel"):
         return float(4 * wl.Hkv * wl.W * G * P.sum() * wl.d), "flops"
@@ -224,7 +224,7 @@ def read_traffic(kernel):
     path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
     if not os.path.exists(path):
         return None
-    src_for = {"bd_expand_kernel": "select.cu", "bd_global_kernel": "select.cu", "bd_lse_kernel": "select.cu",
+    src_for = {"bd_expand_kernel": "select.cu", "bd_global_kernel": "select.cu", "bd_stream_select_kernel": "select.cu",
                "bd_kv_e4m3_to_bf16_kernel": "attn_tc.cu",
                "bd_attn_shared_simt_kernel": "attn_simt.cu", "bd_attn_shared_tc_kernel": "attn_tc.cu",
                "bd_attn_merge_kernel": "attn_merge.cu"}

@@ -88,11 +88,10 @@ int beamdec_read_status(void* workspace, void* stream, int32_t* host_status);
  * on its stream (at most 8192 launches are kept); beamdec_profile_enable(0)
  * stops recording.  beamdec_profile_read synchronises the recorded events and
  * returns the total milliseconds and launch count of one kernel id:
- * 0 bd_expand_kernel, 1 bd_global_kernel, 2 bd_attn_shared_simt_kernel,
- * 3 bd_attn_shared_tc_kernel, 4 bd_attn_merge_kernel, 5 bd_kv_e4m3_to_bf16_kernel,
- * 6 bd_lse_kernel.
- * Host-side state is
- * process-wide; use from one host thread.
+ * 0 bd_expand_kernel (selection when lse_in is given), 1 bd_global_kernel,
+ * 2 bd_attn_shared_simt_kernel, 3 bd_attn_shared_tc_kernel, 4 bd_attn_merge_kernel,
+ * 5 bd_kv_e4m3_to_bf16_kernel, 6 bd_stream_select_kernel (the whole selection
+ * step otherwise).  Host-side state is process-wide; use from one host thread.
  */
 int beamdec_profile_enable(int on);
 int beamdec_profile_read(int kernel_id, float* total_ms, int* launches);

@@ -423,7 +423,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         float sv[128];
         tmem_ld128(tS, sv);
         if (full) {
-          softmax_row<true>(sv, sc, m_used, tS, acc0, acc1);
+          softmax_row<false>(sv, sc, m_used, tS, acc0, acc1);
         } else {
 #pragma unroll
           for (int i = 0; i < 128; ++i)

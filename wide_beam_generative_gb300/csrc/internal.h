@@ -92,7 +92,7 @@ int sm_count();
 
 // ---- per-kernel event timing (off unless beamdec_profile_enable(1)) ---------
 enum KernelId { kKExpand = 0, kKGlobal = 1, kKAttnSimt = 2, kKAttnTc = 3, kKAttnMerge = 4,
-                kKKvConvert = 5, kKLse = 6, kKCount = 7 };
+                kKKvConvert = 5, kKStream = 6, kKCount = 7 };
 void prof_begin(int kid, cudaStream_t s);
 void prof_end(int kid, cudaStream_t s);
 

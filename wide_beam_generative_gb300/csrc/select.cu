@@ -8,16 +8,18 @@
 // reorder.  FlashRec (SGLang PR 31626 thread): fused SID trie in CSR form.
 //
 // One or two launches per step:
-//   bd_expand_kernel   one block per (beam, request): streams the beam's logits
-//                      row once to get its log-sum-exp, scores the trie
-//                      children (or the whole vocabulary), keeps the row's
-//                      top_k by a block radix select and appends them to the
-//                      request's pool as 64-bit keys.  When a request's pool
-//                      is at most 1M keys (W <= 4096), the last of its blocks
-//                      to finish then selects the request's top-W itself
-//                      (radix narrowing, shared-memory sort, outputs), so the
-//                      selection tail of one request overlaps the streaming
-//                      of the others and no second launch is needed.
+//   bd_stream_select_kernel  a few blocks per live beam row (about 32K logits
+//                      each) stream the row once for its log-sum-exp; the
+//                      row's last block then scores the trie children (or
+//                      the whole vocabulary), keeps the row's top_k (block
+//                      radix select) and appends them to the request's pool
+//                      as 64-bit keys while the row is still in L2.  When a
+//                      request's pool is at most 1M keys (W <= 4096), the
+//                      last row of the request selects the request's top-W
+//                      itself (score-bin histogram, bucket sort, outputs), so
+//                      one request's tail overlaps the others' streams.
+//   bd_expand_kernel   the same per-row and per-request work when the caller
+//                      passes the row normalisers (lse_in): one block per row.
 //   bd_global_kernel   larger pools: cooperative grid; per request, radix select of the
 //                      beam_width smallest pool keys (12-bit digits, block-
 //                      private histograms merged in global memory), a bitonic
@@ -63,7 +65,6 @@ struct SelWs {
   unsigned long long* pool;  // [R][W*Kp]
   unsigned long long* cand;  // [R][kSelectCap]
   float2* rowpart;        // [R][W][kMaxRowSplits] per-chunk (max, sum of exp)
-  float* rowlse;          // [R][W] log-sum-exp of each live row
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -77,8 +78,7 @@ __host__ __device__ inline SelWs carve(void* ws, int R, int W, int Kp) {
   s.hist = (uint32_t*)p; p += align256((size_t)R * kBins * sizeof(uint32_t));
   s.pool = (unsigned long long*)p; p += align256((size_t)R * W * Kp * 8);
   s.cand = (unsigned long long*)p; p += align256((size_t)R * kSelectCap * 8);
-  s.rowpart = (float2*)p; p += align256((size_t)R * W * kMaxRowSplits * sizeof(float2));
-  s.rowlse = (float*)p;
+  s.rowpart = (float2*)p;
   return s;
 }
 
@@ -278,52 +278,6 @@ __device__ __forceinline__ float2 stream_max_sum(const float* row, int c0, int c
   return res;
 }
 
-
-// a1 on its own: S blocks per live logits row each fold (max, sum of exp) of
-// one chunk; the last of them (a per-row ticket) combines the chunks into the
-// row's log-sum-exp.  Kept free of the selection code so that it stays at 32
-// registers and four 512-thread blocks per SM keep enough loads in flight.
-__global__ void __launch_bounds__(kExpandThreads, 4)
-bd_lse_kernel(SelectArgs a) {
-  __shared__ ExpandShared sh;
-  const int S = a.row_splits;
-  const int b = blockIdx.x / S, sidx = blockIdx.x - b * S, r = blockIdx.y, tid = threadIdx.x;
-  if (b >= a.n_live_in[r]) return;
-  SelWs ws = carve(a.ws, a.R, a.W, a.Kp);
-  const size_t rowi = (size_t)r * a.W + b;
-  const float* row = a.logits + rowi * (size_t)a.row_stride;
-  const int c0 = sidx * a.row_chunk;
-  const int c1 = min(a.V, c0 + a.row_chunk);
-  const float2 ms = stream_max_sum(row, c0, c1, sh);
-  float lse;
-  if (S == 1) {
-    lse = ms.x + logf(ms.y);
-  } else {
-    if (tid == 0) {
-      ws.rowpart[rowi * kMaxRowSplits + sidx] = ms;
-      __threadfence();
-      sh.count = atomicAdd(ws.rowtick + rowi, 1);
-    }
-    __syncthreads();
-    if (sh.count != S - 1) return;
-    __threadfence();
-    if (tid < 32) {   // one warp: lane k holds chunk k's (max, sum)
-      const float2 p = tid < S ? __ldcg(ws.rowpart + rowi * kMaxRowSplits + tid)
-                               : make_float2(-INFINITY, 0.f);
-      float M = p.x;
-      for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      float tot = (p.y > 0.f) ? p.y * ex2((p.x - M) * kLog2e) : 0.f;
-      for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-      if (tid == 0) sh.lse = M + logf(tot);
-    }
-    __syncthreads();
-    lse = sh.lse;
-  }
-  if (tid == 0) {
-    ws.rowlse[rowi] = lse;
-    if (a.lse_out != nullptr) a.lse_out[rowi] = lse;
-  }
-}
 
 // Rows a2-a3 for beam b of request r: log-sum-exp, trie children, per-beam
 // top_k appended to the request's pool.
@@ -793,20 +747,16 @@ selected:
   emit_outputs(a, ws, r, keys, nt);
 }
 
+// a2-a5 for live beam b of request r once its log-sum-exp is known: the
+// row's candidates go to the request's pool; with kFused the last row of the
+// request to finish (a per-request ticket) runs the request's global top-W.
+// Dynamic shared memory: [key cache 16 KB][score-bin histogram 16 KB, fused
+// only]; the fused tail reuses all of it for candidate keys after the ticket.
 template <bool kFused>
-__global__ void __launch_bounds__(kExpandThreads)
-bd_expand_kernel(SelectArgs a) {
-  __shared__ ExpandShared sh;
-  extern __shared__ __align__(16) unsigned char tail_smem[];
-  const int b = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
-  SelWs ws = carve(a.ws, a.R, a.W, a.Kp);
-  if (b == 0 && r == 0 && tid == 0) ws.hdr->bar_count = 0u;
-  const int nl = a.n_live_in[r];
-  if (b >= nl) return;
-  const size_t rowi = (size_t)r * a.W + b;
-  const float lse = a.lse_in != nullptr ? a.lse_in[rowi] : __ldcg(ws.rowlse + rowi);
-  // dynamic shared memory: [key cache 16 KB][score-bin histogram 16 KB, fused only];
-  // the fused tail reuses all of it for candidate keys after the ticket
+__device__ __forceinline__ void expand_and_select(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
+                                                  int r, int b, int nl, float lse,
+                                                  unsigned char* tail_smem) {
+  const int tid = threadIdx.x;
   uint32_t* kcache = reinterpret_cast<uint32_t*>(tail_smem);
   uint32_t* bins = kFused ? kcache + kKeyCache : nullptr;
   const bool flush = expand_candidates(a, sh, ws, r, b, bins, kcache, lse);
@@ -817,7 +767,6 @@ bd_expand_kernel(SelectArgs a) {
       for (int i = tid; i < kTailBins; i += kExpandThreads)
         if (bins[i]) atomicAdd(gh + i, bins[i]);
     }
-    // the last block of the request to finish runs the request's global top-W
     __syncthreads();
     if (tid == 0) {
       __threadfence();
@@ -828,6 +777,73 @@ bd_expand_kernel(SelectArgs a) {
     __threadfence();
     request_tail(a, sh, ws, r, reinterpret_cast<unsigned long long*>(tail_smem));
   }
+}
+
+// a2-a5 when the caller supplies the row normalisers (lse_in): one block per
+// live beam.
+template <bool kFused>
+__global__ void __launch_bounds__(kExpandThreads)
+bd_expand_kernel(SelectArgs a) {
+  __shared__ ExpandShared sh;
+  extern __shared__ __align__(16) unsigned char tail_smem[];
+  const int b = blockIdx.x, r = blockIdx.y;
+  SelWs ws = carve(a.ws, a.R, a.W, a.Kp);
+  if (b == 0 && r == 0 && threadIdx.x == 0) ws.hdr->bar_count = 0u;
+  const int nl = a.n_live_in[r];
+  if (b >= nl) return;
+  const float lse = a.lse_in[(size_t)r * a.W + b];
+  expand_and_select<kFused>(a, sh, ws, r, b, nl, lse, tail_smem);
+}
+
+// The whole selection step in one launch: S blocks per live logits row each
+// fold (max, sum of exp) of one chunk of the row (a1); the last of them (a
+// per-row ticket) combines the chunks into the row's log-sum-exp and goes on
+// with the row (a2, a3) while the row is still in L2; with kFused the last
+// row of each request selects the request's top-W (a4, a5).  The stream
+// part holds nothing else, so the kernel fits 32 registers and four
+// 512-thread blocks per SM keep enough loads in flight.
+template <bool kFused>
+__global__ void __launch_bounds__(kExpandThreads, 4)
+bd_stream_select_kernel(SelectArgs a) {
+  __shared__ ExpandShared sh;
+  extern __shared__ __align__(16) unsigned char tail_smem[];
+  const int S = a.row_splits;
+  const int b = blockIdx.x / S, sidx = blockIdx.x - b * S, r = blockIdx.y, tid = threadIdx.x;
+  SelWs ws = carve(a.ws, a.R, a.W, a.Kp);
+  if (blockIdx.x == 0 && r == 0 && tid == 0) ws.hdr->bar_count = 0u;
+  const int nl = a.n_live_in[r];
+  if (b >= nl) return;
+  const size_t rowi = (size_t)r * a.W + b;
+  const float* row = a.logits + rowi * (size_t)a.row_stride;
+  const int c0 = sidx * a.row_chunk;
+  const int c1 = min(a.V, c0 + a.row_chunk);
+  const float2 ms = stream_max_sum(row, c0, c1, sh);
+  float lse;
+  if (S == 1) {
+    lse = ms.x + logf(ms.y);
+  } else {
+    if (tid == 0) {
+      ws.rowpart[rowi * kMaxRowSplits + sidx] = ms;
+      __threadfence();
+      sh.count = atomicAdd(ws.rowtick + rowi, 1);
+    }
+    __syncthreads();
+    if (sh.count != S - 1) return;
+    __threadfence();
+    if (tid < 32) {   // one warp: lane k holds chunk k's (max, sum)
+      const float2 p = tid < S ? __ldcg(ws.rowpart + rowi * kMaxRowSplits + tid)
+                               : make_float2(-INFINITY, 0.f);
+      float M = p.x;
+      for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float tot = (p.y > 0.f) ? p.y * ex2((p.x - M) * kLog2e) : 0.f;
+      for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      if (tid == 0) sh.lse = M + logf(tot);
+    }
+    __syncthreads();
+    lse = sh.lse;
+  }
+  if (tid == 0 && a.lse_out != nullptr) a.lse_out[rowi] = lse;
+  expand_and_select<kFused>(a, sh, ws, r, b, nl, lse, tail_smem);
 }
 
 // ---------------------------------------------------------------------------
@@ -986,7 +1002,7 @@ size_t select_workspace_bytes(int R, int W, int K, int V) {
          align256((size_t)R * W * sizeof(int32_t)) +
          align256((size_t)R * kBins * sizeof(uint32_t)) + align256((size_t)R * W * Kp * 8) +
          align256((size_t)R * kSelectCap * 8) +
-         align256((size_t)R * W * kMaxRowSplits * sizeof(float2)) + (size_t)R * W * sizeof(float);
+         (size_t)R * W * kMaxRowSplits * sizeof(float2);
 }
 
 int launch_select(const SelectArgs& a, cudaStream_t stream) {
@@ -1019,24 +1035,25 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
   const size_t zero_bytes = (char*)ws.pool - (char*)ws.state;
   if (cudaMemsetAsync(ws.state, 0, zero_bytes, stream) != cudaSuccess) return BEAMDEC_ERR_CUDA;
 
+  // Pools of at most 1M keys per request (W <= 4096) are selected by the last
+  // row of each request inside the launch; larger ones by the cooperative
+  // grid kernel afterwards.
+  const bool fused = a.W <= kTailCap && (long long)a.W * a.Kp <= (1ll << 20);
+  static_assert(kKeyCache * 4 + kTailBins * 4 <= kTailCap * 8, "fused dynamic shared memory");
+  const size_t dsm = fused ? kTailCap * sizeof(unsigned long long) : kKeyCache * sizeof(uint32_t);
   if (a.lse_in == nullptr) {
     dim3 g0(a.W * S, a.R);
-    prof_begin(kKLse, stream);
-    bd_lse_kernel<<<g0, kExpandThreads, 0, stream>>>(a2);
-    prof_end(kKLse, stream);
-    if (cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
+    prof_begin(kKStream, stream);
+    if (fused) bd_stream_select_kernel<true><<<g0, kExpandThreads, dsm, stream>>>(a2);
+    else bd_stream_select_kernel<false><<<g0, kExpandThreads, dsm, stream>>>(a2);
+    prof_end(kKStream, stream);
+  } else {
+    dim3 g1(a.W, a.R);
+    prof_begin(kKExpand, stream);
+    if (fused) bd_expand_kernel<true><<<g1, kExpandThreads, dsm, stream>>>(a2);
+    else bd_expand_kernel<false><<<g1, kExpandThreads, dsm, stream>>>(a2);
+    prof_end(kKExpand, stream);
   }
-  dim3 g1(a.W, a.R);
-  // Pools of at most 1M keys per request (W <= 4096) are selected by the last
-  // expand block of each request; larger ones by the cooperative grid kernel.
-  const bool fused = a.W <= kTailCap && (long long)a.W * a.Kp <= (1ll << 20);
-  prof_begin(kKExpand, stream);
-  static_assert(kKeyCache * 4 + kTailBins * 4 <= kTailCap * 8, "fused dynamic shared memory");
-  if (fused)
-    bd_expand_kernel<true><<<g1, kExpandThreads, kTailCap * sizeof(unsigned long long), stream>>>(a2);
-  else
-    bd_expand_kernel<false><<<g1, kExpandThreads, kKeyCache * sizeof(uint32_t), stream>>>(a2);
-  prof_end(kKExpand, stream);
   if (cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
   if (fused) return BEAMDEC_OK;
 
