@@ -198,6 +198,10 @@ struct ExpandShared {
   int pool_base;
   float lse;
   uint32_t c_le;
+  // the row's trie range and score, fetched at the start of a stream block
+  // so that the row's expansion does not wait on them (pf_e0 < 0: not fetched)
+  int pf_e0, pf_e1;
+  float pf_cum, pf_ref;
 };
 
 // Running (max, sum of exp(x - max)) of row[c0..c1) for the whole block,
@@ -285,6 +289,8 @@ __device__ __forceinline__ float2 stream_max_sum(const float* row, int c0, int c
 // row that goes through the radix select; rows whose children all enter the
 // pool add theirs straight to the request's histogram in global memory.
 // Returns true when `bins` holds counts the caller must flush.
+// kPf: the row's trie range and scores were fetched into sh.pf_* already.
+template <bool kPf>
 __device__ __forceinline__ bool expand_candidates(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
                                                  int r, int b, uint32_t* bins, uint32_t* kcache,
                                                  float lse) {
@@ -294,20 +300,28 @@ __device__ __forceinline__ bool expand_candidates(const SelectArgs& a, ExpandSha
   const float* row = a.logits + rowi * (size_t)a.row_stride;
 
   if (a.lse_in != nullptr && a.lse_out != nullptr && tid == 0) a.lse_out[rowi] = lse;
-  const float cum = a.cum_in[rowi];
+  const float cum = kPf ? sh.pf_cum : a.cum_in[rowi];
 
   // ---- a2: candidate range (trie children or the whole vocabulary) --------
   int n = a.V;
   const int32_t* code = nullptr;
   int tb = 0;
   if (a.has_trie) {
-    const int node = a.node_in[rowi];
-    if (node < 0 || node >= a.lvl.n_nodes) {
+    int e0, e1;
+    if constexpr (kPf) {
+      e0 = sh.pf_e0;
+      e1 = sh.pf_e1;
+    } else {
+      const int node = a.node_in[rowi];
+      const bool bad = node < 0 || node >= a.lvl.n_nodes;
+      e0 = bad ? -2 : a.lvl.off[node];
+      e1 = bad ? -2 : a.lvl.off[node + 1];
+    }
+    if (e0 < 0) {
       if (tid == 0) set_status(ws.hdr, BEAMDEC_ERR_DEVICE_CHECK);
       return false;
     }
-    const int e0 = a.lvl.off[node];
-    n = a.lvl.off[node + 1] - e0;
+    n = e1 - e0;
     code = a.lvl.code + e0;
     tb = a.lvl.token_base;
   }
@@ -319,7 +333,7 @@ __device__ __forceinline__ bool expand_candidates(const SelectArgs& a, ExpandSha
 
   SelState* st = ws.state + r;
   unsigned long long* pool = ws.pool + (size_t)r * a.W * Kp;
-  const float ref = a.cum_in[(size_t)r * a.W];   // bin reference: the rank-0 beam's score
+  const float ref = kPf ? sh.pf_ref : a.cum_in[(size_t)r * a.W];   // bin reference: the rank-0 beam's score
 
   // ---- a3: per-beam top_k -------------------------------------------------
   if (n <= a.K) {
@@ -438,8 +452,10 @@ __device__ void bitonic_sort(unsigned long long* keys, int np) {
 // a4/a5 outputs of request r from its nt winners, sorted ascending in keys[]:
 // tokens, parents, scores, child nodes, live count and the slot rows
 // (parent's row up to step-1, then step*W + j).
+// poff (optional): poff[j] = first edge of live beam j's trie node, gathered
+// earlier so the decode waits on one load instead of three.
 __device__ void emit_outputs(const SelectArgs& a, const SelWs& ws, int r,
-                             const unsigned long long* keys, int nt) {
+                             const unsigned long long* keys, int nt, const int* poff = nullptr) {
   const int tid = threadIdx.x;
   const size_t o = (size_t)r * a.W;
   for (int j = tid; j < a.W; j += blockDim.x) {
@@ -448,8 +464,7 @@ __device__ void emit_outputs(const SelectArgs& a, const SelWs& ws, int r,
       const int parent = pool_key_beam(k), idx = pool_key_tok(k);
       int tok = idx, node = -1;
       if (a.has_trie) {
-        const int nd = a.node_in[o + parent];
-        node = a.lvl.off[nd] + idx;           // edge index = child node at the next level
+        node = (poff ? poff[parent] : a.lvl.off[a.node_in[o + parent]]) + idx;   // edge index = child node
         tok = a.lvl.token_base + a.lvl.code[node];
       }
       a.tokens[o + j] = tok;
@@ -553,11 +568,11 @@ __device__ uint32_t narrow_pass(const unsigned long long* keys, int n, unsigned 
   return in_bin;
 }
 
-// In-place exclusive prefix sum of the kTailBins bins of hs (kExpandThreads
-// threads, 8 bins each), and the bin holding the need-th key (1-based,
-// need <= sum of all bins): sh.digit = that bin, sh.below = keys in lower
-// bins, sh.c_le = keys in it and below.
-__device__ void block_scan_bins(uint32_t* hs, uint32_t need, ExpandShared& sh) {
+// Exclusive prefix sum of the kTailBins bins of the global histogram gh into
+// hs (kExpandThreads threads, 8 bins each), and the bin holding the need-th
+// key (1-based, need <= sum of all bins): sh.digit = that bin, sh.below =
+// keys in lower bins, sh.c_le = keys in it and below.
+__device__ void block_scan_bins(const uint32_t* gh, uint32_t* hs, uint32_t need, ExpandShared& sh) {
   constexpr int kPer = kTailBins / kExpandThreads;
   static_assert(kPer * kExpandThreads == kTailBins, "bins per thread");
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -566,7 +581,7 @@ __device__ void block_scan_bins(uint32_t* hs, uint32_t need, ExpandShared& sh) {
   uint32_t sum = 0;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
-    v[i] = hs[t * kPer + i];
+    v[i] = __ldcg(gh + t * kPer + i);
     sum += v[i];
   }
   uint32_t inc = sum;
@@ -606,14 +621,18 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
     return;
   }
   // the request's score-bin histogram (complete: every block added its
-  // candidates before taking its ticket), prefix-summed in shared memory (the
-  // upper half of the key buffer); it brackets the nt-th best score
+  // candidates before taking its ticket), prefix-summed into shared memory
+  // (the upper half of the key buffer); it brackets the nt-th best score
   uint32_t* hs = reinterpret_cast<uint32_t*>(keys + kTailCap / 2);
-  {
-    const uint32_t* gh = ws.hist + (size_t)r * kBins;
-    for (int i = threadIdx.x; i < kTailBins; i += blockDim.x) hs[i] = __ldcg(gh + i);
-    __syncthreads();
-    block_scan_bins(hs, (uint32_t)nt, sh);
+  block_scan_bins(ws.hist + (size_t)r * kBins, hs, (uint32_t)nt, sh);
+  // each live beam's first trie edge, for the output decode, gathered now so
+  // its latency hides behind the selection (sh.hist is free on the bucket path)
+  if (a.has_trie && a.W <= 2048) {
+    const int nl = a.n_live_in[r];
+    for (int j = threadIdx.x; j < nl; j += kExpandThreads) {
+      const int nd = a.node_in[(size_t)r * a.W + j];
+      sh.hist[j] = (nd >= 0 && nd < a.lvl.n_nodes) ? (uint32_t)a.lvl.off[nd] : 0u;   // a bad node is never a parent
+    }
   }
   const int Dbin = (int)sh.digit;
   const uint32_t c_le = sh.c_le;
@@ -653,7 +672,8 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
       if (rank < (uint32_t)nt) sorted[rank] = k;
     }
     __syncthreads();
-    emit_outputs(a, ws, r, sorted, nt);
+    emit_outputs(a, ws, r, sorted, nt,
+                 (a.has_trie && a.W <= 2048) ? reinterpret_cast<const int*>(sh.hist) : nullptr);
     return;
   }
   int nc = 0;
@@ -752,14 +772,14 @@ selected:
 // request to finish (a per-request ticket) runs the request's global top-W.
 // Dynamic shared memory: [key cache 16 KB][score-bin histogram 16 KB, fused
 // only]; the fused tail reuses all of it for candidate keys after the ticket.
-template <bool kFused>
+template <bool kFused, bool kPf>
 __device__ __forceinline__ void expand_and_select(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
                                                   int r, int b, int nl, float lse,
                                                   unsigned char* tail_smem) {
   const int tid = threadIdx.x;
   uint32_t* kcache = reinterpret_cast<uint32_t*>(tail_smem);
   uint32_t* bins = kFused ? kcache + kKeyCache : nullptr;
-  const bool flush = expand_candidates(a, sh, ws, r, b, bins, kcache, lse);
+  const bool flush = expand_candidates<kPf>(a, sh, ws, r, b, bins, kcache, lse);
   if constexpr (kFused) {
     __syncthreads();
     if (flush) {
@@ -792,7 +812,7 @@ bd_expand_kernel(SelectArgs a) {
   const int nl = a.n_live_in[r];
   if (b >= nl) return;
   const float lse = a.lse_in[(size_t)r * a.W + b];
-  expand_and_select<kFused>(a, sh, ws, r, b, nl, lse, tail_smem);
+  expand_and_select<kFused, false>(a, sh, ws, r, b, nl, lse, tail_smem);
 }
 
 // The whole selection step in one launch: S blocks per live logits row each
@@ -818,8 +838,25 @@ bd_stream_select_kernel(SelectArgs a) {
   const int c0 = sidx * a.row_chunk;
   const int c1 = min(a.V, c0 + a.row_chunk);
   const float2 ms = stream_max_sum(row, c0, c1, sh);
+  // the row's expansion inputs, fetched by another warp while thread 0
+  // publishes the chunk and takes the row ticket (a block that turns out not
+  // to be the row's last just drops them)
+  if (tid == 32) {
+    sh.pf_cum = a.cum_in[rowi];
+    sh.pf_ref = a.cum_in[(size_t)r * a.W];
+    int e0 = 0, e1 = a.V;
+    if (a.has_trie) {
+      const int node = a.node_in[rowi];
+      const bool bad = node < 0 || node >= a.lvl.n_nodes;
+      e0 = bad ? -2 : a.lvl.off[node];
+      e1 = bad ? -2 : a.lvl.off[node + 1];
+    }
+    sh.pf_e0 = e0;
+    sh.pf_e1 = e1;
+  }
   float lse;
   if (S == 1) {
+    __syncthreads();
     lse = ms.x + logf(ms.y);
   } else {
     if (tid == 0) {
@@ -843,7 +880,7 @@ bd_stream_select_kernel(SelectArgs a) {
     lse = sh.lse;
   }
   if (tid == 0 && a.lse_out != nullptr) a.lse_out[rowi] = lse;
-  expand_and_select<kFused>(a, sh, ws, r, b, nl, lse, tail_smem);
+  expand_and_select<kFused, true>(a, sh, ws, r, b, nl, lse, tail_smem);
 }
 
 // ---------------------------------------------------------------------------
