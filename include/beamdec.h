@@ -94,6 +94,10 @@ int beamdec_read_status(void* workspace, void* stream, int32_t* host_status);
  * step otherwise).  Host-side state is process-wide; use from one host thread.
  */
 int beamdec_profile_enable(int on);
+/* The same with a choice of kernels: bit k of kernel_mask brackets kernel id
+ * k (ids above); 0 stops recording like beamdec_profile_enable(0).  Fewer
+ * event pairs disturb the timed launches less. */
+int beamdec_profile_enable_mask(unsigned kernel_mask);
 int beamdec_profile_read(int kernel_id, float* total_ms, int* launches);
 const char* beamdec_kernel_name(int kernel_id);
 

@@ -32,6 +32,7 @@ _SIGS = {
     "beamdec_version": (ctypes.c_char_p, []),
     "beamdec_read_status": (c_int, [c_p, c_p, c_i32p]),
     "beamdec_profile_enable": (c_int, [c_int]),
+    "beamdec_profile_enable_mask": (c_int, [ctypes.c_uint]),
     "beamdec_profile_read": (c_int, [c_int, ctypes.POINTER(c_f), ctypes.POINTER(c_int)]),
     "beamdec_kernel_name": (ctypes.c_char_p, [c_int]),
     "beam_trie_build": (c_int, [c_p, c_i64, c_int, c_p, c_p, ctypes.c_int32, c_p, ctypes.POINTER(c_p)]),
@@ -182,8 +183,16 @@ KERNELS = ["bd_expand_kernel", "bd_global_kernel", "bd_attn_shared_simt_kernel",
            "bd_stream_select_kernel"]
 
 
-def profile_enable(on=True):
-    _check(lib().beamdec_profile_enable(1 if on else 0), "beamdec_profile_enable")
+def profile_enable(on=True, kernels=None):
+    """Start (or stop) per-kernel event timing; `kernels` (names) limits it
+    to those kernels."""
+    if kernels is None:
+        _check(lib().beamdec_profile_enable(1 if on else 0), "beamdec_profile_enable")
+        return
+    mask = 0
+    for name in kernels:
+        mask |= 1 << KERNELS.index(name)
+    _check(lib().beamdec_profile_enable_mask(mask if on else 0), "beamdec_profile_enable_mask")
 
 
 def profile_read():

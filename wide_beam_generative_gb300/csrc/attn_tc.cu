@@ -138,49 +138,17 @@ __device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-__device__ __forceinline__ f2 f2_sub(f2 a, f2 b) {
-  f2 r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
 
-// 2^x for a pair on the FMA pipe, to take part of the exponentials off the
-// MUFU unit whose ex2 rate bounds the softmax.  Cody and Waite's additive
-// range reduction x = n + f, n = round(x), f in [-1/2, 1/2] (adding 1.5 * 2^23
-// rounds x and leaves n in the low mantissa bits); 2^f from a cubic fitted to
-// 2^f in relative error on [-1/2, 1/2] (largest error 7.5e-5, far below the
-// 2^-9 of the bf16 P it feeds); n then goes into the exponent field: shifted
-// left by 23, the sum's bits are n << 23 (the magic number's bits vanish).  x
-// is clamped at -125 so the exponent stays normal; 2^-125 stands for 0 next
-// to a row sum of at least 1.
-__device__ __forceinline__ f2 exp2_poly2(f2 x) {
-  constexpr float kMagic = 12582912.f;   // 1.5 * 2^23
-  constexpr float c0 = 9.999280572e-01f, c1 = 6.932609677e-01f, c2 = 2.426111251e-01f,
-                  c3 = 5.517165363e-02f;
-  float2 xv = f2_unpack(x);
-  xv.x = fmaxf(xv.x, -125.f);
-  xv.y = fmaxf(xv.y, -125.f);
-  const f2 xc = f2_pack(xv.x, xv.y);
-  const f2 mg = f2_pack(kMagic, kMagic);
-  const f2 t = f2_add(xc, mg);
-  const f2 f = f2_sub(xc, f2_sub(t, mg));
-  f2 q = f2_fma(f2_pack(c3, c3), f, f2_pack(c2, c2));
-  q = f2_fma(q, f, f2_pack(c1, c1));
-  q = f2_fma(q, f, f2_pack(c0, c0));
-  const float2 tv = f2_unpack(t), qv = f2_unpack(q);
-  return f2_pack(__int_as_float(__float_as_int(qv.x) + (__float_as_int(tv.x) << 23)),
-                 __int_as_float(__float_as_int(qv.y) + (__float_as_int(tv.y) << 23)));
-}
-
 // P = 2^(s * sc - m) for the 128 scores of one row as bf16 pairs into TMEM
-// columns 0-63 of the row's S tile, and its sum (two f32x2 chains).  With
-// kPoly three of every eight pairs take the polynomial exponential.
-template <bool kPoly>
+// columns 0-63 of the row's S tile, and its sum (two f32x2 chains).  Every
+// exponential is the MUFU ex2: moving some of them onto the FMA pipe (a
+// range-reduced polynomial) measured slower here, because the softmax warps
+// are short of issue slots as much as of MUFU throughput.
 __device__ __forceinline__ void softmax_row(const float (&sv)[128], float sc, float m_used,
                                             uint32_t tS, f2& acc0, f2& acc1) {
   const f2 scv = f2_pack(sc, sc), nm = f2_pack(-m_used, -m_used);
@@ -191,13 +159,8 @@ __device__ __forceinline__ void softmax_row(const float (&sv)[128], float sc, fl
     for (int i = 0; i < 16; ++i) {
       const int k2 = q * 32 + 2 * i;
       const f2 x = f2_fma(f2_pack(sv[k2], sv[k2 + 1]), scv, nm);
-      f2 pp;
-      if (kPoly && (i & 7) >= 5) {
-        pp = exp2_poly2(x);
-      } else {
-        const float2 xv = f2_unpack(x);
-        pp = f2_pack(ex2(xv.x), ex2(xv.y));
-      }
+      const float2 xv = f2_unpack(x);
+      const f2 pp = f2_pack(ex2(xv.x), ex2(xv.y));
       if (i & 1) acc1 = f2_add(acc1, pp);
       else acc0 = f2_add(acc0, pp);
       const float2 pv = f2_unpack(pp);
@@ -219,6 +182,8 @@ __device__ __forceinline__ void write_empty_partials(const TcParams& p, size_t b
   }
 }
 
+// Ten warps: the register file is handed out in groups of four warps, so a
+// thread may hold at most 65536 / 384 -> 168 registers.
 __global__ void __launch_bounds__(kThreads, 1)
 bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                          const __grid_constant__ CUtensorMap kmap,
@@ -416,20 +381,17 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
         m_used = m_new;
       }
       // pass 2: P = 2^(s - m) as bf16 pairs into TMEM columns 0-63 of S_t
-      // (the last, partial chunk masks its missing keys and stays on ex2,
-      // which gives exact zeros there)
+      // (the last, partial chunk masks its missing keys: ex2 gives exact zeros)
       f2 acc0 = f2_pack(0.f, 0.f), acc1 = f2_pack(0.f, 0.f);
       {
         float sv[128];
         tmem_ld128(tS, sv);
-        if (full) {
-          softmax_row<false>(sv, sc, m_used, tS, acc0, acc1);
-        } else {
+        if (!full) {
 #pragma unroll
           for (int i = 0; i < 128; ++i)
             if (i >= nvalid) sv[i] = -INFINITY;
-          softmax_row<false>(sv, sc, m_used, tS, acc0, acc1);
         }
+        softmax_row(sv, sc, m_used, tS, acc0, acc1);
       }
       {
         const float2 a0 = f2_unpack(acc0), a1 = f2_unpack(acc1);

@@ -15,6 +15,7 @@ namespace {
 constexpr int kMaxPairs = 8192;
 std::mutex g_mu;
 bool g_on = false;
+unsigned g_mask = 0;   // kernel ids (bits) that get bracketed
 int g_n = 0;
 cudaEvent_t g_ev[kMaxPairs][2];
 int g_kid[kMaxPairs];
@@ -29,7 +30,7 @@ const char* kNames[kKCount] = {"bd_expand_kernel", "bd_global_kernel", "bd_attn_
 
 void prof_begin(int kid, cudaStream_t s) {
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_on || g_n >= kMaxPairs) { g_open[kid] = -1; return; }
+  if (!g_on || !((g_mask >> kid) & 1u) || g_n >= kMaxPairs) { g_open[kid] = -1; return; }
   g_kid[g_n] = kid;
   g_open[kid] = g_n;
   cudaEventRecord(g_ev[g_n][0], s);
@@ -47,8 +48,9 @@ void prof_end(int kid, cudaStream_t s) {
 
 using namespace bd;
 
-extern "C" int beamdec_profile_enable(int on) {
+extern "C" int beamdec_profile_enable_mask(unsigned kernel_mask) {
   std::lock_guard<std::mutex> lk(g_mu);
+  const bool on = kernel_mask != 0;
   if (on && !g_created) {
     for (int i = 0; i < kMaxPairs; ++i)
       for (int k = 0; k < 2; ++k)
@@ -59,8 +61,13 @@ extern "C" int beamdec_profile_enable(int on) {
     g_n = 0;
     for (int k = 0; k < kKCount; ++k) g_open[k] = -1;
   }
-  g_on = on != 0;
+  g_on = on;
+  if (on) g_mask = kernel_mask;
   return BEAMDEC_OK;
+}
+
+extern "C" int beamdec_profile_enable(int on) {
+  return beamdec_profile_enable_mask(on ? (1u << kKCount) - 1u : 0u);
 }
 
 extern "C" int beamdec_profile_read(int kernel_id, float* total_ms, int* launches) {

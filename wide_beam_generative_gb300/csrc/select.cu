@@ -624,16 +624,14 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
   // candidates before taking its ticket), prefix-summed into shared memory
   // (the upper half of the key buffer); it brackets the nt-th best score
   uint32_t* hs = reinterpret_cast<uint32_t*>(keys + kTailCap / 2);
+  // each live beam's first trie edge, for the output decode: its two dependent
+  // loads are issued around the scan and the gather so their latency hides
+  // behind them (one beam per thread; stored to sh.hist, free on the bucket path)
+  const bool use_poff = a.has_trie && a.W <= kExpandThreads;
+  const bool pf_live = use_poff && (int)threadIdx.x < a.n_live_in[r];
+  int pnode = pf_live ? a.node_in[(size_t)r * a.W + threadIdx.x] : -1;
   block_scan_bins(ws.hist + (size_t)r * kBins, hs, (uint32_t)nt, sh);
-  // each live beam's first trie edge, for the output decode, gathered now so
-  // its latency hides behind the selection (sh.hist is free on the bucket path)
-  if (a.has_trie && a.W <= 2048) {
-    const int nl = a.n_live_in[r];
-    for (int j = threadIdx.x; j < nl; j += kExpandThreads) {
-      const int nd = a.node_in[(size_t)r * a.W + j];
-      sh.hist[j] = (nd >= 0 && nd < a.lvl.n_nodes) ? (uint32_t)a.lvl.off[nd] : 0u;   // a bad node is never a parent
-    }
-  }
+  const int poffv = (pnode >= 0 && pnode < a.lvl.n_nodes) ? a.lvl.off[pnode] : 0;   // a bad node is never a parent
   const int Dbin = (int)sh.digit;
   const uint32_t c_le = sh.c_le;
   const float ref = a.cum_in[(size_t)r * a.W];
@@ -660,6 +658,7 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
         if (on && slot < c_le) tmp[slot] = kv[u];
       }
     }
+    if (pf_live) sh.hist[threadIdx.x] = (uint32_t)poffv;
     __syncthreads();
     // after the fill hs[b] is the end of bin b and hs[b - 1] its start
     for (int j = threadIdx.x; j < (int)c_le; j += kExpandThreads) {
@@ -672,8 +671,7 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
       if (rank < (uint32_t)nt) sorted[rank] = k;
     }
     __syncthreads();
-    emit_outputs(a, ws, r, sorted, nt,
-                 (a.has_trie && a.W <= 2048) ? reinterpret_cast<const int*>(sh.hist) : nullptr);
+    emit_outputs(a, ws, r, sorted, nt, use_poff ? reinterpret_cast<const int*>(sh.hist) : nullptr);
     return;
   }
   int nc = 0;
