@@ -180,7 +180,7 @@ __device__ __forceinline__ uint32_t warp_bin_reserve(uint32_t* cursor, uint32_t 
 // [0, 4095].  It is monotone (a higher score never gets a higher bin), so a
 // request-wide histogram of bins brackets the W-th best score from one count.
 constexpr int kTailBins = 4096;
-constexpr int kKeyCache = 4096;   // children whose 32-bit keys a block caches in shared memory
+constexpr int kKeyCache = 8192;   // children whose 32-bit keys a block caches in shared memory
 __device__ __forceinline__ int score_bin(float ref, float s) {
   const float u = __fmul_rn(__fsub_rn(ref, s), 64.f);
   if (!(u > 0.f)) return 0;
@@ -285,14 +285,12 @@ __device__ __forceinline__ float2 stream_max_sum(const float* row, int c0, int c
 
 // Rows a2-a3 for beam b of request r: log-sum-exp, trie children, per-beam
 // top_k appended to the request's pool.
-// `bins` (shared memory, fused launches only) collects the score bins of a
-// row that goes through the radix select; rows whose children all enter the
-// pool add theirs straight to the request's histogram in global memory.
-// Returns true when `bins` holds counts the caller must flush.
+// gh (the request's score-bin histogram in global memory; fused launches
+// only) counts every candidate the row adds to the pool.
 // kPf: the row's trie range and scores were fetched into sh.pf_* already.
 template <bool kPf>
-__device__ __forceinline__ bool expand_candidates(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
-                                                 int r, int b, uint32_t* bins, uint32_t* kcache,
+__device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
+                                                 int r, int b, uint32_t* gh, uint32_t* kcache,
                                                  float lse) {
   const int tid = threadIdx.x;
   const int Kp = a.Kp;
@@ -319,7 +317,7 @@ __device__ __forceinline__ bool expand_candidates(const SelectArgs& a, ExpandSha
     }
     if (e0 < 0) {
       if (tid == 0) set_status(ws.hdr, BEAMDEC_ERR_DEVICE_CHECK);
-      return false;
+      return;
     }
     n = e1 - e0;
     code = a.lvl.code + e0;
@@ -342,7 +340,6 @@ __device__ __forceinline__ bool expand_candidates(const SelectArgs& a, ExpandSha
     if (tid == 0) sh.pool_base = n > 0 ? atomicAdd(&st->total, n) : 0;
     __syncthreads();
     const int base = sh.pool_base;
-    uint32_t* gh = bins ? ws.hist + (size_t)r * kBins : nullptr;
     for (int c0 = 0; c0 < n; c0 += kExpandThreads) {   // block-uniform trip count
       const int i = c0 + tid;
       const bool on = i < n;
@@ -350,10 +347,7 @@ __device__ __forceinline__ bool expand_candidates(const SelectArgs& a, ExpandSha
       if (on) pool[base + i] = pool_key(k, b, i);
       if (gh) warp_hist_add(gh, (uint32_t)score_bin(ref, desc_key_value(k)), on);
     }
-    return false;
-  }
-  if (bins) {
-    for (int i = tid; i < kTailBins; i += kExpandThreads) bins[i] = 0;   // ordered by the passes' barriers
+    return;
   }
   // the row's candidate keys, computed once into shared memory when they fit
   // (the radix passes below then read shared memory instead of re-gathering)
@@ -413,7 +407,7 @@ __device__ __forceinline__ bool expand_candidates(const SelectArgs& a, ExpandSha
     const bool on = i < n && k < kth;
     const int pos = warp_reserve(&sh.count, on);
     if (on) pool[base + pos] = pool_key(k, b, i);
-    if (bins) warp_hist_add(bins, (uint32_t)score_bin(ref, desc_key_value(k)), on);
+    if (gh) warp_hist_add(gh, (uint32_t)score_bin(ref, desc_key_value(k)), on);
   }
   __syncthreads();
   const int n_less = sh.count;
@@ -426,10 +420,9 @@ __device__ __forceinline__ bool expand_candidates(const SelectArgs& a, ExpandSha
     const int rk = block_rank(flag, sh.warp_cnt, &tot);
     const bool on = flag && taken + rk < (int)need;
     if (on) pool[base + n_less + taken + rk] = pool_key(kth, b, i);
-    if (bins) warp_hist_add(bins, (uint32_t)score_bin(ref, desc_key_value(kth)), on);
+    if (gh) warp_hist_add(gh, (uint32_t)score_bin(ref, desc_key_value(kth)), on);
     taken += tot;
   }
-  return bins != nullptr;
 }
 
 // Ascending bitonic sort of np (a power of two) 64-bit keys in shared memory.
@@ -768,23 +761,16 @@ selected:
 // a2-a5 for live beam b of request r once its log-sum-exp is known: the
 // row's candidates go to the request's pool; with kFused the last row of the
 // request to finish (a per-request ticket) runs the request's global top-W.
-// Dynamic shared memory: [key cache 16 KB][score-bin histogram 16 KB, fused
-// only]; the fused tail reuses all of it for candidate keys after the ticket.
+// Dynamic shared memory: the row's key cache (32 KB); the fused tail reuses it
+// for candidate keys after the ticket.
 template <bool kFused, bool kPf>
 __device__ __forceinline__ void expand_and_select(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
                                                   int r, int b, int nl, float lse,
                                                   unsigned char* tail_smem) {
   const int tid = threadIdx.x;
   uint32_t* kcache = reinterpret_cast<uint32_t*>(tail_smem);
-  uint32_t* bins = kFused ? kcache + kKeyCache : nullptr;
-  const bool flush = expand_candidates<kPf>(a, sh, ws, r, b, bins, kcache, lse);
+  expand_candidates<kPf>(a, sh, ws, r, b, kFused ? ws.hist + (size_t)r * kBins : nullptr, kcache, lse);
   if constexpr (kFused) {
-    __syncthreads();
-    if (flush) {
-      uint32_t* gh = ws.hist + (size_t)r * kBins;
-      for (int i = tid; i < kTailBins; i += kExpandThreads)
-        if (bins[i]) atomicAdd(gh + i, bins[i]);
-    }
     __syncthreads();
     if (tid == 0) {
       __threadfence();
@@ -1074,7 +1060,7 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
   // row of each request inside the launch; larger ones by the cooperative
   // grid kernel afterwards.
   const bool fused = a.W <= kTailCap && (long long)a.W * a.Kp <= (1ll << 20);
-  static_assert(kKeyCache * 4 + kTailBins * 4 <= kTailCap * 8, "fused dynamic shared memory");
+  static_assert(kKeyCache * 4 <= kTailCap * 8, "fused dynamic shared memory");
   const size_t dsm = fused ? kTailCap * sizeof(unsigned long long) : kKeyCache * sizeof(uint32_t);
   if (a.lse_in == nullptr) {
     dim3 g0(a.W * S, a.R);
