@@ -209,42 +209,89 @@ def test_openvocab_full_size_properties(gpu_lib):
 
 # ---------------------------------------------------------------------------- full path
 
-def test_full_path_own_lse(gpu_lib):
-    """Kernel computes its own normaliser: lse within 1e-5 of float64, and the
-    selection equals the oracle's except where scores tie within 2e-5."""
+def run_chain_own_lse(wl, steps=None, items=None):
+    """The production path (the kernel computes each row's normaliser, so the
+    selection runs in the one-launch stream kernel) against the oracle's own
+    float64 chain.  Each side carries its own state.  Per step: log-sum-exp
+    within 1e-5 of float64; the selected (parent, token, score) rows equal the
+    oracle's, except that candidates whose scores lie within 4e-5 of the cut
+    may trade places (the two sides round their normalisers independently).
+    After such a trade the states differ, so later steps are not compared.
+    Returns the number of steps compared exactly."""
     from wide_beam_generative_gb300 import beamdec as bd
-    from oracle import trie as otrie
-    wl = synth.WORKLOADS["qwen06b"]
-    items = _catalog(wl)
-    gtrie, otr = build_tries(wl, items)
-    W, K, R = wl.W, wl.K, wl.R
-    st = _init_state(R, W, wl.T)
-    for t in range(wl.T):
+    W, K, R, T = wl.W, wl.K, wl.R, wl.T
+    steps = T if steps is None else steps
+    gtrie, otr = build_tries(wl, items) if wl.levels else (None, None)
+    st = _init_state(R, W, T)
+    o_cum = np.zeros((R, W), np.float32)
+    o_node = np.zeros((R, W), np.int64)
+    o_nl = np.ones(R, np.int32)
+    o_slot = np.full((R, W, T), -1, np.int32)
+    ws = bd.workspace(bd.beam_select_workspace_size(R, W, K, wl.V))
+    exact = 0
+    for t in range(steps):
         lg = synth.logits(wl, t, device=DEV)
-        res = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], gtrie, t, t, K)
-        lg_np = lg.cpu().numpy()
-        n_in = st["n_live"].cpu().numpy()
-        ref = osel.beam_select(lg_np, st["cum"].cpu().numpy(), st["node"].cpu().numpy(),
-                               n_in, st["slot"].cpu().numpy(), otr, wl.token_base(), t, t, W, K)
+        res = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], gtrie, t, t, K, ws=ws)
+        assert bd.read_status(ws) == 0
+        ref = osel.beam_select(lg.cpu().numpy(), o_cum, o_node, o_nl, o_slot, otr, wl.token_base(), t, t,
+                               W, K)
         got_lse = res["lse_out"].cpu().numpy()
+        g = {k: res[k].cpu().numpy() for k in ("parents", "tokens", "cum_out", "node_out", "n_live_out",
+                                               "slot_out")}
+        traded = False
         for r in range(R):
-            nl = int(n_in[r])
-            assert np.abs(got_lse[r, :nl] - ref["lse64"][r, :nl]).max() < ATOL_LSE
-        n = int(ref["n_live_out"][0])
-        assert int(res["n_live_out"][0]) == n
-        g_s = res["cum_out"].cpu().numpy()[0, :n].astype(np.float64)
-        o_s = ref["cum_out"][0, :n].astype(np.float64)
-        assert np.abs(g_s - o_s).max() < 2e-5
-        g_set = set(zip(res["parents"].cpu().numpy()[0, :n], res["tokens"].cpu().numpy()[0, :n]))
-        o_set = set(zip(ref["parents"][0, :n], ref["tokens"][0, :n]))
-        if g_set != o_set:   # only candidates within the tie tolerance of the cut may differ
+            nl_in = int(o_nl[r])
+            assert np.abs(got_lse[r, :nl_in].astype(np.float64) - ref["lse64"][r, :nl_in]).max() < ATOL_LSE
+            n = int(ref["n_live_out"][r])
+            assert int(g["n_live_out"][r]) == n
+            g_s = g["cum_out"][r, :n].astype(np.float64)
+            o_s = ref["cum_out"][r, :n].astype(np.float64)
+            assert np.abs(g_s - o_s).max() < 2e-5
+            same = (np.array_equal(g["parents"][r, :n], ref["parents"][r, :n]) and
+                    np.array_equal(g["tokens"][r, :n], ref["tokens"][r, :n]))
+            if same:
+                assert np.array_equal(g["node_out"][r, :n], ref["node_out"][r, :n])
+                assert np.array_equal(g["slot_out"][r, :n], ref["slot_out"][r, :n])
+                continue
+            traded = True
             cut = o_s[-1]
-            diff = g_set ^ o_set
-            lookup = {(p, tk): s for p, tk, s in zip(ref["parents"][0, :n], ref["tokens"][0, :n], o_s)}
-            for key in diff:
+            g_set = set(zip(g["parents"][r, :n], g["tokens"][r, :n]))
+            o_set = set(zip(ref["parents"][r, :n], ref["tokens"][r, :n]))
+            lookup = {(p, tk): sc for p, tk, sc in zip(ref["parents"][r, :n], ref["tokens"][r, :n], o_s)}
+            for key in g_set ^ o_set:
                 if key in lookup:
                     assert abs(lookup[key] - cut) < 4e-5
+            # rows outside the traded band keep their order
+            band = np.abs(o_s - cut) < 4e-5
+            keep = ~band
+            assert np.array_equal(g["parents"][r, :n][keep], ref["parents"][r, :n][keep])
+        if traded:
+            break
+        exact += 1
         st = dict(cum=res["cum_out"], node=res["node_out"], n_live=res["n_live_out"], slot=res["slot_out"])
+        o_cum, o_node, o_nl, o_slot = ref["cum_out"], ref["node_out"], ref["n_live_out"], ref["slot_out"]
+    return exact
+
+
+def test_full_path_own_lse(gpu_lib):
+    """qwen06b, 3 steps, the one-launch selection against the oracle's chain."""
+    wl = synth.WORKLOADS["qwen06b"]
+    assert run_chain_own_lse(wl, items=_catalog(wl)) >= 1
+
+
+def test_onerec17b_full_size_own_lse(gpu_lib):
+    """The benchmarked shape (4 x 512 beams, top_k 512) on the production path:
+    row expansion in each row's last stream block and the request tail in the
+    request's last row, against the oracle's chain."""
+    wl = synth.WORKLOADS["onerec17b"]
+    assert run_chain_own_lse(wl, items=_catalog(wl)) >= 1
+
+
+def test_fp8kv_full_size_own_lse(gpu_lib):
+    """4 x 1000 beams, top_k 128, four SID levels: more than 1024 candidates at
+    or above the cut's bin, so the tail takes the radix-narrowing path."""
+    wl = synth.WORKLOADS["fp8kv"]
+    assert run_chain_own_lse(wl, items=_catalog(wl)) >= 1
 
 
 def test_deterministic_repeat(gpu_lib):
