@@ -327,6 +327,7 @@ def gpu_arm(args, ws, rank, local):
 
     # end-to-end through the C ABI from pinned host buffers
     e2e = None if args.no_e2e else e2e_arm(step, args, ws, flush)
+    chain = None if args.no_chain else chain_arm(step, args, flush)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "beam-rows/s", "n_gpus": ws,
@@ -341,7 +342,7 @@ def gpu_arm(args, ws, rank, local):
         "roofline": roof, "kernels": kernels,
         "kernels_note": "per-kernel event times from a pass of the same steps just before the timed "
                         "region; inside it only the roofline kernel is bracketed by events",
-        "gpu_launches": launches, "clocks": clk, "e2e": e2e,
+        "gpu_launches": launches, "clocks": clk, "e2e": e2e, "chain_graph": chain,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows or 4 * wl.W)
@@ -388,6 +389,42 @@ def e2e_arm(step, args, ws, flush):
     rows = step.rows()
     return {"value": round(rows * ws / (ms / 1e3), 1), "unit": "beam-rows/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 3)}
+
+
+def chain_arm(step, args, flush):
+    """All T decode steps of the workload (selection + attention each) as one
+    CUDA graph replay (DecodeChain), inputs resident: the multi-step loop with
+    no host work between steps.  Reported beside the per-step number."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl, dev = step.wl, step.dev
+    att = [step.attn] + [synth.attention_inputs(wl, t, device=dev) for t in range(1, wl.T)]
+    logits = [synth.logits(wl, t, device=dev) for t in range(wl.T - 1)] + [step.logits]
+    a0 = step.attn
+    ch = bd.DecodeChain(logits, [x["q"] for x in att], a0["shared_k"], a0["shared_v"], a0["prompt_offsets"],
+                        step.maxp, a0["unshared_k"], a0["unshared_v"], step.trie, wl.K,
+                        k_scale=a0["k_scale"], v_scale=a0["v_scale"])
+    for _ in range(3):
+        flush.zero_()
+        ch.replay()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 10))
+    times = []
+    stream = torch.cuda.current_stream()
+    for _ in range(n):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ch.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    assert ch.status() == (0, 0)
+    us = sum(times) / n * 1e3
+    del ch, logits, att
+    torch.cuda.empty_cache()
+    return {"steps": wl.T, "us_per_chain": round(us, 1), "us_per_step": round(us / wl.T, 1),
+            "note": "every decode step of the workload (1, then W live beams) as one CUDA graph; "
+                    "L2 flushed before each replay"}
 
 
 # ------------------------------------------------------------------------------ CPU oracle
@@ -494,6 +531,7 @@ def main():
                     help="beams in the oracle's sample (default 512 for cpu_baseline, 128 per reference step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--no-chain", action="store_true", help="skip the whole-chain CUDA-graph replay")
     ap.add_argument("--requests", type=int, default=None,
                     help="override the workload's request count (smaller cases for profiling)")
     args = ap.parse_args()

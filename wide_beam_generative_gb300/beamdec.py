@@ -300,3 +300,77 @@ def beam_attn_decode(q, shared_k, shared_v, prompt_offsets, max_prompt_len, unsh
                                 _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "beam_attn_decode")
     return out
+
+
+class DecodeChain:
+    """T decode steps (selection, then attention, per step) captured once as a
+    single CUDA graph and replayed with no host work between steps.
+
+    logits[t] [R, W, V] fp32 and q[t] [R, W, Hq, d] are the per-step inputs,
+    resident on the device; the prompt KV and the slot pool of unshared KV
+    are shared by all steps.  Every replay starts from one live beam per
+    request (cum 0, trie root, empty slot rows), exactly as the eager chain
+    does, and leaves step t's outputs in ``sel[t]`` (the beam_select dict)
+    and ``out[t]`` (the attention output).  The C ABI makes this possible:
+    its compute calls neither allocate nor synchronise the host, so graph
+    capture records the same launches an eager call would make.
+    """
+
+    def __init__(self, logits, q, shared_k, shared_v, prompt_offsets, max_prompt_len,
+                 unshared_k, unshared_v, trie, K, k_scale=None, v_scale=None, sm_scale=0.0):
+        T = len(logits)
+        R, W, V = logits[0].shape
+        Hq, d = q[0].shape[2], q[0].shape[3]
+        Hkv = unshared_k.shape[2]
+        dev = logits[0].device
+        self.T = T
+        self._state0 = dict(cum=torch.zeros((R, W), dtype=torch.float32, device=dev),
+                            node=torch.zeros((R, W), dtype=torch.int32, device=dev),
+                            n_live=torch.ones((R,), dtype=torch.int32, device=dev),
+                            slot=torch.full((R, W, T), -1, dtype=torch.int32, device=dev))
+        self._state = {k: torch.empty_like(v) for k, v in self._state0.items()}
+        self.sel = [dict(tokens=torch.empty((R, W), dtype=torch.int32, device=dev),
+                         parents=torch.empty((R, W), dtype=torch.int32, device=dev),
+                         cum_out=torch.empty((R, W), dtype=torch.float32, device=dev),
+                         lse_out=torch.empty((R, W), dtype=torch.float32, device=dev),
+                         node_out=torch.empty((R, W), dtype=torch.int32, device=dev),
+                         n_live_out=torch.empty((R,), dtype=torch.int32, device=dev),
+                         slot_out=torch.empty((R, W, T), dtype=torch.int32, device=dev))
+                    for _ in range(T)]
+        out_dt = torch.float32 if q[0].dtype == torch.float32 else torch.bfloat16
+        self.out = [torch.empty((R, W, Hq, d), dtype=out_dt, device=dev) for _ in range(T)]
+        self._ws_sel = workspace(beam_select_workspace_size(R, W, K, V), dev)
+        self._ws_att = workspace(beam_attn_workspace_size(R, W, Hq, Hkv, d, max_prompt_len,
+                                                          _DT[unshared_k.dtype]), dev)
+
+        def chain():
+            for k, v in self._state0.items():
+                self._state[k].copy_(v)
+            st = self._state
+            for t in range(T):
+                o = beam_select(logits[t], st["cum"], st["node"], st["n_live"], st["slot"], trie, t, t, K,
+                                out=self.sel[t], ws=self._ws_sel)
+                beam_attn_decode(q[t], shared_k, shared_v, prompt_offsets, max_prompt_len, unshared_k,
+                                 unshared_v, o["slot_out"], o["n_live_out"], t, k_scale=k_scale,
+                                 v_scale=v_scale, sm_scale=sm_scale, out=self.out[t], ws=self._ws_att)
+                st = dict(cum=o["cum_out"], node=o["node_out"], n_live=o["n_live_out"], slot=o["slot_out"])
+
+        # one eager pass on a side stream (first-use setup such as kernel
+        # attributes happens outside the capture), then the capture itself
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            chain()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            chain()
+
+    def replay(self):
+        """Run the T steps on the current stream (asynchronously)."""
+        self.graph.replay()
+
+    def status(self):
+        """Device-side status words of the selection and attention workspaces."""
+        return read_status(self._ws_sel), read_status(self._ws_att)
