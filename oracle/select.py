@@ -24,8 +24,15 @@ returned sequence score is the cumulative log-probability):
    unspecified.
 
 Step 0 starts from one live beam per request (the prefill row, cum = 0).
+
+With temperature > 0 (Gumbel top-k, "Deploying FlashRec" serving
+parameters), steps 4 and 5 order by the noisy key of ``oracle.gumbel``
+(fl32(fl32(s * inv_tau) + g), ties as above) instead of s; the returned
+cumulative score stays s, without the noise.
 """
 import numpy as np
+
+from oracle import gumbel as _gumbel
 
 F32 = np.float32
 
@@ -52,14 +59,17 @@ def candidate_scores(x_f32, cum_f32, lse_f32):
 
 
 def beam_select(logits, cum, node, n_live, slot_in, trie, token_base, level, step,
-                W, K, lse32=None):
+                W, K, lse32=None, temperature=0.0, seed=0):
     """One expansion step for every request.
 
     logits [R, >=n_live, V] float32; cum [R, W] float32; node [R, W] int;
     n_live [R]; slot_in [R, W, T] int32.  Returns a dict of numpy arrays:
     tokens, parents, cum_out, node_out [R, W]; n_live_out [R]; slot_out
-    [R, W, T]; lse64 [R, W] (NaN for dead rows).
+    [R, W, T]; lse64 [R, W] (NaN for dead rows).  temperature > 0: Gumbel
+    top-k with the counter-based noise of ``oracle.gumbel`` under ``seed``.
     """
+    gumbel = temperature > 0
+    itau = _gumbel.inv_tau(temperature) if gumbel else None
     logits = np.asarray(logits)
     R, V = logits.shape[0], logits.shape[2]
     T = slot_in.shape[2]
@@ -71,19 +81,21 @@ def beam_select(logits, cum, node, n_live, slot_in, trie, token_base, level, ste
     slot_out = np.full((R, W, T), -1, dtype=np.int32)
     lse_all = np.full((R, W), np.nan)
     for r in range(R):
-        ps, pb, pt, pc = [], [], [], []
+        ps, pb, pt, pc, pk = [], [], [], [], []
         for b in range(int(n_live[r])):
             row = logits[r, b]
             lse_all[r, b] = lse64(row)
             l32 = F32(lse_all[r, b]) if lse32 is None else F32(lse32[r, b])
             tok, kid = candidates(trie, token_base, level, int(node[r, b]), V)
             s = candidate_scores(row[tok], cum[r, b], l32)
-            order = np.lexsort((tok, -s.astype(np.float64)))[: min(K, len(tok))]
+            key = (_gumbel.ordering_keys(s, _gumbel.gumbel(seed, r, step, b, tok), itau) if gumbel else s)
+            order = np.lexsort((tok, -key.astype(np.float64)))[: min(K, len(tok))]
             ps.append(s[order]); pb.append(np.full(len(order), b)); pt.append(tok[order]); pc.append(kid[order])
+            pk.append(key[order])
         if not ps:
             continue
-        s, b, t, c = (np.concatenate(a) for a in (ps, pb, pt, pc))
-        order = np.lexsort((t, b, -s.astype(np.float64)))[:W]
+        s, b, t, c, key = (np.concatenate(a) for a in (ps, pb, pt, pc, pk))
+        order = np.lexsort((t, b, -key.astype(np.float64)))[:W]
         n = len(order)
         n_live_out[r] = n
         tokens[r, :n] = t[order]
@@ -98,13 +110,14 @@ def beam_select(logits, cum, node, n_live, slot_in, trie, token_base, level, ste
 
 
 def beam_select_bruteforce(logits, cum, node, n_live, trie, token_base, level, W, K,
-                           lse32=None):
+                           lse32=None, temperature=0.0, seed=0, step=0):
     """Single-pass restatement used only to pin ``beam_select`` on tiny inputs.
 
     Enumerates every (beam, token) pair of the whole beam x vocab grid, drops the
     pairs the trie forbids, orders all of them by (s desc, beam asc, token asc)
     and walks that order keeping at most top_k per beam, stopping at beam_width.
-    Plain Python loops: tiny sizes only.
+    With temperature > 0 the order is by the noisy key instead (the noise of
+    each pair drawn on its own).  Plain Python loops: tiny sizes only.
     """
     R, V = logits.shape[0], logits.shape[2]
     out = []
@@ -120,7 +133,11 @@ def beam_select_bruteforce(logits, cum, node, n_live, trie, token_base, level, W
             for v in range(V):
                 if v in allowed:
                     s = F32(F32(cum[r, b]) + F32(F32(logits[r, b, v]) - l32))
-                    allc.append((-float(s), b, v, allowed[v], s))
+                    key = s
+                    if temperature > 0:
+                        g = _gumbel.gumbel(seed, r, step, b, np.array([v]))[0]
+                        key = F32(F32(s * _gumbel.inv_tau(temperature)) + g)
+                    allc.append((-float(key), b, v, allowed[v], s))
         allc.sort()
         taken, per_beam = [], {}
         for neg_s, b, v, kid, s in allc:
