@@ -9,10 +9,11 @@ include it.  The pages give no formula beyond that; the reading used here
 * ordering key of a candidate with score s:  k = fl32(fl32(s * inv_tau) + g),
   inv_tau = fl32(1 / temperature);
 * g ~ Gumbel(0, 1), one independent draw per (request r, step t, beam b,
-  token v): g = -ln(-ln(u)), u = (bits24 + 1/2) * 2^-24 from word 0 of
+  token v): g = -ln(-ln(u)), u = (bits23 + 1/2) * 2^-23 from word 0 of
   Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
   easy as 1, 2, 3", SC 2011) at counter (v, b, r, t) and key (seed low
-  32 bits, seed high 32 bits); bits24 = word0 >> 8;
+  32 bits, seed high 32 bits); bits23 = word0 >> 9 (so that u is exact in
+  float32 and never 0 or 1);
 * ln is computed in float32 by the method below, the same operations in the
   same order on both sides, so both take identical ordering decisions.
 
@@ -86,7 +87,7 @@ def gumbel(seed, r, t, b, v):
     seed = int(seed)
     w0 = philox4x32_10(np.asarray(v, dtype=np.int64).astype(U32), U32(b), U32(r), U32(t),
                        seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)[0]
-    u = ((w0 >> U32(8)).astype(F32) + F32(0.5)) * F32(2.0 ** -24)    # exact
+    u = ((w0 >> U32(9)).astype(F32) + F32(0.5)) * F32(2.0 ** -23)    # exact
     y = (-ln_f32(u.astype(F32))).astype(F32)
     return (-ln_f32(y)).astype(F32)
 
