@@ -226,6 +226,32 @@ int beam_select(const float* logits, int64_t row_stride, const float* lse_in,
                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * beam_select with temperature > 0: Gumbel top-k.  "Deploying FlashRec"
+ * (serving parameters): a positive temperature makes the selection Gumbel
+ * top-k, the noise only orders the candidates and the returned sequence score
+ * does not include it.  Here each candidate (request r, step t, beam b, token
+ * v) with score s = fl32(cum + fl32(logit - lse)) is ordered (per beam, then
+ * per request, ties as in beam_select) by the key
+ *     fl32(fl32(s * fl32(1 / temperature)) + g),
+ *     g = -ln(-ln(u)),  u = ((word0 >> 9) + 1/2) * 2^-23,
+ * word0 = first output word of Philox4x32-10 (Salmon et al., SC 2011) at
+ * counter (v, b, r, t) and key (seed & 0xffffffff, seed >> 32); ln is a
+ * float32 atanh-series logarithm with every step rounded to nearest.  The
+ * same seed, step and inputs give the same selection.  cum_out holds s (no
+ * noise); every other argument, output and error is as for beam_select, and
+ * the workspace is the same size.
+ * Errors: INVALID_ARG also for temperature <= 0, not finite, or so small that
+ * 1 / temperature overflows float32.
+ */
+int beam_select_gumbel(const float* logits, int64_t row_stride, const float* lse_in,
+                       const float* cum_in, const int32_t* node_in, const int32_t* n_live_in,
+                       const int32_t* slot_in, const beamdec_trie* trie, int level, int step,
+                       int R, int W, int K, int V, int T, float temperature, uint64_t seed,
+                       int32_t* tokens, int32_t* parents, float* cum_out, float* lse_out,
+                       int32_t* node_out, int32_t* n_live_out, int32_t* slot_out,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * beam_select_static — beam_select without a caller-provided workspace.
  * The pages have no counterpart to this entry point; it serves callers of
  * this library that cannot allocate device memory: a plugin interface that

@@ -129,3 +129,13 @@ def test_static_select_rejects_oversized_shapes_on_host(L):
                               2, 5000, 5000, 151936, 2, fake, fake, fake, None, fake, fake,
                               ctypes.c_void_p(0x2000), None)
     assert rc == bd.ERR_UNSUPPORTED
+
+
+def test_gumbel_select_validates_temperature_on_host(L):
+    from wide_beam_generative_gb300 import beamdec as bd
+    args = [FAKE, 512, None, FAKE, FAKE, FAKE, FAKE, None, 0, 0, 1, 8, 8, 512, 3]
+    outs = [FAKE, FAKE, FAKE, None, FAKE, FAKE, ctypes.c_void_p(0x2000), FAKE, 0, None]
+    for t in (0.0, -1.0, float("nan"), float("inf"), 1e-40):
+        assert L.beam_select_gumbel(*args, t, 7, *outs) == bd.ERR_INVALID_ARG, t
+    # a valid temperature reaches the same shape checks as beam_select
+    assert L.beam_select_gumbel(*args, 0.7, 7, *outs) == bd.ERR_WORKSPACE

@@ -30,8 +30,10 @@ def _init_state(R, W, T):
                 slot=torch.full((R, W, T), -1, dtype=torch.int32, device=DEV))
 
 
-def run_chain(wl, items=None, steps=None, K=None, W=None, logit_fn=None, check=True):
-    """Decode `steps` steps on the GPU and in the oracle in lockstep."""
+def run_chain(wl, items=None, steps=None, K=None, W=None, logit_fn=None, check=True, temperature=0.0,
+              seed=0):
+    """Decode `steps` steps on the GPU and in the oracle in lockstep
+    (temperature > 0: Gumbel top-k under `seed` on both sides)."""
     from wide_beam_generative_gb300 import beamdec as bd
     W = W or wl.W
     K = K or wl.K
@@ -53,9 +55,10 @@ def run_chain(wl, items=None, steps=None, K=None, W=None, logit_fn=None, check=T
         lg_np = lg.cpu().numpy()
         lse32 = oracle_lse32(lg_np, o_nl)
         res = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], gtrie, t, t, K,
-                             lse_in=torch.from_numpy(np.nan_to_num(lse32)).to(DEV), ws=ws)
+                             lse_in=torch.from_numpy(np.nan_to_num(lse32)).to(DEV), ws=ws,
+                             temperature=temperature, seed=seed)
         ref = osel.beam_select(lg_np, o_cum, o_node, o_nl, o_slot, otr, wl.token_base(), t, t, W, K,
-                               lse32=lse32)
+                               lse32=lse32, temperature=temperature, seed=seed)
         if check:
             compare_select(res, ref, t, f"{wl.name} step {t}")
         assert bd.read_status(ws) == 0
@@ -209,7 +212,7 @@ def test_openvocab_full_size_properties(gpu_lib):
 
 # ---------------------------------------------------------------------------- full path
 
-def run_chain_own_lse(wl, steps=None, items=None):
+def run_chain_own_lse(wl, steps=None, items=None, temperature=0.0, seed=0):
     """The production path (the kernel computes each row's normaliser, so the
     selection runs in the one-launch stream kernel) against the oracle's own
     float64 chain.  Each side carries its own state.  Per step: log-sum-exp
@@ -231,10 +234,11 @@ def run_chain_own_lse(wl, steps=None, items=None):
     exact = 0
     for t in range(steps):
         lg = synth.logits(wl, t, device=DEV)
-        res = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], gtrie, t, t, K, ws=ws)
+        res = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], gtrie, t, t, K, ws=ws,
+                             temperature=temperature, seed=seed)
         assert bd.read_status(ws) == 0
         ref = osel.beam_select(lg.cpu().numpy(), o_cum, o_node, o_nl, o_slot, otr, wl.token_base(), t, t,
-                               W, K)
+                               W, K, temperature=temperature, seed=seed)
         got_lse = res["lse_out"].cpu().numpy()
         g = {k: res[k].cpu().numpy() for k in ("parents", "tokens", "cum_out", "node_out", "n_live_out",
                                                "slot_out")}
@@ -322,3 +326,53 @@ def test_bad_node_sets_device_check(gpu_lib):
     assert bd.read_status(ws) == bd.ERR_DEVICE_CHECK
     assert int(res["n_live_out"][0]) == 0                       # the bad beam contributed nothing
     assert bd.read_status(ws) == 0                              # reading clears the word
+
+
+# ---------------------------------------------------------------------------- Gumbel top-k
+
+@pytest.mark.parametrize("temperature,seed", [(1.0, 1), (0.5, 2), (2.0, (1 << 40) + 3)])
+def test_gumbel_tiny_chain_bitexact(gpu_lib, temperature, seed):
+    """Temperature > 0: Gumbel top-k with the counter-based noise drawn on each
+    side by its own Philox4x32-10 and float32 logarithm; selections, scores
+    (noise-free), nodes and slot rows equal the oracle's bit for bit."""
+    wl = synth.WORKLOADS["tiny"]
+    run_chain(wl, _catalog(wl), temperature=temperature, seed=seed)
+
+
+def test_gumbel_tiny_open_vocab(gpu_lib):
+    wl = synth.WORKLOADS["tiny"].scaled(levels=0, n_items=0)
+    run_chain(wl, K=5, temperature=0.8, seed=11)
+
+
+def test_gumbel_qwen06b_chain_bitexact(gpu_lib):
+    wl = synth.WORKLOADS["qwen06b"]
+    run_chain(wl, _catalog(wl), temperature=1.0, seed=20261202)
+
+
+def test_gumbel_onerec17b_full_size_bitexact(gpu_lib):
+    """The 4 x 512-beam shape with the noise (first two steps)."""
+    wl = synth.WORKLOADS["onerec17b"]
+    run_chain(wl, _catalog(wl), steps=2, temperature=0.7, seed=5)
+
+
+def test_gumbel_production_path(gpu_lib):
+    """Own log-sum-exp (the one-launch stream kernel) in Gumbel mode against the
+    oracle's chain."""
+    wl = synth.WORKLOADS["qwen06b"]
+    assert run_chain_own_lse(wl, items=_catalog(wl), temperature=1.0, seed=99) >= 1
+
+
+def test_gumbel_differs_from_deterministic_and_repeats(gpu_lib):
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl = synth.WORKLOADS["qwen06b"]
+    gtrie, _ = build_tries(wl, _catalog(wl))
+    st = _init_state(wl.R, wl.W, wl.T)
+    lg = synth.logits(wl, 0, device=DEV)
+    det = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], gtrie, 0, 0, wl.K)
+    g1 = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], gtrie, 0, 0, wl.K,
+                        temperature=1.0, seed=4)
+    g2 = bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], gtrie, 0, 0, wl.K,
+                        temperature=1.0, seed=4)
+    assert not torch.equal(det["tokens"], g1["tokens"])
+    for k in ("tokens", "parents", "cum_out", "node_out", "n_live_out", "slot_out"):
+        assert torch.equal(g1[k], g2[k]), k

@@ -44,6 +44,9 @@ _SIGS = {
     "beam_select": (c_int, [c_p, c_i64, c_p, c_p, c_p, c_p, c_p, c_p, c_int, c_int,
                             c_int, c_int, c_int, c_int, c_int,
                             c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]),
+    "beam_select_gumbel": (c_int, [c_p, c_i64, c_p, c_p, c_p, c_p, c_p, c_p, c_int, c_int,
+                                   c_int, c_int, c_int, c_int, c_int, c_f, ctypes.c_uint64,
+                                   c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]),
     "beam_select_static": (c_int, [c_p, c_i64, c_p, c_p, c_p, c_p, c_p, c_p, c_int, c_int,
                                    c_int, c_int, c_int, c_int, c_int,
                                    c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p]),
@@ -212,11 +215,13 @@ def read_status(ws, stream=None):
 
 
 def beam_select(logits, cum, node, n_live, slot_in, trie, level, step, K, T=None,
-                lse_in=None, out=None, ws=None, stream=None, want_lse=True):
+                lse_in=None, out=None, ws=None, stream=None, want_lse=True, temperature=0.0, seed=0):
     """One expansion step.  logits [R, W, V] fp32 (row b of request r at
     logits[r, b]); cum [R, W] fp32; node [R, W] int32 (ignored without trie);
     n_live [R] int32; slot_in [R, W, T] int32.  Returns a dict of output
-    tensors: tokens, parents, cum_out, lse_out, node_out, n_live_out, slot_out."""
+    tensors: tokens, parents, cum_out, lse_out, node_out, n_live_out, slot_out.
+    temperature > 0 selects by Gumbel top-k (beam_select_gumbel) with the
+    64-bit ``seed``."""
     R, W = cum.shape
     V = logits.shape[-1]
     if logits.dim() != 3 or logits.shape[0] != R or logits.shape[1] != W or logits.stride(2) != 1 \
@@ -235,13 +240,17 @@ def beam_select(logits, cum, node, n_live, slot_in, trie, level, step, K, T=None
                    slot_out=torch.empty((R, W, T), dtype=torch.int32, device=dev))
     if ws is None:
         ws = workspace(beam_select_workspace_size(R, W, K, V), dev)
-    rc = lib().beam_select(_ptr(logits), logits.stride(1), _ptr(lse_in), _ptr(cum), _ptr(node),
-                           _ptr(n_live), _ptr(slot_in), trie.handle if trie is not None else None,
-                           level, step, R, W, K, V, T,
-                           _ptr(out["tokens"]), _ptr(out["parents"]), _ptr(out["cum_out"]),
-                           _ptr(out.get("lse_out")), _ptr(out["node_out"]), _ptr(out["n_live_out"]),
-                           _ptr(out["slot_out"]), _ptr(ws), ws.numel(), _stream(stream))
-    _check(rc, "beam_select")
+    head = (_ptr(logits), logits.stride(1), _ptr(lse_in), _ptr(cum), _ptr(node), _ptr(n_live),
+            _ptr(slot_in), trie.handle if trie is not None else None, level, step, R, W, K, V, T)
+    tail = (_ptr(out["tokens"]), _ptr(out["parents"]), _ptr(out["cum_out"]), _ptr(out.get("lse_out")),
+            _ptr(out["node_out"]), _ptr(out["n_live_out"]), _ptr(out["slot_out"]), _ptr(ws), ws.numel(),
+            _stream(stream))
+    if temperature > 0:
+        rc = lib().beam_select_gumbel(*head, float(temperature), int(seed) & (2 ** 64 - 1), *tail)
+        _check(rc, "beam_select_gumbel")
+    else:
+        rc = lib().beam_select(*head, *tail)
+        _check(rc, "beam_select")
     return out
 
 

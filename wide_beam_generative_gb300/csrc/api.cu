@@ -123,14 +123,14 @@ extern "C" int beam_select_workspace_size(int R, int W, int K, int V, size_t* by
   return BEAMDEC_OK;
 }
 
-extern "C" int beam_select(const float* logits, int64_t row_stride, const float* lse_in,
+static int select_entry(const float* logits, int64_t row_stride, const float* lse_in,
                            const float* cum_in, const int32_t* node_in,
                            const int32_t* n_live_in, const int32_t* slot_in,
                            const beamdec_trie* trie, int level, int step, int R, int W, int K,
                            int V, int T, int32_t* tokens, int32_t* parents, float* cum_out,
                            float* lse_out, int32_t* node_out, int32_t* n_live_out,
                            int32_t* slot_out, void* workspace, size_t workspace_bytes,
-                           void* stream) {
+                           void* stream, float temperature, uint64_t seed) {
   if (logits == nullptr || cum_in == nullptr || n_live_in == nullptr || tokens == nullptr ||
       parents == nullptr || cum_out == nullptr || node_out == nullptr ||
       n_live_out == nullptr || slot_out == nullptr || workspace == nullptr)
@@ -162,7 +162,39 @@ extern "C" int beam_select(const float* logits, int64_t row_stride, const float*
   a.tokens = tokens; a.parents = parents; a.cum_out = cum_out; a.lse_out = lse_out;
   a.node_out = node_out; a.n_live_out = n_live_out; a.slot_out = slot_out;
   a.ws = workspace;
+  a.inv_tau = temperature > 0.f ? (float)(1.0 / (double)temperature) : 0.f;
+  a.seed_lo = (uint32_t)(seed & 0xFFFFFFFFull);
+  a.seed_hi = (uint32_t)(seed >> 32);
   return launch_select(a, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int beam_select(const float* logits, int64_t row_stride, const float* lse_in,
+                           const float* cum_in, const int32_t* node_in,
+                           const int32_t* n_live_in, const int32_t* slot_in,
+                           const beamdec_trie* trie, int level, int step, int R, int W, int K,
+                           int V, int T, int32_t* tokens, int32_t* parents, float* cum_out,
+                           float* lse_out, int32_t* node_out, int32_t* n_live_out,
+                           int32_t* slot_out, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  return select_entry(logits, row_stride, lse_in, cum_in, node_in, n_live_in, slot_in, trie, level,
+                      step, R, W, K, V, T, tokens, parents, cum_out, lse_out, node_out, n_live_out,
+                      slot_out, workspace, workspace_bytes, stream, 0.f, 0);
+}
+
+extern "C" int beam_select_gumbel(const float* logits, int64_t row_stride, const float* lse_in,
+                                  const float* cum_in, const int32_t* node_in,
+                                  const int32_t* n_live_in, const int32_t* slot_in,
+                                  const beamdec_trie* trie, int level, int step, int R, int W,
+                                  int K, int V, int T, float temperature, uint64_t seed,
+                                  int32_t* tokens, int32_t* parents, float* cum_out,
+                                  float* lse_out, int32_t* node_out, int32_t* n_live_out,
+                                  int32_t* slot_out, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  if (!(temperature > 0.f) || !(temperature < INFINITY)) return BEAMDEC_ERR_INVALID_ARG;
+  if (!((float)(1.0 / (double)temperature) < INFINITY)) return BEAMDEC_ERR_INVALID_ARG;
+  return select_entry(logits, row_stride, lse_in, cum_in, node_in, n_live_in, slot_in, trie, level,
+                      step, R, W, K, V, T, tokens, parents, cum_out, lse_out, node_out, n_live_out,
+                      slot_out, workspace, workspace_bytes, stream, temperature, seed);
 }
 
 static bool attn_types_ok(int q, int kv, int o) {

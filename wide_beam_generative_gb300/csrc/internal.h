@@ -48,6 +48,8 @@ struct SelectArgs {
   int32_t* tokens; int32_t* parents; float* cum_out; float* lse_out;
   int32_t* node_out; int32_t* n_live_out; int32_t* slot_out;
   void* ws;
+  float inv_tau;                  // fl32(1 / temperature); 0 = deterministic top-k
+  uint32_t seed_lo, seed_hi;      // Gumbel noise key (temperature > 0)
 };
 int launch_select(const SelectArgs& a, cudaStream_t stream);
 

@@ -31,6 +31,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "gumbel.cuh"
 #include "internal.h"
 
 namespace bd {
@@ -65,6 +66,7 @@ struct SelWs {
   unsigned long long* pool;  // [R][W*Kp]
   unsigned long long* cand;  // [R][kSelectCap]
   float2* rowpart;        // [R][W][kMaxRowSplits] per-chunk (max, sum of exp)
+  float* rowlse;          // [R][W] row log-sum-exp (Gumbel mode: the outputs recompute scores)
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -78,7 +80,8 @@ __host__ __device__ inline SelWs carve(void* ws, int R, int W, int Kp) {
   s.hist = (uint32_t*)p; p += align256((size_t)R * kBins * sizeof(uint32_t));
   s.pool = (unsigned long long*)p; p += align256((size_t)R * W * Kp * 8);
   s.cand = (unsigned long long*)p; p += align256((size_t)R * kSelectCap * 8);
-  s.rowpart = (float2*)p;
+  s.rowpart = (float2*)p; p += align256((size_t)R * W * kMaxRowSplits * sizeof(float2));
+  s.rowlse = (float*)p;
   return s;
 }
 
@@ -188,6 +191,14 @@ __device__ __forceinline__ int score_bin(float ref, float s) {
   return (int)u;
 }
 
+// Reference of the score bins: the request's rank-0 cumulative score, or in
+// Gumbel mode (kG) its ordering-key scale plus 16 (a Gumbel draw exceeds 16
+// with probability 1e-7; keys above the reference all land in bin 0).
+template <bool kG>
+__device__ __forceinline__ float bin_ref(const SelectArgs& a, float cum0) {
+  return kG ? __fadd_rn(__fmul_rn(cum0, a.inv_tau), 16.f) : cum0;
+}
+
 struct ExpandShared {
   uint32_t hist[2048];
   float red_m[32];
@@ -288,7 +299,8 @@ __device__ __forceinline__ float2 stream_max_sum(const float* row, int c0, int c
 // gh (the request's score-bin histogram in global memory; fused launches
 // only) counts every candidate the row adds to the pool.
 // kPf: the row's trie range and scores were fetched into sh.pf_* already.
-template <bool kPf>
+// kG: Gumbel top-k; candidates are ordered by fl32(fl32(s * inv_tau) + g).
+template <bool kPf, bool kG>
 __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
                                                  int r, int b, uint32_t* gh, uint32_t* kcache,
                                                  float lse) {
@@ -324,14 +336,20 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
     tb = a.lvl.token_base;
   }
   auto tok_of = [&](int i) -> int { return code ? tb + __ldg(code + i) : i; };
-  auto key_of = [&](int tok) -> uint32_t {
-    const float x = __ldg(row + tok);
-    return desc_key(__fadd_rn(cum, __fsub_rn(x, lse)));
+  // ordering key of token tok whose logit is x
+  auto score_key = [&](float x, int tok) -> uint32_t {
+    const float sc = __fadd_rn(cum, __fsub_rn(x, lse));
+    if constexpr (kG)
+      return desc_key(__fadd_rn(__fmul_rn(sc, a.inv_tau),
+                                gumbel_noise(a.seed_lo, a.seed_hi, r, a.step, b, tok)));
+    else
+      return desc_key(sc);
   };
+  auto key_of = [&](int tok) -> uint32_t { return score_key(__ldg(row + tok), tok); };
 
   SelState* st = ws.state + r;
   unsigned long long* pool = ws.pool + (size_t)r * a.W * Kp;
-  const float ref = kPf ? sh.pf_ref : a.cum_in[(size_t)r * a.W];   // bin reference: the rank-0 beam's score
+  const float ref = bin_ref<kG>(a, kPf ? sh.pf_ref : a.cum_in[(size_t)r * a.W]);
 
   // ---- a3: per-beam top_k -------------------------------------------------
   if (n <= a.K) {
@@ -367,7 +385,7 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int i = c0 + u * kExpandThreads + tid;
-        if (i < n) kcache[i] = desc_key(__fadd_rn(cum, __fsub_rn(x[u], lse)));
+        if (i < n) kcache[i] = score_key(x[u], tk[u]);
       }
     }
     __syncthreads();
@@ -447,6 +465,9 @@ __device__ void bitonic_sort(unsigned long long* keys, int np) {
 // (parent's row up to step-1, then step*W + j).
 // poff (optional): poff[j] = first edge of live beam j's trie node, gathered
 // earlier so the decode waits on one load instead of three.
+// kG: the pool keys hold the noisy ordering key, so the returned score is
+// recomputed from the parent's row: fl32(cum + fl32(logit - lse)).
+template <bool kG>
 __device__ void emit_outputs(const SelectArgs& a, const SelWs& ws, int r,
                              const unsigned long long* keys, int nt, const int* poff = nullptr) {
   const int tid = threadIdx.x;
@@ -462,7 +483,14 @@ __device__ void emit_outputs(const SelectArgs& a, const SelWs& ws, int r,
       }
       a.tokens[o + j] = tok;
       a.parents[o + j] = parent;
-      a.cum_out[o + j] = desc_key_value((uint32_t)(k >> 32));
+      if constexpr (kG) {
+        const size_t pr = o + parent;
+        const float lse = a.lse_in != nullptr ? a.lse_in[pr] : __ldcg(ws.rowlse + pr);
+        const float x = a.logits[pr * (size_t)a.row_stride + tok];
+        a.cum_out[o + j] = __fadd_rn(a.cum_in[pr], __fsub_rn(x, lse));
+      } else {
+        a.cum_out[o + j] = desc_key_value((uint32_t)(k >> 32));
+      }
       a.node_out[o + j] = node;
     } else {
       a.tokens[o + j] = -1;
@@ -603,6 +631,7 @@ __device__ void block_scan_bins(const uint32_t* gh, uint32_t* hs, uint32_t need,
 
 // Fused a4 for one request, run by the last expand block of the request:
 // select the min(W, pool) smallest pool keys, sort them, emit outputs.
+template <bool kG>
 __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs& ws, int r,
                              unsigned long long* keys) {
   const volatile SelState* st = ws.state + r;
@@ -610,7 +639,7 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
   const int nt = total < a.W ? total : a.W;
   const unsigned long long* pool = ws.pool + (size_t)r * a.W * a.Kp;
   if (total == 0) {
-    emit_outputs(a, ws, r, keys, 0);
+    emit_outputs<kG>(a, ws, r, keys, 0);
     return;
   }
   // the request's score-bin histogram (complete: every block added its
@@ -627,7 +656,7 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
   const int poffv = (pnode >= 0 && pnode < a.lvl.n_nodes) ? a.lvl.off[pnode] : 0;   // a bad node is never a parent
   const int Dbin = (int)sh.digit;
   const uint32_t c_le = sh.c_le;
-  const float ref = a.cum_in[(size_t)r * a.W];
+  const float ref = bin_ref<kG>(a, a.cum_in[(size_t)r * a.W]);
   constexpr int kPer = 4;   // rounds of kPer x blockDim keys: the loads of a round overlap
   if (c_le <= (uint32_t)(2 * kExpandThreads)) {
     // bucket sort: the candidates of bins <= Dbin go to their bin's slots
@@ -664,7 +693,7 @@ __device__ void request_tail(const SelectArgs& a, ExpandShared& sh, const SelWs&
       if (rank < (uint32_t)nt) sorted[rank] = k;
     }
     __syncthreads();
-    emit_outputs(a, ws, r, sorted, nt, use_poff ? reinterpret_cast<const int*>(sh.hist) : nullptr);
+    emit_outputs<kG>(a, ws, r, sorted, nt, use_poff ? reinterpret_cast<const int*>(sh.hist) : nullptr);
     return;
   }
   int nc = 0;
@@ -715,7 +744,7 @@ selected:
   __syncthreads();
   if (nc <= 2 * kExpandThreads) {   // small candidate sets: sort them all, keep the first nt
     block_sort_small(keys, nc);
-    emit_outputs(a, ws, r, keys, nt);
+    emit_outputs<kG>(a, ws, r, keys, nt);
     return;
   }
   if (nc > nt) {   // exact threshold: narrow until the keys at or below it number nt
@@ -747,7 +776,7 @@ selected:
   }
   if (nt <= 2 * kExpandThreads) {   // winners now in keys[0..nt)
     block_sort_small(keys, nt);
-    emit_outputs(a, ws, r, keys, nt);
+    emit_outputs<kG>(a, ws, r, keys, nt);
     return;
   }
   int np = 32;
@@ -755,7 +784,7 @@ selected:
   for (int i = nt + threadIdx.x; i < np; i += blockDim.x) keys[i] = ~0ull;
   __syncthreads();
   bitonic_sort(keys, np);
-  emit_outputs(a, ws, r, keys, nt);
+  emit_outputs<kG>(a, ws, r, keys, nt);
 }
 
 // a2-a5 for live beam b of request r once its log-sum-exp is known: the
@@ -763,13 +792,13 @@ selected:
 // request to finish (a per-request ticket) runs the request's global top-W.
 // Dynamic shared memory: the row's key cache (32 KB); the fused tail reuses it
 // for candidate keys after the ticket.
-template <bool kFused, bool kPf>
+template <bool kFused, bool kPf, bool kG>
 __device__ __forceinline__ void expand_and_select(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
                                                   int r, int b, int nl, float lse,
                                                   unsigned char* tail_smem) {
   const int tid = threadIdx.x;
   uint32_t* kcache = reinterpret_cast<uint32_t*>(tail_smem);
-  expand_candidates<kPf>(a, sh, ws, r, b, kFused ? ws.hist + (size_t)r * kBins : nullptr, kcache, lse);
+  expand_candidates<kPf, kG>(a, sh, ws, r, b, kFused ? ws.hist + (size_t)r * kBins : nullptr, kcache, lse);
   if constexpr (kFused) {
     __syncthreads();
     if (tid == 0) {
@@ -779,13 +808,13 @@ __device__ __forceinline__ void expand_and_select(const SelectArgs& a, ExpandSha
     __syncthreads();
     if (sh.count != nl - 1) return;
     __threadfence();
-    request_tail(a, sh, ws, r, reinterpret_cast<unsigned long long*>(tail_smem));
+    request_tail<kG>(a, sh, ws, r, reinterpret_cast<unsigned long long*>(tail_smem));
   }
 }
 
 // a2-a5 when the caller supplies the row normalisers (lse_in): one block per
 // live beam.
-template <bool kFused>
+template <bool kFused, bool kG>
 __global__ void __launch_bounds__(kExpandThreads)
 bd_expand_kernel(SelectArgs a) {
   __shared__ ExpandShared sh;
@@ -796,7 +825,7 @@ bd_expand_kernel(SelectArgs a) {
   const int nl = a.n_live_in[r];
   if (b >= nl) return;
   const float lse = a.lse_in[(size_t)r * a.W + b];
-  expand_and_select<kFused, false>(a, sh, ws, r, b, nl, lse, tail_smem);
+  expand_and_select<kFused, false, kG>(a, sh, ws, r, b, nl, lse, tail_smem);
 }
 
 // The whole selection step in one launch: S blocks per live logits row each
@@ -806,7 +835,7 @@ bd_expand_kernel(SelectArgs a) {
 // row of each request selects the request's top-W (a4, a5).  The stream
 // part holds nothing else, so the kernel fits 32 registers and four
 // 512-thread blocks per SM keep enough loads in flight.
-template <bool kFused>
+template <bool kFused, bool kG>
 __global__ void __launch_bounds__(kExpandThreads, 4)
 bd_stream_select_kernel(SelectArgs a) {
   __shared__ ExpandShared sh;
@@ -864,7 +893,8 @@ bd_stream_select_kernel(SelectArgs a) {
     lse = sh.lse;
   }
   if (tid == 0 && a.lse_out != nullptr) a.lse_out[rowi] = lse;
-  expand_and_select<kFused, true>(a, sh, ws, r, b, nl, lse, tail_smem);
+  if (kG && tid == 0) ws.rowlse[rowi] = lse;   // read by the outputs' score recomputation
+  expand_and_select<kFused, true, kG>(a, sh, ws, r, b, nl, lse, tail_smem);
 }
 
 // ---------------------------------------------------------------------------
@@ -1005,7 +1035,8 @@ bd_global_kernel(SelectArgs a) {
     for (int i = tid; i < np; i += kGlobalThreads) keys[i] = i < nc ? __ldcg(cand + i) : ~0ull;
     __syncthreads();
     bitonic_sort(keys, np);
-    emit_outputs(a, ws, r, keys, nt);
+    if (a.inv_tau > 0.f) emit_outputs<true>(a, ws, r, keys, nt);
+    else emit_outputs<false>(a, ws, r, keys, nt);
     __syncthreads();
   }
 }
@@ -1023,7 +1054,7 @@ size_t select_workspace_bytes(int R, int W, int K, int V) {
          align256((size_t)R * W * sizeof(int32_t)) +
          align256((size_t)R * kBins * sizeof(uint32_t)) + align256((size_t)R * W * Kp * 8) +
          align256((size_t)R * kSelectCap * 8) +
-         (size_t)R * W * kMaxRowSplits * sizeof(float2);
+         align256((size_t)R * W * kMaxRowSplits * sizeof(float2)) + (size_t)R * W * sizeof(float);
 }
 
 int launch_select(const SelectArgs& a, cudaStream_t stream) {
@@ -1062,17 +1093,28 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
   const bool fused = a.W <= kTailCap && (long long)a.W * a.Kp <= (1ll << 20);
   static_assert(kKeyCache * 4 <= kTailCap * 8, "fused dynamic shared memory");
   const size_t dsm = fused ? kTailCap * sizeof(unsigned long long) : kKeyCache * sizeof(uint32_t);
+  const bool gumbel = a.inv_tau > 0.f;
   if (a.lse_in == nullptr) {
     dim3 g0(a.W * S, a.R);
     prof_begin(kKStream, stream);
-    if (fused) bd_stream_select_kernel<true><<<g0, kExpandThreads, dsm, stream>>>(a2);
-    else bd_stream_select_kernel<false><<<g0, kExpandThreads, dsm, stream>>>(a2);
+    if (gumbel) {
+      if (fused) bd_stream_select_kernel<true, true><<<g0, kExpandThreads, dsm, stream>>>(a2);
+      else bd_stream_select_kernel<false, true><<<g0, kExpandThreads, dsm, stream>>>(a2);
+    } else {
+      if (fused) bd_stream_select_kernel<true, false><<<g0, kExpandThreads, dsm, stream>>>(a2);
+      else bd_stream_select_kernel<false, false><<<g0, kExpandThreads, dsm, stream>>>(a2);
+    }
     prof_end(kKStream, stream);
   } else {
     dim3 g1(a.W, a.R);
     prof_begin(kKExpand, stream);
-    if (fused) bd_expand_kernel<true><<<g1, kExpandThreads, dsm, stream>>>(a2);
-    else bd_expand_kernel<false><<<g1, kExpandThreads, dsm, stream>>>(a2);
+    if (gumbel) {
+      if (fused) bd_expand_kernel<true, true><<<g1, kExpandThreads, dsm, stream>>>(a2);
+      else bd_expand_kernel<false, true><<<g1, kExpandThreads, dsm, stream>>>(a2);
+    } else {
+      if (fused) bd_expand_kernel<true, false><<<g1, kExpandThreads, dsm, stream>>>(a2);
+      else bd_expand_kernel<false, false><<<g1, kExpandThreads, dsm, stream>>>(a2);
+    }
     prof_end(kKExpand, stream);
   }
   if (cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
