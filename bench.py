@@ -328,6 +328,8 @@ def gpu_arm(args, ws, rank, local):
     # end-to-end through the C ABI from pinned host buffers
     e2e = None if args.no_e2e else e2e_arm(step, args, ws, flush)
     chain = None if args.no_chain else chain_arm(step, args, flush)
+    gumbel = None if args.no_chain else gumbel_arm(step, args, flush)
+    lmhead = None if args.no_chain else lmhead_arm(step, args, flush)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "beam-rows/s", "n_gpus": ws,
@@ -342,7 +344,8 @@ def gpu_arm(args, ws, rank, local):
         "roofline": roof, "kernels": kernels,
         "kernels_note": "per-kernel event times from a pass of the same steps just before the timed "
                         "region; inside it only the roofline kernel is bracketed by events",
-        "gpu_launches": launches, "clocks": clk, "e2e": e2e, "chain_graph": chain,
+        "gpu_launches": launches, "clocks": clk, "e2e": e2e, "chain_graph": chain, "gumbel_select": gumbel,
+        "lmhead_select": lmhead,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows or 4 * wl.W)
@@ -389,6 +392,93 @@ def e2e_arm(step, args, ws, flush):
     rows = step.rows()
     return {"value": round(rows * ws / (ms / 1e3), 1), "unit": "beam-rows/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 3)}
+
+
+def lmhead_arm(step, args, flush, H=2048):
+    """The step before the selection folded in: synthetic hidden states [R*W,
+    H] and LM head [V, H] (bf16, H = 2048 as in Qwen3-1.7B).  fused: the head
+    GEMM reduces each row to its log-sum-exp and writes only the SID level's
+    8192 logits, then the selection runs with lse_in.  materialised: the same
+    GEMM writes all V logits and the selection streams them (the path of the
+    main measurement)."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl, s, dev = step.wl, step.state, step.dev
+    rows, V = wl.R * wl.W, wl.V
+    g = torch.Generator(device=dev).manual_seed(3)
+    h = torch.randn(rows, H, generator=g, device=dev).to(torch.bfloat16)
+    w = (torch.randn(V, H, generator=g, device=dev) * (2.0 / H ** 0.5)).to(torch.bfloat16)
+    lse = torch.empty(rows, dtype=torch.float32, device=dev)
+    logits = torch.empty((rows, V), dtype=torch.float32, device=dev)
+    ws = bd.workspace(bd.beam_lmhead_workspace_size(rows, V), dev)
+    tb = int(wl.token_base()[step.step]) if wl.levels else 0
+    win = wl.C if wl.levels else V
+    stream = torch.cuda.current_stream()
+
+    def fused():
+        bd.beam_lmhead_lse(h, w, tb, win, lse_out=lse, logits_out=logits, ws=ws)
+        bd.beam_select(logits.view(wl.R, wl.W, V), s["cum"], s["node"], s["n_live"], s["slot"], step.trie,
+                       step.step, step.step, wl.K, lse_in=lse.view(wl.R, wl.W), out=step.out_sel, ws=step.ws_sel)
+
+    def materialised():
+        bd.beam_lmhead_lse(h, w, 0, V, lse_out=lse, logits_out=logits, ws=ws)
+        bd.beam_select(logits.view(wl.R, wl.W, V), s["cum"], s["node"], s["n_live"], s["slot"], step.trie,
+                       step.step, step.step, wl.K, out=step.out_sel, ws=step.ws_sel)
+
+    def head_only():
+        bd.beam_lmhead_lse(h, w, tb, win, lse_out=lse, logits_out=logits, ws=ws)
+
+    res = {"hidden": H, "rows": rows, "vocab": V}
+    for name, fn in (("fused_us", fused), ("materialised_us", materialised), ("head_gemm_us", head_only)):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        n = max(1, min(args.steps, 10))
+        times = []
+        for _ in range(n):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        res[name] = round(sum(times) / n * 1e3, 1)
+    res["head_tflops"] = round(2.0 * rows * H * V / (res["head_gemm_us"] * 1e-6) / 1e12, 1)
+    assert bd.read_status(step.ws_sel) == 0 and bd.read_status(ws) == 0
+    del h, w, logits, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def gumbel_arm(step, args, flush):
+    """The benchmarked step's selection with temperature 1 (Gumbel top-k),
+    beside the deterministic one, on the same resident inputs."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl, s = step.wl, step.state
+    stream = torch.cuda.current_stream()
+
+    def sel(temp):
+        return bd.beam_select(step.logits, s["cum"], s["node"], s["n_live"], s["slot"], step.trie, step.step,
+                              step.step, wl.K, out=step.out_sel, ws=step.ws_sel, temperature=temp, seed=12345)
+
+    res = {}
+    for name, temp in (("deterministic", 0.0), ("temperature_1", 1.0)):
+        for _ in range(3):
+            flush.zero_()
+            sel(temp)
+        n = max(1, min(args.steps, 10))
+        times = []
+        for _ in range(n):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            sel(temp)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        res[name + "_us"] = round(sum(times) / n * 1e3, 1)
+    assert bd.read_status(step.ws_sel) == 0
+    return res
 
 
 def chain_arm(step, args, flush):

@@ -83,6 +83,34 @@ const char* beamdec_version(void);
 int beamdec_read_status(void* workspace, void* stream, int32_t* host_status);
 
 /*
+ * The step before the selection, with the selection's normaliser fused in:
+ * logits = hidden x weight^T over the whole vocabulary (bf16 in, fp32
+ * accumulate), reduced inside the GEMM to each row's log-sum-exp, while only
+ * the token columns [window_start, window_start + window_len) - the current
+ * SID level's code range - are written out.  "Generative recommendation
+ * design" (xLLM) §4.3 filters invalid items before they become candidates:
+ * the full [rows, V] logits never reach HBM, and beam_select then runs with
+ * lse_in = lse_out on the window (it reads only the trie children's logits
+ * when lse_in is given).
+ *   hidden      [rows][hidden_dim] bf16, row-major, 16-byte aligned
+ *   weight      [V][hidden_dim] bf16 (the LM head, one row per token)
+ *   hidden_dim  multiple of 64
+ *   lse_out     [rows] fp32, ln sum_v exp(logit[row, v])
+ *   logits_out  fp32 rows of logits_row_stride floats; only the window's
+ *               columns are written (pass stride >= V and the same pointer to
+ *               beam_select).  May be NULL when window_len is 0.
+ * The workspace (beam_lmhead_workspace_size bytes, 256-byte aligned) holds
+ * per-tile partials; it needs no clearing.
+ * Errors: INVALID_ARG, UNSUPPORTED (hidden_dim not a multiple of 64, V above
+ * BEAMDEC_MAX_VOCAB), WORKSPACE, CUDA.
+ */
+int beam_lmhead_workspace_size(int rows, int V, size_t* bytes);
+int beam_lmhead_lse(const void* hidden, const void* weight, int rows, int hidden_dim, int V,
+                    int window_start, int window_len, float* lse_out, float* logits_out,
+                    int64_t logits_row_stride, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/*
  * Per-kernel timing for benchmarks.  beamdec_profile_enable(1) clears the
  * record and brackets every following kernel launch with a CUDA event pair
  * on its stream (at most 8192 launches are kept); beamdec_profile_enable(0)
@@ -91,7 +119,7 @@ int beamdec_read_status(void* workspace, void* stream, int32_t* host_status);
  * 0 bd_expand_kernel (selection when lse_in is given), 1 bd_global_kernel,
  * 2 bd_attn_shared_simt_kernel, 3 bd_attn_shared_tc_kernel, 4 bd_attn_merge_kernel,
  * 5 bd_kv_e4m3_to_bf16_kernel, 6 bd_stream_select_kernel (the whole selection
- * step otherwise).  Host-side state is process-wide; use from one host thread.
+ * step otherwise), 7 bd_lmhead_kernel, 8 bd_lmhead_lse_kernel.  Host-side state is process-wide; use from one host thread.
  */
 int beamdec_profile_enable(int on);
 /* The same with a choice of kernels: bit k of kernel_mask brackets kernel id

@@ -47,6 +47,9 @@ _SIGS = {
     "beam_select_gumbel": (c_int, [c_p, c_i64, c_p, c_p, c_p, c_p, c_p, c_p, c_int, c_int,
                                    c_int, c_int, c_int, c_int, c_int, c_f, ctypes.c_uint64,
                                    c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]),
+    "beam_lmhead_workspace_size": (c_int, [c_int, c_int, ctypes.POINTER(c_sz)]),
+    "beam_lmhead_lse": (c_int, [c_p, c_p, c_int, c_int, c_int, c_int, c_int, c_p, c_p, c_i64, c_p, c_sz,
+                                c_p]),
     "beam_select_static": (c_int, [c_p, c_i64, c_p, c_p, c_p, c_p, c_p, c_p, c_int, c_int,
                                    c_int, c_int, c_int, c_int, c_int,
                                    c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p]),
@@ -183,7 +186,7 @@ def beam_attn_workspace_size(R, W, Hq, Hkv, d, max_prompt_len, kv_dtype):
 
 KERNELS = ["bd_expand_kernel", "bd_global_kernel", "bd_attn_shared_simt_kernel",
            "bd_attn_shared_tc_kernel", "bd_attn_merge_kernel", "bd_kv_e4m3_to_bf16_kernel",
-           "bd_stream_select_kernel"]
+           "bd_stream_select_kernel", "bd_lmhead_kernel", "bd_lmhead_lse_kernel"]
 
 
 def profile_enable(on=True, kernels=None):
@@ -383,3 +386,33 @@ class DecodeChain:
     def status(self):
         """Device-side status words of the selection and attention workspaces."""
         return read_status(self._ws_sel), read_status(self._ws_att)
+
+
+def beam_lmhead_workspace_size(rows, V):
+    n = c_sz()
+    _check(lib().beam_lmhead_workspace_size(rows, V, ctypes.byref(n)), "beam_lmhead_workspace_size")
+    return n.value
+
+
+def beam_lmhead_lse(hidden, weight, window_start=0, window_len=0, lse_out=None, logits_out=None, ws=None,
+                    stream=None):
+    """LM head with the log-sum-exp fused in: hidden [rows, H] bf16, weight
+    [V, H] bf16.  Returns (lse [rows] fp32, logits [rows, V] fp32 of which
+    only the window's columns are written, or None without a window)."""
+    _need_cuda(hidden, weight)
+    rows, H = hidden.shape
+    V = weight.shape[0]
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16 or weight.shape[1] != H:
+        raise ValueError("hidden [rows, H] and weight [V, H] must be bf16")
+    dev = hidden.device
+    if lse_out is None:
+        lse_out = torch.empty(rows, dtype=torch.float32, device=dev)
+    if window_len and logits_out is None:
+        logits_out = torch.empty((rows, V), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(beam_lmhead_workspace_size(rows, V), dev)
+    stride = logits_out.stride(0) if logits_out is not None else 0
+    rc = lib().beam_lmhead_lse(_ptr(hidden), _ptr(weight), rows, H, V, window_start, window_len, _ptr(lse_out),
+                               _ptr(logits_out), stride, _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "beam_lmhead_lse")
+    return lse_out, logits_out

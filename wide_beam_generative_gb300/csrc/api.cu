@@ -269,3 +269,32 @@ extern "C" int beam_attn_decode(const void* q, const void* shared_k, const void*
   if (rc != BEAMDEC_OK) return rc;
   return launch_attn_merge(a, p, st);
 }
+
+// ---- LM head with fused log-sum-exp ---------------------------------------------
+
+extern "C" int beam_lmhead_workspace_size(int rows, int V, size_t* bytes) {
+  if (bytes == nullptr || rows < 1 || V < 1) return BEAMDEC_ERR_INVALID_ARG;
+  *bytes = bd::lmhead_workspace_bytes(rows, V);
+  return BEAMDEC_OK;
+}
+
+extern "C" int beam_lmhead_lse(const void* hidden, const void* weight, int rows, int hidden_dim,
+                               int V, int window_start, int window_len, float* lse_out,
+                               float* logits_out, int64_t logits_row_stride, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (hidden == nullptr || weight == nullptr || lse_out == nullptr || workspace == nullptr)
+    return BEAMDEC_ERR_INVALID_ARG;
+  if (rows < 1 || V < 1 || hidden_dim < 64 || window_start < 0 || window_len < 0 ||
+      (int64_t)window_start + window_len > V)
+    return BEAMDEC_ERR_INVALID_ARG;
+  if (hidden_dim % 64 != 0 || V > BEAMDEC_MAX_VOCAB || hidden_dim > 65536) return BEAMDEC_ERR_UNSUPPORTED;
+  if (window_len > 0 && (logits_out == nullptr || logits_row_stride < (int64_t)window_start + window_len))
+    return BEAMDEC_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(hidden) & 15u) || (reinterpret_cast<uintptr_t>(weight) & 15u) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return BEAMDEC_ERR_INVALID_ARG;
+  if (workspace_bytes < bd::lmhead_workspace_bytes(rows, V)) return BEAMDEC_ERR_WORKSPACE;
+  return bd::launch_lmhead(hidden, weight, rows, hidden_dim, V, window_start,
+                           window_start + window_len, lse_out, window_len > 0 ? logits_out : nullptr,
+                           logits_row_stride, workspace, static_cast<cudaStream_t>(stream));
+}

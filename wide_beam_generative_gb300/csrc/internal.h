@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libbeamdec.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -78,6 +79,16 @@ size_t attn_workspace_bytes(int R, int W, int Hq, int Hkv, int d, const AttnPlan
 int launch_attn_shared_simt(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 bool attn_tc_supported(int q_dtype, int kv_dtype, int d, int G);
+
+// ---- LM head (lmhead.cu) ------------------------------------------------------
+size_t lmhead_workspace_bytes(int rows, int V);
+int launch_lmhead(const void* hidden, const void* weight, int rows, int hidden_dim, int V,
+                  int win0, int win1, float* lse_out, float* logits_out, int64_t out_stride,
+                  void* ws, cudaStream_t stream);
+
+// 128-byte-swizzled tiled TMA tensor map (tmap.cu); false if encoding fails.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
+              const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box);
 int launch_attn_merge(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 
 // Partial-triple layout in the attention workspace (after the 256-byte header):
@@ -94,7 +105,7 @@ int sm_count();
 
 // ---- per-kernel event timing (off unless beamdec_profile_enable(1)) ---------
 enum KernelId { kKExpand = 0, kKGlobal = 1, kKAttnSimt = 2, kKAttnTc = 3, kKAttnMerge = 4,
-                kKKvConvert = 5, kKStream = 6, kKCount = 7 };
+                kKKvConvert = 5, kKStream = 6, kKLmhead = 7, kKLmheadLse = 8, kKCount = 9 };
 void prof_begin(int kid, cudaStream_t s);
 void prof_end(int kid, cudaStream_t s);
 
