@@ -56,7 +56,10 @@ def _peak_value(d, *names):
 
 
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
+    """nvidia-smi clock and throttle-reason samples (every 20 ms) taken from
+    just before the per-kernel breakdown pass until 0.25 s after the timed
+    region: the timed steps alone last only milliseconds, shorter than the
+    sampler's start-up, so the samples bracket them under the same load."""
 
     FIELDS = "index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active," \
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown," \
@@ -65,23 +68,41 @@ class Clocks:
     def __init__(self, index):
         self.index = index
         self.p = None
+        self.lines = []
+        self.t = None
+
+    def _pump(self):
+        for line in self.p.stdout:
+            self.lines.append(line)
 
     def start(self):
+        import threading
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                       "-i", str(self.index), "-lms", "200"],
+                                       "-i", str(self.index), "-lms", "20"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.p = None
+            return
+        self.t = threading.Thread(target=self._pump, daemon=True)
+        self.t.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5.0:   # the sampler is running once it has printed
+            time.sleep(0.01)
 
     def stop(self):
         if self.p is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
         self.p.terminate()
-        out, _ = self.p.communicate(timeout=10)
+        try:
+            self.p.wait(timeout=10)
+        except Exception:
+            self.p.kill()
+        self.t.join(timeout=5)
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for line in self.lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -94,7 +115,8 @@ class Clocks:
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window": "every 20 ms from the breakdown pass to 0.25 s after the timed steps"}
 
 
 def dist_setup():
@@ -259,6 +281,8 @@ def gpu_arm(args, ws, rank, local):
         step.run()
     torch.cuda.synchronize()
     assert bd.read_status(step.ws_sel) == 0 and bd.read_status(step.ws_att) == 0
+    clocks = Clocks(local)
+    clocks.start()
     # per-kernel breakdown: one pass of the same steps with every kernel
     # bracketed by events (outside the timed region, whose value those
     # events would slow down)
@@ -273,12 +297,10 @@ def gpu_arm(args, ws, rank, local):
         raise SystemExit("no kernel launches were recorded")
     dom_name = max(breakdown.items(), key=lambda kv: kv[1][0])[0]
 
-    clocks = Clocks(local)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     barrier(ws)
     torch.cuda.synchronize()
-    clocks.start()
     bd.profile_enable(True, kernels=[dom_name])   # the roofline kernel, timed live
     for i in range(args.steps):
         flush.zero_()

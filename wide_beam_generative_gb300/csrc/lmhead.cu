@@ -134,11 +134,15 @@ bd_lmhead_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant
     const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
     bool ok = warp_wait_lm(&bars.done, 0);
     if (!ok) abort_sh = 1;
+    // the window's columns leave through shared memory (the K ring is idle
+    // once every MMA is done): each thread stages its row, 16-byte chunks
+    // swizzled by the row, then each warp stores whole row segments, coalesced
+    const bool has_win = p.out != nullptr && col0 < p.win1 && col0 + kBN > p.win0;
+    float* stage = reinterpret_cast<float*>(sm);   // [128 rows][256 cols]
     if (ok) {
       fence_after_sync();
       float m = -INFINITY, l = 0.f;
-      const bool live = row < p.rows;
-      float* orow = (live && p.out != nullptr) ? p.out + (int64_t)row * p.out_stride : nullptr;
+      const int srow = q * 32 + lane;
 #pragma unroll 1
       for (int c = 0; c < kBN / 64; ++c) {
         float v[64];
@@ -156,15 +160,32 @@ bd_lmhead_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant
           if (cb + j < p.V) acc += ex2(fmaf(v[j], kLog2e, -mn));
         l = (l > 0.f ? l * ex2(m - mn) : 0.f) + acc;
         m = mn;
-        if (orow != nullptr && cb < p.win1 && cb + 64 > p.win0) {
+        if (has_win) {
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const int col = cb + j;
-            if (col >= p.win0 && col < p.win1 && col < p.V) orow[col] = v[j];
+          for (int j4 = 0; j4 < 16; ++j4) {
+            const int slot = c * 16 + (j4 ^ (srow & 15));
+            reinterpret_cast<float4*>(stage + srow * kBN)[slot] =
+                make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
           }
         }
       }
-      if (live) p.part[(int64_t)row * p.n_tiles + blockIdx.y] = make_float2(m, l);
+      if (row < p.rows) p.part[(int64_t)row * p.n_tiles + blockIdx.y] = make_float2(m, l);
+    }
+    if (has_win) {
+      named_bar(1, 128);   // the four epilogue warps; every one arrives, ok or not
+      if (ok) {
+        const int c_lo = max(p.win0, col0), c_hi = min(min(p.win1, p.V), col0 + kBN);
+        for (int rr = q * 32; rr < q * 32 + 32; ++rr) {
+          const int grow = row0 + rr;
+          if (grow >= p.rows) break;
+          float* orow = p.out + (int64_t)grow * p.out_stride;
+          for (int cc = c_lo + lane; cc < c_hi; cc += 32) {
+            const int j = cc - col0;   // column inside the tile
+            const int slot = (j >> 6) * 16 + (((j & 63) >> 2) ^ (rr & 15));
+            orow[cc] = stage[rr * kBN + slot * 4 + (j & 3)];
+          }
+        }
+      }
     }
   }
   fence_before_sync();
