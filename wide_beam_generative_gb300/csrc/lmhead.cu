@@ -8,17 +8,23 @@
 // [rows, V] logits never reach HBM.  The selection then runs on that window
 // with the row normalisers passed in (beam_select with lse_in).
 //
-// One CTA computes a 128-row x 256-column tile over the hidden dimension:
+// A persistent grid (one CTA per SM) walks the 128-row x 256-column output
+// tiles, row tiles fastest so that the CTAs running together share one slab
+// of W in L2:
 //   warp 0       TMA producer: 64-wide K slabs of hidden (128 x 64) and W
-//                (256 x 64), SWIZZLE_128B, through a 4-stage ring;
-//   warp 1       allocates 256 TMEM columns and issues the kind::f16 MMAs
-//                (M 128, N 256, K 16; bf16 in, fp32 accumulate);
-//   warps 2-5    epilogue, one row per thread (TMEM lane): the tile's
-//                (max, sum of exp) in log2 units per row, and the window
-//                columns of the tile stored as fp32.
+//                (256 x 64), SWIZZLE_128B, through a 4-stage ring that runs
+//                on across tiles;
+//   warp 1       allocates 512 TMEM columns (two 256-column accumulators)
+//                and issues the kind::f16 MMAs (M 128, N 256, K 16; bf16 in,
+//                fp32 accumulate) of tile i into accumulator i % 2;
+//   warps 2-5    epilogue, one row per thread (TMEM lane), on the other
+//                accumulator meanwhile: the tile's (max, sum of exp) in log2
+//                units per row, and the window columns stored through a
+//                shared-memory staging chunk in coalesced row segments.
 // A second kernel folds each row's per-tile partials into its log-sum-exp.
-// Every mbarrier wait is bounded; a timeout records BEAMDEC_ERR_TIMEOUT, lets
-// the copies in flight land and still frees TMEM.
+// Every mbarrier wait is bounded; a timeout records BEAMDEC_ERR_TIMEOUT, the
+// other roles stop at their next wait, the copies in flight land and TMEM
+// is still freed.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -38,10 +44,11 @@ constexpr int kStages = 4;
 constexpr uint32_t kABytes = kBM * kBK * 2;              // 16 KB
 constexpr uint32_t kBBytes = kBN * kBK * 2;              // 32 KB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kLmSmem = kStages * kStageBytes + 1024;
+constexpr uint32_t kOutChunkBytes = kBM * 64 * 4;        // 32 KB: 64 fp32 columns of 128 rows
+constexpr uint32_t kLmSmem = kStages * kStageBytes + kOutChunkBytes + 1024;
 
 struct LmParams {
-  int rows, hidden, V, n_tiles, win0, win1;
+  int rows, hidden, V, n_tiles, m_tiles, win0, win1;
   int64_t out_stride;
   float* out;        // window logits (may be null when the window is empty)
   float2* part;      // [rows][n_tiles] (max, sum of 2^(x - max)), log2 units
@@ -50,8 +57,12 @@ struct LmParams {
 
 struct LmBars {
   uint64_t full[kStages], empty[kStages];
-  uint64_t done;
+  uint64_t acc_full[2], acc_empty[2];
 };
+
+__device__ __forceinline__ bool warp_flag(volatile int* f) {
+  return __shfl_sync(0xffffffffu, *f, 0) != 0;
+}
 
 __device__ __forceinline__ bool warp_wait_lm(uint64_t* bar, uint32_t parity) {
   bool ok = false;
@@ -71,8 +82,8 @@ bd_lmhead_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row0 = blockIdx.x * kBM, col0 = blockIdx.y * kBN;
   const int nk = p.hidden / kBK;
+  const int total = p.m_tiles * p.n_tiles;
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
@@ -80,10 +91,13 @@ bd_lmhead_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant
       mbar_init(&bars.full[s], 1);
       mbar_init(&bars.empty[s], 1);
     }
-    mbar_init(&bars.done, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bars.acc_full[a], 1);
+      mbar_init(&bars.acc_empty[a], 128);
+    }
     mbar_fence_init();
   }
-  if (warp == 1) tmem_alloc(&tmem_base_sh, kBN);
+  if (warp == 1) tmem_alloc(&tmem_base_sh, 2 * kBN);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
@@ -93,99 +107,120 @@ bd_lmhead_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant
     // ------------------------------------------------------------ TMA producer
     prefetch_tmap(&amap);
     prefetch_tmap(&bmap);
-    int issued = 0;
-    for (int k = 0; k < nk; ++k) {
-      const int s = k % kStages;
-      if (!mbar_wait(&bars.empty[s], ((uint32_t)(k / kStages) & 1u) ^ 1u)) { abort_sh = 1; break; }
-      unsigned char* a_dst = sm + s * kStageBytes;
-      mbar_expect_tx(&bars.full[s], kStageBytes);
-      tma_load_2d(a_dst, &amap, &bars.full[s], k * kBK, row0);
-      tma_load_2d(a_dst + kABytes, &bmap, &bars.full[s], k * kBK, col0);
-      issued = k + 1;
-      if (abort_sh) break;
+    uint32_t g = 0, issued = 0;
+    for (int t = blockIdx.x; t < total && !abort_sh; t += gridDim.x) {
+      const int row0 = (t % p.m_tiles) * kBM, col0 = (t / p.m_tiles) * kBN;
+      for (int k = 0; k < nk; ++k, ++g) {
+        const int s = (int)(g % kStages);
+        if (!mbar_wait(&bars.empty[s], ((g / kStages) & 1u) ^ 1u)) { abort_sh = 1; break; }
+        unsigned char* dst = sm + s * kStageBytes;
+        mbar_expect_tx(&bars.full[s], kStageBytes);
+        tma_load_2d(dst, &amap, &bars.full[s], k * kBK, row0);
+        tma_load_2d(dst + kABytes, &bmap, &bars.full[s], k * kBK, col0);
+        issued = g + 1;
+      }
     }
     if (abort_sh) {   // let every copy this thread started land before exiting
-      for (int k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
-        mbar_wait(&bars.full[k % kStages], (uint32_t)(k / kStages) & 1u);
+      for (uint32_t i = (issued > (uint32_t)kStages ? issued - kStages : 0); i < issued; ++i)
+        mbar_wait(&bars.full[i % kStages], (i / kStages) & 1u);
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = idesc_bf16_f32(kBM, kBN, false, false);
     const uint32_t base = smem_u32(sm);
+    uint32_t g = 0;
+    int i = 0;
     bool ok = true;
-    for (int k = 0; k < nk; ++k) {
-      const int s = k % kStages;
-      if (!mbar_wait(&bars.full[s], (uint32_t)(k / kStages) & 1u)) { ok = false; break; }
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++i) {
+      const int acc = i & 1;
+      if (!mbar_wait(&bars.acc_empty[acc], ((uint32_t)(i >> 1) & 1u) ^ 1u)) { ok = false; break; }
       fence_after_sync();
-      const uint32_t a0 = base + s * kStageBytes, b0 = a0 + kABytes;
+      const uint32_t d = tmem + acc * kBN;
+      for (int k = 0; k < nk; ++k, ++g) {
+        const int s = (int)(g % kStages);
+        if (!mbar_wait(&bars.full[s], (g / kStages) & 1u)) { ok = false; break; }
+        fence_after_sync();
+        const uint32_t a0 = base + s * kStageBytes, b0 = a0 + kABytes;
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk)
-        mma_bf16(tmem, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024), idesc,
-                 (k > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(&bars.empty[s]);   // the slot is free once these MMAs have read it
-      if (abort_sh) { ok = false; break; }
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          mma_bf16(d, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024), idesc,
+                   (k > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.empty[s]);   // the slot is free once these MMAs have read it
+      }
+      if (!ok) break;
+      mma_commit(&bars.acc_full[acc]);
+      if (abort_sh) ok = false;
     }
-    if (ok) mma_commit(&bars.done);
-    else abort_sh = 1;
+    if (!ok) abort_sh = 1;
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // TMEM lane group of this warp
-    const int row = row0 + q * 32 + lane;
-    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-    bool ok = warp_wait_lm(&bars.done, 0);
-    if (!ok) abort_sh = 1;
-    // the window's columns leave through shared memory (the K ring is idle
-    // once every MMA is done): each thread stages its row, 16-byte chunks
-    // swizzled by the row, then each warp stores whole row segments, coalesced
-    const bool has_win = p.out != nullptr && col0 < p.win1 && col0 + kBN > p.win0;
-    float* stage = reinterpret_cast<float*>(sm);   // [128 rows][256 cols]
-    if (ok) {
-      fence_after_sync();
+    const int srow = q * 32 + lane;               // row inside the tile
+    float* stage = reinterpret_cast<float*>(sm + kStages * kStageBytes);   // [128][64]
+    int i = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+      const int acc = i & 1;
+      const int row0 = (t % p.m_tiles) * kBM, col0 = (t / p.m_tiles) * kBN;
+      const int row = row0 + srow;
+      // every epilogue warp runs the same barrier sequence; a timeout only
+      // skips the work
+      bool ok = !warp_flag(&abort_sh) && warp_wait_lm(&bars.acc_full[acc], (uint32_t)(i >> 1) & 1u);
+      if (!ok) abort_sh = 1;
+      if (ok) fence_after_sync();
+      const uint32_t taddr = tmem + acc * kBN + ((uint32_t)(q * 32) << 16);
+      const bool win_tile = p.out != nullptr && col0 < p.win1 && col0 + kBN > p.win0;
       float m = -INFINITY, l = 0.f;
-      const int srow = q * 32 + lane;
 #pragma unroll 1
       for (int c = 0; c < kBN / 64; ++c) {
-        float v[64];
-        tmem_ld64(taddr + c * 64, v);
         const int cb = col0 + c * 64;
-        float mc = -INFINITY;
+        float v[64];
+        if (ok) {
+          tmem_ld64(taddr + c * 64, v);
+          float mc = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
-          if (cb + j < p.V) mc = fmaxf(mc, v[j]);
-        mc *= kLog2e;
-        const float mn = fmaxf(m, mc);
-        float acc = 0.f;
+          for (int j = 0; j < 64; ++j)
+            if (cb + j < p.V) mc = fmaxf(mc, v[j]);
+          mc *= kLog2e;
+          const float mn = fmaxf(m, mc);
+          float sum = 0.f;
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
-          if (cb + j < p.V) acc += ex2(fmaf(v[j], kLog2e, -mn));
-        l = (l > 0.f ? l * ex2(m - mn) : 0.f) + acc;
-        m = mn;
-        if (has_win) {
+          for (int j = 0; j < 64; ++j)
+            if (cb + j < p.V) sum += ex2(fmaf(v[j], kLog2e, -mn));
+          l = (l > 0.f ? l * ex2(m - mn) : 0.f) + sum;
+          m = mn;
+        }
+        if (win_tile && cb < p.win1 && cb + 64 > p.win0) {   // uniform over the epilogue warps
+          if (ok) {
 #pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4) {
-            const int slot = c * 16 + (j4 ^ (srow & 15));
-            reinterpret_cast<float4*>(stage + srow * kBN)[slot] =
-                make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+            for (int j4 = 0; j4 < 16; ++j4)
+              reinterpret_cast<float4*>(stage + srow * 64)[j4 ^ (srow & 15)] =
+                  make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
           }
+          named_bar(1, 128);
+          if (ok) {
+            const int c_lo = max(p.win0, cb), c_hi = min(min(p.win1, p.V), cb + 64);
+            for (int rr = q * 32; rr < q * 32 + 32; ++rr) {
+              const int grow = row0 + rr;
+              if (grow >= p.rows) break;
+              const int cc = c_lo + lane;   // 64 columns: two per lane
+              float* orow = p.out + (int64_t)grow * p.out_stride;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int col = cc + 32 * h;
+                if (col < c_hi) {
+                  const int j = col - cb;
+                  orow[col] = stage[rr * 64 + (((j >> 2) ^ (rr & 15)) << 2) + (j & 3)];
+                }
+              }
+            }
+          }
+          named_bar(1, 128);   // the chunk buffer is free again
         }
       }
-      if (row < p.rows) p.part[(int64_t)row * p.n_tiles + blockIdx.y] = make_float2(m, l);
-    }
-    if (has_win) {
-      named_bar(1, 128);   // the four epilogue warps; every one arrives, ok or not
-      if (ok) {
-        const int c_lo = max(p.win0, col0), c_hi = min(min(p.win1, p.V), col0 + kBN);
-        for (int rr = q * 32; rr < q * 32 + 32; ++rr) {
-          const int grow = row0 + rr;
-          if (grow >= p.rows) break;
-          float* orow = p.out + (int64_t)grow * p.out_stride;
-          for (int cc = c_lo + lane; cc < c_hi; cc += 32) {
-            const int j = cc - col0;   // column inside the tile
-            const int slot = (j >> 6) * 16 + (((j & 63) >> 2) ^ (rr & 15));
-            orow[cc] = stage[rr * kBN + slot * 4 + (j & 3)];
-          }
-        }
-      }
+      // this accumulator's TMEM reads are complete (tcgen05.wait::ld): hand it back
+      fence_before_sync();
+      mbar_arrive(&bars.acc_empty[acc]);
+      if (ok && row < p.rows) p.part[(int64_t)row * p.n_tiles + (t / p.m_tiles)] = make_float2(m, l);
     }
   }
   fence_before_sync();
@@ -193,7 +228,7 @@ bd_lmhead_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant
   if (abort_sh && threadIdx.x == 0) set_status(p.hdr, BEAMDEC_ERR_TIMEOUT);
   if (warp == 1) {
     fence_after_sync();
-    tmem_dealloc(tmem, kBN);
+    tmem_dealloc(tmem, 2 * kBN);
   }
 }
 
@@ -255,11 +290,13 @@ int launch_lmhead(const void* hidden, const void* weight, int rows, int hidden_d
   LmParams p;
   p.rows = rows; p.hidden = hidden_dim; p.V = V;
   p.n_tiles = (V + kBN - 1) / kBN;
+  p.m_tiles = (rows + kBM - 1) / kBM;
   p.win0 = win0; p.win1 = win1;
   p.out = logits_out; p.out_stride = out_stride;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   p.part = reinterpret_cast<float2*>(static_cast<char*>(ws) + kWsHeaderBytes);
-  dim3 grid((rows + kBM - 1) / kBM, p.n_tiles);
+  const int tiles = p.m_tiles * p.n_tiles;
+  dim3 grid(tiles < sm_count() ? tiles : sm_count());
   prof_begin(kKLmhead, stream);
   bd_lmhead_kernel<<<grid, kLmThreads, kLmSmem, stream>>>(am, bm, p);
   prof_end(kKLmhead, stream);
