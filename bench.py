@@ -472,6 +472,29 @@ def lmhead_arm(step, args, flush, H=2048):
     return res
 
 
+def lmhead_only(V, rows=2048, H=2048):
+    from wide_beam_generative_gb300 import beamdec as bd
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(3)
+    h = torch.randn(rows, H, generator=g, device=dev).to(torch.bfloat16)
+    w = (torch.randn(V, H, generator=g, device=dev) * (2.0 / H ** 0.5)).to(torch.bfloat16)
+    lse = torch.empty(rows, dtype=torch.float32, device=dev)
+    logits = torch.empty((rows, V), dtype=torch.float32, device=dev)
+    ws = bd.workspace(bd.beam_lmhead_workspace_size(rows, V), dev)
+    win0, win = max(0, V - 8192), min(V, 8192)
+    bd.beam_lmhead_lse(h, w, win0, win, lse_out=lse, logits_out=logits, ws=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    bd.beam_lmhead_lse(h, w, win0, win, lse_out=lse, logits_out=logits, ws=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3
+    assert bd.read_status(ws) == 0
+    print(json.dumps({"lmhead_only": {"rows": rows, "hidden": H, "vocab": V, "us": round(us, 1),
+                                      "tflops": round(2.0 * rows * H * V / (us * 1e-6) / 1e12, 1)}}))
+
+
 def gumbel_arm(step, args, flush):
     """The benchmarked step's selection with temperature 1 (Gumbel top-k),
     beside the deterministic one, on the same resident inputs."""
@@ -646,8 +669,14 @@ def main():
     ap.add_argument("--no-chain", action="store_true", help="skip the whole-chain CUDA-graph replay")
     ap.add_argument("--requests", type=int, default=None,
                     help="override the workload's request count (smaller cases for profiling)")
+    ap.add_argument("--lmhead-only", type=int, default=0, metavar="VOCAB",
+                    help="profiling aid: run only the fused LM head (2048 rows, hidden 2048) over VOCAB "
+                         "tokens, warm-up + 1 launch, and print its time")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
+    if args.lmhead_only:
+        lmhead_only(args.lmhead_only)
+        return
     if args.impl == "reference":
         line = reference_arm(args, ws, rank)
     else:
