@@ -352,6 +352,7 @@ def gpu_arm(args, ws, rank, local):
     chain = None if args.no_chain else chain_arm(step, args, flush)
     gumbel = None if args.no_chain else gumbel_arm(step, args, flush)
     lmhead = None if args.no_chain else lmhead_arm(step, args, flush)
+    dense = None if args.no_chain else dense_arm(step, args, flush)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "beam-rows/s", "n_gpus": ws,
@@ -367,7 +368,7 @@ def gpu_arm(args, ws, rank, local):
         "kernels_note": "per-kernel event times from a pass of the same steps just before the timed "
                         "region; inside it only the roofline kernel is bracketed by events",
         "gpu_launches": launches, "clocks": clk, "e2e": e2e, "chain_graph": chain, "gumbel_select": gumbel,
-        "lmhead_select": lmhead,
+        "lmhead_select": lmhead, "dense_trie": dense,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows or 4 * wl.W)
@@ -468,6 +469,68 @@ def lmhead_arm(step, args, flush, H=2048):
     res["head_tflops"] = round(2.0 * rows * H * V / (res["head_gemm_us"] * 1e-6) / 1e12, 1)
     assert bd.read_status(step.ws_sel) == 0 and bd.read_status(ws) == 0
     del h, w, logits, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def dense_arm(step, args, flush):
+    """The selection of every decode step given each row's log-sum-exp
+    (lse_in, the path the fused LM head feeds), with the trie levels as CSR
+    and with dense child masks where they fit (levels whose masks exceed
+    1 GiB stay CSR), on resident logits; per-step microseconds.  The
+    normalisers come from an untimed one-launch selection of the same step."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl, dev, trie = step.wl, step.dev, step.trie
+    if trie is None:
+        return None
+    R, W, T = wl.R, wl.W, wl.T
+    logits = [synth.logits(wl, t, device=dev) for t in range(T - 1)] + [step.logits]
+    stream = torch.cuda.current_stream()
+
+    def chain_times():
+        st = dict(cum=torch.zeros((R, W), dtype=torch.float32, device=dev),
+                  node=torch.zeros((R, W), dtype=torch.int32, device=dev),
+                  n_live=torch.ones((R,), dtype=torch.int32, device=dev),
+                  slot=torch.full((R, W, T), -1, dtype=torch.int32, device=dev))
+        out = []
+        for t in range(T):
+            lse = bd.beam_select(logits[t], st["cum"], st["node"], st["n_live"], st["slot"], trie, t, t,
+                                 wl.K, ws=step.ws_sel)["lse_out"]
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            o = bd.beam_select(logits[t], st["cum"], st["node"], st["n_live"], st["slot"], trie, t, t, wl.K,
+                               lse_in=lse, ws=step.ws_sel)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            out.append(e0.elapsed_time(e1) * 1e3)
+            st = dict(cum=o["cum_out"], node=o["node_out"], n_live=o["n_live_out"], slot=o["slot_out"])
+        return out
+
+    def timed():
+        for _ in range(2):
+            chain_times()
+        n = max(1, min(args.steps, 5))
+        acc = [0.0] * T
+        for _ in range(n):
+            for t, x in enumerate(chain_times()):
+                acc[t] += x / n
+        return [round(x, 1) for x in acc]
+
+    res = {"csr_us_per_step": timed()}
+    dense_levels = []
+    for lv in range(wl.levels):
+        try:
+            trie.make_dense(lv)
+            dense_levels.append(lv)
+        except bd.BeamdecError:
+            pass
+    res["dense_levels"] = dense_levels
+    res["dense_us_per_step"] = timed()
+    for lv in dense_levels:
+        trie.drop_dense(lv)
+    assert bd.read_status(step.ws_sel) == 0
+    del logits
     torch.cuda.empty_cache()
     return res
 

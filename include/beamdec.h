@@ -189,6 +189,25 @@ int beam_trie_info(const beamdec_trie* trie, int* levels, int32_t* vocab,
 int beam_trie_export(const beamdec_trie* trie, int level, const int32_t** off,
                      const int32_t** code);
 
+/*
+ * Dense child masks for one level (the FlashRec announcement's fused SID trie
+ * has a dense and a CSR form).  Bit c of node n's mask (ceil(C/32) 32-bit words
+ * per node, device memory owned by the trie) is set when code c is one of n's
+ * children.  While a level has masks, beam_select and beam_select_gumbel
+ * called WITH lse_in enumerate that level's candidates from the mask (bit
+ * order = code order = child order) instead of the CSR code list; without
+ * lse_in (the one-launch path) they keep the CSR list.  The selections are
+ * identical either way.  beam_trie_make_dense
+ * builds them from the level's CSR (a host round trip on `stream`,
+ * synchronised); beam_trie_drop_dense frees them; beam_trie_export_dense
+ * returns the device pointer (NULL without masks) and words per node.
+ * Errors: INVALID_ARG (bad level), UNSUPPORTED (C > 16384, or masks above
+ * 1 GiB), ALLOC, CUDA.
+ */
+int beam_trie_make_dense(beamdec_trie* trie, int level, void* stream);
+int beam_trie_drop_dense(beamdec_trie* trie, int level);
+int beam_trie_export_dense(const beamdec_trie* trie, int level, const uint32_t** mask, int32_t* words);
+
 /* ======================================================================== *
  * Beam selection
  * ======================================================================== */

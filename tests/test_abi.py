@@ -139,3 +139,10 @@ def test_gumbel_select_validates_temperature_on_host(L):
         assert L.beam_select_gumbel(*args, t, 7, *outs) == bd.ERR_INVALID_ARG, t
     # a valid temperature reaches the same shape checks as beam_select
     assert L.beam_select_gumbel(*args, 0.7, 7, *outs) == bd.ERR_WORKSPACE
+
+
+def test_dense_trie_validation_before_any_device_call(L):
+    from wide_beam_generative_gb300 import beamdec as bd
+    assert L.beam_trie_make_dense(None, 0, None) == bd.ERR_INVALID_ARG
+    assert L.beam_trie_drop_dense(None, 0) == bd.ERR_INVALID_ARG
+    assert L.beam_trie_export_dense(None, 0, None, None) == bd.ERR_INVALID_ARG

@@ -31,7 +31,7 @@ def _init_state(R, W, T):
 
 
 def run_chain(wl, items=None, steps=None, K=None, W=None, logit_fn=None, check=True, temperature=0.0,
-              seed=0):
+              seed=0, dense_levels=()):
     """Decode `steps` steps on the GPU and in the oracle in lockstep
     (temperature > 0: Gumbel top-k under `seed` on both sides)."""
     from wide_beam_generative_gb300 import beamdec as bd
@@ -41,6 +41,8 @@ def run_chain(wl, items=None, steps=None, K=None, W=None, logit_fn=None, check=T
     steps = T if steps is None else steps
     if wl.levels:
         gtrie, otr = build_tries(wl, items)
+        for lv in dense_levels:
+            gtrie.make_dense(lv)
     else:
         gtrie, otr = None, None
     st = _init_state(wl.R, W, T)
@@ -212,7 +214,7 @@ def test_openvocab_full_size_properties(gpu_lib):
 
 # ---------------------------------------------------------------------------- full path
 
-def run_chain_own_lse(wl, steps=None, items=None, temperature=0.0, seed=0):
+def run_chain_own_lse(wl, steps=None, items=None, temperature=0.0, seed=0, dense_levels=()):
     """The production path (the kernel computes each row's normaliser, so the
     selection runs in the one-launch stream kernel) against the oracle's own
     float64 chain.  Each side carries its own state.  Per step: log-sum-exp
@@ -225,6 +227,8 @@ def run_chain_own_lse(wl, steps=None, items=None, temperature=0.0, seed=0):
     W, K, R, T = wl.W, wl.K, wl.R, wl.T
     steps = T if steps is None else steps
     gtrie, otr = build_tries(wl, items) if wl.levels else (None, None)
+    for lv in dense_levels:
+        gtrie.make_dense(lv)
     st = _init_state(R, W, T)
     o_cum = np.zeros((R, W), np.float32)
     o_node = np.zeros((R, W), np.int64)
@@ -376,3 +380,49 @@ def test_gumbel_differs_from_deterministic_and_repeats(gpu_lib):
     assert not torch.equal(det["tokens"], g1["tokens"])
     for k in ("tokens", "parents", "cum_out", "node_out", "n_live_out", "slot_out"):
         assert torch.equal(g1[k], g2[k]), k
+
+
+# ---------------------------------------------------------------------------- dense trie levels
+
+def test_dense_masks_match_the_oracle_trie(gpu_lib):
+    """Bit c of node n's mask is set exactly for the codes of n's children in
+    the oracle's trie."""
+    wl = synth.WORKLOADS["qwen06b"]
+    gtrie, otr = build_tries(wl, _catalog(wl))
+    for lv in (0, 1):
+        assert gtrie.export_dense(lv) is None
+        gtrie.make_dense(lv)
+        m = gtrie.export_dense(lv).cpu().numpy().view(np.uint32)
+        n_nodes = m.shape[0]
+        for node in list(range(min(n_nodes, 300))) + [n_nodes - 1]:
+            codes, _ = otr.children(lv, node)
+            bits = np.zeros(m.shape[1] * 32, bool)
+            bits[codes] = True
+            got = ((m[node][:, None] >> np.arange(32, dtype=np.uint32)) & 1).astype(bool).reshape(-1)
+            assert np.array_equal(got, bits), (lv, node)
+        gtrie.drop_dense(lv)
+        assert gtrie.export_dense(lv) is None
+
+
+def test_dense_tiny_chain_bitexact(gpu_lib):
+    wl = synth.WORKLOADS["tiny"]
+    run_chain(wl, _catalog(wl), dense_levels=(0, 1, 2))
+
+
+def test_dense_qwen06b_chain_bitexact(gpu_lib):
+    wl = synth.WORKLOADS["qwen06b"]
+    run_chain(wl, _catalog(wl), dense_levels=(0, 1))
+
+
+def test_dense_onerec17b_bitexact_and_gumbel(gpu_lib):
+    wl = synth.WORKLOADS["onerec17b"]
+    items = _catalog(wl)
+    run_chain(wl, items, steps=2, dense_levels=(0, 1))
+    run_chain(wl, items, steps=2, dense_levels=(0, 1), temperature=0.9, seed=77)
+
+
+def test_dense_masks_leave_the_one_launch_path_unchanged(gpu_lib):
+    """With masks on levels 0 and 1 the one-launch path (no lse_in) still
+    matches the oracle's chain: it enumerates the CSR lists."""
+    wl = synth.WORKLOADS["qwen06b"]
+    assert run_chain_own_lse(wl, items=_catalog(wl), dense_levels=(0, 1)) >= 1

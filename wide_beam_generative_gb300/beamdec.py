@@ -47,6 +47,9 @@ _SIGS = {
     "beam_select_gumbel": (c_int, [c_p, c_i64, c_p, c_p, c_p, c_p, c_p, c_p, c_int, c_int,
                                    c_int, c_int, c_int, c_int, c_int, c_f, ctypes.c_uint64,
                                    c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]),
+    "beam_trie_make_dense": (c_int, [c_p, c_int, c_p]),
+    "beam_trie_drop_dense": (c_int, [c_p, c_int]),
+    "beam_trie_export_dense": (c_int, [c_p, c_int, ctypes.POINTER(c_p), ctypes.POINTER(ctypes.c_int32)]),
     "beam_lmhead_workspace_size": (c_int, [c_int, c_int, ctypes.POINTER(c_sz)]),
     "beam_lmhead_lse": (c_int, [c_p, c_p, c_int, c_int, c_int, c_int, c_int, c_p, c_p, c_i64, c_p, c_sz,
                                 c_p]),
@@ -145,6 +148,28 @@ class Trie:
         o = torch.as_tensor(_DevArray(off.value, info["n_nodes"][level] + 1), device="cuda").clone()
         c = torch.as_tensor(_DevArray(code.value, info["n_edges"][level]), device="cuda").clone()
         return o, c
+
+    def make_dense(self, level, stream=None):
+        """Build dense child masks for `level`; selections given ``lse_in``
+        then enumerate that level's candidates from them (the one-launch
+        path without ``lse_in`` keeps the CSR list; results are identical)."""
+        _check(lib().beam_trie_make_dense(self.handle, level, _stream(stream)), "beam_trie_make_dense")
+
+    def drop_dense(self, level):
+        _check(lib().beam_trie_drop_dense(self.handle, level), "beam_trie_drop_dense")
+
+    def export_dense(self, level):
+        """[n_nodes, words] int32 copy of the level's masks (bit c = code c), or None."""
+        ptr, words = c_p(), ctypes.c_int32()
+        _check(lib().beam_trie_export_dense(self.handle, level, ctypes.byref(ptr), ctypes.byref(words)),
+               "beam_trie_export_dense")
+        if not ptr.value:
+            return None
+        n_nodes = int(self.info()["n_nodes"][level])
+        out = torch.empty((n_nodes, words.value), dtype=torch.int32, device="cuda")
+        src = torch.as_tensor(_DevArray(ptr.value, n_nodes * words.value), device="cuda")
+        out.copy_(src.view(n_nodes, words.value))
+        return out
 
     def __del__(self):
         if getattr(self, "_h", None) and _lib is not None:

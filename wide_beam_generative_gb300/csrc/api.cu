@@ -153,6 +153,8 @@ static int select_entry(const float* logits, int64_t row_stride, const float* ls
     a.lvl.code = trie->code[level];
     a.lvl.n_nodes = (int32_t)trie->n_nodes[level];
     a.lvl.token_base = trie->token_base[level];
+    a.lvl.mask = trie->mask[level];
+    a.lvl.words = trie->mask_words[level];
   }
   if (workspace_bytes < select_workspace_bytes(R, W, K, V)) return BEAMDEC_ERR_WORKSPACE;
   a.logits = logits; a.row_stride = row_stride; a.lse_in = lse_in;

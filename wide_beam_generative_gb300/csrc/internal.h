@@ -20,6 +20,8 @@ struct beamdec_trie {
   int32_t max_children[BEAMDEC_MAX_LEVELS];
   int32_t* off[BEAMDEC_MAX_LEVELS];       // device [n_nodes+1]
   int32_t* code[BEAMDEC_MAX_LEVELS];      // device [n_edges]
+  uint32_t* mask[BEAMDEC_MAX_LEVELS];     // device [n_nodes][mask_words] or null
+  int32_t mask_words[BEAMDEC_MAX_LEVELS];
   int device;
 };
 
@@ -33,6 +35,8 @@ struct TrieLevel {
   const int32_t* code;
   int32_t n_nodes;
   int32_t token_base;
+  const uint32_t* mask;   // dense child masks [n_nodes][words], or null (CSR only)
+  int32_t words;          // 32-bit words per mask
 };
 
 // ---- select ----------------------------------------------------------------

@@ -135,6 +135,28 @@ __device__ __forceinline__ int block_rank(int flag, int* warp_cnt, int* total) {
   return base + r;
 }
 
+// Block-wide exclusive prefix sum of v over the block's threads, and the total.
+__device__ __forceinline__ int block_excl_sum(int v, int* warp_cnt, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) warp_cnt[warp] = inc;
+  __syncthreads();
+  int base = 0, tot = 0;
+  for (int w = 0; w < nw; ++w) {
+    const int c = warp_cnt[w];
+    if (w < warp) base += c;
+    tot += c;
+  }
+  __syncthreads();
+  *total = tot;
+  return base + inc - v;
+}
+
 // Adds one to hist[bin] for every lane with `on`: lanes that share a bin add
 // their count once, so a histogram whose keys crowd into a few bins costs one
 // atomic per bin and warp instead of one per key.  Every lane of the warp
@@ -300,10 +322,15 @@ __device__ __forceinline__ float2 stream_max_sum(const float* row, int c0, int c
 // only) counts every candidate the row adds to the pool.
 // kPf: the row's trie range and scores were fetched into sh.pf_* already.
 // kG: Gumbel top-k; candidates are ordered by fl32(fl32(s * inv_tau) + g).
-template <bool kPf, bool kG>
+// kD: the level has dense child masks; candidates are enumerated from the
+//     node's mask (bit order = code order = child order) instead of its CSR
+//     code list.  Built into the expansion kernel only (lse_in given): the
+//     32-register stream kernel keeps the CSR enumeration.
+template <bool kPf, bool kG, bool kD>
 __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
                                                  int r, int b, uint32_t* gh, uint32_t* kcache,
                                                  float lse) {
+  static_assert(!(kPf && kD), "dense masks are enumerated by the expansion kernel only");
   const int tid = threadIdx.x;
   const int Kp = a.Kp;
   const size_t rowi = (size_t)r * a.W + b;
@@ -316,13 +343,14 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
   int n = a.V;
   const int32_t* code = nullptr;
   int tb = 0;
+  int node = -1;
   if (a.has_trie) {
     int e0, e1;
     if constexpr (kPf) {
       e0 = sh.pf_e0;
       e1 = sh.pf_e1;
     } else {
-      const int node = a.node_in[rowi];
+      node = a.node_in[rowi];
       const bool bad = node < 0 || node >= a.lvl.n_nodes;
       e0 = bad ? -2 : a.lvl.off[node];
       e1 = bad ? -2 : a.lvl.off[node + 1];
@@ -346,6 +374,43 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
       return desc_key(sc);
   };
   auto key_of = [&](int tok) -> uint32_t { return score_key(__ldg(row + tok), tok); };
+  // kD: every child (index, token, key) from the node's dense mask, handed to
+  // sink(on, child, key) by every thread of the block (block-uniform rounds
+  // of four positions per thread; logits only for set bits)
+  auto dense_children = [&](auto&& sink) {
+    const int words = a.lvl.words;
+    uint32_t* wsm = sh.hist;           // the node's mask words
+    uint32_t* pre = sh.hist + 1024;    // children in the words before each word
+    const uint32_t wv = tid < words ? __ldg(a.lvl.mask + (size_t)node * words + tid) : 0u;
+    int tot;
+    const int ex = block_excl_sum(__popc(wv), sh.warp_cnt, &tot);
+    if (tid < words) {
+      wsm[tid] = wv;
+      pre[tid] = (uint32_t)ex;
+    }
+    __syncthreads();
+    constexpr int kU = 4;
+    const int C = 32 * words;
+    for (int c0 = 0; c0 < C; c0 += kU * kExpandThreads) {
+      bool on[kU];
+      int child[kU];
+      float x[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int pos = c0 + u * kExpandThreads + tid;
+        const uint32_t w = pos < C ? wsm[pos >> 5] : 0u;
+        on[u] = (w >> (pos & 31)) & 1u;
+        child[u] = (int)pre[pos < C ? pos >> 5 : 0] + __popc(w & ((1u << (pos & 31)) - 1u));
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) x[u] = on[u] ? __ldg(row + tb + c0 + u * kExpandThreads + tid) : 0.f;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int tok = tb + c0 + u * kExpandThreads + tid;
+        sink(on[u], child[u], on[u] ? score_key(x[u], tok) : 0u);
+      }
+    }
+  };
 
   SelState* st = ws.state + r;
   unsigned long long* pool = ws.pool + (size_t)r * a.W * Kp;
@@ -353,6 +418,15 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
 
   // ---- a3: per-beam top_k -------------------------------------------------
   if (n <= a.K) {
+    if constexpr (kD) {
+      if (tid == 0) sh.pool_base = n > 0 ? atomicAdd(&st->total, n) : 0;
+      __syncthreads();   // (dense_children's own barriers follow; pool_base is read after them)
+      dense_children([&](bool on, int child, uint32_t k) {
+        if (on) pool[sh.pool_base + child] = pool_key(k, b, child);
+        if (gh) warp_hist_add(gh, (uint32_t)score_bin(ref, desc_key_value(k)), on);
+      });
+      return;
+    }
     // the first round's gathers are in flight while the pool slots are reserved
     const uint32_t k_first = tid < n ? key_of(tok_of(tid)) : 0u;
     if (tid == 0) sh.pool_base = n > 0 ? atomicAdd(&st->total, n) : 0;
@@ -370,7 +444,12 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
   // the row's candidate keys, computed once into shared memory when they fit
   // (the radix passes below then read shared memory instead of re-gathering)
   const bool cached = kcache != nullptr && n <= kKeyCache;
-  if (cached) {   // four children per thread in flight: codes first, then their logits
+  if (kD && cached) {
+    dense_children([&](bool on, int child, uint32_t k) {
+      if (on) kcache[child] = k;
+    });
+    __syncthreads();
+  } else if (cached) {   // four children per thread in flight: codes first, then their logits
     constexpr int kU = 4;
     for (int c0 = 0; c0 < n; c0 += kU * kExpandThreads) {
       int tk[kU];
@@ -792,13 +871,13 @@ selected:
 // request to finish (a per-request ticket) runs the request's global top-W.
 // Dynamic shared memory: the row's key cache (32 KB); the fused tail reuses it
 // for candidate keys after the ticket.
-template <bool kFused, bool kPf, bool kG>
+template <bool kFused, bool kPf, bool kG, bool kD>
 __device__ __forceinline__ void expand_and_select(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
                                                   int r, int b, int nl, float lse,
                                                   unsigned char* tail_smem) {
   const int tid = threadIdx.x;
   uint32_t* kcache = reinterpret_cast<uint32_t*>(tail_smem);
-  expand_candidates<kPf, kG>(a, sh, ws, r, b, kFused ? ws.hist + (size_t)r * kBins : nullptr, kcache, lse);
+  expand_candidates<kPf, kG, kD>(a, sh, ws, r, b, kFused ? ws.hist + (size_t)r * kBins : nullptr, kcache, lse);
   if constexpr (kFused) {
     __syncthreads();
     if (tid == 0) {
@@ -814,7 +893,7 @@ __device__ __forceinline__ void expand_and_select(const SelectArgs& a, ExpandSha
 
 // a2-a5 when the caller supplies the row normalisers (lse_in): one block per
 // live beam.
-template <bool kFused, bool kG>
+template <bool kFused, bool kG, bool kD>
 __global__ void __launch_bounds__(kExpandThreads)
 bd_expand_kernel(SelectArgs a) {
   __shared__ ExpandShared sh;
@@ -825,7 +904,7 @@ bd_expand_kernel(SelectArgs a) {
   const int nl = a.n_live_in[r];
   if (b >= nl) return;
   const float lse = a.lse_in[(size_t)r * a.W + b];
-  expand_and_select<kFused, false, kG>(a, sh, ws, r, b, nl, lse, tail_smem);
+  expand_and_select<kFused, false, kG, kD>(a, sh, ws, r, b, nl, lse, tail_smem);
 }
 
 // The whole selection step in one launch: S blocks per live logits row each
@@ -894,7 +973,7 @@ bd_stream_select_kernel(SelectArgs a) {
   }
   if (tid == 0 && a.lse_out != nullptr) a.lse_out[rowi] = lse;
   if (kG && tid == 0) ws.rowlse[rowi] = lse;   // read by the outputs' score recomputation
-  expand_and_select<kFused, true, kG>(a, sh, ws, r, b, nl, lse, tail_smem);
+  expand_and_select<kFused, true, kG, false>(a, sh, ws, r, b, nl, lse, tail_smem);
 }
 
 // ---------------------------------------------------------------------------
@@ -1048,6 +1127,12 @@ struct GlobalLaunchCfg {
 
 }  // namespace
 
+template <bool kG, bool kD>
+void launch_expand(bool fused, dim3 grid, size_t dsm, cudaStream_t stream, const SelectArgs& a) {
+  if (fused) bd_expand_kernel<true, kG, kD><<<grid, kExpandThreads, dsm, stream>>>(a);
+  else bd_expand_kernel<false, kG, kD><<<grid, kExpandThreads, dsm, stream>>>(a);
+}
+
 size_t select_workspace_bytes(int R, int W, int K, int V) {
   const int Kp = K < V ? K : V;
   return kWsHeaderBytes + align256((size_t)R * sizeof(SelState)) +
@@ -1094,6 +1179,7 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
   static_assert(kKeyCache * 4 <= kTailCap * 8, "fused dynamic shared memory");
   const size_t dsm = fused ? kTailCap * sizeof(unsigned long long) : kKeyCache * sizeof(uint32_t);
   const bool gumbel = a.inv_tau > 0.f;
+  const bool dense = a.has_trie && a.lvl.mask != nullptr;
   if (a.lse_in == nullptr) {
     dim3 g0(a.W * S, a.R);
     prof_begin(kKStream, stream);
@@ -1109,11 +1195,11 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
     dim3 g1(a.W, a.R);
     prof_begin(kKExpand, stream);
     if (gumbel) {
-      if (fused) bd_expand_kernel<true, true><<<g1, kExpandThreads, dsm, stream>>>(a2);
-      else bd_expand_kernel<false, true><<<g1, kExpandThreads, dsm, stream>>>(a2);
+      if (dense) launch_expand<true, true>(fused, g1, dsm, stream, a2);
+      else launch_expand<true, false>(fused, g1, dsm, stream, a2);
     } else {
-      if (fused) bd_expand_kernel<true, false><<<g1, kExpandThreads, dsm, stream>>>(a2);
-      else bd_expand_kernel<false, false><<<g1, kExpandThreads, dsm, stream>>>(a2);
+      if (dense) launch_expand<false, true>(fused, g1, dsm, stream, a2);
+      else launch_expand<false, false>(fused, g1, dsm, stream, a2);
     }
     prof_end(kKExpand, stream);
   }

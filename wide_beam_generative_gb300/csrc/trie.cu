@@ -155,6 +155,7 @@ extern "C" void beam_trie_free(beamdec_trie* t) {
   for (int l = 0; l < BEAMDEC_MAX_LEVELS; ++l) {
     if (t->off[l]) cudaFree(t->off[l]);
     if (t->code[l]) cudaFree(t->code[l]);
+    if (t->mask[l]) cudaFree(t->mask[l]);
   }
   delete t;
 }
@@ -179,5 +180,57 @@ extern "C" int beam_trie_export(const beamdec_trie* t, int level, const int32_t*
   if (t == nullptr || level < 0 || level >= t->levels) return BEAMDEC_ERR_INVALID_ARG;
   if (off) *off = t->off[level];
   if (code) *code = t->code[level];
+  return BEAMDEC_OK;
+}
+
+// Dense child masks of one level (the FlashRec announcement's fused SID trie
+// has a dense and a CSR form): bit c of node n's mask is set when code c is one of
+// n's children.  Built from the level's CSR (copied back to the host once);
+// the CSR stays, the selection enumerates candidates from the mask.
+extern "C" int beam_trie_make_dense(beamdec_trie* t, int level, void* stream_ptr) {
+  if (t == nullptr || level < 0 || level >= t->levels) return BEAMDEC_ERR_INVALID_ARG;
+  const int32_t C = t->C[level];
+  const int64_t words = (C + 31) / 32;
+  if (C > 16384 || t->n_nodes[level] * words * 4 > ((int64_t)1 << 30)) return BEAMDEC_ERR_UNSUPPORTED;
+  if (t->mask[level] != nullptr) return BEAMDEC_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int64_t nn = t->n_nodes[level], ne = t->n_edges[level];
+  std::vector<int32_t> off(nn + 1), code(ne);
+  if (cudaMemcpyAsync(off.data(), t->off[level], (nn + 1) * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                      stream) != cudaSuccess ||
+      cudaMemcpyAsync(code.data(), t->code[level], ne * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                      stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return BEAMDEC_ERR_CUDA;
+  std::vector<uint32_t> mask((size_t)(nn * words), 0u);
+  for (int64_t n = 0; n < nn; ++n)
+    for (int32_t e = off[n]; e < off[n + 1]; ++e)
+      mask[n * words + code[e] / 32] |= 1u << (code[e] % 32);
+  uint32_t* d = nullptr;
+  if (cudaMalloc(&d, mask.size() * sizeof(uint32_t)) != cudaSuccess) return BEAMDEC_ERR_ALLOC;
+  if (cudaMemcpyAsync(d, mask.data(), mask.size() * sizeof(uint32_t), cudaMemcpyHostToDevice, stream) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaFree(d);
+    return BEAMDEC_ERR_CUDA;
+  }
+  t->mask[level] = d;
+  t->mask_words[level] = (int32_t)words;
+  return BEAMDEC_OK;
+}
+
+extern "C" int beam_trie_drop_dense(beamdec_trie* t, int level) {
+  if (t == nullptr || level < 0 || level >= t->levels) return BEAMDEC_ERR_INVALID_ARG;
+  if (t->mask[level] != nullptr) cudaFree(t->mask[level]);
+  t->mask[level] = nullptr;
+  t->mask_words[level] = 0;
+  return BEAMDEC_OK;
+}
+
+extern "C" int beam_trie_export_dense(const beamdec_trie* t, int level, const uint32_t** mask,
+                                      int32_t* words) {
+  if (t == nullptr || level < 0 || level >= t->levels) return BEAMDEC_ERR_INVALID_ARG;
+  if (mask) *mask = t->mask[level];
+  if (words) *words = t->mask_words[level];
   return BEAMDEC_OK;
 }
