@@ -239,6 +239,40 @@ def algorithmic(wl, rows, kernel):
     return 0, "bytes"
 
 
+def step_roofline(wl, rows, ms_per_step, kernels, pk):
+    """The metric's second half: algorithmic HBM bytes of attention + selection
+    per step (prompt KV counted once per request) over the step time, as a
+    fraction of the HBM peak; and the attention alone against its binding
+    roof, max(bytes / HBM peak, shared-stage flops / bf16 peak), over the
+    attention kernels' time from the per-kernel breakdown."""
+    P = synth.prompt_lens(wl)
+    b_kv = 1 if wl.kv_dtype == synth.E4M3 else (4 if wl.kv_dtype == synth.F32 else 2)
+    b_q = 4 if wl.q_dtype == synth.F32 else 2
+    shared = int(P.sum()) * wl.Hkv * wl.d * 2 * b_kv
+    unshared = rows * wl.T * wl.Hkv * wl.d * 2 * b_kv
+    qo = 2 * rows * wl.Hq * wl.d * b_q
+    attn_bytes = shared + unshared + qo
+    sel_bytes = rows * wl.V * 4
+    flops = 4.0 * wl.Hkv * wl.W * wl.G * P.sum() * wl.d
+    hbm = _peak_value(pk, "hbm_gbs", "hbm_GBs", "hbm") or FALLBACK_PEAKS["hbm_gbs"]
+    tc = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
+    step_gbs = (attn_bytes + sel_bytes) / (ms_per_step / 1e3) / 1e9
+    attn_us = sum(v["us_per_launch"] for k, v in kernels.items()
+                  if k.startswith("bd_attn") or k == "bd_kv_e4m3_to_bf16_kernel")
+    out = {"attn_select_bytes": attn_bytes + sel_bytes, "attn_select_gbs": round(step_gbs, 1),
+           "hbm_peak_gbs": hbm, "hbm_frac": round(step_gbs / hbm, 4)}
+    if attn_us > 0:
+        roof_hbm_us = attn_bytes / (hbm * 1e9) * 1e6
+        roof_tc_us = flops / (tc * 1e12) * 1e6
+        out["attention"] = {"us": round(attn_us, 2), "bytes": attn_bytes, "flops": float(flops),
+                            "hbm_frac": round(roof_hbm_us / attn_us, 4),
+                            "roof_us": {"hbm": round(float(roof_hbm_us), 2), "tensor": round(float(roof_tc_us), 2)},
+                            "binding": "tensor" if roof_tc_us > roof_hbm_us else "hbm",
+                            "binding_frac": round(float(max(roof_hbm_us, roof_tc_us) / attn_us), 4),
+                            "tensor_peak_tflops": tc}
+    return out
+
+
 def read_traffic(kernel):
     """dram bytes per launch of `kernel` from the committed ncu summary, if it
     was taken on the current source of that kernel."""
@@ -346,6 +380,7 @@ def gpu_arm(args, ws, rank, local):
     kernels = {k: {"us_per_launch": round(ms / n * 1e3, 2), "launches": n,
                    "share": round(ms / max(1e-9, sum(x for x, _ in breakdown.values())), 4)}
                for k, (ms, n) in breakdown.items()}
+    step_roof = step_roofline(wl, rows, ms_per_step, kernels, pk)
 
     # end-to-end through the C ABI from pinned host buffers
     e2e = None if args.no_e2e else e2e_arm(step, args, ws, flush)
@@ -364,7 +399,7 @@ def gpu_arm(args, ws, rank, local):
                                f"catalog {wl.n_items} step {step.step + 1}/{wl.T}",
                    "rows_per_step_per_gpu": rows, "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MB write) before each step",
                    "parallelism": f"request-sharded replicas x{ws}"},
-        "roofline": roof, "kernels": kernels,
+        "roofline": roof, "step_roofline": step_roof, "kernels": kernels,
         "kernels_note": "per-kernel event times from a pass of the same steps just before the timed "
                         "region; inside it only the roofline kernel is bracketed by events",
         "gpu_launches": launches, "clocks": clk, "e2e": e2e, "chain_graph": chain, "gumbel_select": gumbel,

@@ -269,6 +269,7 @@ extern "C" int beam_attn_decode(const void* q, const void* shared_k, const void*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc = p.tensor_core ? launch_attn_shared_tc(a, p, st) : launch_attn_shared_simt(a, p, st);
   if (rc != BEAMDEC_OK) return rc;
+  if (p.tensor_core && attn_tc_fused(a, p)) return BEAMDEC_OK;   // merged in the shared stage
   return launch_attn_merge(a, p, st);
 }
 

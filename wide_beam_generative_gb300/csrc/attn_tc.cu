@@ -6,7 +6,10 @@
 // group form one dense matrix Q [W*G x d] against the prompt's K and V: the
 // shared stage is a flash-attention contraction with M = W*G rows.  Its
 // output is the partial (max, sum, unnormalised output) of every query row,
-// merged later with the unshared stage.
+// merged later with the unshared stage (§4.2.2).  When the whole prompt is
+// one split, every row's shared partial stays in its CTA, so the epilogue
+// runs the unshared stage and the merge itself and writes the output rows;
+// otherwise the partials go to the merge kernel.
 //
 // One CTA owns 256 query rows (two 128-row tiles) of one (request, kv head,
 // prompt split), so every K/V tile it loads feeds two tiles of MMAs:
@@ -23,6 +26,8 @@
 //                max/sum in log2 units and writes P (bf16, two per column)
 //                back into TMEM over the first 64 columns of its S tile,
 //                where the PV MMA reads it as its A operand.
+//   warp 10      when the merge is fused (one prompt split): pulls the CTA's
+//                unshared K/V rows into L2 for the epilogue.
 // The output O accumulates in TMEM across chunks (S0 O0 S1 O1, 128 columns
 // each).  P_t(c) overwrites S_t(c) only after the softmax has read all of it,
 // and S_t(c+1) is issued after PV_t(c) by the same thread, so the tensor core
@@ -51,7 +56,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 320;   // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr int kThreads = 352;   // warps 0-7 softmax, 8 TMA, 9 MMA, 10 L2 prefetch
 constexpr uint32_t kHalfBytes = 16384;           // 128 rows x 128 B
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 128 x 128 bf16
 constexpr int kSlots = 5;                        // K/V ring
@@ -78,6 +83,14 @@ struct TcParams {
   float* pl;
   float* po;
   WsHeader* hdr;
+  // fuse != 0: the prompt is one split, so the epilogue runs the unshared
+  // stage and the merge itself and writes the output rows (bf16 KV only)
+  int fuse, L, T;
+  const int32_t* slot_table;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* uk;
+  const __nv_bfloat16* uv;
+  __nv_bfloat16* out;
 };
 
 struct Bars {
@@ -182,8 +195,158 @@ __device__ __forceinline__ void write_empty_partials(const TcParams& p, size_t b
   }
 }
 
-// Ten warps: the register file is handed out in groups of four warps, so a
-// thread may hold at most 65536 / 384 -> 168 registers.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ uint32_t bf_pack(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Output row of query row `row` of (request r, kv head g): beam j = row / G,
+// query head g * G + row % G.
+__device__ __forceinline__ size_t out_row(const TcParams& p, int r, int g, int row) {
+  const int j = row / p.G, h = row - j * p.G;
+  return (((size_t)r * p.W + j) * p.Hq + (size_t)g * p.G + h) * 128;
+}
+
+// Fused epilogue, one query row per thread: the unshared stage over the
+// beam's decode tokens (reached through its slot-table row; each K row is
+// scored with the shared stage's log2-unit scale) and the online-softmax
+// merge with the shared stage's (m, l, O):
+//     M = max(m, s_u),  Lsum = l 2^(m - M) + sum_u 2^(s_u - M),
+//     out = (O 2^(m - M) + sum_u 2^(s_u - M) v_u) / Lsum,
+// written as bf16.  Dead beams' rows are written as zeros.  Every lane of a
+// warp calls it (the TMEM loads of O are warp-wide).  have_o: O, m and l
+// come from this CTA's shared stage; otherwise the prompt is empty.  The
+// query row comes from the CTA's swizzled Q tile, or from global memory
+// when qtile is null.  ps: scratch in shared memory, stride 128 words.
+__device__ __forceinline__ void fused_row(const TcParams& p, int r, int g, int row,
+                                         const unsigned char* qtile, int rit, uint32_t tO,
+                                         bool have_o, float m_used, float l, float sc, float* ps) {
+  const int j = row / p.G;
+  const bool in = row < p.rows;
+  const bool live = in && j < p.n_live[r];
+  const int L = p.L, TW = p.T * p.W;
+  const bool shared_ok = have_o && l > 0.f;
+  float M = shared_ok ? m_used : -INFINITY;
+  const size_t qoff = in ? out_row(p, r, g, row) : 0;
+  int* pslot = reinterpret_cast<int*>(ps + (size_t)L * 128);
+  // the beam's slots, all loads in one round
+  for (int u = 0; u < L; ++u) {
+    int sl = live ? __ldg(p.slot_table + ((size_t)r * p.W + j) * p.T + u) : -1;
+    if (live && (sl < 0 || sl >= TW)) {
+      set_status(p.hdr, BEAMDEC_ERR_DEVICE_CHECK);
+      sl = -1;
+    }
+    pslot[u * 128] = sl;
+  }
+  const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+  auto kv_row = [&](const __nv_bfloat16* base, int sl) {
+    return reinterpret_cast<const uint4*>(base + (((size_t)r * TW + (sl >= 0 ? sl : 0)) * p.Hkv + g) * 128);
+  };
+  // scores, the K rows of two tokens per round of loads
+  for (int u0 = 0; u0 < L; u0 += 2) {
+    const int sl0 = pslot[u0 * 128];
+    const int sl1 = u0 + 1 < L ? pslot[(u0 + 1) * 128] : -1;
+    const uint4* k0p = kv_row(p.uk, sl0);
+    const uint4* k1p = kv_row(p.uk, sl1);
+    uint4 k0[16], k1[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) k0[c] = sl0 >= 0 ? __ldg(k0p + c) : z4;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) k1[c] = sl1 >= 0 ? __ldg(k1p + c) : z4;
+    float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 qw = qtile ? *reinterpret_cast<const uint4*>(qtile + (c >> 3) * kHalfBytes + rit * 128 +
+                                                              (((c & 7) ^ (rit & 7)) << 4))
+                             : __ldg(reinterpret_cast<const uint4*>(p.q + qoff) + c);
+      const float q0 = bf_lo(qw.x), q1 = bf_hi(qw.x), q2 = bf_lo(qw.y), q3 = bf_hi(qw.y);
+      const float q4 = bf_lo(qw.z), q5 = bf_hi(qw.z), q6 = bf_lo(qw.w), q7 = bf_hi(qw.w);
+      a0 = fmaf(q0, bf_lo(k0[c].x), a0); b0 = fmaf(q1, bf_hi(k0[c].x), b0);
+      a0 = fmaf(q2, bf_lo(k0[c].y), a0); b0 = fmaf(q3, bf_hi(k0[c].y), b0);
+      a0 = fmaf(q4, bf_lo(k0[c].z), a0); b0 = fmaf(q5, bf_hi(k0[c].z), b0);
+      a0 = fmaf(q6, bf_lo(k0[c].w), a0); b0 = fmaf(q7, bf_hi(k0[c].w), b0);
+      a1 = fmaf(q0, bf_lo(k1[c].x), a1); b1 = fmaf(q1, bf_hi(k1[c].x), b1);
+      a1 = fmaf(q2, bf_lo(k1[c].y), a1); b1 = fmaf(q3, bf_hi(k1[c].y), b1);
+      a1 = fmaf(q4, bf_lo(k1[c].z), a1); b1 = fmaf(q5, bf_hi(k1[c].z), b1);
+      a1 = fmaf(q6, bf_lo(k1[c].w), a1); b1 = fmaf(q7, bf_hi(k1[c].w), b1);
+    }
+    const float s0 = sl0 >= 0 ? (a0 + b0) * sc : -INFINITY;
+    ps[u0 * 128] = s0;
+    M = fmaxf(M, s0);
+    if (u0 + 1 < L) {
+      const float s1 = sl1 >= 0 ? (a1 + b1) * sc : -INFINITY;
+      ps[(u0 + 1) * 128] = s1;
+      M = fmaxf(M, s1);
+    }
+  }
+  const float a = shared_ok ? ex2(m_used - M) : 0.f;
+  float Ls = shared_ok ? l * a : 0.f;
+  for (int u = 0; u < L; ++u) {
+    const float w = pslot[u * 128] >= 0 ? ex2(ps[u * 128] - M) : 0.f;
+    ps[u * 128] = w;
+    Ls += w;
+  }
+  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll 1
+  for (int q4 = 0; q4 < 4; ++q4) {
+    float o[32];
+    if (have_o) tmem_ld32(tO + q4 * 32, o);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] = shared_ok ? o[i] * a : 0.f;
+    for (int u0 = 0; u0 < L; u0 += 4) {   // the V chunks of four tokens per round of loads
+      uint4 vw[4][4];
+      float wt[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int sl = u0 + x < L ? pslot[(u0 + x) * 128] : -1;
+        wt[x] = sl >= 0 ? ps[(u0 + x) * 128] : 0.f;
+        const uint4* vp = kv_row(p.uv, sl) + q4 * 4;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) vw[x][c] = sl >= 0 ? __ldg(vp + c) : z4;
+      }
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const float w = wt[x];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          o[8 * c + 0] = fmaf(w, bf_lo(vw[x][c].x), o[8 * c + 0]);
+          o[8 * c + 1] = fmaf(w, bf_hi(vw[x][c].x), o[8 * c + 1]);
+          o[8 * c + 2] = fmaf(w, bf_lo(vw[x][c].y), o[8 * c + 2]);
+          o[8 * c + 3] = fmaf(w, bf_hi(vw[x][c].y), o[8 * c + 3]);
+          o[8 * c + 4] = fmaf(w, bf_lo(vw[x][c].z), o[8 * c + 4]);
+          o[8 * c + 5] = fmaf(w, bf_hi(vw[x][c].z), o[8 * c + 5]);
+          o[8 * c + 6] = fmaf(w, bf_lo(vw[x][c].w), o[8 * c + 6]);
+          o[8 * c + 7] = fmaf(w, bf_hi(vw[x][c].w), o[8 * c + 7]);
+        }
+      }
+    }
+    if (in) {
+      uint4* dst = reinterpret_cast<uint4*>(p.out + qoff + q4 * 32);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        dst[c] = live ? make_uint4(bf_pack(o[8 * c] * inv, o[8 * c + 1] * inv),
+                                   bf_pack(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                   bf_pack(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                                   bf_pack(o[8 * c + 6] * inv, o[8 * c + 7] * inv))
+                      : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
+// Zero output rows [row0, row0 + 256) of (request r, kv head g): a CTA whose
+// beams are all dead, when the merge is fused.
+__device__ __forceinline__ void zero_rows(const TcParams& p, int r, int g, int row0) {
+  for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
+    const int row = row0 + (i >> 4);
+    if (row < p.rows) reinterpret_cast<uint4*>(p.out + out_row(p, r, g, row))[i & 15] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+// Eleven warps: the register file is handed out in groups of four warps, so a
+// thread may hold at most 65536 / 384 -> 168 registers (a tenth or eleventh
+// warp costs no registers).
 __global__ void __launch_bounds__(kThreads, 1)
 bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                          const __grid_constant__ CUtensorMap kmap,
@@ -204,14 +367,24 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 &&
       (int64_t)p.prompt_offsets[p.R] != p.shared_rows)
     set_status(p.hdr, BEAMDEC_ERR_DEVICE_CHECK);   // the K/V maps end at shared_rows
-  if (row0 >= p.n_live[r] * G) return;   // every row of the CTA is a dead beam
+  if (row0 >= p.n_live[r] * G) {   // every row of the CTA is a dead beam
+    if (p.fuse) zero_rows(p, r, g, row0);
+    return;
+  }
   const int pbase = p.prompt_offsets[r];
   const int P = p.prompt_offsets[r + 1] - pbase;
   const int k0 = sp * p.split_len;
   const int k1 = min(P, k0 + p.split_len);
   const size_t prow_base = (((size_t)sp * p.R + r) * p.Hkv + g) * p.rows;
   if (k1 <= k0) {   // this split holds no key of the request
-    write_empty_partials(p, prow_base, row0);
+    if (!p.fuse) {
+      write_empty_partials(p, prow_base, row0);
+    } else if (threadIdx.x < 256) {   // empty prompt: the unshared tokens alone
+      const int t = threadIdx.x >> 7, rit = threadIdx.x & 127;
+      float* ps = reinterpret_cast<float*>(sm + kOffKV + (uint32_t)t * (128u * 512u)) + rit;
+      fused_row(p, r, g, row0 + threadIdx.x, nullptr, rit, 0u, false, -INFINITY, 0.f,
+                p.scale_log2 * (p.k_scale ? p.k_scale[g] : 1.f), ps);
+    }
     return;
   }
   const int nchunks = (k1 - k0 + 127) / 128;
@@ -323,6 +496,21 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     }
     if (ok) mma_commit(&bars.done);
     else abort_sh = 1;
+  } else if (warp == 10 && p.fuse) {
+    // ------------------------------------------------------------ L2 prefetch
+    // pulls this CTA's unshared K/V rows into L2 while the shared stage runs,
+    // so the fused epilogue reads them from L2
+    const int TW = p.T * p.W, nb = 256 / G, j0 = row0 / G, nl = p.n_live[r];
+    for (int i = lane; i < nb * p.L; i += 32) {
+      const int jj = i / p.L, u = i - jj * p.L;
+      const int j = j0 + jj;
+      if (j >= nl) continue;
+      const int sl = __ldg(p.slot_table + ((size_t)r * p.W + j) * p.T + u);
+      if (sl < 0 || sl >= TW) continue;
+      const size_t e = (((size_t)r * TW + sl) * p.Hkv + g) * 128;
+      bulk_prefetch_l2(p.uk + e, 256);
+      bulk_prefetch_l2(p.uv + e, 256);
+    }
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax rows
     const int t = warp >> 2;                       // tile
@@ -405,36 +593,44 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     if (ok && !warp_wait(&bars.done, 0)) ok = false;
     if (!ok) abort_sh = 1;
     const int row = row0 + t * 128 + row_in_tile;
-    // O_t leaves through shared memory (the K/V ring is idle once every MMA
-    // is done): each thread puts its row there, 16-byte chunks swizzled by
-    // the row, then each warp stores whole 512-byte rows, coalesced
-    unsigned char* stage = sm + kOffKV + (uint32_t)t * (128u * 512u);
-    if (ok) {
-      fence_after_sync();
+    if (p.fuse) {   // unshared stage + merge here; the K/V ring is idle now
+      if (ok) {
+        fence_after_sync();
+        float* ps = reinterpret_cast<float*>(sm + kOffKV + (uint32_t)t * (128u * 512u)) + row_in_tile;
+        fused_row(p, r, g, row, sm + kOffQ + t * kTileBytes, row_in_tile, tO, true, m_used, l, sc, ps);
+      }
+    } else {
+      // O_t leaves through shared memory (the K/V ring is idle once every MMA
+      // is done): each thread puts its row there, 16-byte chunks swizzled by
+      // the row, then each warp stores whole 512-byte rows, coalesced
+      unsigned char* stage = sm + kOffKV + (uint32_t)t * (128u * 512u);
+      if (ok) {
+        fence_after_sync();
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float v[32];
-        tmem_ld32(tO + q * 32, v);
+        for (int q = 0; q < 4; ++q) {
+          float v[32];
+          tmem_ld32(tO + q * 32, v);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int chunk = q * 8 + i;
-          *reinterpret_cast<float4*>(stage + row_in_tile * 512 + ((chunk ^ (row_in_tile & 7)) << 4)) =
-              make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          for (int i = 0; i < 8; ++i) {
+            const int chunk = q * 8 + i;
+            *reinterpret_cast<float4*>(stage + row_in_tile * 512 + ((chunk ^ (row_in_tile & 7)) << 4)) =
+                make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
         }
       }
-    }
-    named_bar(1 + t, 128);   // the tile's four warps; every one of them arrives, ok or not
-    if (ok) {
-      for (int rr = warp & 3; rr < 128; rr += 4) {
-        const int grow = row0 + t * 128 + rr;
-        if (grow < p.rows) {
-          const float4 v = *reinterpret_cast<const float4*>(stage + rr * 512 + ((lane ^ (rr & 7)) << 4));
-          reinterpret_cast<float4*>(p.po + (prow_base + grow) * 128)[lane] = v;
+      named_bar(1 + t, 128);   // the tile's four warps; every one of them arrives, ok or not
+      if (ok) {
+        for (int rr = warp & 3; rr < 128; rr += 4) {
+          const int grow = row0 + t * 128 + rr;
+          if (grow < p.rows) {
+            const float4 v = *reinterpret_cast<const float4*>(stage + rr * 512 + ((lane ^ (rr & 7)) << 4));
+            reinterpret_cast<float4*>(p.po + (prow_base + grow) * 128)[lane] = v;
+          }
         }
-      }
-      if (row < p.rows) {
-        p.pm[prow_base + row] = m_used;
-        p.pl[prow_base + row] = l;
+        if (row < p.rows) {
+          p.pm[prow_base + row] = m_used;
+          p.pl[prow_base + row] = l;
+        }
       }
     }
   }
@@ -485,6 +681,17 @@ bd_kv_e4m3_to_bf16_kernel(const uint8_t* __restrict__ k8, const uint8_t* __restr
 bool attn_tc_supported(int q_dtype, int kv_dtype, int d, int G) {
   return q_dtype == BEAMDEC_BF16 && (kv_dtype == BEAMDEC_BF16 || kv_dtype == BEAMDEC_E4M3) &&
          d == 128 && G >= 1 && G <= 16 && (128 % G) == 0;
+}
+
+// The merge runs in the shared stage's epilogue when the whole prompt is one
+// split (every query row's shared partial stays in its CTA), the KV is bf16,
+// the unshared tokens fit the epilogue's scratch and the rows are 16-byte
+// aligned for vector loads and stores.
+bool attn_tc_fused(const AttnArgs& a, const AttnPlan& pl) {
+  const auto al16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
+  return pl.tensor_core && pl.n_split == 1 && a.kv_dtype == BEAMDEC_BF16 && a.out_dtype == BEAMDEC_BF16 &&
+         a.d == 128 && a.step + 1 <= 64 && al16(a.q) && al16(a.unshared_k) && al16(a.unshared_v) &&
+         al16(a.out);
 }
 
 int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t stream) {
@@ -549,6 +756,14 @@ int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t st
   AttnPartials part = attn_partials(a.ws, a.R, a.W, a.Hq, a.Hkv, a.d, pl.n_split);
   p.pm = part.m; p.pl = part.l; p.po = part.o;
   p.hdr = reinterpret_cast<WsHeader*>(a.ws);
+  p.fuse = attn_tc_fused(a, pl) ? 1 : 0;
+  p.L = a.step + 1;
+  p.T = a.T;
+  p.slot_table = a.slot_table;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.uk = static_cast<const __nv_bfloat16*>(a.unshared_k);
+  p.uv = static_cast<const __nv_bfloat16*>(a.unshared_v);
+  p.out = static_cast<__nv_bfloat16*>(a.out);
   dim3 grid((p.rows + 255) / 256, a.Hkv * pl.n_split, a.R);
   prof_begin(kKAttnTc, stream);
   bd_attn_shared_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qm, km, vm, p);

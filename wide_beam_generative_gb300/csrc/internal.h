@@ -83,6 +83,7 @@ size_t attn_workspace_bytes(int R, int W, int Hq, int Hkv, int d, const AttnPlan
 int launch_attn_shared_simt(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 bool attn_tc_supported(int q_dtype, int kv_dtype, int d, int G);
+bool attn_tc_fused(const AttnArgs& a, const AttnPlan& p);   // merge inside the shared stage
 
 // ---- LM head (lmhead.cu) ------------------------------------------------------
 size_t lmhead_workspace_bytes(int rows, int V);
