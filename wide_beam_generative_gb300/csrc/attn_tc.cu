@@ -220,6 +220,9 @@ __device__ __forceinline__ size_t out_row(const TcParams& p, int r, int g, int r
 // come from this CTA's shared stage; otherwise the prompt is empty.  The
 // query row comes from the CTA's swizzled Q tile, or from global memory
 // when qtile is null.  ps: scratch in shared memory, stride 128 words.
+// The epilogue runs once per CTA, so its instructions are fetched cold: one
+// token's loads at a time (a small body) measured faster than unrolled
+// batches of tokens, and than half-warps sharing rows with shuffles.
 __device__ __forceinline__ void fused_row(const TcParams& p, int r, int g, int row,
                                          const unsigned char* qtile, int rit, uint32_t tO,
                                          bool have_o, float m_used, float l, float sc, float* ps) {
@@ -231,55 +234,38 @@ __device__ __forceinline__ void fused_row(const TcParams& p, int r, int g, int r
   float M = shared_ok ? m_used : -INFINITY;
   const size_t qoff = in ? out_row(p, r, g, row) : 0;
   int* pslot = reinterpret_cast<int*>(ps + (size_t)L * 128);
-  // the beam's slots, all loads in one round
   for (int u = 0; u < L; ++u) {
     int sl = live ? __ldg(p.slot_table + ((size_t)r * p.W + j) * p.T + u) : -1;
     if (live && (sl < 0 || sl >= TW)) {
       set_status(p.hdr, BEAMDEC_ERR_DEVICE_CHECK);
       sl = -1;
     }
+    float s = -INFINITY;
+    if (sl >= 0) {
+      const uint4* kr = reinterpret_cast<const uint4*>(p.uk + (((size_t)r * TW + sl) * p.Hkv + g) * 128);
+      uint4 kw[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) kw[c] = __ldg(kr + c);
+      float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 qw = qtile ? *reinterpret_cast<const uint4*>(qtile + (c >> 3) * kHalfBytes + rit * 128 +
+                                                                (((c & 7) ^ (rit & 7)) << 4))
+                               : __ldg(reinterpret_cast<const uint4*>(p.q + qoff) + c);
+        d0 = fmaf(bf_lo(qw.x), bf_lo(kw[c].x), d0);
+        d1 = fmaf(bf_hi(qw.x), bf_hi(kw[c].x), d1);
+        d0 = fmaf(bf_lo(qw.y), bf_lo(kw[c].y), d0);
+        d1 = fmaf(bf_hi(qw.y), bf_hi(kw[c].y), d1);
+        d0 = fmaf(bf_lo(qw.z), bf_lo(kw[c].z), d0);
+        d1 = fmaf(bf_hi(qw.z), bf_hi(kw[c].z), d1);
+        d0 = fmaf(bf_lo(qw.w), bf_lo(kw[c].w), d0);
+        d1 = fmaf(bf_hi(qw.w), bf_hi(kw[c].w), d1);
+      }
+      s = (d0 + d1) * sc;
+    }
+    ps[u * 128] = s;
     pslot[u * 128] = sl;
-  }
-  const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-  auto kv_row = [&](const __nv_bfloat16* base, int sl) {
-    return reinterpret_cast<const uint4*>(base + (((size_t)r * TW + (sl >= 0 ? sl : 0)) * p.Hkv + g) * 128);
-  };
-  // scores, the K rows of two tokens per round of loads
-  for (int u0 = 0; u0 < L; u0 += 2) {
-    const int sl0 = pslot[u0 * 128];
-    const int sl1 = u0 + 1 < L ? pslot[(u0 + 1) * 128] : -1;
-    const uint4* k0p = kv_row(p.uk, sl0);
-    const uint4* k1p = kv_row(p.uk, sl1);
-    uint4 k0[16], k1[16];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) k0[c] = sl0 >= 0 ? __ldg(k0p + c) : z4;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) k1[c] = sl1 >= 0 ? __ldg(k1p + c) : z4;
-    float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const uint4 qw = qtile ? *reinterpret_cast<const uint4*>(qtile + (c >> 3) * kHalfBytes + rit * 128 +
-                                                              (((c & 7) ^ (rit & 7)) << 4))
-                             : __ldg(reinterpret_cast<const uint4*>(p.q + qoff) + c);
-      const float q0 = bf_lo(qw.x), q1 = bf_hi(qw.x), q2 = bf_lo(qw.y), q3 = bf_hi(qw.y);
-      const float q4 = bf_lo(qw.z), q5 = bf_hi(qw.z), q6 = bf_lo(qw.w), q7 = bf_hi(qw.w);
-      a0 = fmaf(q0, bf_lo(k0[c].x), a0); b0 = fmaf(q1, bf_hi(k0[c].x), b0);
-      a0 = fmaf(q2, bf_lo(k0[c].y), a0); b0 = fmaf(q3, bf_hi(k0[c].y), b0);
-      a0 = fmaf(q4, bf_lo(k0[c].z), a0); b0 = fmaf(q5, bf_hi(k0[c].z), b0);
-      a0 = fmaf(q6, bf_lo(k0[c].w), a0); b0 = fmaf(q7, bf_hi(k0[c].w), b0);
-      a1 = fmaf(q0, bf_lo(k1[c].x), a1); b1 = fmaf(q1, bf_hi(k1[c].x), b1);
-      a1 = fmaf(q2, bf_lo(k1[c].y), a1); b1 = fmaf(q3, bf_hi(k1[c].y), b1);
-      a1 = fmaf(q4, bf_lo(k1[c].z), a1); b1 = fmaf(q5, bf_hi(k1[c].z), b1);
-      a1 = fmaf(q6, bf_lo(k1[c].w), a1); b1 = fmaf(q7, bf_hi(k1[c].w), b1);
-    }
-    const float s0 = sl0 >= 0 ? (a0 + b0) * sc : -INFINITY;
-    ps[u0 * 128] = s0;
-    M = fmaxf(M, s0);
-    if (u0 + 1 < L) {
-      const float s1 = sl1 >= 0 ? (a1 + b1) * sc : -INFINITY;
-      ps[(u0 + 1) * 128] = s1;
-      M = fmaxf(M, s1);
-    }
+    M = fmaxf(M, s);
   }
   const float a = shared_ok ? ex2(m_used - M) : 0.f;
   float Ls = shared_ok ? l * a : 0.f;
@@ -295,31 +281,24 @@ __device__ __forceinline__ void fused_row(const TcParams& p, int r, int g, int r
     if (have_o) tmem_ld32(tO + q4 * 32, o);
 #pragma unroll
     for (int i = 0; i < 32; ++i) o[i] = shared_ok ? o[i] * a : 0.f;
-    for (int u0 = 0; u0 < L; u0 += 4) {   // the V chunks of four tokens per round of loads
-      uint4 vw[4][4];
-      float wt[4];
+    for (int u = 0; u < L; ++u) {
+      const int sl = pslot[u * 128];
+      if (sl < 0) continue;
+      const float w = ps[u * 128];
+      const uint4* vr = reinterpret_cast<const uint4*>(p.uv + (((size_t)r * TW + sl) * p.Hkv + g) * 128 + q4 * 32);
+      uint4 vw[4];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int sl = u0 + x < L ? pslot[(u0 + x) * 128] : -1;
-        wt[x] = sl >= 0 ? ps[(u0 + x) * 128] : 0.f;
-        const uint4* vp = kv_row(p.uv, sl) + q4 * 4;
+      for (int c = 0; c < 4; ++c) vw[c] = __ldg(vr + c);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) vw[x][c] = sl >= 0 ? __ldg(vp + c) : z4;
-      }
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const float w = wt[x];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          o[8 * c + 0] = fmaf(w, bf_lo(vw[x][c].x), o[8 * c + 0]);
-          o[8 * c + 1] = fmaf(w, bf_hi(vw[x][c].x), o[8 * c + 1]);
-          o[8 * c + 2] = fmaf(w, bf_lo(vw[x][c].y), o[8 * c + 2]);
-          o[8 * c + 3] = fmaf(w, bf_hi(vw[x][c].y), o[8 * c + 3]);
-          o[8 * c + 4] = fmaf(w, bf_lo(vw[x][c].z), o[8 * c + 4]);
-          o[8 * c + 5] = fmaf(w, bf_hi(vw[x][c].z), o[8 * c + 5]);
-          o[8 * c + 6] = fmaf(w, bf_lo(vw[x][c].w), o[8 * c + 6]);
-          o[8 * c + 7] = fmaf(w, bf_hi(vw[x][c].w), o[8 * c + 7]);
-        }
+      for (int c = 0; c < 4; ++c) {
+        o[8 * c + 0] = fmaf(w, bf_lo(vw[c].x), o[8 * c + 0]);
+        o[8 * c + 1] = fmaf(w, bf_hi(vw[c].x), o[8 * c + 1]);
+        o[8 * c + 2] = fmaf(w, bf_lo(vw[c].y), o[8 * c + 2]);
+        o[8 * c + 3] = fmaf(w, bf_hi(vw[c].y), o[8 * c + 3]);
+        o[8 * c + 4] = fmaf(w, bf_lo(vw[c].z), o[8 * c + 4]);
+        o[8 * c + 5] = fmaf(w, bf_hi(vw[c].z), o[8 * c + 5]);
+        o[8 * c + 6] = fmaf(w, bf_lo(vw[c].w), o[8 * c + 6]);
+        o[8 * c + 7] = fmaf(w, bf_hi(vw[c].w), o[8 * c + 7]);
       }
     }
     if (in) {
