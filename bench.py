@@ -213,6 +213,22 @@ class Step:
         return int(self.state["n_live"].sum().item())
 
 
+class L2Flush:
+    """Between timed steps: write a buffer larger than L2 (no input of the
+    previous step stays cached), then read another one, so that the lines
+    left in L2 are clean and the timed work does not pay the write-back of
+    the flush buffer."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.acc = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.acc)
+
+
 def algorithmic(wl, rows, kernel):
     """Algorithmic bytes or flops of one launch of `kernel` at this step."""
     G = wl.G
@@ -308,10 +324,10 @@ def gpu_arm(args, ws, rank, local):
                        list(wl.prompt_lens[:1]) * args.requests)
     step = Step(wl, dev)
     rows = step.rows()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step.run()
     torch.cuda.synchronize()
     assert bd.read_status(step.ws_sel) == 0 and bd.read_status(step.ws_att) == 0
@@ -322,7 +338,7 @@ def gpu_arm(args, ws, rank, local):
     # events would slow down)
     bd.profile_enable(True)
     for _ in range(args.steps):
-        flush.zero_()
+        flush()
         step.run()
     torch.cuda.synchronize()
     bd.profile_enable(False)
@@ -337,7 +353,7 @@ def gpu_arm(args, ws, rank, local):
     torch.cuda.synchronize()
     bd.profile_enable(True, kernels=[dom_name])   # the roofline kernel, timed live
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
         step.run()
         ev[i][1].record(stream)
@@ -397,7 +413,9 @@ def gpu_arm(args, ws, rank, local):
         "config": {"workload": f"{wl.name}: R{wl.R} P{int(synth.prompt_lens(wl).max())} Hq{wl.Hq} Hkv{wl.Hkv} "
                                f"d{wl.d} W{wl.W} K{wl.K} V{wl.V} SID {wl.levels}x{wl.C} "
                                f"catalog {wl.n_items} step {step.step + 1}/{wl.T}",
-                   "rows_per_step_per_gpu": rows, "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MB write) before each step",
+                   "rows_per_step_per_gpu": rows, "l2": f"flushed before each step: a {L2_FLUSH_BYTES >> 20} MB write, then a "
+                         f"{L2_FLUSH_BYTES >> 20} MB read so that no dirty line of the flush is left to "
+                         f"write back inside the timed step",
                    "parallelism": f"request-sharded replicas x{ws}"},
         "roofline": roof, "step_roofline": step_roof, "kernels": kernels,
         "kernels_note": "per-kernel event times from a pass of the same steps just before the timed "
@@ -439,7 +457,7 @@ def e2e_arm(step, args, ws, flush):
     n = max(1, min(args.steps, 10))
     times = []
     for _ in range(n):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         one()
@@ -488,12 +506,12 @@ def lmhead_arm(step, args, flush, H=2048):
     res = {"hidden": H, "rows": rows, "vocab": V}
     for name, fn in (("fused_us", fused), ("materialised_us", materialised), ("head_gemm_us", head_only)):
         for _ in range(3):
-            flush.zero_()
+            flush()
             fn()
         n = max(1, min(args.steps, 10))
         times = []
         for _ in range(n):
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             fn()
@@ -531,7 +549,7 @@ def dense_arm(step, args, flush):
         for t in range(T):
             lse = bd.beam_select(logits[t], st["cum"], st["node"], st["n_live"], st["slot"], trie, t, t,
                                  wl.K, ws=step.ws_sel)["lse_out"]
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             o = bd.beam_select(logits[t], st["cum"], st["node"], st["n_live"], st["slot"], trie, t, t, wl.K,
@@ -607,12 +625,12 @@ def gumbel_arm(step, args, flush):
     res = {}
     for name, temp in (("deterministic", 0.0), ("temperature_1", 1.0)):
         for _ in range(3):
-            flush.zero_()
+            flush()
             sel(temp)
         n = max(1, min(args.steps, 10))
         times = []
         for _ in range(n):
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             sel(temp)
@@ -637,14 +655,14 @@ def chain_arm(step, args, flush):
                         step.maxp, a0["unshared_k"], a0["unshared_v"], step.trie, wl.K,
                         k_scale=a0["k_scale"], v_scale=a0["v_scale"])
     for _ in range(3):
-        flush.zero_()
+        flush()
         ch.replay()
     torch.cuda.synchronize()
     n = max(1, min(args.steps, 10))
     times = []
     stream = torch.cuda.current_stream()
     for _ in range(n):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         ch.replay()

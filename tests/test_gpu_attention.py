@@ -191,3 +191,34 @@ def test_fused_merge_bad_slot_sets_device_check(gpu_lib):
                         a["unshared_k"], a["unshared_v"], slot.to(DEV),
                         torch.tensor([wl.W], dtype=torch.int32, device=DEV), 1, ws=ws)
     assert bd.read_status(ws) == bd.ERR_DEVICE_CHECK
+
+
+@pytest.mark.parametrize("G,W,plens", [(1, 300, [128, 77]), (4, 70, [100, 128]), (8, 33, [128, 1]),
+                                       (16, 20, [64, 128])])
+def test_fused_merge_group_sizes(gpu_lib, G, W, plens):
+    """Fused epilogue at every supported GQA group size, partial tiles and a
+    one-key prompt (prompts of at most 128 keys: one split)."""
+    wl = synth.WORKLOADS["qwen06b"].scaled(name="fusedg", R=len(plens), prompt_lens=plens, Hq=2 * G, Hkv=2,
+                                           W=W, T=3)
+    res = {}
+
+    def run():
+        res["v"] = _run(wl, 2, [W, max(1, W - 7)])
+    assert _merge_launches(run) == 0
+    got, want, _ = res["v"]
+    _check(wl, got, want, out_rounding=True)
+    assert np.all(got[1, max(1, W - 7):] == 0)
+
+
+def test_fused_merge_token_limit(gpu_lib):
+    """64 unshared tokens per beam are merged in the epilogue (its scratch
+    holds 64); 65 go through the merge kernel; both against the oracle."""
+    wl = synth.WORKLOADS["qwen06b"].scaled(name="fusedl", R=1, prompt_lens=[100], W=40, T=65)
+    for step, launches in ((63, 0), (64, 1)):
+        res = {}
+
+        def run():
+            res["v"] = _run(wl, step, [40])
+        assert _merge_launches(run) == launches
+        got, want, _ = res["v"]
+        _check(wl, got, want)

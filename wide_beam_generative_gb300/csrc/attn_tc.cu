@@ -65,6 +65,9 @@ constexpr uint32_t kOffKV = 2 * kTileBytes;      // kSlots tiles
 constexpr uint32_t kSmemBytes = kOffKV + kSlots * kTileBytes + 1024;
 constexpr uint32_t kTmemCols = 512;              // S0 O0 S1 O1
 constexpr float kRescale = 8.f;                  // log2 headroom before O is rescaled
+// unshared tokens the fused epilogue's scratch holds: a score and a slot per
+// token for each of a tile's 128 rows, in the tile's 64 KB of the idle ring
+constexpr int kFusedMaxL = 64;
 
 // MN-major B operand (V, d contiguous): the leading byte offset is the stride
 // between the two 64-column swizzle atoms along d (the two 16 KB halves), the
@@ -669,7 +672,7 @@ bool attn_tc_supported(int q_dtype, int kv_dtype, int d, int G) {
 bool attn_tc_fused(const AttnArgs& a, const AttnPlan& pl) {
   const auto al16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
   return pl.tensor_core && pl.n_split == 1 && a.kv_dtype == BEAMDEC_BF16 && a.out_dtype == BEAMDEC_BF16 &&
-         a.d == 128 && a.step + 1 <= 64 && al16(a.q) && al16(a.unshared_k) && al16(a.unshared_v) &&
+         a.d == 128 && a.step + 1 <= kFusedMaxL && al16(a.q) && al16(a.unshared_k) && al16(a.unshared_v) &&
          al16(a.out);
 }
 
