@@ -336,7 +336,8 @@ int beam_select_static(const float* logits, int64_t row_stride, const float* lse
 
 /*
  * Workspace bytes for beam_attn_decode (partial (max, sum, output) triples of
- * the shared stage, one per prompt split and query row).
+ * the shared stage, one per prompt split and query row; sized for the split
+ * path even when the merge runs inside the shared stage).
  */
 int beam_attn_workspace_size(int R, int W, int Hq, int Hkv, int d, int max_prompt_len,
                              int kv_dtype, size_t* bytes);
@@ -375,7 +376,10 @@ int beam_attn_workspace_size(int R, int W, int Hq, int Hkv, int d, int max_promp
  * F32/F32/F32, BF16/BF16/BF16, BF16/E4M3/BF16.  BF16 queries with d = 128
  * and a group size dividing 128 take the tensor-core shared stage (fp8 KV is
  * first dequantised to bf16 in the workspace); other shapes run it on CUDA
- * cores.
+ * cores.  When that stage covers every prompt in one split (bf16 KV, at most
+ * 64 unshared tokens, q / unshared K, V / out 16-byte aligned), the unshared
+ * stage and the merge run in its epilogue and the partials never leave the
+ * kernel; otherwise a merge kernel reads them from the workspace.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  */
 int beam_attn_decode(const void* q, const void* shared_k, const void* shared_v,
