@@ -429,45 +429,93 @@ def gpu_arm(args, ws, rank, local):
 
 
 def e2e_arm(step, args, ws, flush):
+    """Steps through the public API from pinned host buffers: every step
+    copies its inputs (logits, queries, beam state) to the device, runs the
+    selection and the attention, and reads the selection's outputs and the
+    attention output back.  Timed two ways: one step at a time (serial), and
+    as a serving loop that copies step i + 1's inputs on a second stream
+    into a second set of device buffers while step i computes (pipelined;
+    the value).  Every step's copies stay inside the timed region."""
     wl, dev = step.wl, step.dev
     s = step.state
     host = {"logits": step.logits.cpu().pin_memory(), "q": step.attn["q"].cpu().pin_memory()}
     for k in ("cum", "node", "n_live", "slot"):
         host[k] = s[k].cpu().pin_memory()
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    bufs = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
     outs = ["tokens", "parents", "cum_out", "node_out", "n_live_out", "slot_out"]
     host_out = {k: torch.empty_like(step.out_sel[k], device="cpu").pin_memory() for k in outs}
     host_att = torch.empty_like(step.out_att, device="cpu").pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values()) + host_att.numel() * host_att.element_size()
     stream = torch.cuda.current_stream()
+    copy_stream = torch.cuda.Stream(device=dev)
 
-    def one():
+    def h2d_into(b):
         for k, v in host.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        st = dict(cum=dev_in["cum"], node=dev_in["node"], n_live=dev_in["n_live"], slot=dev_in["slot"])
-        step.run(logits=dev_in["logits"], q=dev_in["q"], state=st)
+            bufs[b][k].copy_(v, non_blocking=True)
+
+    def compute_from(b):
+        d = bufs[b]
+        st = dict(cum=d["cum"], node=d["node"], n_live=d["n_live"], slot=d["slot"])
+        step.run(logits=d["logits"], q=d["q"], state=st)
         for k in outs:
             host_out[k].copy_(step.out_sel[k], non_blocking=True)
         host_att.copy_(step.out_att, non_blocking=True)
 
+    def serial():
+        h2d_into(0)
+        compute_from(0)
+
+    def pipelined(n):
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
+        consumed = [torch.cuda.Event(), torch.cuda.Event()]
+        copy_stream.wait_stream(stream)
+        with torch.cuda.stream(copy_stream):
+            h2d_into(0)
+            copied[0].record(copy_stream)
+        for i in range(n):
+            b = i & 1
+            if i + 1 < n:
+                nb = b ^ 1
+                with torch.cuda.stream(copy_stream):
+                    if i >= 1:
+                        copy_stream.wait_event(consumed[nb])   # step i - 1 is done with it
+                    h2d_into(nb)
+                    copied[nb].record(copy_stream)
+            stream.wait_event(copied[b])
+            compute_from(b)
+            consumed[b].record(stream)
+        stream.wait_stream(copy_stream)
+
     for _ in range(max(1, min(args.warmup, 3))):
-        one()
+        serial()
     torch.cuda.synchronize()
-    n = max(1, min(args.steps, 10))
+    n = max(2, min(args.steps, 10))
     times = []
     for _ in range(n):
         flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        one()
-        b.record(stream)
+        serial()
+        e.record(stream)
         torch.cuda.synchronize()
-        times.append(a.elapsed_time(b))
-    ms = max_over_ranks(sum(times) / n, ws)
+        times.append(a.elapsed_time(e))
+    ms_serial = max_over_ranks(sum(times) / n, ws)
+    pipelined(2)
+    torch.cuda.synchronize()
+    flush()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    pipelined(n)
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(e) / n, ws)
     rows = step.rows()
     return {"value": round(rows * ws / (ms / 1e3), 1), "unit": "beam-rows/s",
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 3)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 3),
+            "mode": f"pipelined over {n} steps (step i + 1's inputs copied while step i computes)",
+            "serial_ms_per_step": round(ms_serial, 3),
+            "serial_value": round(rows * ws / (ms_serial / 1e3), 1)}
 
 
 def lmhead_arm(step, args, flush, H=2048):
