@@ -219,10 +219,12 @@ def run_chain_own_lse(wl, steps=None, items=None, temperature=0.0, seed=0, dense
     selection runs in the one-launch stream kernel) against the oracle's own
     float64 chain.  Each side carries its own state.  Per step: log-sum-exp
     within 1e-5 of float64; the selected (parent, token, score) rows equal the
-    oracle's, except that candidates whose scores lie within 4e-5 of the cut
-    may trade places (the two sides round their normalisers independently).
-    After such a trade the states differ, so later steps are not compared.
-    Returns the number of steps compared exactly."""
+    oracle's, except where the two sides' independently rounded normalisers
+    reorder near-ties: candidates whose scores lie within 4e-5 of the cut may
+    trade places with ones outside, and two selected candidates whose scores
+    differ by less than 4e-5 may swap ranks.  After such a difference the
+    states differ, so later steps are not compared.  Returns the number of
+    steps compared exactly."""
     from wide_beam_generative_gb300 import beamdec as bd
     W, K, R, T = wl.W, wl.K, wl.R, wl.T
     steps = T if steps is None else steps
@@ -269,10 +271,16 @@ def run_chain_own_lse(wl, steps=None, items=None, temperature=0.0, seed=0, dense
             for key in g_set ^ o_set:
                 if key in lookup:
                     assert abs(lookup[key] - cut) < 4e-5
-            # rows outside the traded band keep their order
-            band = np.abs(o_s - cut) < 4e-5
-            keep = ~band
-            assert np.array_equal(g["parents"][r, :n][keep], ref["parents"][r, :n][keep])
+            # the GPU's order of the selected candidates inverts no pair
+            # whose oracle scores differ by 4e-5 or more
+            # (a candidate only the GPU selected stands in with its own
+            # score, which must lie near the cut as well)
+            g_lookup = {(p, tk): sc for p, tk, sc in zip(g["parents"][r, :n], g["tokens"][r, :n], g_s)}
+            for key in g_set - o_set:
+                assert abs(g_lookup[key] - cut) < 6e-5
+            o_score = np.array([lookup.get(key, g_lookup[key])
+                                for key in zip(g["parents"][r, :n], g["tokens"][r, :n])])
+            assert np.all(np.minimum.accumulate(o_score)[:-1] >= o_score[1:] - 4e-5)
         if traded:
             break
         exact += 1
