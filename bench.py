@@ -410,9 +410,7 @@ def gpu_arm(args, ws, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "step_us": round(ms_per_step * 1e3, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp32 logits / bf16 KV", "data": "synthetic (seeded; see synth)",
-        "config": {"workload": f"{wl.name}: R{wl.R} P{int(synth.prompt_lens(wl).max())} Hq{wl.Hq} Hkv{wl.Hkv} "
-                               f"d{wl.d} W{wl.W} K{wl.K} V{wl.V} SID {wl.levels}x{wl.C} "
-                               f"catalog {wl.n_items} step {step.step + 1}/{wl.T}",
+        "config": {"workload": workload_name(wl, step.step),
                    "rows_per_step_per_gpu": rows, "l2": f"flushed before each step: a {L2_FLUSH_BYTES >> 20} MB write, then a "
                          f"{L2_FLUSH_BYTES >> 20} MB read so that no dirty line of the flush is left to "
                          f"write back inside the timed step",
@@ -789,11 +787,18 @@ def cpu_baseline(wl, rows):
     t0 = time.time()
     done = cpu_run(wl, s)
     dt = time.time() - t0
-    return {"value": round(done / dt, 2), "unit": "beam-rows/s", "cores": os.cpu_count(),
+    return {"value": round(done / dt, 2), "unit": "beam-rows/s", "cores": len(os.sched_getaffinity(0)),
             "kind": "oracle", "seconds": round(dt, 2),
             "sample": f"{done} beams ({min(wl.R, (rows + wl.W - 1) // wl.W)} requests x up to {wl.W}) of the "
                       f"last decode step: float64 log-sum-exp + trie children + full sorts, float64 "
                       f"attention over prompt + ancestry (numpy; BLAS matmuls may use every core)"}
+
+
+def workload_name(wl, step_idx):
+    """The workload as both arms name it in `config`."""
+    return (f"{wl.name}: R{wl.R} P{int(synth.prompt_lens(wl).max())} Hq{wl.Hq} Hkv{wl.Hkv} "
+            f"d{wl.d} W{wl.W} K{wl.K} V{wl.V} SID {wl.levels}x{wl.C} "
+            f"catalog {wl.n_items} step {step_idx + 1}/{wl.T}")
 
 
 def reference_arm(args, ws, rank):
@@ -812,10 +817,10 @@ def reference_arm(args, ws, rank):
             "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; see synth)",
             "impl": "reference",
-            "config": {"workload": f"{wl.name} (bounded sample of {s['rows']} beams per step)",
-                       "requests": wl.R},
-            "cpu_baseline": {"value": v, "unit": "beam-rows/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": f"{s['rows']} beams of the last decode step"},
+            "config": {"workload": workload_name(wl, wl.T - 1),
+                       "sample": f"{s['rows']} of the step's beams per timed step (a bounded sample)"},
+            "cpu_baseline": {"value": v, "unit": "beam-rows/s", "cores": len(os.sched_getaffinity(0)),
+                             "kind": "oracle", "sample": f"{s['rows']} beams of the last decode step"},
             "e2e": {"value": v, "unit": "beam-rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
