@@ -271,7 +271,7 @@ def step_roofline(wl, rows, ms_per_step, kernels, pk):
     sel_bytes = rows * wl.V * 4
     flops = 4.0 * wl.Hkv * wl.W * wl.G * P.sum() * wl.d
     hbm = _peak_value(pk, "hbm_gbs", "hbm_GBs", "hbm") or FALLBACK_PEAKS["hbm_gbs"]
-    tc = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
+    tc = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops_sustained"]
     step_gbs = (attn_bytes + sel_bytes) / (ms_per_step / 1e3) / 1e9
     attn_us = sum(v["us_per_launch"] for k, v in kernels.items()
                   if k.startswith("bd_attn") or k == "bd_kv_e4m3_to_bf16_kernel")
