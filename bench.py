@@ -9,7 +9,9 @@ request has 512 live beams at trie level 2 and 3 unshared tokens per beam.
 One JSON line on rank 0.  `value` is beam rows per second (rows = live beams
 processed per step, summed over requests and ranks) with inputs resident in
 HBM; `e2e` is the same metric through the C ABI from pinned host buffers with
-the step's inputs copied in and its outputs copied out inside the timed region.
+every step's inputs copied in and its outputs copied out inside the timed
+region (as a serving loop: the next step's copy overlaps the current step's
+compute; the one-step-at-a-time figure is reported beside it).
 With --impl reference the CPU oracle is timed instead on a bounded sample.
 """
 import argparse
