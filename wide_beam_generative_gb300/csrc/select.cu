@@ -480,11 +480,29 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
     const int sh_next = shift - w;
     for (int i = tid; i < nb; i += kExpandThreads) sh.hist[i] = 0;
     __syncthreads();
-    for (int c0 = 0; c0 < n; c0 += kExpandThreads) {   // block-uniform trip count
-      const int i = c0 + tid;
-      const uint32_t k = i < n ? kc(i) : 0u;
-      const bool on = i < n && (shift == 32 || (k >> shift) == (prefix >> shift));
-      warp_hist_add(sh.hist, (k >> sh_next) & (nb - 1), on);
+    if (cached) {
+      for (int c0 = 0; c0 < n; c0 += kExpandThreads) {   // block-uniform trip count
+        const int i = c0 + tid;
+        const uint32_t k = i < n ? kcache[i] : 0u;
+        const bool on = i < n && (shift == 32 || (k >> shift) == (prefix >> shift));
+        warp_hist_add(sh.hist, (k >> sh_next) & (nb - 1), on);
+      }
+    } else {   // keys from the row again: four logits per thread in flight
+      for (int c0 = 0; c0 < n; c0 += 4 * kExpandThreads) {   // block-uniform trip count
+        float x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = c0 + u * kExpandThreads + tid;
+          x[u] = i < n ? __ldg(row + tok_of(i)) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = c0 + u * kExpandThreads + tid;
+          const uint32_t k = i < n ? score_key(x[u], tok_of(i)) : 0u;
+          const bool on = i < n && (shift == 32 || (k >> shift) == (prefix >> shift));
+          warp_hist_add(sh.hist, (k >> sh_next) & (nb - 1), on);
+        }
+      }
     }
     __syncthreads();
     if (tid < 32) warp_find_digit(sh.hist, nb, need, &sh.digit, &sh.below);
@@ -498,13 +516,31 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
   if (tid == 0) { sh.count = 0; sh.pool_base = atomicAdd(&st->total, a.K); }
   __syncthreads();
   const int base = sh.pool_base;
-  for (int c0 = 0; c0 < n; c0 += kExpandThreads) {   // block-uniform trip count
-    const int i = c0 + tid;
-    const uint32_t k = i < n ? kc(i) : 0u;
+  auto take_below = [&](int i, uint32_t k) {   // every key below the K-th goes to the pool
     const bool on = i < n && k < kth;
     const int pos = warp_reserve(&sh.count, on);
     if (on) pool[base + pos] = pool_key(k, b, i);
     if (gh) warp_hist_add(gh, (uint32_t)score_bin(ref, desc_key_value(k)), on);
+  };
+  if (cached) {
+    for (int c0 = 0; c0 < n; c0 += kExpandThreads) {   // block-uniform trip count
+      const int i = c0 + tid;
+      take_below(i, i < n ? kcache[i] : 0u);
+    }
+  } else {   // four logits per thread in flight, as in the radix passes
+    for (int c0 = 0; c0 < n; c0 += 4 * kExpandThreads) {   // block-uniform trip count
+      float x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = c0 + u * kExpandThreads + tid;
+        x[u] = i < n ? __ldg(row + tok_of(i)) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = c0 + u * kExpandThreads + tid;
+        take_below(i, i < n ? score_key(x[u], tok_of(i)) : 0u);
+      }
+    }
   }
   __syncthreads();
   const int n_less = sh.count;
