@@ -222,3 +222,19 @@ def test_fused_merge_token_limit(gpu_lib):
         assert _merge_launches(run) == launches
         got, want, _ = res["v"]
         _check(wl, got, want)
+
+
+def test_all_prompts_empty(gpu_lib):
+    """No prompt key in any request (max_prompt_len 0, no shared K/V): the
+    output is the softmax over the beams' unshared tokens alone."""
+    wl = synth.WORKLOADS["qwen06b"].scaled(name="noprompt", R=2, prompt_lens=[0, 0], W=24, T=3)
+    from wide_beam_generative_gb300 import beamdec as bd
+    a = synth.attention_inputs(wl, 2, device=DEV)
+    slot = _slots(wl, 2, [24, 10])
+    nl = torch.tensor([24, 10], dtype=torch.int32)
+    out = bd.beam_attn_decode(a["q"], None, None, a["prompt_offsets"], 0, a["unshared_k"], a["unshared_v"],
+                              slot.to(DEV), nl.to(DEV), 2)
+    inp = oracle_attn_inputs(a, a["q"], wl)
+    want = oatt.attention_decode(inp, slot.numpy(), nl.numpy(), 2)
+    _check(wl, out.double().cpu().numpy(), want, out_rounding=True)
+    assert np.all(out[1, 10:].float().cpu().numpy() == 0)

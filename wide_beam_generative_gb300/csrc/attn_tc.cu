@@ -691,8 +691,12 @@ int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t st
       return BEAMDEC_ERR_CUDA;
     attr_set[dev] = true;
   }
-  const void* kbase = a.shared_k;
-  const void* vbase = a.shared_v;
+  // with no prompt key at all (shared_rows = 0, K/V may be NULL) the K/V
+  // maps are never loaded from; they are encoded over the queries' memory,
+  // which holds at least one [Hkv][d] row, so that the encode sees a valid
+  // address
+  const void* kbase = a.shared_rows > 0 ? a.shared_k : a.q;
+  const void* vbase = a.shared_rows > 0 ? a.shared_v : a.q;
   if (a.kv_dtype == BEAMDEC_E4M3 && a.shared_rows > 0) {
     // dequantise the prompt KV once into the workspace (bf16, same layout)
     __nv_bfloat16* k16 = attn_kv16(a.ws, a.R, a.W, a.Hq, a.Hkv, a.d, pl.n_split);
