@@ -108,7 +108,12 @@ def _np_rng(seed: int, stream: int, sub: int = 0) -> np.random.Generator:
 
 def _torch_gen(seed: int, stream: int, sub: int, device) -> torch.Generator:
     g = torch.Generator(device=device)
-    g.manual_seed((seed * 1_000_003 + stream) * 65_537 + sub)
+    s = (seed * 1_000_003 + stream) * 65_537 + sub
+    if torch.device(device).type == "cpu":
+        # the CPU generator keeps only the low 32 bits of its seed, and `sub`
+        # carries the decode step above bit 31: fold the high half in
+        s = ((s & 0xFFFFFFFF) ^ (((s >> 32) * 0x9E3779B1) & 0xFFFFFFFF))
+    g.manual_seed(s)
     return g
 
 
