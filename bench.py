@@ -257,7 +257,7 @@ def algorithmic(wl, rows, kernel):
     return 0, "bytes"
 
 
-def step_roofline(wl, rows, ms_per_step, kernels, pk):
+def step_roofline(wl, rows, ms_per_step, kernels, pk, unique_slots=None):
     """The metric's second half: algorithmic HBM bytes of attention + selection
     per step (prompt KV counted once per request) over the step time, as a
     fraction of the HBM peak; and the attention alone against its binding
@@ -273,7 +273,9 @@ def step_roofline(wl, rows, ms_per_step, kernels, pk):
     sel_bytes = rows * wl.V * 4
     flops = 4.0 * wl.Hkv * wl.W * wl.G * P.sum() * wl.d
     hbm = _peak_value(pk, "hbm_gbs", "hbm_GBs", "hbm") or FALLBACK_PEAKS["hbm_gbs"]
-    tc = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops_sustained"]
+    # the attention kernels run on their own (each after the selection, with
+    # no other kernel beside them) for tens of microseconds: the burst peak
+    tc = _peak_value(pk, "bf16_tflops", "bf16_tflops_sustained") or FALLBACK_PEAKS["bf16_tflops"]
     step_gbs = (attn_bytes + sel_bytes) / (ms_per_step / 1e3) / 1e9
     attn_us = sum(v["us_per_launch"] for k, v in kernels.items()
                   if k.startswith("bd_attn") or k == "bd_kv_e4m3_to_bf16_kernel")
@@ -287,13 +289,28 @@ def step_roofline(wl, rows, ms_per_step, kernels, pk):
                             "roof_us": {"hbm": round(float(roof_hbm_us), 2), "tensor": round(float(roof_tc_us), 2)},
                             "binding": "tensor" if roof_tc_us > roof_hbm_us else "hbm",
                             "binding_frac": round(float(max(roof_hbm_us, roof_tc_us) / attn_us), 4),
-                            "tensor_peak_tflops": tc}
+                            "tensor_peak_tflops": tc, "tensor_peak": "bf16 burst (measured)"}
+        if unique_slots is not None:
+            # the conservative denominator: each distinct unshared K/V row the
+            # live beams reference counted once (beams share ancestry)
+            uniq = unique_slots * wl.Hkv * wl.d * 2 * b_kv
+            ub = shared + uniq + qo
+            out["attention"]["unique_slots"] = int(unique_slots)
+            out["attention"]["bytes_unique_slots"] = int(ub)
+            out["attention"]["hbm_frac_unique_slots"] = round(ub / (hbm * 1e9) * 1e6 / attn_us, 4)
     return out
 
 
-def read_traffic(kernel):
-    """dram bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current source of that kernel."""
+def workload_dtype(wl):
+    """The arithmetic types the step computes in for this workload."""
+    names = {synth.F32: "f32", synth.BF16: "bf16", synth.E4M3: "e4m3"}
+    return (f"f32 logits; {names[wl.q_dtype]} q / {names[wl.kv_dtype]} KV / {names[wl.out_dtype]} out, "
+            f"f32 accumulate")
+
+
+def read_traffic(kernel, workload):
+    """dram bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, if it was taken on the current source of that kernel."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
     if not os.path.exists(path):
@@ -309,9 +326,9 @@ def read_traffic(kernel):
     for line in open(path):
         f = line.strip().strip("|").split("|")
         f = [x.strip() for x in f]
-        if len(f) >= 4 and f[0] == kernel and f[2] == sha:
+        if len(f) >= 5 and f[0] == kernel and f[1] == workload and f[3] == sha:
             try:
-                return float(f[1])
+                return float(f[2])
             except ValueError:
                 return None
     return None
@@ -368,6 +385,13 @@ def gpu_arm(args, ws, rank, local):
     total_ms = max_over_ranks(sum(times), ws)
     ms_per_step = total_ms / args.steps
     value = rows * ws / (ms_per_step / 1e3)
+    srt = sorted(times)
+    dist = {"median_us": round(statistics.median(times) * 1e3, 2),
+            "p90_us": round(srt[min(len(srt) - 1, int(0.9 * len(srt)))] * 1e3, 2),
+            "min_us": round(srt[0] * 1e3, 2), "max_us": round(srt[-1] * 1e3, 2)}
+    # distinct unshared K/V rows the live beams' slot rows reference this step
+    so, nlo = step.out_sel["slot_out"], step.out_sel["n_live_out"].tolist()
+    unique_slots = sum(int(torch.unique(so[r, :nlo[r], :step.step + 1]).numel()) for r in range(wl.R))
     # launches of our kernels in the timed region: the same steps as the
     # breakdown pass launch the same kernels
     launches = sum(n for _, n in breakdown.values())
@@ -390,15 +414,15 @@ def gpu_arm(args, ws, rank, local):
         src = "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz"
     else:
         achieved = units / (kms / kn / 1e3) / 1e12
-        peak = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
-        roof = {"bound": "tensor", "unit": "TFLOP/s"}
+        peak = _peak_value(pk, "bf16_tflops", "bf16_tflops_sustained") or FALLBACK_PEAKS["bf16_tflops"]
+        roof = {"bound": "tensor", "unit": "TFLOP/s", "peak_kind": "bf16 burst"}
     roof.update(kernel=kname, achieved=round(achieved, 2), peak=peak, frac=round(achieved / peak, 4),
-                traffic=read_traffic(kname), peak_source=src,
+                traffic=read_traffic(kname, wl.name), peak_source=src,
                 algorithmic_per_launch=units, launch_us=round(kms / kn * 1e3, 2))
     kernels = {k: {"us_per_launch": round(ms / n * 1e3, 2), "launches": n,
                    "share": round(ms / max(1e-9, sum(x for x, _ in breakdown.values())), 4)}
                for k, (ms, n) in breakdown.items()}
-    step_roof = step_roofline(wl, rows, ms_per_step, kernels, pk)
+    step_roof = step_roofline(wl, rows, ms_per_step, kernels, pk, unique_slots=unique_slots)
 
     # end-to-end through the C ABI from pinned host buffers
     e2e = None if args.no_e2e else e2e_arm(step, args, ws, flush)
@@ -410,8 +434,9 @@ def gpu_arm(args, ws, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "beam-rows/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "step_us": round(ms_per_step * 1e3, 2), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp32 logits / bf16 KV", "data": "synthetic (seeded; see synth)",
+        "step_us": round(ms_per_step * 1e3, 2), "step_us_distribution": dist,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": workload_dtype(wl), "data": "synthetic (seeded; see synth)",
         "config": {"workload": workload_name(wl, step.step),
                    "rows_per_step_per_gpu": rows, "l2": f"flushed before each step: a {L2_FLUSH_BYTES >> 20} MB write, then a "
                          f"{L2_FLUSH_BYTES >> 20} MB read so that no dirty line of the flush is left to "
@@ -424,7 +449,8 @@ def gpu_arm(args, ws, rank, local):
         "lmhead_select": lmhead, "dense_trie": dense,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows or 4 * wl.W)
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows or 4 * wl.W,
+                                            one_thread_rows=max(1, (args.cpu_rows or 4 * wl.W) // 8))
     return line
 
 
@@ -784,16 +810,37 @@ def cpu_run(wl, s):
     return s["rows"]
 
 
-def cpu_baseline(wl, rows):
+def cpu_baseline(wl, rows, one_thread_rows=None):
     s = cpu_sample(wl, rows)
     t0 = time.time()
     done = cpu_run(wl, s)
     dt = time.time() - t0
-    return {"value": round(done / dt, 2), "unit": "beam-rows/s", "cores": len(os.sched_getaffinity(0)),
-            "kind": "oracle", "seconds": round(dt, 2),
-            "sample": f"{done} beams ({min(wl.R, (rows + wl.W - 1) // wl.W)} requests x up to {wl.W}) of the "
-                      f"last decode step: float64 log-sum-exp + trie children + full sorts, float64 "
-                      f"attention over prompt + ancestry (numpy; BLAS matmuls may use every core)"}
+    res = {"value": round(done / dt, 2), "unit": "beam-rows/s", "cores": len(os.sched_getaffinity(0)),
+           "kind": "oracle", "seconds": round(dt, 2),
+           "sample": f"{done} beams ({min(wl.R, (rows + wl.W - 1) // wl.W)} requests x up to {wl.W}) of the "
+                     f"last decode step: float64 log-sum-exp + trie children + full sorts, float64 "
+                     f"attention over prompt + ancestry (numpy; BLAS matmuls may use every core)"}
+    if one_thread_rows:
+        res["one_thread"] = cpu_baseline_one_thread(wl, one_thread_rows)
+    return res
+
+
+def cpu_baseline_one_thread(wl, rows):
+    """The same oracle step on one core: a child process pinned to one CPU
+    with every BLAS / OpenMP pool at one thread (set before numpy loads)."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cpu = sorted(os.sched_getaffinity(0))[0]
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-sample-only", str(rows), "--workload", wl.name,
+           "--pin-cpu", str(cpu)]
+    try:
+        p = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        line = [x for x in p.stdout.splitlines() if x.startswith("{")][-1]
+        return json.loads(line)
+    except Exception as e:   # the main figure stands without it
+        return {"unavailable": f"one-thread oracle run failed: {type(e).__name__}"}
 
 
 def workload_name(wl, step_idx):
@@ -843,7 +890,22 @@ def main():
     ap.add_argument("--lmhead-only", type=int, default=0, metavar="VOCAB",
                     help="profiling aid: run only the fused LM head (2048 rows, hidden 2048) over VOCAB "
                          "tokens, warm-up + 1 launch, and print its time")
+    ap.add_argument("--cpu-sample-only", type=int, default=0, metavar="ROWS",
+                    help="internal: time the oracle on ROWS beams of the workload and print one JSON object")
+    ap.add_argument("--pin-cpu", type=int, default=None, help="internal: run on this one CPU core")
     args = ap.parse_args()
+    if args.cpu_sample_only:
+        if args.pin_cpu is not None:
+            os.sched_setaffinity(0, {args.pin_cpu})
+        wl = synth.WORKLOADS[args.workload]
+        s = cpu_sample(wl, args.cpu_sample_only)
+        t0 = time.time()
+        done = cpu_run(wl, s)
+        dt = time.time() - t0
+        print(json.dumps({"value": round(done / dt, 2), "unit": "beam-rows/s",
+                          "cores": len(os.sched_getaffinity(0)), "threads": 1, "seconds": round(dt, 2),
+                          "sample": f"{done} beams of the last decode step"}))
+        return
     ws, rank, local = dist_setup()
     if args.lmhead_only:
         lmhead_only(args.lmhead_only)

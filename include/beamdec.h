@@ -37,6 +37,14 @@
  *   counters that must start at zero; the library keeps them consistent
  *   afterwards).  A workspace may be reused across calls on one stream;
  *   calls that run concurrently need separate workspaces.
+ * - Bounded waits: every device-side wait (grid barrier, mbarrier) gives up
+ *   after a fixed number of polls and records BEAMDEC_ERR_TIMEOUT.  Two
+ *   uint32 words of a workspace are test hooks of those waits, zero in normal
+ *   use (the library never writes them): bytes 12-15 replace the default
+ *   poll count when nonzero; bytes 16-19 (beam_select workspaces) add that
+ *   many arrivals to the grid barrier of the large-pool selection, which no
+ *   block ever supplies, so its waits run out.  Tests use them to reach the
+ *   timeout path without faulting or hanging a GPU.
  */
 #ifndef BEAMDEC_H
 #define BEAMDEC_H
@@ -299,6 +307,36 @@ int beam_select_gumbel(const float* logits, int64_t row_stride, const float* lse
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * beam_select_fixed_lse - the one-launch selection (the kernel beam_select
+ * runs when lse_in is NULL: every live row streamed for its log-sum-exp,
+ * then expanded and selected in the same launch) with the candidates scored
+ * against a caller-supplied normaliser.  "Generative recommendation design"
+ * §4.1.1 (the beam_width x top_k pool and the global top beam_width): the
+ * selection is a function of the float32 candidate scores, so a reference
+ * implementation that rounds its own normaliser can check this kernel's
+ * decisions bit for bit only when both sides score against the same float32
+ * value.
+ *   score_lse  [R][W] fp32 (device, required): candidate scores are
+ *              s = fl32(cum_in[b] + fl32(logit - score_lse[b])); read for
+ *              live rows only.
+ *   lse_out    still receives the kernel's OWN log-sum-exp of every live row
+ *              (NULL to skip), computed exactly as in beam_select.
+ *   temperature, seed  0 for deterministic top-k, or a positive temperature
+ *              for Gumbel top-k exactly as in beam_select_gumbel.
+ * Every other argument, output, limit and error is as for beam_select
+ * (lse_in does not exist here), and the workspace is the same size.
+ * Errors: INVALID_ARG also for a NULL score_lse or a temperature that is
+ * neither 0 nor valid for beam_select_gumbel.
+ */
+int beam_select_fixed_lse(const float* logits, int64_t row_stride, const float* score_lse,
+                          const float* cum_in, const int32_t* node_in, const int32_t* n_live_in,
+                          const int32_t* slot_in, const beamdec_trie* trie, int level, int step,
+                          int R, int W, int K, int V, int T, float temperature, uint64_t seed,
+                          int32_t* tokens, int32_t* parents, float* cum_out, float* lse_out,
+                          int32_t* node_out, int32_t* n_live_out, int32_t* slot_out,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * beam_select_static — beam_select without a caller-provided workspace.
  * The pages have no counterpart to this entry point; it serves callers of
  * this library that cannot allocate device memory: a plugin interface that
@@ -313,8 +351,11 @@ int beam_select_gumbel(const float* logits, int64_t row_stride, const float* lse
  * beam_select_workspace_size exceeds it are rejected with
  * BEAMDEC_ERR_UNSUPPORTED before anything is launched.  Nothing is allocated.
  * The first call on a device looks up the array's device address (with that
- * device current) and caches it: make that first call before any stream
- * capture.  All calls on a device share the array and it keeps the last
+ * device current) and caches it with the current context (a call under a
+ * different context looks it up again): make that first call before any
+ * stream capture.  Resetting the device (cudaDeviceReset) while the library
+ * stays loaded is not supported.  Arguments are checked before the array is
+ * touched, so a refused call writes nothing.  All calls on a device share the array and it keeps the last
  * call's contents; each call clears the status word and counters it needs on
  * its own stream first, so calls in stream order are independent, but calls
  * that overlap on the GPU (unordered streams) race on the array.  The status

@@ -146,3 +146,17 @@ def test_dense_trie_validation_before_any_device_call(L):
     assert L.beam_trie_make_dense(None, 0, None) == bd.ERR_INVALID_ARG
     assert L.beam_trie_drop_dense(None, 0) == bd.ERR_INVALID_ARG
     assert L.beam_trie_export_dense(None, 0, None, None) == bd.ERR_INVALID_ARG
+
+
+def test_fixed_lse_select_validates_on_host(L):
+    from wide_beam_generative_gb300 import beamdec as bd
+    head = [FAKE, 512]
+    rest = [FAKE, FAKE, FAKE, FAKE, None, 0, 0, 1, 8, 8, 512, 3]
+    outs = [FAKE, FAKE, FAKE, None, FAKE, FAKE, ctypes.c_void_p(0x2000), FAKE, 0, None]
+    # score_lse is required
+    assert L.beam_select_fixed_lse(*head, None, *rest, 0.0, 0, *outs) == bd.ERR_INVALID_ARG
+    # temperature 0 (deterministic) or a valid Gumbel temperature; nothing else
+    for t in (-1.0, float("nan"), float("inf"), 1e-40):
+        assert L.beam_select_fixed_lse(*head, FAKE, *rest, t, 0, *outs) == bd.ERR_INVALID_ARG, t
+    for t in (0.0, 0.7):   # valid: reaches the same shape checks as beam_select
+        assert L.beam_select_fixed_lse(*head, FAKE, *rest, t, 0, *outs) == bd.ERR_WORKSPACE

@@ -27,11 +27,39 @@ def test_step_roofline_counts_prompt_kv_once_per_request():
     assert out["attn_select_bytes"] == shared + unshared + qo + 2048 * 151936 * 4
     assert abs(out["attn_select_gbs"] - out["attn_select_bytes"] / 0.3e-3 / 1e9) < 0.1
     assert out["attention"]["us"] == 80.0 and out["attention"]["binding"] == "tensor"
-    # binding roof: the tensor time at the fallback sustained peak
-    assert abs(out["attention"]["roof_us"]["tensor"] - 68719476736 / 1.7e15 * 1e6) < 0.01
+    # binding roof: the tensor time at the bf16 burst peak (the attention
+    # kernels run alone for tens of microseconds); fallback 1.9 PFLOP/s here
+    assert abs(out["attention"]["roof_us"]["tensor"] - 68719476736 / 1.9e15 * 1e6) < 0.01
+    # the conservative denominator: distinct unshared rows instead of per-beam reads
+    out2 = bench.step_roofline(wl, 2048, 0.3, kernels, {}, unique_slots=1000)
+    assert out2["attention"]["bytes_unique_slots"] == shared + 1000 * 8 * 128 * 2 * 2 + qo
+
+
+def test_workload_dtype_names_each_workloads_types():
+    assert bench.workload_dtype(synth.WORKLOADS["onerec17b"]) == \
+        "f32 logits; bf16 q / bf16 KV / bf16 out, f32 accumulate"
+    assert bench.workload_dtype(synth.WORKLOADS["fp8kv"]).startswith("f32 logits; bf16 q / e4m3 KV")
+    assert bench.workload_dtype(synth.WORKLOADS["tiny"]).startswith("f32 logits; f32 q / f32 KV")
 
 
 def test_both_arms_name_the_workload_alike():
     wl = synth.WORKLOADS["onerec17b"]
     assert bench.workload_name(wl, wl.T - 1) == ("onerec17b: R4 P4096 Hq16 Hkv8 d128 W512 K512 V151936 "
                                                  "SID 3x8192 catalog 4000000 step 3/3")
+
+
+def test_traffic_rows_count_only_for_their_workload_and_source(tmp_path, monkeypatch):
+    import hashlib
+    csrc = tmp_path / "wide_beam_generative_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "select.cu").write_text("// kernel source\n")
+    sha = hashlib.sha256(b"// kernel source\n").hexdigest()[:12]
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "ncu_traffic.md").write_text(
+        "| kernel | workload | bytes per launch | source sha256[:12] | capture |\n|---|---|---|---|---|\n"
+        f"| bd_stream_select_kernel | onerec17b | 1234 | {sha} | x |\n"
+        "| bd_stream_select_kernel | fp8kv | 99 | 000000000000 | stale source |\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.read_traffic("bd_stream_select_kernel", "onerec17b") == 1234.0
+    assert bench.read_traffic("bd_stream_select_kernel", "openvocab") is None   # no row for it
+    assert bench.read_traffic("bd_stream_select_kernel", "fp8kv") is None       # taken on other source

@@ -3,11 +3,21 @@
 The graph holds the same launches as the eager calls, so every output of
 every step must equal the eager chain's bit for bit, on the first replay
 and on later ones (each replay restarts from one live beam per request).
+The graph is also tied to the oracle: replayed with every step's candidates
+scored against the oracle's float32 normalisers, each step's selection equals
+the oracle's chain bit for bit, and each step's attention output, computed
+over the slot rows the chain's own selection produced, matches the float64
+oracle within the bf16 tolerance on beams from every 256-row tile of the
+tensor-core shared stage.
 """
+import numpy as np
 import pytest
 import torch
 
 import synth
+from oracle import attention as oatt
+from oracle import select as osel
+from tests._helpers import ATOL_ATTN, build_tries, compare_select, oracle_attn_inputs
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -64,3 +74,54 @@ def test_graph_chain_equals_eager(gpu_lib, name):
             for k in ("tokens", "parents", "cum_out", "node_out", "n_live_out", "slot_out"):
                 assert torch.equal(chain.sel[t][k], o[k]), (rep, t, k)
             assert torch.equal(chain.out[t], y), (rep, t)
+
+
+def _tile_beams(wl):
+    """Beams whose query rows fall in every 256-row tile of the shared stage
+    (rows j*G .. j*G + G-1 of beam j): the first and last beam of each tile."""
+    per = max(1, 256 // wl.G)
+    beams = set()
+    for j0 in range(0, wl.W, per):
+        beams.update({j0, min(wl.W, j0 + per) - 1})
+    return sorted(beams)
+
+
+@pytest.mark.parametrize("name", ["qwen06b", "onerec17b"])
+def test_graph_chain_matches_oracle(gpu_lib, name):
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl = synth.WORKLOADS[name]
+    items = synth.catalog(wl)
+    trie, otr = build_tries(wl, items)
+    att = [synth.attention_inputs(wl, t, device=DEV) for t in range(wl.T)]
+    logits = [synth.logits(wl, t, device=DEV) for t in range(wl.T)]
+    lg_np = [lg.cpu().numpy() for lg in logits]
+    # the oracle's float64 normaliser of every row, rounded to float32
+    lse32 = [np.array([[osel.lse64(x[r, b]) for b in range(wl.W)] for r in range(wl.R)], np.float32)
+             for x in lg_np]
+    a0 = att[0]
+    chain = bd.DecodeChain(logits, [a["q"] for a in att], a0["shared_k"], a0["shared_v"],
+                           a0["prompt_offsets"], int(synth.prompt_lens(wl).max()), a0["unshared_k"],
+                           a0["unshared_v"], trie, wl.K, k_scale=a0["k_scale"], v_scale=a0["v_scale"],
+                           score_lse=[torch.from_numpy(x).to(DEV) for x in lse32])
+    chain.replay()
+    torch.cuda.synchronize()
+    assert chain.status() == (0, 0)
+    R, W, T = wl.R, wl.W, wl.T
+    o_cum, o_node = np.zeros((R, W), np.float32), np.zeros((R, W), np.int64)
+    o_nl, o_slot = np.ones(R, np.int32), np.full((R, W, T), -1, np.int32)
+    beams = _tile_beams(wl)
+    for t in range(T):
+        ref = osel.beam_select(lg_np[t], o_cum, o_node, o_nl, o_slot, otr, wl.token_base(), t, t, W, wl.K,
+                               lse32=lse32[t])
+        compare_select(chain.sel[t], ref, t, f"graph {name} step {t}")
+        o_cum, o_node, o_nl, o_slot = ref["cum_out"], ref["node_out"], ref["n_live_out"], ref["slot_out"]
+        # attention over the chain's slot rows (equal to the oracle's, checked above)
+        inp = oracle_attn_inputs(a0, att[t]["q"], wl)
+        todo = [(r, j) for r in range(R) for j in beams if j < int(o_nl[r])]
+        want = oatt.attention_decode(inp, o_slot, o_nl, t, beams=todo)
+        got = chain.out[t].double().cpu().numpy()
+        err = max(float(np.abs(got[r, j] - want[r, j]).max()) for r, j in todo)
+        assert err < ATOL_ATTN[wl.kv_dtype], (t, err)
+        dead = [(r, j) for r in range(R) for j in range(int(o_nl[r]), W)]
+        for r, j in dead[:8]:
+            assert not np.any(got[r, j]), (t, r, j)

@@ -47,6 +47,9 @@ _SIGS = {
     "beam_select_gumbel": (c_int, [c_p, c_i64, c_p, c_p, c_p, c_p, c_p, c_p, c_int, c_int,
                                    c_int, c_int, c_int, c_int, c_int, c_f, ctypes.c_uint64,
                                    c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]),
+    "beam_select_fixed_lse": (c_int, [c_p, c_i64, c_p, c_p, c_p, c_p, c_p, c_p, c_int, c_int,
+                                      c_int, c_int, c_int, c_int, c_int, c_f, ctypes.c_uint64,
+                                      c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]),
     "beam_trie_make_dense": (c_int, [c_p, c_int, c_p]),
     "beam_trie_drop_dense": (c_int, [c_p, c_int]),
     "beam_trie_export_dense": (c_int, [c_p, c_int, ctypes.POINTER(c_p), ctypes.POINTER(ctypes.c_int32)]),
@@ -243,20 +246,25 @@ def read_status(ws, stream=None):
 
 
 def beam_select(logits, cum, node, n_live, slot_in, trie, level, step, K, T=None,
-                lse_in=None, out=None, ws=None, stream=None, want_lse=True, temperature=0.0, seed=0):
+                lse_in=None, out=None, ws=None, stream=None, want_lse=True, temperature=0.0, seed=0,
+                score_lse=None):
     """One expansion step.  logits [R, W, V] fp32 (row b of request r at
     logits[r, b]); cum [R, W] fp32; node [R, W] int32 (ignored without trie);
     n_live [R] int32; slot_in [R, W, T] int32.  Returns a dict of output
     tensors: tokens, parents, cum_out, lse_out, node_out, n_live_out, slot_out.
     temperature > 0 selects by Gumbel top-k (beam_select_gumbel) with the
-    64-bit ``seed``."""
+    64-bit ``seed``.  score_lse [R, W] fp32 runs the one-launch kernel with
+    the candidates scored against these normalisers
+    (beam_select_fixed_lse); lse_out still holds the kernel's own."""
     R, W = cum.shape
     V = logits.shape[-1]
     if logits.dim() != 3 or logits.shape[0] != R or logits.shape[1] != W or logits.stride(2) != 1 \
             or logits.stride(0) != W * logits.stride(1):
         raise ValueError("logits must be [R, W, V] with unit stride in V and rows packed per request")
     T = slot_in.shape[2] if T is None else T
-    _need_cuda(cum, node, n_live, slot_in, lse_in)
+    _need_cuda(cum, node, n_live, slot_in, lse_in, score_lse)
+    if lse_in is not None and score_lse is not None:
+        raise ValueError("lse_in and score_lse are exclusive")
     dev = cum.device
     if out is None:
         out = dict(tokens=torch.empty((R, W), dtype=torch.int32, device=dev),
@@ -268,12 +276,16 @@ def beam_select(logits, cum, node, n_live, slot_in, trie, level, step, K, T=None
                    slot_out=torch.empty((R, W, T), dtype=torch.int32, device=dev))
     if ws is None:
         ws = workspace(beam_select_workspace_size(R, W, K, V), dev)
-    head = (_ptr(logits), logits.stride(1), _ptr(lse_in), _ptr(cum), _ptr(node), _ptr(n_live),
-            _ptr(slot_in), trie.handle if trie is not None else None, level, step, R, W, K, V, T)
+    head = (_ptr(logits), logits.stride(1), _ptr(lse_in if score_lse is None else score_lse), _ptr(cum),
+            _ptr(node), _ptr(n_live), _ptr(slot_in), trie.handle if trie is not None else None, level, step,
+            R, W, K, V, T)
     tail = (_ptr(out["tokens"]), _ptr(out["parents"]), _ptr(out["cum_out"]), _ptr(out.get("lse_out")),
             _ptr(out["node_out"]), _ptr(out["n_live_out"]), _ptr(out["slot_out"]), _ptr(ws), ws.numel(),
             _stream(stream))
-    if temperature > 0:
+    if score_lse is not None:
+        rc = lib().beam_select_fixed_lse(*head, float(temperature), int(seed) & (2 ** 64 - 1), *tail)
+        _check(rc, "beam_select_fixed_lse")
+    elif temperature > 0:
         rc = lib().beam_select_gumbel(*head, float(temperature), int(seed) & (2 ** 64 - 1), *tail)
         _check(rc, "beam_select_gumbel")
     else:
@@ -348,13 +360,17 @@ class DecodeChain:
     are shared by all steps.  Every replay starts from one live beam per
     request (cum 0, trie root, empty slot rows), exactly as the eager chain
     does, and leaves step t's outputs in ``sel[t]`` (the beam_select dict)
-    and ``out[t]`` (the attention output).  The C ABI makes this possible:
+    and ``out[t]`` (the attention output).  ``score_lse`` (optional, one
+    [R, W] fp32 tensor per step) scores every step's candidates against
+    those normalisers (beam_select_fixed_lse), for comparisons with a
+    reference that rounds its own.  The C ABI makes this possible:
     its compute calls neither allocate nor synchronise the host, so graph
     capture records the same launches an eager call would make.
     """
 
     def __init__(self, logits, q, shared_k, shared_v, prompt_offsets, max_prompt_len,
-                 unshared_k, unshared_v, trie, K, k_scale=None, v_scale=None, sm_scale=0.0):
+                 unshared_k, unshared_v, trie, K, k_scale=None, v_scale=None, sm_scale=0.0,
+                 score_lse=None):
         T = len(logits)
         R, W, V = logits[0].shape
         Hq, d = q[0].shape[2], q[0].shape[3]
@@ -386,7 +402,8 @@ class DecodeChain:
             st = self._state
             for t in range(T):
                 o = beam_select(logits[t], st["cum"], st["node"], st["n_live"], st["slot"], trie, t, t, K,
-                                out=self.sel[t], ws=self._ws_sel)
+                                out=self.sel[t], ws=self._ws_sel,
+                                score_lse=None if score_lse is None else score_lse[t])
                 beam_attn_decode(q[t], shared_k, shared_v, prompt_offsets, max_prompt_len, unshared_k,
                                  unshared_v, o["slot_out"], o["n_live_out"], t, k_scale=k_scale,
                                  v_scale=v_scale, sm_scale=sm_scale, out=self.out[t], ws=self._ws_att)

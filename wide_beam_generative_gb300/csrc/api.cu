@@ -9,16 +9,16 @@
 namespace bd {
 
 int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {   // every thread that races here stores the same value
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
       n = 148;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -123,50 +123,64 @@ extern "C" int beam_select_workspace_size(int R, int W, int K, int V, size_t* by
   return BEAMDEC_OK;
 }
 
-static int select_entry(const float* logits, int64_t row_stride, const float* lse_in,
-                           const float* cum_in, const int32_t* node_in,
-                           const int32_t* n_live_in, const int32_t* slot_in,
-                           const beamdec_trie* trie, int level, int step, int R, int W, int K,
-                           int V, int T, int32_t* tokens, int32_t* parents, float* cum_out,
-                           float* lse_out, int32_t* node_out, int32_t* n_live_out,
-                           int32_t* slot_out, void* workspace, size_t workspace_bytes,
-                           void* stream, float temperature, uint64_t seed) {
-  if (logits == nullptr || cum_in == nullptr || n_live_in == nullptr || tokens == nullptr ||
-      parents == nullptr || cum_out == nullptr || node_out == nullptr ||
-      n_live_out == nullptr || slot_out == nullptr || workspace == nullptr)
+namespace bd {
+
+int select_validate(const SelectCall& c, SelectArgs* out) {
+  if (c.logits == nullptr || c.cum_in == nullptr || c.n_live_in == nullptr || c.tokens == nullptr ||
+      c.parents == nullptr || c.cum_out == nullptr || c.node_out == nullptr ||
+      c.n_live_out == nullptr || c.slot_out == nullptr || c.ws == nullptr)
     return BEAMDEC_ERR_INVALID_ARG;
-  if (R < 1 || W < 1 || K < 1 || V < 1 || T < 1 || step < 0 || step >= T || row_stride < V)
+  if (c.R < 1 || c.W < 1 || c.K < 1 || c.V < 1 || c.T < 1 || c.step < 0 || c.step >= c.T ||
+      c.row_stride < c.V)
     return BEAMDEC_ERR_INVALID_ARG;
-  if (step > 0 && slot_in == nullptr) return BEAMDEC_ERR_INVALID_ARG;
-  if (slot_in != nullptr && slot_in == slot_out) return BEAMDEC_ERR_INVALID_ARG;
-  if (W > BEAMDEC_MAX_BEAM_WIDTH || V > BEAMDEC_MAX_VOCAB) return BEAMDEC_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BEAMDEC_ERR_INVALID_ARG;
+  if (c.step > 0 && c.slot_in == nullptr) return BEAMDEC_ERR_INVALID_ARG;
+  if (c.slot_in != nullptr && c.slot_in == c.slot_out) return BEAMDEC_ERR_INVALID_ARG;
+  if (c.lse_in != nullptr && c.score_lse != nullptr) return BEAMDEC_ERR_INVALID_ARG;
+  if (c.W > BEAMDEC_MAX_BEAM_WIDTH || c.V > BEAMDEC_MAX_VOCAB) return BEAMDEC_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(c.ws) & 255u) != 0) return BEAMDEC_ERR_INVALID_ARG;
   SelectArgs a{};
-  a.has_trie = trie != nullptr;
+  a.has_trie = c.trie != nullptr;
   if (a.has_trie) {
-    if (node_in == nullptr || level < 0 || level >= trie->levels) return BEAMDEC_ERR_INVALID_ARG;
-    if (trie->vocab != V) return BEAMDEC_ERR_INVALID_ARG;
+    const beamdec_trie* trie = c.trie;
+    if (c.node_in == nullptr || c.level < 0 || c.level >= trie->levels) return BEAMDEC_ERR_INVALID_ARG;
+    if (trie->vocab != c.V) return BEAMDEC_ERR_INVALID_ARG;
     int dev = 0;
-    cudaGetDevice(&dev);
+    if (cudaGetDevice(&dev) != cudaSuccess) return BEAMDEC_ERR_CUDA;
     if (dev != trie->device) return BEAMDEC_ERR_INVALID_ARG;
-    a.lvl.off = trie->off[level];
-    a.lvl.code = trie->code[level];
-    a.lvl.n_nodes = (int32_t)trie->n_nodes[level];
-    a.lvl.token_base = trie->token_base[level];
-    a.lvl.mask = trie->mask[level];
-    a.lvl.words = trie->mask_words[level];
+    a.lvl.off = trie->off[c.level];
+    a.lvl.code = trie->code[c.level];
+    a.lvl.n_nodes = (int32_t)trie->n_nodes[c.level];
+    a.lvl.token_base = trie->token_base[c.level];
+    a.lvl.mask = trie->mask[c.level];
+    a.lvl.words = trie->mask_words[c.level];
   }
-  if (workspace_bytes < select_workspace_bytes(R, W, K, V)) return BEAMDEC_ERR_WORKSPACE;
-  a.logits = logits; a.row_stride = row_stride; a.lse_in = lse_in;
-  a.cum_in = cum_in; a.node_in = node_in; a.n_live_in = n_live_in; a.slot_in = slot_in;
-  a.level = level; a.step = step; a.R = R; a.W = W; a.K = K; a.V = V; a.T = T;
-  a.Kp = K < V ? K : V;
-  a.tokens = tokens; a.parents = parents; a.cum_out = cum_out; a.lse_out = lse_out;
-  a.node_out = node_out; a.n_live_out = n_live_out; a.slot_out = slot_out;
-  a.ws = workspace;
-  a.inv_tau = temperature > 0.f ? (float)(1.0 / (double)temperature) : 0.f;
-  a.seed_lo = (uint32_t)(seed & 0xFFFFFFFFull);
-  a.seed_hi = (uint32_t)(seed >> 32);
+  if (c.ws_bytes < select_workspace_bytes(c.R, c.W, c.K, c.V)) return BEAMDEC_ERR_WORKSPACE;
+  a.logits = c.logits; a.row_stride = c.row_stride; a.lse_in = c.lse_in; a.score_lse = c.score_lse;
+  a.cum_in = c.cum_in; a.node_in = c.node_in; a.n_live_in = c.n_live_in; a.slot_in = c.slot_in;
+  a.level = c.level; a.step = c.step; a.R = c.R; a.W = c.W; a.K = c.K; a.V = c.V; a.T = c.T;
+  a.Kp = c.K < c.V ? c.K : c.V;
+  a.tokens = c.tokens; a.parents = c.parents; a.cum_out = c.cum_out; a.lse_out = c.lse_out;
+  a.node_out = c.node_out; a.n_live_out = c.n_live_out; a.slot_out = c.slot_out;
+  a.ws = c.ws;
+  a.inv_tau = c.temperature > 0.f ? (float)(1.0 / (double)c.temperature) : 0.f;
+  a.seed_lo = (uint32_t)(c.seed & 0xFFFFFFFFull);
+  a.seed_hi = (uint32_t)(c.seed >> 32);
+  *out = a;
+  return BEAMDEC_OK;
+}
+
+}  // namespace bd
+
+static int check_temperature(float temperature) {
+  if (!(temperature > 0.f) || !(temperature < INFINITY)) return BEAMDEC_ERR_INVALID_ARG;
+  if (!((float)(1.0 / (double)temperature) < INFINITY)) return BEAMDEC_ERR_INVALID_ARG;
+  return BEAMDEC_OK;
+}
+
+static int select_run(const SelectCall& c, void* stream) {
+  SelectArgs a;
+  const int rc = select_validate(c, &a);
+  if (rc != BEAMDEC_OK) return rc;
   return launch_select(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -178,9 +192,10 @@ extern "C" int beam_select(const float* logits, int64_t row_stride, const float*
                            float* lse_out, int32_t* node_out, int32_t* n_live_out,
                            int32_t* slot_out, void* workspace, size_t workspace_bytes,
                            void* stream) {
-  return select_entry(logits, row_stride, lse_in, cum_in, node_in, n_live_in, slot_in, trie, level,
-                      step, R, W, K, V, T, tokens, parents, cum_out, lse_out, node_out, n_live_out,
-                      slot_out, workspace, workspace_bytes, stream, 0.f, 0);
+  const SelectCall c{logits, row_stride, lse_in, nullptr, cum_in, node_in, n_live_in, slot_in,
+                     trie, level, step, R, W, K, V, T, tokens, parents, cum_out, lse_out,
+                     node_out, n_live_out, slot_out, workspace, workspace_bytes, 0.f, 0};
+  return select_run(c, stream);
 }
 
 extern "C" int beam_select_gumbel(const float* logits, int64_t row_stride, const float* lse_in,
@@ -192,11 +207,32 @@ extern "C" int beam_select_gumbel(const float* logits, int64_t row_stride, const
                                   float* lse_out, int32_t* node_out, int32_t* n_live_out,
                                   int32_t* slot_out, void* workspace, size_t workspace_bytes,
                                   void* stream) {
-  if (!(temperature > 0.f) || !(temperature < INFINITY)) return BEAMDEC_ERR_INVALID_ARG;
-  if (!((float)(1.0 / (double)temperature) < INFINITY)) return BEAMDEC_ERR_INVALID_ARG;
-  return select_entry(logits, row_stride, lse_in, cum_in, node_in, n_live_in, slot_in, trie, level,
-                      step, R, W, K, V, T, tokens, parents, cum_out, lse_out, node_out, n_live_out,
-                      slot_out, workspace, workspace_bytes, stream, temperature, seed);
+  const int tc = check_temperature(temperature);
+  if (tc != BEAMDEC_OK) return tc;
+  const SelectCall c{logits, row_stride, lse_in, nullptr, cum_in, node_in, n_live_in, slot_in,
+                     trie, level, step, R, W, K, V, T, tokens, parents, cum_out, lse_out,
+                     node_out, n_live_out, slot_out, workspace, workspace_bytes, temperature, seed};
+  return select_run(c, stream);
+}
+
+extern "C" int beam_select_fixed_lse(const float* logits, int64_t row_stride, const float* score_lse,
+                                     const float* cum_in, const int32_t* node_in,
+                                     const int32_t* n_live_in, const int32_t* slot_in,
+                                     const beamdec_trie* trie, int level, int step, int R, int W,
+                                     int K, int V, int T, float temperature, uint64_t seed,
+                                     int32_t* tokens, int32_t* parents, float* cum_out,
+                                     float* lse_out, int32_t* node_out, int32_t* n_live_out,
+                                     int32_t* slot_out, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  if (score_lse == nullptr) return BEAMDEC_ERR_INVALID_ARG;
+  if (temperature != 0.f) {
+    const int tc = check_temperature(temperature);
+    if (tc != BEAMDEC_OK) return tc;
+  }
+  const SelectCall c{logits, row_stride, nullptr, score_lse, cum_in, node_in, n_live_in, slot_in,
+                     trie, level, step, R, W, K, V, T, tokens, parents, cum_out, lse_out,
+                     node_out, n_live_out, slot_out, workspace, workspace_bytes, temperature, seed};
+  return select_run(c, stream);
 }
 
 static bool attn_types_ok(int q, int kv, int o) {

@@ -682,15 +682,12 @@ int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t st
   if ((reinterpret_cast<uintptr_t>(a.q) & 15) || (reinterpret_cast<uintptr_t>(a.shared_k) & 15) ||
       (reinterpret_cast<uintptr_t>(a.shared_v) & 15))
     return BEAMDEC_ERR_INVALID_ARG;
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BEAMDEC_ERR_CUDA;
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(bd_attn_shared_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
-      return BEAMDEC_ERR_CUDA;
-    attr_set[dev] = true;
-  }
+  static PerDeviceOnce attr_once;
+  const int arc = once_per_device(attr_once, [](int) {
+    return cudaFuncSetAttribute(bd_attn_shared_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSmemBytes) == cudaSuccess ? BEAMDEC_OK : BEAMDEC_ERR_CUDA;
+  });
+  if (arc != BEAMDEC_OK) return arc;
   // with no prompt key at all (shared_rows = 0, K/V may be NULL) the K/V
   // maps are never loaded from; they are encoded over the queries' memory,
   // which holds at least one [Hkv][d] row, so that the encode sees a valid

@@ -15,7 +15,14 @@ struct WsHeader {
   int32_t status;        // first device-detected error (BEAMDEC_ERR_*), 0 = clean
   uint32_t bar_count;    // grid barrier arrivals (returns to 0 after each barrier)
   uint32_t bar_gen;      // grid barrier generation
-  uint32_t pad[61];
+  // Test hooks of the bounded waits, written by the caller (0 in normal use;
+  // the zero-filled workspace starts that way and the library never sets
+  // them): poll_limit replaces the default poll count of every bounded wait;
+  // bar_extra adds arrivals that no block ever supplies to the grid barrier,
+  // so each of its waits runs out and reports BEAMDEC_ERR_TIMEOUT.
+  uint32_t poll_limit;
+  uint32_t bar_extra;
+  uint32_t pad[59];
 };
 static_assert(sizeof(WsHeader) == kWsHeaderBytes, "header size");
 
@@ -74,15 +81,17 @@ __device__ __forceinline__ float warp_sum(float v) {
 // Every block of the grid must call it the same number of times.  The wait is
 // bounded: after `limit` polls the block records BEAMDEC_ERR_TIMEOUT and goes
 // on, so a broken launch ends with an error instead of a hung GPU.
-__device__ __forceinline__ void grid_barrier(WsHeader* h, unsigned nblocks,
-                                             long long limit = (1ll << 26)) {
+__device__ __forceinline__ void grid_barrier(WsHeader* h, unsigned nblocks) {
   __syncthreads();
   if (threadIdx.x == 0) {
+    const uint32_t hook = *reinterpret_cast<volatile uint32_t*>(&h->poll_limit);
+    const long long limit = hook ? (long long)hook : (1ll << 26);
+    const uint32_t target = nblocks + *reinterpret_cast<volatile uint32_t*>(&h->bar_extra);
     volatile uint32_t* gen = &h->bar_gen;
     uint32_t g = *gen;
     __threadfence();
     uint32_t arrived = atomicAdd(&h->bar_count, 1u) + 1u;
-    if (arrived == nblocks) {
+    if (arrived == target) {
       atomicExch(&h->bar_count, 0u);
       __threadfence();
       atomicAdd(&h->bar_gen, 1u);

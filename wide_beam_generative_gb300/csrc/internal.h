@@ -7,6 +7,9 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/beamdec.h"
 
 struct beamdec_trie {
@@ -27,6 +30,25 @@ struct beamdec_trie {
 
 namespace bd {
 
+// Per-device one-time host set-up (kernel attributes, occupancy queries),
+// safe when several host threads make their first call at once: fn(dev)
+// runs under a lock until it succeeds once for the current device.
+struct PerDeviceOnce {
+  std::mutex mu;
+  std::atomic<int> done[64] = {};
+};
+template <class F>
+int once_per_device(PerDeviceOnce& o, F&& fn) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BEAMDEC_ERR_CUDA;
+  if (o.done[dev].load(std::memory_order_acquire)) return BEAMDEC_OK;
+  std::lock_guard<std::mutex> lk(o.mu);
+  if (o.done[dev].load(std::memory_order_relaxed)) return BEAMDEC_OK;
+  const int rc = fn(dev);
+  if (rc == BEAMDEC_OK) o.done[dev].store(1, std::memory_order_release);
+  return rc;
+}
+
 constexpr size_t kWsHeaderBytesHost = 256;   // status word + grid-barrier counters
 
 // Device view of one trie level for kernels.
@@ -45,6 +67,10 @@ size_t select_workspace_bytes(int R, int W, int K, int V);
 
 struct SelectArgs {
   const float* logits; int64_t row_stride; const float* lse_in;
+  // one-launch path only: the normaliser the candidate scores use, given by
+  // the caller, while the kernel still streams every row for lse_out
+  // (null: the kernel's own log-sum-exp scores the candidates)
+  const float* score_lse;
   const float* cum_in; const int32_t* node_in; const int32_t* n_live_in;
   const int32_t* slot_in;
   bool has_trie; TrieLevel lvl;
@@ -57,6 +83,21 @@ struct SelectArgs {
   uint32_t seed_lo, seed_hi;      // Gumbel noise key (temperature > 0)
 };
 int launch_select(const SelectArgs& a, cudaStream_t stream);
+
+// The arguments of one selection call as the C ABI receives them.
+struct SelectCall {
+  const float* logits; int64_t row_stride; const float* lse_in; const float* score_lse;
+  const float* cum_in; const int32_t* node_in; const int32_t* n_live_in; const int32_t* slot_in;
+  const beamdec_trie* trie; int level, step, R, W, K, V, T;
+  int32_t* tokens; int32_t* parents; float* cum_out; float* lse_out; int32_t* node_out;
+  int32_t* n_live_out; int32_t* slot_out;
+  void* ws; size_t ws_bytes;
+  float temperature;   // 0 = deterministic top-k
+  uint64_t seed;
+};
+// Host-side checks of a selection call (nothing is launched or written);
+// on BEAMDEC_OK `a` holds the kernel arguments for launch_select.
+int select_validate(const SelectCall& c, SelectArgs* a);
 
 // ---- attention ---------------------------------------------------------------
 struct AttnArgs {

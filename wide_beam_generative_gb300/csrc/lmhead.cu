@@ -265,15 +265,12 @@ size_t lmhead_workspace_bytes(int rows, int V) {
 int launch_lmhead(const void* hidden, const void* weight, int rows, int hidden_dim, int V,
                   int win0, int win1, float* lse_out, float* logits_out, int64_t out_stride,
                   void* ws, cudaStream_t stream) {
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BEAMDEC_ERR_CUDA;
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(bd_lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kLmSmem) != cudaSuccess)
-      return BEAMDEC_ERR_CUDA;
-    attr_set[dev] = true;
-  }
+  static PerDeviceOnce attr_once;
+  const int arc = once_per_device(attr_once, [](int) {
+    return cudaFuncSetAttribute(bd_lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kLmSmem) == cudaSuccess ? BEAMDEC_OK : BEAMDEC_ERR_CUDA;
+  });
+  if (arc != BEAMDEC_OK) return arc;
   CUtensorMap am, bm;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)hidden_dim, (cuuint64_t)rows};

@@ -1008,6 +1008,9 @@ bd_stream_select_kernel(SelectArgs a) {
     lse = sh.lse;
   }
   if (tid == 0 && a.lse_out != nullptr) a.lse_out[rowi] = lse;
+  // the candidates are scored against the caller's normaliser when one is
+  // given (the rest of the launch is the same code path)
+  if (a.score_lse != nullptr) lse = __ldg(a.score_lse + rowi);
   if (kG && tid == 0) ws.rowlse[rowi] = lse;   // read by the outputs' score recomputation
   expand_and_select<kFused, true, kG, false>(a, sh, ws, r, b, nl, lse, tail_smem);
 }
@@ -1180,10 +1183,9 @@ size_t select_workspace_bytes(int R, int W, int K, int V) {
 
 int launch_select(const SelectArgs& a, cudaStream_t stream) {
   static GlobalLaunchCfg cfg[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BEAMDEC_ERR_CUDA;
+  static PerDeviceOnce cfg_once;
   const size_t smem = kGlobalKeysOffset + (size_t)kSelectCap * 8;
-  if (cfg[dev].max_blocks == 0) {
+  const int crc = once_per_device(cfg_once, [smem](int d) {
     if (cudaFuncSetAttribute(bd_global_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return BEAMDEC_ERR_CUDA;
@@ -1191,9 +1193,13 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bd_global_kernel, kGlobalThreads,
                                                       smem) != cudaSuccess || per_sm < 1)
       return BEAMDEC_ERR_CUDA;
-    cfg[dev].max_blocks = per_sm * sm_count();
-    cfg[dev].smem = smem;
-  }
+    cfg[d].max_blocks = per_sm * sm_count();
+    cfg[d].smem = smem;
+    return BEAMDEC_OK;
+  });
+  if (crc != BEAMDEC_OK) return crc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BEAMDEC_ERR_CUDA;
   SelectArgs a2 = a;
   // blocks per logits row: about 25K logits each (the row's tail of partial
   // waves shrinks with the work unit), at most kMaxRowSplits.  At V = 151936
