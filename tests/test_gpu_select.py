@@ -190,6 +190,42 @@ def test_open_vocab_large_vocab(gpu_lib, mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
+def test_large_rows_with_ties(gpu_lib, mode):
+    """Rows of 151936 candidates (more than the key cache holds) with
+    whole-number logits, so exact score ties surround the top_k-th key, with
+    top_k below and above beam_width; and constant rows of 20000, where every
+    key ties (one bin holds them all: the radix fallback)."""
+    wl = synth.WORKLOADS["openvocab"].scaled(name="ov-ties", R=2, W=64, K=64, T=3)
+
+    def whole(t):
+        return torch.round(synth.logits(wl, t, device=DEV))
+    run_chain(wl, None, steps=3, logit_fn=whole, mode=mode)
+    run_chain(wl, None, steps=2, K=700, logit_fn=whole, mode=mode)
+    run_chain(wl, None, steps=2, K=9, logit_fn=whole, mode=mode)
+    wc = synth.WORKLOADS["openvocab"].scaled(name="ov-const", R=1, W=16, K=16, T=2, V=20000)
+    run_chain(wc, None, steps=2, logit_fn=lambda t: torch.full((1, 16, 20000), 1.5, device=DEV), mode=mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_trie_node_above_key_cache(gpu_lib, mode):
+    """A root with 16384 children (more than the 8192 keys a block caches):
+    the large-row path enumerates the node's CSR code list."""
+    wl = synth.WORKLOADS["qwen06b"].scaled(name="wide-root", levels=2, C=16384, n_items=120_000, zipf=None,
+                                           W=32, K=32, T=2)
+    items = _catalog(wl)
+    run_chain(wl, items, mode=mode)
+    run_chain(wl, items, K=3000, mode=mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_gumbel_large_rows(gpu_lib, mode):
+    """Gumbel top-k over the whole 151936-token vocabulary (ordering keys
+    with noise through the large-row path)."""
+    wl = synth.WORKLOADS["openvocab"].scaled(name="ov-gumbel", R=1, W=40, K=40, T=2)
+    run_chain(wl, None, steps=2, temperature=0.9, seed=31, mode=mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
 def test_onerec17b_full_size_bitexact(gpu_lib, mode):
     """The benchmarked workload at full size: 4 requests x 512 beams, top_k 512,
     4M-item Zipf catalog, vocab 151936, all three steps (the third is the
