@@ -180,6 +180,44 @@ def test_split_prompt_keeps_the_merge_kernel(gpu_lib):
     _check(wl, got, want)
 
 
+def test_fused_merge_fp8_kv(gpu_lib):
+    """e4m3 KV with one prompt split: the epilogue reads the unshared rows as
+    fp8 (K scale in the softmax scale, V scale on the output) and no merge
+    kernel runs; an empty prompt, a one-key prompt and dead beams included."""
+    wl = synth.WORKLOADS["fp8kv"].scaled(name="fused8", R=3, prompt_lens=[0, 1, 128], p_range=None, W=60, T=4)
+    res = {}
+
+    def run():
+        res["v"] = _run(wl, 3, [60, 33, 1])
+    assert _merge_launches(run) == 0
+    got, want, _ = res["v"]
+    _check(wl, got, want, out_rounding=True)
+    assert np.all(got[1, 33:] == 0) and np.all(got[2, 1:] == 0)
+
+
+def test_workspace_reused_across_calls(gpu_lib):
+    """Three calls on one workspace (bf16 and e4m3 KV, split and unsplit
+    prompts) give identical outputs, equal to the oracle's."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    for wl, n_live in ((synth.WORKLOADS["qwen06b"], [50]),
+                       (synth.WORKLOADS["fp8kv"].scaled(name="reuse8", R=2, prompt_lens=[700, 90], p_range=None,
+                                                        W=30), [30, 11])):
+        a = synth.attention_inputs(wl, 1, device=DEV)
+        slot = _slots(wl, 1, n_live).to(DEV)
+        nl = torch.tensor(n_live, dtype=torch.int32, device=DEV)
+        maxp = int(synth.prompt_lens(wl).max())
+        ws = bd.workspace(bd.beam_attn_workspace_size(wl.R, wl.W, wl.Hq, wl.Hkv, wl.d, maxp, wl.kv_dtype))
+        outs = [bd.beam_attn_decode(a["q"], a["shared_k"], a["shared_v"], a["prompt_offsets"], maxp,
+                                    a["unshared_k"], a["unshared_v"], slot, nl, 1, k_scale=a["k_scale"],
+                                    v_scale=a["v_scale"], ws=ws).clone()
+                for _ in range(3)]
+        assert bd.read_status(ws) == 0
+        assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+        inp = oracle_attn_inputs(a, a["q"], wl)
+        want = oatt.attention_decode(inp, slot.cpu().numpy(), nl.cpu().numpy(), 1)
+        _check(wl, outs[2].double().cpu().numpy(), want, out_rounding=True)
+
+
 def test_fused_merge_bad_slot_sets_device_check(gpu_lib):
     from wide_beam_generative_gb300 import beamdec as bd
     wl = synth.WORKLOADS["qwen06b"].scaled(name="fused", R=1, prompt_lens=[128], W=64, T=3)

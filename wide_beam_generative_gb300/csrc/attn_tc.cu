@@ -94,6 +94,12 @@ struct TcParams {
   const __nv_bfloat16* uk;
   const __nv_bfloat16* uv;
   __nv_bfloat16* out;
+  // e4m3 KV: the unshared rows are read as fp8 by the fused epilogue (the
+  // prompt KV reaches the tensor cores as bf16) and the output takes v_scale
+  int kv8;
+  const uint8_t* uk8;
+  const uint8_t* uv8;
+  const float* v_scale;
 };
 
 struct Bars {
@@ -212,6 +218,92 @@ __device__ __forceinline__ size_t out_row(const TcParams& p, int r, int g, int r
   return (((size_t)r * p.W + j) * p.Hq + (size_t)g * p.G + h) * 128;
 }
 
+// One unshared K row (128 elements, bf16 or e4m3 unscaled: the K scale is in
+// the softmax scale) dotted with the query row, from the CTA's swizzled Q
+// tile or from global memory when qtile is null.
+__device__ __forceinline__ float unshared_dot(const TcParams& p, size_t e, const unsigned char* qtile, int rit,
+                                              size_t qoff) {
+  float d0 = 0.f, d1 = 0.f;
+  auto qword = [&](int c) -> uint4 {   // bf16 query elements 8c .. 8c + 7
+    return qtile ? *reinterpret_cast<const uint4*>(qtile + (c >> 3) * kHalfBytes + rit * 128 +
+                                                   (((c & 7) ^ (rit & 7)) << 4))
+                 : __ldg(reinterpret_cast<const uint4*>(p.q + qoff) + c);
+  };
+  if (p.kv8) {
+    const uint4* kr = reinterpret_cast<const uint4*>(p.uk8 + e);
+    uint4 kw[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) kw[c] = __ldg(kr + c);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {   // 16 key elements per 16-byte word
+      const uint32_t w4[4] = {kw[c].x, kw[c].y, kw[c].z, kw[c].w};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint4 qw = qword(2 * c + h);
+        const uint32_t qv[4] = {qw.x, qw.y, qw.z, qw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t kk = w4[2 * h + (i >> 1)] >> (16 * (i & 1));
+          const float2 kf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(
+              (__nv_fp8x2_storage_t)(kk & 0xffffu), __NV_E4M3)));
+          d0 = fmaf(bf_lo(qv[i]), kf.x, d0);
+          d1 = fmaf(bf_hi(qv[i]), kf.y, d1);
+        }
+      }
+    }
+  } else {
+    const uint4* kr = reinterpret_cast<const uint4*>(p.uk + e);
+    uint4 kw[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) kw[c] = __ldg(kr + c);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 qw = qword(c);
+      d0 = fmaf(bf_lo(qw.x), bf_lo(kw[c].x), d0);
+      d1 = fmaf(bf_hi(qw.x), bf_hi(kw[c].x), d1);
+      d0 = fmaf(bf_lo(qw.y), bf_lo(kw[c].y), d0);
+      d1 = fmaf(bf_hi(qw.y), bf_hi(kw[c].y), d1);
+      d0 = fmaf(bf_lo(qw.z), bf_lo(kw[c].z), d0);
+      d1 = fmaf(bf_hi(qw.z), bf_hi(kw[c].z), d1);
+      d0 = fmaf(bf_lo(qw.w), bf_lo(kw[c].w), d0);
+      d1 = fmaf(bf_hi(qw.w), bf_hi(kw[c].w), d1);
+    }
+  }
+  return d0 + d1;
+}
+
+// o += w x (unshared V row e, columns q4*32 .. q4*32 + 31; e4m3 unscaled).
+__device__ __forceinline__ void unshared_axpy(const TcParams& p, size_t e, int q4, float w, float (&o)[32]) {
+  if (p.kv8) {
+    const uint4* vr = reinterpret_cast<const uint4*>(p.uv8 + e + q4 * 32);
+    const uint4 v0 = __ldg(vr), v1 = __ldg(vr + 1);
+    const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(
+          (__nv_fp8x2_storage_t)((wv[i >> 1] >> (16 * (i & 1))) & 0xffffu), __NV_E4M3)));
+      o[2 * i] = fmaf(w, f.x, o[2 * i]);
+      o[2 * i + 1] = fmaf(w, f.y, o[2 * i + 1]);
+    }
+  } else {
+    const uint4* vr = reinterpret_cast<const uint4*>(p.uv + e + q4 * 32);
+    uint4 vw[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) vw[c] = __ldg(vr + c);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      o[8 * c + 0] = fmaf(w, bf_lo(vw[c].x), o[8 * c + 0]);
+      o[8 * c + 1] = fmaf(w, bf_hi(vw[c].x), o[8 * c + 1]);
+      o[8 * c + 2] = fmaf(w, bf_lo(vw[c].y), o[8 * c + 2]);
+      o[8 * c + 3] = fmaf(w, bf_hi(vw[c].y), o[8 * c + 3]);
+      o[8 * c + 4] = fmaf(w, bf_lo(vw[c].z), o[8 * c + 4]);
+      o[8 * c + 5] = fmaf(w, bf_hi(vw[c].z), o[8 * c + 5]);
+      o[8 * c + 6] = fmaf(w, bf_lo(vw[c].w), o[8 * c + 6]);
+      o[8 * c + 7] = fmaf(w, bf_hi(vw[c].w), o[8 * c + 7]);
+    }
+  }
+}
+
 // Fused epilogue, one query row per thread: the unshared stage over the
 // beam's decode tokens (reached through its slot-table row; each K row is
 // scored with the shared stage's log2-unit scale) and the online-softmax
@@ -244,28 +336,7 @@ __device__ __forceinline__ void fused_row(const TcParams& p, int r, int g, int r
       sl = -1;
     }
     float s = -INFINITY;
-    if (sl >= 0) {
-      const uint4* kr = reinterpret_cast<const uint4*>(p.uk + (((size_t)r * TW + sl) * p.Hkv + g) * 128);
-      uint4 kw[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) kw[c] = __ldg(kr + c);
-      float d0 = 0.f, d1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 qw = qtile ? *reinterpret_cast<const uint4*>(qtile + (c >> 3) * kHalfBytes + rit * 128 +
-                                                                (((c & 7) ^ (rit & 7)) << 4))
-                               : __ldg(reinterpret_cast<const uint4*>(p.q + qoff) + c);
-        d0 = fmaf(bf_lo(qw.x), bf_lo(kw[c].x), d0);
-        d1 = fmaf(bf_hi(qw.x), bf_hi(kw[c].x), d1);
-        d0 = fmaf(bf_lo(qw.y), bf_lo(kw[c].y), d0);
-        d1 = fmaf(bf_hi(qw.y), bf_hi(kw[c].y), d1);
-        d0 = fmaf(bf_lo(qw.z), bf_lo(kw[c].z), d0);
-        d1 = fmaf(bf_hi(qw.z), bf_hi(kw[c].z), d1);
-        d0 = fmaf(bf_lo(qw.w), bf_lo(kw[c].w), d0);
-        d1 = fmaf(bf_hi(qw.w), bf_hi(kw[c].w), d1);
-      }
-      s = (d0 + d1) * sc;
-    }
+    if (sl >= 0) s = unshared_dot(p, (((size_t)r * TW + sl) * p.Hkv + g) * 128, qtile, rit, qoff) * sc;
     ps[u * 128] = s;
     pslot[u * 128] = sl;
     M = fmaxf(M, s);
@@ -277,7 +348,8 @@ __device__ __forceinline__ void fused_row(const TcParams& p, int r, int g, int r
     ps[u * 128] = w;
     Ls += w;
   }
-  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+  const float vs = (p.kv8 && p.v_scale) ? p.v_scale[g] : 1.f;   // e4m3 V is unscaled up to here
+  const float inv = Ls > 0.f ? vs / Ls : 0.f;
 #pragma unroll 1
   for (int q4 = 0; q4 < 4; ++q4) {
     float o[32];
@@ -287,22 +359,7 @@ __device__ __forceinline__ void fused_row(const TcParams& p, int r, int g, int r
     for (int u = 0; u < L; ++u) {
       const int sl = pslot[u * 128];
       if (sl < 0) continue;
-      const float w = ps[u * 128];
-      const uint4* vr = reinterpret_cast<const uint4*>(p.uv + (((size_t)r * TW + sl) * p.Hkv + g) * 128 + q4 * 32);
-      uint4 vw[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) vw[c] = __ldg(vr + c);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        o[8 * c + 0] = fmaf(w, bf_lo(vw[c].x), o[8 * c + 0]);
-        o[8 * c + 1] = fmaf(w, bf_hi(vw[c].x), o[8 * c + 1]);
-        o[8 * c + 2] = fmaf(w, bf_lo(vw[c].y), o[8 * c + 2]);
-        o[8 * c + 3] = fmaf(w, bf_hi(vw[c].y), o[8 * c + 3]);
-        o[8 * c + 4] = fmaf(w, bf_lo(vw[c].z), o[8 * c + 4]);
-        o[8 * c + 5] = fmaf(w, bf_hi(vw[c].z), o[8 * c + 5]);
-        o[8 * c + 6] = fmaf(w, bf_lo(vw[c].w), o[8 * c + 6]);
-        o[8 * c + 7] = fmaf(w, bf_hi(vw[c].w), o[8 * c + 7]);
-      }
+      unshared_axpy(p, (((size_t)r * TW + sl) * p.Hkv + g) * 128, q4, ps[u * 128], o);
     }
     if (in) {
       uint4* dst = reinterpret_cast<uint4*>(p.out + qoff + q4 * 32);
@@ -490,8 +547,13 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       const int sl = __ldg(p.slot_table + ((size_t)r * p.W + j) * p.T + u);
       if (sl < 0 || sl >= TW) continue;
       const size_t e = (((size_t)r * TW + sl) * p.Hkv + g) * 128;
-      bulk_prefetch_l2(p.uk + e, 256);
-      bulk_prefetch_l2(p.uv + e, 256);
+      if (p.kv8) {
+        bulk_prefetch_l2(p.uk8 + e, 128);
+        bulk_prefetch_l2(p.uv8 + e, 128);
+      } else {
+        bulk_prefetch_l2(p.uk + e, 256);
+        bulk_prefetch_l2(p.uv + e, 256);
+      }
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax rows
@@ -666,12 +728,14 @@ bool attn_tc_supported(int q_dtype, int kv_dtype, int d, int G) {
 }
 
 // The merge runs in the shared stage's epilogue when the whole prompt is one
-// split (every query row's shared partial stays in its CTA), the KV is bf16,
-// the unshared tokens fit the epilogue's scratch and the rows are 16-byte
-// aligned for vector loads and stores.
+// split (every query row's shared partial stays in its CTA), the KV is bf16
+// or e4m3 (the epilogue reads e4m3 unshared rows as fp8 and scales the output
+// by v_scale), the unshared tokens fit the epilogue's scratch and the rows
+// are 16-byte aligned for vector loads and stores.
 bool attn_tc_fused(const AttnArgs& a, const AttnPlan& pl) {
   const auto al16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
-  return pl.tensor_core && pl.n_split == 1 && a.kv_dtype == BEAMDEC_BF16 && a.out_dtype == BEAMDEC_BF16 &&
+  return pl.tensor_core && pl.n_split == 1 && (a.kv_dtype == BEAMDEC_BF16 || a.kv_dtype == BEAMDEC_E4M3) &&
+         a.out_dtype == BEAMDEC_BF16 &&
          a.d == 128 && a.step + 1 <= kFusedMaxL && al16(a.q) && al16(a.unshared_k) && al16(a.unshared_v) &&
          al16(a.out);
 }
@@ -747,6 +811,10 @@ int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t st
   p.uk = static_cast<const __nv_bfloat16*>(a.unshared_k);
   p.uv = static_cast<const __nv_bfloat16*>(a.unshared_v);
   p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.kv8 = a.kv_dtype == BEAMDEC_E4M3 ? 1 : 0;
+  p.uk8 = static_cast<const uint8_t*>(a.unshared_k);
+  p.uv8 = static_cast<const uint8_t*>(a.unshared_v);
+  p.v_scale = a.kv_dtype == BEAMDEC_E4M3 ? a.v_scale : nullptr;
   dim3 grid((p.rows + 255) / 256, a.Hkv * pl.n_split, a.R);
   prof_begin(kKAttnTc, stream);
   bd_attn_shared_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qm, km, vm, p);
