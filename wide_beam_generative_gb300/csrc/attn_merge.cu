@@ -246,29 +246,42 @@ bd_attn_merge_kernel(AttnArgs a, int n_split, AttnPartials part) {
       float O[PL];
 #pragma unroll
       for (int i = 0; i < PL; ++i) O[i] = o[u][i] * wu;
-      for (int c = 0; c < n_split; ++c) {
-        const size_t pi = (((size_t)c * a.R + r) * a.Hkv + g) * rows + row;
-        const float mc = c < 32 ? __shfl_sync(0xffffffffu, pm[u], c) : part.m[pi];
-        const float lc = c < 32 ? __shfl_sync(0xffffffffu, pl[u], c) : part.l[pi];
-        if (lc == 0.f) continue;
-        const float w = ex2(mc - M);
-        Lsum = fmaf(lc, w, Lsum);
-        float oc[PL];
-        if (c == 0) {
+      // splits in batches of kBatch whose partial outputs are loaded together
+      // (one memory round trip per batch instead of one per split); split 0's
+      // output was prefetched with the queries
+      constexpr int kBatch = 8;
+      for (int c0 = 0; c0 < n_split; c0 += kBatch) {
+        float oc[kBatch][PL];
 #pragma unroll
-          for (int i = 0; i < PL; ++i) oc[i] = o0[u][i];
-        } else {
-          const float* src = part.o + pi * D + lane * PL;
-          if constexpr (PL == 4) {
-            const float4 x = *reinterpret_cast<const float4*>(src);
-            oc[0] = x.x; oc[1] = x.y; oc[2] = x.z; oc[3] = x.w;
-          } else {
-            const float2 x = *reinterpret_cast<const float2*>(src);
-            oc[0] = x.x; oc[1] = x.y;
+        for (int k = 0; k < kBatch; ++k) {
+          const int c = c0 + k;
+          if (c == 0) {
+#pragma unroll
+            for (int i = 0; i < PL; ++i) oc[k][i] = o0[u][i];
+          } else if (c < n_split) {
+            const float* src = part.o + ((((size_t)c * a.R + r) * a.Hkv + g) * rows + row) * D + lane * PL;
+            if constexpr (PL == 4) {
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+              oc[k][0] = x.x; oc[k][1] = x.y; oc[k][2] = x.z; oc[k][3] = x.w;
+            } else {
+              const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+              oc[k][0] = x.x; oc[k][1] = x.y;
+            }
           }
         }
 #pragma unroll
-        for (int i = 0; i < PL; ++i) O[i] = fmaf(oc[i], w, O[i]);
+        for (int k = 0; k < kBatch; ++k) {
+          const int c = c0 + k;
+          if (c >= n_split) break;
+          const size_t pi = (((size_t)c * a.R + r) * a.Hkv + g) * rows + row;
+          const float mc = c < 32 ? __shfl_sync(0xffffffffu, pm[u], c) : part.m[pi];
+          const float lc = c < 32 ? __shfl_sync(0xffffffffu, pl[u], c) : part.l[pi];
+          if (lc == 0.f) continue;
+          const float w = ex2(mc - M);
+          Lsum = fmaf(lc, w, Lsum);
+#pragma unroll
+          for (int i = 0; i < PL; ++i) O[i] = fmaf(oc[k][i], w, O[i]);
+        }
       }
       const float inv = vs / Lsum;
 #pragma unroll
