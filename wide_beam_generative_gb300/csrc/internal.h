@@ -81,6 +81,9 @@ struct SelectArgs {
   void* ws;
   float inv_tau;                  // fl32(1 / temperature); 0 = deterministic top-k
   uint32_t seed_lo, seed_hi;      // Gumbel noise key (temperature > 0)
+  // one-launch kernel only: store each live row's scoring normaliser in the
+  // workspace and stop (the expansion kernel then selects the rows)
+  int lse_only;
 };
 int launch_select(const SelectArgs& a, cudaStream_t stream);
 

@@ -63,6 +63,8 @@ struct SelWs {
   SelState* state;        // [R]
   int32_t* rowtick;       // [R][W] finished chunk blocks per row
   uint32_t* hist;         // [R][kBins]
+  uint32_t* cuthist;      // [R][kBins] score-bin counts of the pool when the
+                          // cooperative kernel selects (the fused tail keeps them in hist)
   unsigned long long* pool;  // [R][W*Kp]
   unsigned long long* cand;  // [R][kSelectCap]
   float2* rowpart;        // [R][W][kMaxRowSplits] per-chunk (max, sum of exp)
@@ -78,6 +80,7 @@ __host__ __device__ inline SelWs carve(void* ws, int R, int W, int Kp) {
   s.state = (SelState*)p; p += align256((size_t)R * sizeof(SelState));
   s.rowtick = (int32_t*)p; p += align256((size_t)R * W * sizeof(int32_t));
   s.hist = (uint32_t*)p; p += align256((size_t)R * kBins * sizeof(uint32_t));
+  s.cuthist = (uint32_t*)p; p += align256((size_t)R * kBins * sizeof(uint32_t));
   s.pool = (unsigned long long*)p; p += align256((size_t)R * W * Kp * 8);
   s.cand = (unsigned long long*)p; p += align256((size_t)R * kSelectCap * 8);
   s.rowpart = (float2*)p; p += align256((size_t)R * W * kMaxRowSplits * sizeof(float2));
@@ -229,6 +232,7 @@ struct ExpandShared {
   uint32_t digit, below;
   int count;
   int pool_base;
+  int cnt2, cnt3;   // slot counters of the wide-row path
   float lse;
   uint32_t c_le;
   // the row's trie range and score, fetched at the start of a stream block
@@ -326,6 +330,25 @@ __device__ __forceinline__ float2 stream_max_sum(const float* row, int c0, int c
 //     node's mask (bit order = code order = child order) instead of its CSR
 //     code list.  Built into the expansion kernel only (lse_in given): the
 //     32-register stream kernel keeps the CSR enumeration.
+// Ordering key of a candidate of beam b (request r) with logit x and token
+// tok: s = fl32(cum + fl32(x - lse)), or with kG the Gumbel key
+// fl32(fl32(s * inv_tau) + g), as a 32-bit key (smaller = better).
+template <bool kG>
+__device__ __forceinline__ uint32_t cand_key(const SelectArgs& a, float cum, float lse, float x, int r,
+                                             int b, int tok) {
+  const float sc = __fadd_rn(cum, __fsub_rn(x, lse));
+  if constexpr (kG)
+    return desc_key(__fadd_rn(__fmul_rn(sc, a.inv_tau), gumbel_noise(a.seed_lo, a.seed_hi, r, a.step, b, tok)));
+  else
+    return desc_key(sc);
+}
+
+template <bool kG>
+__device__ __forceinline__ bool expand_wide(const SelectArgs& a, ExpandShared& sh, SelState* st,
+                                            unsigned long long* pool, uint32_t* gh, unsigned char* dyn,
+                                            const float* row, const int32_t* code, int tb, int n, int r,
+                                            int b, float cum, float lse, float ref);
+
 template <bool kPf, bool kG, bool kD>
 __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
                                                  int r, int b, uint32_t* gh, uint32_t* kcache,
@@ -365,14 +388,7 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
   }
   auto tok_of = [&](int i) -> int { return code ? tb + __ldg(code + i) : i; };
   // ordering key of token tok whose logit is x
-  auto score_key = [&](float x, int tok) -> uint32_t {
-    const float sc = __fadd_rn(cum, __fsub_rn(x, lse));
-    if constexpr (kG)
-      return desc_key(__fadd_rn(__fmul_rn(sc, a.inv_tau),
-                                gumbel_noise(a.seed_lo, a.seed_hi, r, a.step, b, tok)));
-    else
-      return desc_key(sc);
-  };
+  auto score_key = [&](float x, int tok) -> uint32_t { return cand_key<kG>(a, cum, lse, x, r, b, tok); };
   auto key_of = [&](int tok) -> uint32_t { return score_key(__ldg(row + tok), tok); };
   // kD: every child (index, token, key) from the node's dense mask, handed to
   // sink(on, child, key) by every thread of the block (block-uniform rounds
@@ -468,6 +484,15 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
       }
     }
     __syncthreads();
+  }
+  // more candidates than the key cache holds (the expansion kernel): two
+  // passes over a score-bin histogram; the radix passes below remain the
+  // exact fallback for heavy ties
+  if constexpr (!kPf) {
+    if (!cached && kcache != nullptr && gh != nullptr &&
+        expand_wide<kG>(a, sh, st, pool, gh, reinterpret_cast<unsigned char*>(kcache), row, code, tb, n, r,
+                        b, cum, lse, ref))
+      return;
   }
   auto kc = [&](int i) -> uint32_t { return cached ? kcache[i] : key_of(tok_of(i)); };
   // radix select of the K-th smallest 32-bit score key: digits of 11, 11, 10 bits
@@ -744,6 +769,263 @@ __device__ void block_scan_bins(const uint32_t* gh, uint32_t* hs, uint32_t need,
   __syncthreads();
 }
 
+// The bin holding the need-th key (need >= 1) of a shared-memory histogram of
+// kTailBins bins: sh.digit = that bin and sh.below = keys in lower bins, or,
+// when the histogram holds fewer than need keys, sh.digit = kTailBins and
+// sh.below = all of them.  Every thread of a kExpandThreads block calls it.
+__device__ void block_find_bin_smem(const uint32_t* h, uint32_t need, ExpandShared& sh) {
+  constexpr int kPer = kTailBins / kExpandThreads;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  uint32_t v[kPer];
+  uint32_t sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    v[i] = h[t * kPer + i];
+    sum += v[i];
+  }
+  uint32_t inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) sh.warp_cnt[warp] = (int)inc;
+  __syncthreads();
+  uint32_t run = inc - sum, tot = 0;
+  for (int w = 0; w < kExpandThreads / 32; ++w) {
+    const uint32_t c = (uint32_t)sh.warp_cnt[w];
+    if (w < warp) run += c;
+    tot += c;
+  }
+  if (t == 0 && tot < need) {
+    sh.digit = kTailBins;
+    sh.below = tot;
+  }
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const uint32_t c = v[j];
+    if (run < need && need <= run + c) {
+      sh.digit = (uint32_t)(t * kPer + j);
+      sh.below = run;
+    }
+    run += c;
+  }
+  __syncthreads();
+}
+
+// Moves the nt smallest of the nc distinct 64-bit keys in shared memory to
+// keys[0..nt) (in no particular order), 0 < nt < nc.
+__device__ void smem_take_smallest(unsigned long long* keys, int nc, int nt, ExpandShared& sh) {
+  if (nc <= 2 * kExpandThreads) {   // sorted ascending: the first nt are the smallest
+    block_sort_small(keys, nc);
+    return;
+  }
+  unsigned long long prefix = 0;
+  int shift = 64;
+  uint32_t need = (uint32_t)nt, sure = 0;
+  while (true) {
+    const uint32_t in_bin = narrow_pass<false>(keys, nc, prefix, shift, need, sure, sh);
+    if (sure + in_bin == (uint32_t)nt || shift == 0) break;
+  }
+  if (threadIdx.x == 0) sh.count = 0;
+  __syncthreads();
+  for (int c0 = 0; c0 < nc; c0 += blockDim.x) {   // block-uniform trip count
+    const int i = c0 + threadIdx.x;
+    unsigned long long k = 0;
+    int flag = 0;
+    if (i < nc) {
+      k = keys[i];
+      flag = (k >> shift) <= prefix;
+    }
+    int tot;
+    const int rk = block_rank(flag, sh.warp_cnt, &tot);   // all reads of the chunk precede writes
+    if (flag) keys[sh.count + rk] = k;
+    __syncthreads();
+    if (threadIdx.x == 0) sh.count += tot;
+    __syncthreads();
+  }
+}
+
+// Per-beam top_k of a row with more candidates than the key cache holds (the
+// open vocabulary; trie nodes above kKeyCache children), in the expansion
+// kernel.  Candidates are scored in two passes over the row, four 16-byte
+// loads in flight per thread for a contiguous row:
+//   the request's cut: gh counts every candidate already in the request's
+//     pool by score bin (bins of 1/64 below the rank-0 beam's score, so a
+//     higher score never has a higher bin); once W of them lie at or above
+//     bin b*, a candidate in a later bin ranks below W pool members and can
+//     never be selected, so it is not emitted (the candidates that pass form
+//     a prefix of the row's order, and the row's top_k among them is its
+//     top_k restricted to them);
+//   pass 1: a shared-memory histogram of the passing candidates' bins gives
+//     the bin D holding the top_k-th one (or all of them pass);
+//   pass 2: candidates in bins below D go to the pool, those in bin D to a
+//     shared buffer, of which the smallest (key, index) complete the top_k.
+// Returns false, having emitted nothing, when bin D holds more than kWideBuf
+// candidates (heavy ties); the caller then runs the radix passes.
+// dyn: the 32 KB dynamic buffer (histogram in the lower 16 KB, bin D's
+// candidates in the upper 16 KB).
+constexpr int kWideBuf = 2048;   // (key << 32 | index) entries
+template <bool kG>
+__device__ __forceinline__ bool expand_wide(const SelectArgs& a, ExpandShared& sh, SelState* st,
+                                            unsigned long long* pool, uint32_t* gh, unsigned char* dyn,
+                                            const float* row, const int32_t* code, int tb, int n, int r,
+                                            int b, float cum, float lse, float ref) {
+  static_assert(kTailBins * 4 + kWideBuf * 8 <= kTailCap * 8, "wide-row buffers");
+  const int tid = threadIdx.x;
+  const int K = a.K;
+  uint32_t* lh = reinterpret_cast<uint32_t*>(dyn);
+  unsigned long long* buf = reinterpret_cast<unsigned long long*>(dyn + kTailBins * 4);
+  // every candidate (valid, index, token, logit) in block-uniform rounds
+  const bool vec = code == nullptr && (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  auto rounds = [&](auto&& fn) {
+    if (vec) {
+      constexpr int kV = 8;   // 16-byte loads in flight per thread
+      const int nv = n >> 2;
+      const float4* r4 = reinterpret_cast<const float4*>(row);
+      for (int g0 = 0; g0 < nv; g0 += kV * kExpandThreads) {   // block-uniform trip count
+        float4 v[kV];
+#pragma unroll
+        for (int u = 0; u < kV; ++u) {
+          const int g = g0 + u * kExpandThreads + tid;
+          v[u] = g < nv ? __ldg(r4 + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kV; ++u) {
+          const int g = g0 + u * kExpandThreads + tid;
+          const bool on = g < nv;
+          fn(on, 4 * g, 4 * g, v[u].x);
+          fn(on, 4 * g + 1, 4 * g + 1, v[u].y);
+          fn(on, 4 * g + 2, 4 * g + 2, v[u].z);
+          fn(on, 4 * g + 3, 4 * g + 3, v[u].w);
+        }
+      }
+      for (int c0 = nv * 4; c0 < n; c0 += kExpandThreads) {   // the last n % 4 candidates
+        const int i = c0 + tid;
+        fn(i < n, i, i, i < n ? __ldg(row + i) : 0.f);
+      }
+    } else {
+      for (int c0 = 0; c0 < n; c0 += 4 * kExpandThreads) {   // block-uniform trip count
+        int tk[4];
+        float x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = c0 + u * kExpandThreads + tid;
+          tk[u] = i < n ? (code ? tb + __ldg(code + i) : i) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[u] = (c0 + u * kExpandThreads + tid < n) ? __ldg(row + tk[u]) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = c0 + u * kExpandThreads + tid;
+          fn(i < n, i, tk[u], x[u]);
+        }
+      }
+    }
+  };
+  // the request's cut (a snapshot: counts only grow, so it stays valid)
+  block_scan_bins(gh, lh, (uint32_t)a.W, sh);
+  const int bstar = (int)sh.digit;
+  for (int i = tid; i < kTailBins; i += kExpandThreads) lh[i] = 0;
+  __syncthreads();
+  // A logit below x_lo(bin) cannot reach that bin: its score lies more than
+  // one bin (1/64) below the bin's edge, and near that edge the two float32
+  // roundings of the score move it by at most (|ref - cum| + |ref| + 128) x
+  // 2^-23, under 1e-3 while |ref|, |cum| and |lse| stay below 4096 (log
+  // probabilities always do; otherwise nothing is skipped), so one comparison
+  // skips it.  The Gumbel noise has no bound, so kG keeps every candidate.
+  const bool small = fabsf(ref) + fabsf(cum) + fabsf(lse) < 4096.f;
+  auto x_lo = [&](int bin) -> float {
+    return (kG || !small || bin >= kTailBins - 1) ? -INFINITY
+                                                   : (ref - (float)(bin + 2) * (1.f / 64.f)) - cum + lse;
+  };
+  const float xl1 = x_lo(bstar);
+  if (tid == 0) sh.cnt3 = 0;
+  __syncthreads();
+  // pass 1: histogram of the passing candidates' bins; the first kWideBuf
+  // passing candidates are also kept, so that a row with few of them (every
+  // row once the request's cut has formed) needs no second pass
+  rounds([&](bool on, int i, int tok, float x) {
+    const bool maybe = on && !(x < xl1);
+    if (!__any_sync(0xffffffffu, maybe)) return;
+    const uint32_t k = maybe ? cand_key<kG>(a, cum, lse, x, r, b, tok) : 0u;
+    const int bin = maybe ? score_bin(ref, desc_key_value(k)) : kTailBins;
+    const bool pass = maybe && bin <= bstar;
+    if (pass) atomicAdd(lh + bin, 1u);
+    const int pos = warp_reserve(&sh.cnt3, pass);
+    if (pass && pos < kWideBuf) buf[pos] = ((unsigned long long)k << 32) | (uint32_t)i;
+  });
+  __syncthreads();
+  {
+    const int npass = sh.cnt3;
+    if (npass <= kWideBuf) {   // every passing candidate is in the buffer
+      const int take = npass < K ? npass : K;
+      __syncthreads();
+      if (take < npass) smem_take_smallest(buf, npass, take, sh);
+      if (tid == 0) sh.pool_base = take > 0 ? atomicAdd(&st->total, take) : 0;
+      __syncthreads();
+      const int base = sh.pool_base;
+      for (int c0 = 0; c0 < take; c0 += kExpandThreads) {   // block-uniform trip count
+        const int j = c0 + tid;
+        const bool on = j < take;
+        const unsigned long long e = on ? buf[j] : 0ull;
+        const uint32_t k = (uint32_t)(e >> 32);
+        if (on) pool[base + j] = pool_key(k, b, (int)(e & 0xFFFFFFFFull));
+        warp_hist_add(gh, (uint32_t)(on ? score_bin(ref, desc_key_value(k)) : 0), on);
+      }
+      return true;
+    }
+  }
+  block_find_bin_smem(lh, (uint32_t)K, sh);
+  const int D = (int)sh.digit;
+  const uint32_t below = sh.below;
+  const uint32_t nD = D < kTailBins ? lh[D] : 0u;
+  __syncthreads();   // every thread has read the histogram before it is reused
+  if (nD > (uint32_t)kWideBuf) return false;
+  const int take = D < kTailBins ? K : (int)below;
+  const int need2 = D < kTailBins ? K - (int)below : 0;
+  if (tid == 0) {
+    sh.pool_base = take > 0 ? atomicAdd(&st->total, take) : 0;
+    sh.cnt2 = 0;
+    sh.cnt3 = 0;
+  }
+  __syncthreads();
+  const int base = sh.pool_base;
+  // pass 2: bins below D to the pool, bin D to the buffer (the warp-wide
+  // slot reservations run only where some lane of the warp has a candidate)
+  const int blim = D < bstar ? D : bstar;
+  const float xl2 = x_lo(blim);
+  rounds([&](bool on, int i, int tok, float x) {
+    const bool maybe = on && !(x < xl2);
+    if (!__any_sync(0xffffffffu, maybe)) return;
+    const uint32_t k = maybe ? cand_key<kG>(a, cum, lse, x, r, b, tok) : 0u;
+    const int bin = maybe ? score_bin(ref, desc_key_value(k)) : kTailBins;
+    const bool pass = maybe && bin <= bstar;
+    const bool direct = pass && bin < D;
+    const bool atd = pass && bin == D;
+    const int slot = warp_reserve(&sh.cnt2, direct);
+    if (direct) pool[base + slot] = pool_key(k, b, i);
+    warp_hist_add(gh, (uint32_t)(direct ? bin : 0), direct);
+    const int pos = warp_reserve(&sh.cnt3, atd);
+    if (atd) buf[pos] = ((unsigned long long)k << 32) | (uint32_t)i;   // pos < nD <= kWideBuf
+  });
+  __syncthreads();
+  if (need2 > 0) {
+    const int first = sh.cnt2;   // == below
+    __syncthreads();
+    if (need2 < (int)nD) smem_take_smallest(buf, (int)nD, need2, sh);
+    for (int c0 = 0; c0 < need2; c0 += kExpandThreads) {   // block-uniform trip count
+      const int j = c0 + tid;
+      const bool on = j < need2;
+      const unsigned long long e = on ? buf[j] : 0ull;
+      const uint32_t k = (uint32_t)(e >> 32);
+      if (on) pool[base + first + j] = pool_key(k, b, (int)(e & 0xFFFFFFFFull));
+      warp_hist_add(gh, (uint32_t)(on ? score_bin(ref, desc_key_value(k)) : 0), on);
+    }
+  }
+  return true;
+}
+
 // Fused a4 for one request, run by the last expand block of the request:
 // select the min(W, pool) smallest pool keys, sort them, emit outputs.
 template <bool kG>
@@ -913,7 +1195,8 @@ __device__ __forceinline__ void expand_and_select(const SelectArgs& a, ExpandSha
                                                   unsigned char* tail_smem) {
   const int tid = threadIdx.x;
   uint32_t* kcache = reinterpret_cast<uint32_t*>(tail_smem);
-  expand_candidates<kPf, kG, kD>(a, sh, ws, r, b, kFused ? ws.hist + (size_t)r * kBins : nullptr, kcache, lse);
+  expand_candidates<kPf, kG, kD>(a, sh, ws, r, b, (kFused ? ws.hist : ws.cuthist) + (size_t)r * kBins,
+                                 kcache, lse);
   if constexpr (kFused) {
     __syncthreads();
     if (tid == 0) {
@@ -1011,7 +1294,10 @@ bd_stream_select_kernel(SelectArgs a) {
   // the candidates are scored against the caller's normaliser when one is
   // given (the rest of the launch is the same code path)
   if (a.score_lse != nullptr) lse = __ldg(a.score_lse + rowi);
-  if (kG && tid == 0) ws.rowlse[rowi] = lse;   // read by the outputs' score recomputation
+  // the outputs' score recomputation (Gumbel) and the expansion kernel
+  // (lse-only mode) read the scoring normaliser back
+  if ((kG || a.lse_only) && tid == 0) ws.rowlse[rowi] = lse;
+  if (a.lse_only) return;
   expand_and_select<kFused, true, kG, false>(a, sh, ws, r, b, nl, lse, tail_smem);
 }
 
@@ -1176,7 +1462,7 @@ size_t select_workspace_bytes(int R, int W, int K, int V) {
   const int Kp = K < V ? K : V;
   return kWsHeaderBytes + align256((size_t)R * sizeof(SelState)) +
          align256((size_t)R * W * sizeof(int32_t)) +
-         align256((size_t)R * kBins * sizeof(uint32_t)) + align256((size_t)R * W * Kp * 8) +
+         2 * align256((size_t)R * kBins * sizeof(uint32_t)) + align256((size_t)R * W * Kp * 8) +
          align256((size_t)R * kSelectCap * 8) +
          align256((size_t)R * W * kMaxRowSplits * sizeof(float2)) + (size_t)R * W * sizeof(float);
 }
@@ -1224,7 +1510,25 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
   const size_t dsm = fused ? kTailCap * sizeof(unsigned long long) : kKeyCache * sizeof(uint32_t);
   const bool gumbel = a.inv_tau > 0.f;
   const bool dense = a.has_trie && a.lvl.mask != nullptr;
-  if (a.lse_in == nullptr) {
+  // Open-vocabulary rows wider than the key cache: the one-launch kernel only
+  // streams each row for its normaliser (kept in the workspace), and the
+  // expansion kernel, whose register budget holds the two-pass wide-row
+  // select, expands the rows.
+  const bool two_phase = a.lse_in == nullptr && !a.has_trie && a.V > kKeyCache && a.K < a.V;
+  if (two_phase) {
+    SelectArgs s1 = a2;
+    s1.lse_only = 1;
+    dim3 g0(a.W * S, a.R);
+    prof_begin(kKStream, stream);
+    if (gumbel) bd_stream_select_kernel<false, true><<<g0, kExpandThreads, dsm, stream>>>(s1);
+    else bd_stream_select_kernel<false, false><<<g0, kExpandThreads, dsm, stream>>>(s1);
+    prof_end(kKStream, stream);
+    if (cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
+    a2.lse_in = ws.rowlse;   // the scoring normaliser of every live row
+    a2.lse_out = nullptr;    // already written with the kernel's own value
+    a2.score_lse = nullptr;
+  }
+  if (a2.lse_in == nullptr) {
     dim3 g0(a.W * S, a.R);
     prof_begin(kKStream, stream);
     if (gumbel) {
