@@ -266,7 +266,9 @@ int beam_select_workspace_size(int R, int W, int K, int V, size_t* bytes);
  *   n_live_out  [R] int32 = min(W, pool size).
  *   slot_out    [R][W][T] int32: entries 0..step-1 copied from the parent's
  *               row, entry step = step*W + j, later entries -1; dead rows -1.
- *               Must not alias slot_in.
+ * No output may overlap an input (the kernels write outputs while other
+ * blocks still read inputs); slot_out == slot_in, cum_out == cum_in,
+ * node_out == node_in and n_live_out == n_live_in are rejected.
  * Per beam, candidates are ranked by (score desc, token asc) and the first
  * min(top_k, #candidates) enter the pool.
  * Errors: INVALID_ARG, UNSUPPORTED (W, V, K limits; a trie node with more

@@ -41,13 +41,15 @@ def test_error_strings(L):
 
 
 FAKE = ctypes.c_void_p(0x1000)   # never dereferenced: validation fails first
+# distinct fake outputs (an output equal to its input is rejected as aliasing)
+CUM_OUT, NODE_OUT, NLIVE_OUT, SLOT_OUT = (ctypes.c_void_p(v) for v in (0x4000, 0x5000, 0x6000, 0x2000))
 
 
 def _select(L, **kw):
     args = dict(logits=FAKE, row_stride=512, lse_in=None, cum=FAKE, node=FAKE, n_live=FAKE,
                 slot_in=FAKE, trie=None, level=0, step=0, R=1, W=8, K=8, V=512, T=3,
-                tokens=FAKE, parents=FAKE, cum_out=FAKE, lse_out=None, node_out=FAKE,
-                n_live_out=FAKE, slot_out=ctypes.c_void_p(0x2000), ws=FAKE, ws_bytes=0, stream=None)
+                tokens=FAKE, parents=FAKE, cum_out=CUM_OUT, lse_out=None, node_out=NODE_OUT,
+                n_live_out=NLIVE_OUT, slot_out=SLOT_OUT, ws=FAKE, ws_bytes=0, stream=None)
     args.update(kw)
     return L.beam_select(*args.values())
 
@@ -60,6 +62,9 @@ def test_select_validation(L):
     assert _select(L, row_stride=100) == bd.ERR_INVALID_ARG
     assert _select(L, step=1, slot_in=None) == bd.ERR_INVALID_ARG
     assert _select(L, slot_out=FAKE) == bd.ERR_INVALID_ARG          # aliasing slot_in
+    assert _select(L, cum_out=FAKE) == bd.ERR_INVALID_ARG           # aliasing cum_in
+    assert _select(L, n_live_out=FAKE) == bd.ERR_INVALID_ARG        # aliasing n_live_in
+    assert _select(L, node_out=FAKE) == bd.ERR_INVALID_ARG          # aliasing node_in
     assert _select(L, W=9000) == bd.ERR_UNSUPPORTED
     assert _select(L, V=300000, row_stride=300000) == bd.ERR_UNSUPPORTED
     assert _select(L, ws=ctypes.c_void_p(0x1010)) == bd.ERR_INVALID_ARG   # not 256-aligned
@@ -126,15 +131,15 @@ def test_static_select_rejects_oversized_shapes_on_host(L):
     from wide_beam_generative_gb300 import beamdec as bd
     fake = ctypes.c_void_p(0x1000)
     rc = L.beam_select_static(fake, 151936, None, fake, fake, fake, fake, None, 0, 0,
-                              2, 5000, 5000, 151936, 2, fake, fake, fake, None, fake, fake,
-                              ctypes.c_void_p(0x2000), None)
+                              2, 5000, 5000, 151936, 2, fake, fake, CUM_OUT, None, NODE_OUT, NLIVE_OUT,
+                              SLOT_OUT, None)
     assert rc == bd.ERR_UNSUPPORTED
 
 
 def test_gumbel_select_validates_temperature_on_host(L):
     from wide_beam_generative_gb300 import beamdec as bd
     args = [FAKE, 512, None, FAKE, FAKE, FAKE, FAKE, None, 0, 0, 1, 8, 8, 512, 3]
-    outs = [FAKE, FAKE, FAKE, None, FAKE, FAKE, ctypes.c_void_p(0x2000), FAKE, 0, None]
+    outs = [FAKE, FAKE, CUM_OUT, None, NODE_OUT, NLIVE_OUT, SLOT_OUT, FAKE, 0, None]
     for t in (0.0, -1.0, float("nan"), float("inf"), 1e-40):
         assert L.beam_select_gumbel(*args, t, 7, *outs) == bd.ERR_INVALID_ARG, t
     # a valid temperature reaches the same shape checks as beam_select
@@ -152,7 +157,7 @@ def test_fixed_lse_select_validates_on_host(L):
     from wide_beam_generative_gb300 import beamdec as bd
     head = [FAKE, 512]
     rest = [FAKE, FAKE, FAKE, FAKE, None, 0, 0, 1, 8, 8, 512, 3]
-    outs = [FAKE, FAKE, FAKE, None, FAKE, FAKE, ctypes.c_void_p(0x2000), FAKE, 0, None]
+    outs = [FAKE, FAKE, CUM_OUT, None, NODE_OUT, NLIVE_OUT, SLOT_OUT, FAKE, 0, None]
     # score_lse is required
     assert L.beam_select_fixed_lse(*head, None, *rest, 0.0, 0, *outs) == bd.ERR_INVALID_ARG
     # temperature 0 (deterministic) or a valid Gumbel temperature; nothing else

@@ -135,6 +135,10 @@ int select_validate(const SelectCall& c, SelectArgs* out) {
     return BEAMDEC_ERR_INVALID_ARG;
   if (c.step > 0 && c.slot_in == nullptr) return BEAMDEC_ERR_INVALID_ARG;
   if (c.slot_in != nullptr && c.slot_in == c.slot_out) return BEAMDEC_ERR_INVALID_ARG;
+  // outputs are written while other blocks still read the inputs
+  if (c.cum_out == c.cum_in || (const void*)c.n_live_out == (const void*)c.n_live_in ||
+      (c.node_in != nullptr && (const void*)c.node_out == (const void*)c.node_in))
+    return BEAMDEC_ERR_INVALID_ARG;
   if (c.lse_in != nullptr && c.score_lse != nullptr) return BEAMDEC_ERR_INVALID_ARG;
   if (c.W > BEAMDEC_MAX_BEAM_WIDTH || c.V > BEAMDEC_MAX_VOCAB) return BEAMDEC_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(c.ws) & 255u) != 0) return BEAMDEC_ERR_INVALID_ARG;

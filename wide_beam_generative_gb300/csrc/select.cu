@@ -54,7 +54,9 @@ struct SelState {
   int32_t done;
   int32_t ncand;
   int32_t tickets;            // expand blocks of the request that have finished
-  int32_t pad[6];
+  int32_t bin_mode;           // 1: the pool is gathered by score bin (no radix passes)
+  int32_t bin_cut;            // last score bin gathered in bin mode
+  int32_t pad[4];
 };
 static_assert(sizeof(SelState) == 64, "state size");
 
@@ -652,6 +654,52 @@ __device__ void emit_outputs(const SelectArgs& a, const SelWs& ws, int r,
   if (tid == 0) a.n_live_out[r] = nt;
 }
 
+// Output row j < n_target of request r for pool key k, as emit_outputs
+// writes it, by a group of eight threads (part 0..7): part 0 the token,
+// parent, score and node, the eight together the slot row.
+template <bool kG>
+__device__ __forceinline__ void emit_row(const SelectArgs& a, const SelWs& ws, int r, int j,
+                                         unsigned long long k, int part) {
+  const size_t o = (size_t)r * a.W;
+  const int parent = pool_key_beam(k);
+  if (part == 0) {
+    const int idx = pool_key_tok(k);
+    int tok = idx, node = -1;
+    if (a.has_trie) {
+      node = a.lvl.off[a.node_in[o + parent]] + idx;   // edge index = child node
+      tok = a.lvl.token_base + a.lvl.code[node];
+    }
+    a.tokens[o + j] = tok;
+    a.parents[o + j] = parent;
+    if constexpr (kG) {
+      const size_t pr = o + parent;
+      const float lse = a.lse_in != nullptr ? a.lse_in[pr] : __ldcg(ws.rowlse + pr);
+      const float x = a.logits[pr * (size_t)a.row_stride + tok];
+      a.cum_out[o + j] = __fadd_rn(a.cum_in[pr], __fsub_rn(x, lse));
+    } else {
+      a.cum_out[o + j] = desc_key_value((uint32_t)(k >> 32));
+    }
+    a.node_out[o + j] = node;
+  }
+  const int T = a.T;
+  for (int t = part; t < T; t += 8) {
+    int v = -1;
+    if (t < a.step) v = a.slot_in[(o + parent) * T + t];
+    else if (t == a.step) v = a.step * a.W + j;
+    a.slot_out[(o + j) * T + t] = v;
+  }
+}
+
+// Output row j >= n_target of request r (a dead beam), as emit_outputs writes it.
+__device__ __forceinline__ void emit_dead_row(const SelectArgs& a, int r, int j) {
+  const size_t o = (size_t)r * a.W;
+  a.tokens[o + j] = -1;
+  a.parents[o + j] = -1;
+  a.cum_out[o + j] = -INFINITY;
+  a.node_out[o + j] = -1;
+  for (int t = 0; t < a.T; ++t) a.slot_out[(o + j) * a.T + t] = -1;
+}
+
 // Sorts keys[0..n) ascending in place, n <= 2 * kExpandThreads, called by
 // every thread of a kExpandThreads-thread block.  A bitonic network over
 // 2 * kExpandThreads slots held in registers, slots t and t + kExpandThreads
@@ -848,8 +896,10 @@ __device__ void smem_take_smallest(unsigned long long* keys, int nc, int nt, Exp
 
 // Per-beam top_k of a row with more candidates than the key cache holds (the
 // open vocabulary; trie nodes above kKeyCache children), in the expansion
-// kernel.  Candidates are scored in two passes over the row, four 16-byte
-// loads in flight per thread for a contiguous row:
+// kernel.  The row is read in block-uniform rounds (eight 16-byte loads in
+// flight per thread for a contiguous row); a round in which no lane of a warp
+// holds a logit above the pass's lower bound costs one vote, and the warp
+// stages the logits above it in shared memory and scores them 32 at a time:
 //   the request's cut: gh counts every candidate already in the request's
 //     pool by score bin (bins of 1/64 below the rank-0 beam's score, so a
 //     higher score never has a higher bin); once W of them lie at or above
@@ -857,28 +907,57 @@ __device__ void smem_take_smallest(unsigned long long* keys, int nc, int nt, Exp
 //     never be selected, so it is not emitted (the candidates that pass form
 //     a prefix of the row's order, and the row's top_k among them is its
 //     top_k restricted to them);
-//   pass 1: a shared-memory histogram of the passing candidates' bins gives
-//     the bin D holding the top_k-th one (or all of them pass);
-//   pass 2: candidates in bins below D go to the pool, those in bin D to a
-//     shared buffer, of which the smallest (key, index) complete the top_k.
+//   a counting pass, only while the request has no cut: per-thread counts,
+//     over a leading part of the row, of the logits that reach each bin of a
+//     ladder give a bin at or above which the row holds K candidates; it cuts
+//     the row the same way;
+//   pass 1: a shared-memory histogram of the passing candidates' bins; the
+//     first kWideBuf of them are also buffered, and when that is all of
+//     them the top_k is taken from the buffer;
+//   pass 2 (otherwise): the histogram gives the bin D holding the top_k-th
+//     candidate; those in bins below D go to the pool, those in bin D to the
+//     buffer, of which the smallest (key, index) complete the top_k.
+// The emitted candidates' bins reach gh once per bin at the end of the row.
 // Returns false, having emitted nothing, when bin D holds more than kWideBuf
 // candidates (heavy ties); the caller then runs the radix passes.
-// dyn: the 32 KB dynamic buffer (histogram in the lower 16 KB, bin D's
-// candidates in the upper 16 KB).
+// dyn: the 32 KB dynamic buffer (histogram in the lower 16 KB, candidates in
+// the upper 16 KB); sh.hist holds the warps' staged logits during a pass.
 constexpr int kWideBuf = 2048;   // (key << 32 | index) entries
+// Bins of the counting ladder, counted from the bin of the beam's own score:
+// 1.5 to 24 nats below it (64 bins per nat).
+constexpr int kLadder = 12;
+__host__ __device__ constexpr int ladder_bins(int j) {
+  return j == 0 ? 96 : j == 1 ? 128 : j == 2 ? 192 : j == 3 ? 256 : j == 4 ? 320 : j == 5 ? 384
+       : j == 6 ? 448 : j == 7 ? 512 : j == 8 ? 640 : j == 9 ? 768 : j == 10 ? 1024 : 1536;
+}
+// Adds to the request's cut histogram the bins of a row's emitted candidates:
+// every candidate lh counts below bin D, and extra of bin D (one atomic per
+// occupied bin, not one per candidate: the rows of a request share the few
+// bins near its cut).
+__device__ __forceinline__ void add_cut_hist(uint32_t* gh, const uint32_t* lh, int D, uint32_t extra) {
+  for (int i = threadIdx.x; i < kTailBins; i += kExpandThreads) {
+    const uint32_t c = i < D ? lh[i] : (i == D ? extra : 0u);
+    if (c != 0u) atomicAdd(gh + i, c);
+  }
+}
 template <bool kG>
 __device__ __forceinline__ bool expand_wide(const SelectArgs& a, ExpandShared& sh, SelState* st,
                                             unsigned long long* pool, uint32_t* gh, unsigned char* dyn,
                                             const float* row, const int32_t* code, int tb, int n, int r,
                                             int b, float cum, float lse, float ref) {
   static_assert(kTailBins * 4 + kWideBuf * 8 <= kTailCap * 8, "wide-row buffers");
-  const int tid = threadIdx.x;
+  static_assert(kExpandThreads / 32 * 128 <= 2048, "64 staged pairs per warp in sh.hist");
+  static_assert(kLadder <= 32, "ladder counts in sh.warp_cnt");
+  const int tid = threadIdx.x, lane = tid & 31;
   const int K = a.K;
   uint32_t* lh = reinterpret_cast<uint32_t*>(dyn);
   unsigned long long* buf = reinterpret_cast<unsigned long long*>(dyn + kTailBins * 4);
-  // every candidate (valid, index, token, logit) in block-uniform rounds
+  float* stx = reinterpret_cast<float*>(sh.hist) + (tid >> 5) * 128;   // staged logits
+  int* sti = reinterpret_cast<int*>(sh.hist) + (tid >> 5) * 128 + 64;  // and their indices
   const bool vec = code == nullptr && (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
-  auto rounds = [&](auto&& fn) {
+  // fn(keep, index, token, logit) for every candidate, by all lanes of a warp,
+  // in the rounds where some lane of the warp keeps one (keep: not below lo)
+  auto rounds = [&](float lo, auto&& fn) {
     if (vec) {
       constexpr int kV = 8;   // 16-byte loads in flight per thread
       const int nv = n >> 2;
@@ -888,21 +967,28 @@ __device__ __forceinline__ bool expand_wide(const SelectArgs& a, ExpandShared& s
 #pragma unroll
         for (int u = 0; u < kV; ++u) {
           const int g = g0 + u * kExpandThreads + tid;
-          v[u] = g < nv ? __ldg(r4 + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[u] = g < nv ? __ldg(r4 + g) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         }
+        bool any = false;
+#pragma unroll
+        for (int u = 0; u < kV; ++u)
+          any |= !(v[u].x < lo) | !(v[u].y < lo) | !(v[u].z < lo) | !(v[u].w < lo);
+        if (!__any_sync(0xffffffffu, any)) continue;
 #pragma unroll
         for (int u = 0; u < kV; ++u) {
           const int g = g0 + u * kExpandThreads + tid;
           const bool on = g < nv;
-          fn(on, 4 * g, 4 * g, v[u].x);
-          fn(on, 4 * g + 1, 4 * g + 1, v[u].y);
-          fn(on, 4 * g + 2, 4 * g + 2, v[u].z);
-          fn(on, 4 * g + 3, 4 * g + 3, v[u].w);
+          fn(on && !(v[u].x < lo), 4 * g, 4 * g, v[u].x);
+          fn(on && !(v[u].y < lo), 4 * g + 1, 4 * g + 1, v[u].y);
+          fn(on && !(v[u].z < lo), 4 * g + 2, 4 * g + 2, v[u].z);
+          fn(on && !(v[u].w < lo), 4 * g + 3, 4 * g + 3, v[u].w);
         }
       }
       for (int c0 = nv * 4; c0 < n; c0 += kExpandThreads) {   // the last n % 4 candidates
         const int i = c0 + tid;
-        fn(i < n, i, i, i < n ? __ldg(row + i) : 0.f);
+        const float x = i < n ? __ldg(row + i) : 0.f;
+        const bool keep = i < n && !(x < lo);
+        if (__any_sync(0xffffffffu, keep)) fn(keep, i, i, x);
       }
     } else {
       for (int c0 = 0; c0 < n; c0 += 4 * kExpandThreads) {   // block-uniform trip count
@@ -915,64 +1001,168 @@ __device__ __forceinline__ bool expand_wide(const SelectArgs& a, ExpandShared& s
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) x[u] = (c0 + u * kExpandThreads + tid < n) ? __ldg(row + tk[u]) : 0.f;
+        bool keep[4], any = false;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int i = c0 + u * kExpandThreads + tid;
-          fn(i < n, i, tk[u], x[u]);
+          keep[u] = c0 + u * kExpandThreads + tid < n && !(x[u] < lo);
+          any |= keep[u];
         }
+        if (!__any_sync(0xffffffffu, any)) continue;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) fn(keep[u], c0 + u * kExpandThreads + tid, tk[u], x[u]);
       }
     }
   };
+  // Staging (deterministic keys only: their token is not needed): the warp's
+  // kept (logit, index) pairs queue in its 64 shared slots, and heavy(on,
+  // index, token, logit) scores them when 32 are queued.
+  int queued = 0;   // warp-uniform
+  auto stage = [&](bool keep, int i, float x, auto&& heavy) {
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    if (m == 0u) return;
+    if (keep) {
+      const int p = queued + __popc(m & ((1u << lane) - 1u));
+      stx[p] = x;
+      sti[p] = i;
+    }
+    queued += __popc(m);
+    if (queued >= 32) {
+      __syncwarp();
+      const float xs = stx[lane];
+      const int is = sti[lane];
+      const int rest = queued - 32;
+      if (lane < rest) {   // the overflow moves to the front (slot lane is this lane's own)
+        stx[lane] = stx[32 + lane];
+        sti[lane] = sti[32 + lane];
+      }
+      queued = rest;
+      __syncwarp();
+      heavy(true, is, is, xs);
+    }
+  };
+  auto drain = [&](auto&& heavy) {
+    __syncwarp();
+    const bool on = lane < queued;
+    const int is = on ? sti[lane] : 0;
+    heavy(on, is, is, on ? stx[lane] : 0.f);
+    queued = 0;
+  };
+
   // the request's cut (a snapshot: counts only grow, so it stays valid)
   block_scan_bins(gh, lh, (uint32_t)a.W, sh);
-  const int bstar = (int)sh.digit;
-  for (int i = tid; i < kTailBins; i += kExpandThreads) lh[i] = 0;
-  __syncthreads();
-  // A logit below x_lo(bin) cannot reach that bin: its score lies more than
-  // one bin (1/64) below the bin's edge, and near that edge the two float32
-  // roundings of the score move it by at most (|ref - cum| + |ref| + 128) x
-  // 2^-23, under 1e-3 while |ref|, |cum| and |lse| stay below 4096 (log
-  // probabilities always do; otherwise nothing is skipped), so one comparison
-  // skips it.  The Gumbel noise has no bound, so kG keeps every candidate.
+  int bcut = (int)sh.digit;
+  // A logit below x_lo(bin) cannot reach that bin, and one at or above
+  // x_hi(bin) reaches it or an earlier one: each bound lies one bin (1/64)
+  // beyond the bin's edge, and near that edge the float32 roundings of the
+  // score and of the bound move them by at most (|ref - cum| + |ref| + 128)
+  // x 2^-23, under 1e-3 while |ref|, |cum| and |lse| stay below 4096 (log
+  // probabilities always do; otherwise neither bound is used).  The Gumbel
+  // noise has no bound, so kG keeps every candidate.
   const bool small = fabsf(ref) + fabsf(cum) + fabsf(lse) < 4096.f;
   auto x_lo = [&](int bin) -> float {
     return (kG || !small || bin >= kTailBins - 1) ? -INFINITY
                                                    : (ref - (float)(bin + 2) * (1.f / 64.f)) - cum + lse;
   };
-  const float xl1 = x_lo(bstar);
+  if (tid < kLadder) sh.warp_cnt[tid] = 0;
+  for (int i = tid; i < kTailBins; i += kExpandThreads) lh[i] = 0;
+  __syncthreads();
+  // No request cut yet (fewer than W candidates in the pool): count, over the
+  // first quarter of the row (at least 4 K candidates), the logits at or
+  // above x_hi of each ladder bin B0 + ladder_bins(j); the lowest such bin
+  // with K of them cuts the row (every candidate in a later bin ranks below
+  // those K), so the passes below score only the candidates above it.  B0 is
+  // the bin of the beam's own score, which no candidate exceeds by more than
+  // rounding.
+  if constexpr (!kG) {
+    if (bcut >= kTailBins - 1 && n > kWideBuf && small) {
+      const int b0 = score_bin(ref, cum);
+      float th[kLadder];
+      uint32_t c[kLadder];
+#pragma unroll
+      for (int j = 0; j < kLadder; ++j) {
+        th[j] = (ref - (float)(b0 + ladder_bins(j)) * (1.f / 64.f)) - cum + lse;
+        c[j] = 0;
+      }
+      auto count = [&](float x) {
+#pragma unroll
+        for (int j = 0; j < kLadder; ++j) c[j] += (x < th[j]) ? 0u : 1u;
+      };
+      if (vec) {
+        const int nv = n >> 2;
+        const int ns = min(nv, max(nv >> 2, K));   // float4 groups counted
+        const float4* r4 = reinterpret_cast<const float4*>(row);
+        for (int g0 = 0; g0 < ns; g0 += 4 * kExpandThreads) {
+          float4 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int g = g0 + u * kExpandThreads + tid;
+            v[u] = g < ns ? __ldg(r4 + g) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            count(v[u].x);
+            count(v[u].y);
+            count(v[u].z);
+            count(v[u].w);
+          }
+        }
+      } else {
+        const int ns = min(n, max(n >> 2, 4 * K));
+        for (int i = tid; i < ns; i += kExpandThreads)
+          count(__ldg(row + (code ? tb + __ldg(code + i) : i)));
+      }
+#pragma unroll
+      for (int j = 0; j < kLadder; ++j) {
+        const uint32_t t = __reduce_add_sync(0xffffffffu, c[j]);
+        if (lane == 0) atomicAdd(&sh.warp_cnt[j], (int)t);
+      }
+      __syncthreads();
+      for (int j = kLadder - 1; j >= 0; --j)   // the lowest ladder bin with K candidates
+        if ((uint32_t)sh.warp_cnt[j] >= (uint32_t)K && b0 + ladder_bins(j) < bcut) bcut = b0 + ladder_bins(j);
+    }
+  }
   if (tid == 0) sh.cnt3 = 0;
   __syncthreads();
   // pass 1: histogram of the passing candidates' bins; the first kWideBuf
   // passing candidates are also kept, so that a row with few of them (every
   // row once the request's cut has formed) needs no second pass
-  rounds([&](bool on, int i, int tok, float x) {
-    const bool maybe = on && !(x < xl1);
-    if (!__any_sync(0xffffffffu, maybe)) return;
-    const uint32_t k = maybe ? cand_key<kG>(a, cum, lse, x, r, b, tok) : 0u;
-    const int bin = maybe ? score_bin(ref, desc_key_value(k)) : kTailBins;
-    const bool pass = maybe && bin <= bstar;
+  auto score1 = [&](bool on, int i, int tok, float x) {
+    const uint32_t k = on ? cand_key<kG>(a, cum, lse, x, r, b, tok) : 0u;
+    const int bin = on ? score_bin(ref, desc_key_value(k)) : kTailBins;
+    const bool pass = on && bin <= bcut;
     if (pass) atomicAdd(lh + bin, 1u);
     const int pos = warp_reserve(&sh.cnt3, pass);
     if (pass && pos < kWideBuf) buf[pos] = ((unsigned long long)k << 32) | (uint32_t)i;
-  });
+  };
+  if constexpr (kG) {
+    rounds(-INFINITY, score1);
+  } else {
+    rounds(x_lo(bcut), [&](bool keep, int i, int, float x) { stage(keep, i, x, score1); });
+    drain(score1);
+  }
   __syncthreads();
   {
     const int npass = sh.cnt3;
     if (npass <= kWideBuf) {   // every passing candidate is in the buffer
       const int take = npass < K ? npass : K;
-      __syncthreads();
-      if (take < npass) smem_take_smallest(buf, npass, take, sh);
-      if (tid == 0) sh.pool_base = take > 0 ? atomicAdd(&st->total, take) : 0;
+      if (take == 0) return true;
+      // the emitted candidates' bins: all of lh below bin D and take - below of bin D
+      int D = kTailBins;
+      uint32_t extra = 0;
+      if (take < npass) {
+        block_find_bin_smem(lh, (uint32_t)take, sh);
+        D = (int)sh.digit;
+        extra = (uint32_t)take - sh.below;
+        smem_take_smallest(buf, npass, take, sh);
+      }
+      if (tid == 0) sh.pool_base = atomicAdd(&st->total, take);
       __syncthreads();
       const int base = sh.pool_base;
-      for (int c0 = 0; c0 < take; c0 += kExpandThreads) {   // block-uniform trip count
-        const int j = c0 + tid;
-        const bool on = j < take;
-        const unsigned long long e = on ? buf[j] : 0ull;
-        const uint32_t k = (uint32_t)(e >> 32);
-        if (on) pool[base + j] = pool_key(k, b, (int)(e & 0xFFFFFFFFull));
-        warp_hist_add(gh, (uint32_t)(on ? score_bin(ref, desc_key_value(k)) : 0), on);
+      for (int j = tid; j < take; j += kExpandThreads) {
+        const unsigned long long e = buf[j];
+        pool[base + j] = pool_key((uint32_t)(e >> 32), b, (int)(e & 0xFFFFFFFFull));
       }
+      add_cut_hist(gh, lh, D, extra);
       return true;
     }
   }
@@ -980,7 +1170,7 @@ __device__ __forceinline__ bool expand_wide(const SelectArgs& a, ExpandShared& s
   const int D = (int)sh.digit;
   const uint32_t below = sh.below;
   const uint32_t nD = D < kTailBins ? lh[D] : 0u;
-  __syncthreads();   // every thread has read the histogram before it is reused
+  __syncthreads();   // every thread has read the search's result before sh is reused
   if (nD > (uint32_t)kWideBuf) return false;
   const int take = D < kTailBins ? K : (int)below;
   const int need2 = D < kTailBins ? K - (int)below : 0;
@@ -991,38 +1181,36 @@ __device__ __forceinline__ bool expand_wide(const SelectArgs& a, ExpandShared& s
   }
   __syncthreads();
   const int base = sh.pool_base;
-  // pass 2: bins below D to the pool, bin D to the buffer (the warp-wide
-  // slot reservations run only where some lane of the warp has a candidate)
-  const int blim = D < bstar ? D : bstar;
-  const float xl2 = x_lo(blim);
-  rounds([&](bool on, int i, int tok, float x) {
-    const bool maybe = on && !(x < xl2);
-    if (!__any_sync(0xffffffffu, maybe)) return;
-    const uint32_t k = maybe ? cand_key<kG>(a, cum, lse, x, r, b, tok) : 0u;
-    const int bin = maybe ? score_bin(ref, desc_key_value(k)) : kTailBins;
-    const bool pass = maybe && bin <= bstar;
+  // pass 2: bins below D to the pool, bin D to the buffer
+  const int blim = D < bcut ? D : bcut;
+  auto score2 = [&](bool on, int i, int tok, float x) {
+    const uint32_t k = on ? cand_key<kG>(a, cum, lse, x, r, b, tok) : 0u;
+    const int bin = on ? score_bin(ref, desc_key_value(k)) : kTailBins;
+    const bool pass = on && bin <= bcut;
     const bool direct = pass && bin < D;
     const bool atd = pass && bin == D;
     const int slot = warp_reserve(&sh.cnt2, direct);
     if (direct) pool[base + slot] = pool_key(k, b, i);
-    warp_hist_add(gh, (uint32_t)(direct ? bin : 0), direct);
     const int pos = warp_reserve(&sh.cnt3, atd);
     if (atd) buf[pos] = ((unsigned long long)k << 32) | (uint32_t)i;   // pos < nD <= kWideBuf
-  });
+  };
+  if constexpr (kG) {
+    rounds(-INFINITY, score2);
+  } else {
+    rounds(x_lo(blim), [&](bool keep, int i, int, float x) { stage(keep, i, x, score2); });
+    drain(score2);
+  }
   __syncthreads();
   if (need2 > 0) {
     const int first = sh.cnt2;   // == below
     __syncthreads();
     if (need2 < (int)nD) smem_take_smallest(buf, (int)nD, need2, sh);
-    for (int c0 = 0; c0 < need2; c0 += kExpandThreads) {   // block-uniform trip count
-      const int j = c0 + tid;
-      const bool on = j < need2;
-      const unsigned long long e = on ? buf[j] : 0ull;
-      const uint32_t k = (uint32_t)(e >> 32);
-      if (on) pool[base + first + j] = pool_key(k, b, (int)(e & 0xFFFFFFFFull));
-      warp_hist_add(gh, (uint32_t)(on ? score_bin(ref, desc_key_value(k)) : 0), on);
+    for (int j = tid; j < need2; j += kExpandThreads) {
+      const unsigned long long e = buf[j];
+      pool[base + first + j] = pool_key((uint32_t)(e >> 32), b, (int)(e & 0xFFFFFFFFull));
     }
   }
+  add_cut_hist(gh, lh, D, need2 > 0 ? (uint32_t)need2 : 0u);
   return true;
 }
 
@@ -1211,13 +1399,13 @@ __device__ __forceinline__ void expand_and_select(const SelectArgs& a, ExpandSha
 }
 
 // a2-a5 when the caller supplies the row normalisers (lse_in): one block per
-// live beam.
+// live beam.  The deterministic variants fit 64 registers, two blocks per SM.
 template <bool kFused, bool kG, bool kD>
-__global__ void __launch_bounds__(kExpandThreads)
+__global__ void __launch_bounds__(kExpandThreads, kG ? 1 : 2)
 bd_expand_kernel(SelectArgs a) {
   __shared__ ExpandShared sh;
   extern __shared__ __align__(16) unsigned char tail_smem[];
-  const int b = blockIdx.x, r = blockIdx.y;
+  const int r = blockIdx.x, b = blockIdx.y;   // the first rows of every request run first
   SelWs ws = carve(a.ws, a.R, a.W, a.Kp);
   if (b == 0 && r == 0 && threadIdx.x == 0) ws.hdr->bar_count = 0u;
   const int nl = a.n_live_in[r];
@@ -1320,20 +1508,37 @@ bd_global_kernel(SelectArgs a) {
   const unsigned G = gridDim.x;
   SelWs ws = carve(a.ws, a.R, a.W, a.Kp);
 
-  // phase 0: targets
+  // phase 0: targets.  Small pools skip straight to the sort.  The expansion
+  // counted every pool key in the request's score-bin histogram (cuthist);
+  // when the bin holding the nt-th best key closes a prefix of at most
+  // kSelectCap keys, the pool is gathered by bin and the radix passes are
+  // skipped.
   for (int r = blockIdx.x; r < a.R; r += G) {
+    volatile SelState* st = ws.state + r;
+    const int total = st->total;
+    const int nt = total < a.W ? total : a.W;
+    const bool big = total > kSelectCap && nt > 0;   // block-uniform
+    if (big) {
+      const uint32_t* ch = ws.cuthist + (size_t)r * kBins;
+      for (int i = tid; i < kBins; i += kGlobalThreads) sh.hist[i] = __ldcg(ch + i);
+      if (tid == 0) sh.digit = kBins;   // stays kBins if the bins hold fewer than nt keys
+      __syncthreads();
+      if (tid < 32) warp_find_digit(sh.hist, kBins, (uint32_t)nt, &sh.digit, &sh.below);
+      __syncthreads();
+    }
     if (tid == 0) {
-      volatile SelState* st = ws.state + r;
-      const int total = st->total;
-      const int nt = total < a.W ? total : a.W;
+      const bool by_bin = big && sh.digit < (uint32_t)kBins && sh.below + sh.hist[sh.digit] <= (uint32_t)kSelectCap;
       st->n_target = nt;
       st->need = nt;
       st->sure = 0;
       st->prefix = 0ull;
       st->shift = 64;
       st->ncand = 0;
-      st->done = (total <= kSelectCap) ? 1 : 0;   // small pools skip straight to the sort
+      st->bin_mode = by_bin ? 1 : 0;
+      st->bin_cut = by_bin ? (int)sh.digit : 0;
+      st->done = (total <= kSelectCap || by_bin) ? 1 : 0;
     }
+    __syncthreads();   // sh is reused for the next request
   }
   grid_barrier(ws.hdr, G);
 
@@ -1396,12 +1601,17 @@ bd_global_kernel(SelectArgs a) {
     grid_barrier(ws.hdr, G);
   }
 
-  // gather every key at or below the threshold prefix
+  // gather every key at or below the threshold prefix (bin mode: in a score
+  // bin up to the cut, the bin computed as the expansion computed it)
   for (int r = 0; r < a.R; ++r) {
     volatile SelState* st = ws.state + r;
     const int shift = st->shift;
     const unsigned long long prefix = st->prefix;
     const int total = st->total;
+    const bool by_bin = st->bin_mode != 0;
+    const int bin_cut = st->bin_cut;
+    const float cum0 = a.cum_in[(size_t)r * a.W];
+    const float ref = a.inv_tau > 0.f ? bin_ref<true>(a, cum0) : bin_ref<false>(a, cum0);
     const unsigned long long* pool = ws.pool + (size_t)r * a.W * a.Kp;
     unsigned long long* cand = ws.cand + (size_t)r * kSelectCap;
     const int per = (total + G - 1) / G;
@@ -1412,7 +1622,8 @@ bd_global_kernel(SelectArgs a) {
       int flag = 0;
       if (i < i1) {
         k = pool[i];
-        flag = (shift == 64) || ((k >> shift) <= prefix);
+        flag = by_bin ? score_bin(ref, desc_key_value((uint32_t)(k >> 32))) <= bin_cut
+                      : (shift == 64) || ((k >> shift) <= prefix);
       }
       int tot;
       const int rk = block_rank(flag, sh.warp_cnt, &tot);
@@ -1428,20 +1639,46 @@ bd_global_kernel(SelectArgs a) {
   }
   grid_barrier(ws.hdr, G);
 
-  // per request: sort the survivors, emit outputs and slot rows
-  for (int r = blockIdx.x; r < a.R; r += G) {
+  // per request: the survivors' keys are distinct, so each one's rank among
+  // them (a count of smaller keys) is its output row.  The request's slices
+  // of kRankSlice survivors are dealt round the grid; a block holds all of
+  // the request's survivors in shared memory and eight threads rank each key.
+  constexpr int kRankSlice = kGlobalThreads / 8;
+  int wbase = 0;   // slices of the requests before r (the same in every block)
+  for (int r = 0; r < a.R; ++r) {
     const volatile SelState* st = ws.state + r;
     const int nc = min((int)st->ncand, kSelectCap);
     const int nt = st->n_target;
+    const int ns = (nc + kRankSlice - 1) / kRankSlice;
     const unsigned long long* cand = ws.cand + (size_t)r * kSelectCap;
-    int np = 32;
-    while (np < nc) np <<= 1;
-    for (int i = tid; i < np; i += kGlobalThreads) keys[i] = i < nc ? __ldcg(cand + i) : ~0ull;
+    const int first = (int)((blockIdx.x + G - (unsigned)(wbase % (int)G)) % G);
+    wbase += ns;
+    if (first >= ns) continue;   // block-uniform
+    for (int i = tid; i < nc; i += kGlobalThreads) keys[i] = __ldcg(cand + i);
     __syncthreads();
-    bitonic_sort(keys, np);
-    if (a.inv_tau > 0.f) emit_outputs<true>(a, ws, r, keys, nt);
-    else emit_outputs<false>(a, ws, r, keys, nt);
-    __syncthreads();
+    const int part = tid & 7;
+    for (int sl = first; sl < ns; sl += G) {
+      const int q = sl * kRankSlice + (tid >> 3);
+      const unsigned long long kq = q < nc ? keys[q] : 0ull;
+      int rank = 0;
+      for (int i = part; i < nc; i += 8) rank += keys[i] < kq ? 1 : 0;
+      rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+      rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+      rank += __shfl_xor_sync(0xffffffffu, rank, 4);
+      if (q < nc && rank < nt) {
+        if (a.inv_tau > 0.f) emit_row<true>(a, ws, r, rank, kq, part);
+        else emit_row<false>(a, ws, r, rank, kq, part);
+      }
+    }
+    __syncthreads();   // every rank is counted before the next request's keys arrive
+  }
+  // rows past each request's n_target, and n_live_out
+  const size_t nrows = (size_t)a.R * a.W;
+  for (size_t e = (size_t)blockIdx.x * kGlobalThreads + tid; e < nrows; e += (size_t)G * kGlobalThreads) {
+    const int r = (int)(e / a.W), j = (int)(e - (size_t)r * a.W);
+    const int nt = ((const volatile SelState*)(ws.state + r))->n_target;
+    if (j >= nt) emit_dead_row(a, r, j);
+    if (j == 0) a.n_live_out[r] = nt;
   }
 }
 
@@ -1481,6 +1718,17 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
       return BEAMDEC_ERR_CUDA;
     cfg[d].max_blocks = per_sm * sm_count();
     cfg[d].smem = smem;
+    // two expansion blocks per SM need more shared memory than the driver's
+    // default split gives one kernel
+    const void* row_kernels[] = {
+        (const void*)bd_expand_kernel<false, false, false>, (const void*)bd_expand_kernel<false, false, true>,
+        (const void*)bd_expand_kernel<false, true, false>,  (const void*)bd_expand_kernel<false, true, true>,
+        (const void*)bd_expand_kernel<true, false, false>,  (const void*)bd_expand_kernel<true, false, true>,
+        (const void*)bd_expand_kernel<true, true, false>,   (const void*)bd_expand_kernel<true, true, true>};
+    for (const void* f : row_kernels)
+      if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return BEAMDEC_ERR_CUDA;
     return BEAMDEC_OK;
   });
   if (crc != BEAMDEC_OK) return crc;
@@ -1540,7 +1788,10 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
     }
     prof_end(kKStream, stream);
   } else {
-    dim3 g1(a.W, a.R);
+    // requests inner: until W candidates of a request reach its pool, its
+    // rows meet no cut and cost an extra pass, so the first rows of all
+    // requests share the first wave of blocks
+    const dim3 g1(a.R, a.W);
     prof_begin(kKExpand, stream);
     if (gumbel) {
       if (dense) launch_expand<true, true>(fused, g1, dsm, stream, a2);
