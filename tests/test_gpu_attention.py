@@ -231,35 +231,52 @@ def test_fused_merge_bad_slot_sets_device_check(gpu_lib):
     assert bd.read_status(ws) == bd.ERR_DEVICE_CHECK
 
 
-@pytest.mark.parametrize("G,W,plens", [(1, 300, [128, 77]), (4, 70, [100, 128]), (8, 33, [128, 1]),
-                                       (16, 20, [64, 128])])
-def test_fused_merge_group_sizes(gpu_lib, G, W, plens):
-    """Fused epilogue at every supported GQA group size, partial tiles and a
-    one-key prompt (prompts of at most 128 keys: one split)."""
+@pytest.mark.parametrize("G,W,plens,merge", [(1, 300, [128, 77], 0), (4, 70, [100, 128], 0),
+                                             (8, 33, [128, 1], 0), (16, 20, [64, 128], 0)])
+def test_fused_merge_group_sizes(gpu_lib, G, W, plens, merge):
+    """One prompt split: the epilogue merges at every supported GQA group
+    size; partial tiles and a one-key prompt."""
     wl = synth.WORKLOADS["qwen06b"].scaled(name="fusedg", R=len(plens), prompt_lens=plens, Hq=2 * G, Hkv=2,
                                            W=W, T=3)
     res = {}
 
     def run():
         res["v"] = _run(wl, 2, [W, max(1, W - 7)])
-    assert _merge_launches(run) == 0
+    assert _merge_launches(run) == merge
     got, want, _ = res["v"]
     _check(wl, got, want, out_rounding=True)
     assert np.all(got[1, max(1, W - 7):] == 0)
 
 
-def test_fused_merge_token_limit(gpu_lib):
-    """64 unshared tokens per beam are merged in the epilogue (its scratch
-    holds 64); 65 go through the merge kernel; both against the oracle."""
-    wl = synth.WORKLOADS["qwen06b"].scaled(name="fusedl", R=1, prompt_lens=[100], W=40, T=65)
-    for step, launches in ((63, 0), (64, 1)):
-        res = {}
+@pytest.mark.parametrize("step,merge", [(0, 0), (4, 0), (5, 0), (6, 1), (32, 1)])
+def test_fused_merge_token_limit(gpu_lib, step, merge):
+    """Up to 6 unshared tokens per beam are merged in the epilogue; 7 and
+    more (here up to 33) go through the merge kernel; both against the
+    oracle, with dead beams."""
+    wl = synth.WORKLOADS["qwen06b"].scaled(name="fusedl", R=2, prompt_lens=[100, 128], W=40, T=33)
+    res = {}
 
-        def run():
-            res["v"] = _run(wl, step, [40])
-        assert _merge_launches(run) == launches
-        got, want, _ = res["v"]
-        _check(wl, got, want)
+    def run():
+        res["v"] = _run(wl, step, [40, 23])
+    assert _merge_launches(run) == merge
+    got, want, _ = res["v"]
+    _check(wl, got, want)
+    assert np.all(got[1, 23:] == 0)
+
+
+@pytest.mark.parametrize("step,merge", [(5, 0), (31, 1)])
+def test_fused_merge_fp8_kv_long(gpu_lib, step, merge):
+    """e4m3 KV, one prompt split: 6 unshared tokens per beam merged in the
+    epilogue, 32 in the merge kernel."""
+    wl = synth.WORKLOADS["fp8kv"].scaled(name="fused8l", R=2, prompt_lens=[96, 128], p_range=None, W=50, T=32)
+    res = {}
+
+    def run():
+        res["v"] = _run(wl, step, [50, 17])
+    assert _merge_launches(run) == merge
+    got, want, _ = res["v"]
+    _check(wl, got, want, out_rounding=True)
+    assert np.all(got[1, 17:] == 0)
 
 
 def test_all_prompts_empty(gpu_lib):
