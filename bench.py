@@ -248,6 +248,10 @@ def algorithmic(wl, rows, kernel):
         qo = 2 * rows * wl.Hq * wl.d * b_q
         return unshared + qo, "bytes"
     if kernel == "bd_expand_kernel":
+        if not wl.levels:
+            # open vocabulary: every live logits row is read in full (its
+            # first pass from HBM; a row's later passes mostly hit L2)
+            return rows * wl.V * 4, "bytes"
         # trie children windows (code + logit) dominate; a bound, not a count
         return rows * 2 * 4 * min(wl.K, 512), "bytes"
     if kernel == "bd_kv_e4m3_to_bf16_kernel":

@@ -15,6 +15,17 @@ def test_algorithmic_units_of_the_benchmarked_step():
     assert kind == "flops" and flops == 4 * 8 * (512 * 2) * (4 * 4096) * 128 == 68719476736
 
 
+def test_algorithmic_units_of_the_open_vocabulary_selection():
+    wl = synth.WORKLOADS["openvocab"]
+    rows = wl.R * wl.W                                                 # 10000 live beams
+    # the expansion kernel reads every live logits row in full, like the normaliser stream
+    assert bench.algorithmic(wl, rows, "bd_expand_kernel") == (10000 * 151936 * 4, "bytes")
+    assert bench.algorithmic(wl, rows, "bd_stream_select_kernel") == (10000 * 151936 * 4, "bytes")
+    # with a trie the expansion reads only children windows: a bound of 2 x 4 B per kept candidate
+    tr = synth.WORKLOADS["onerec17b"]
+    assert bench.algorithmic(tr, 2048, "bd_expand_kernel") == (2048 * 2 * 4 * 512, "bytes")
+
+
 def test_step_roofline_counts_prompt_kv_once_per_request():
     wl = synth.WORKLOADS["onerec17b"]
     kernels = {"bd_stream_select_kernel": {"us_per_launch": 200.0},
