@@ -453,8 +453,8 @@ def gpu_arm(args, ws, rank, local):
         "lmhead_select": lmhead, "dense_trie": dense,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows or 4 * wl.W,
-                                            one_thread_rows=max(1, (args.cpu_rows or 4 * wl.W) // 8))
+        crows = args.cpu_rows or default_cpu_rows(wl)
+        line["cpu_baseline"] = cpu_baseline(wl, crows, one_thread_rows=max(1, crows // 8))
     return line
 
 
@@ -812,6 +812,14 @@ def cpu_run(wl, s):
                                wl.token_base(), step, step, n, min(wl.K, n))
         oatt.attention_decode(p["inp"], sel["slot_out"], sel["n_live_out"], step)
     return s["rows"]
+
+
+def default_cpu_rows(wl):
+    """Rows of the oracle's timed sample: four requests' worth, bounded so
+    that the sample takes about 10-30 s on 16 cores (the oracle spends about
+    8 ms per row on a trie step and about 16 ms on an open-vocabulary row,
+    whose candidates are the whole vocabulary)."""
+    return min(4 * wl.W, 2048 if wl.levels else 1024)
 
 
 def cpu_baseline(wl, rows, one_thread_rows=None):

@@ -74,3 +74,11 @@ def test_traffic_rows_count_only_for_their_workload_and_source(tmp_path, monkeyp
     assert bench.read_traffic("bd_stream_select_kernel", "onerec17b") == 1234.0
     assert bench.read_traffic("bd_stream_select_kernel", "openvocab") is None   # no row for it
     assert bench.read_traffic("bd_stream_select_kernel", "fp8kv") is None       # taken on other source
+
+
+def test_cpu_sample_is_bounded():
+    """The oracle's timed sample stays at four requests' worth of rows,
+    capped for the wide open-vocabulary rows."""
+    assert bench.default_cpu_rows(synth.WORKLOADS["onerec17b"]) == 2048
+    assert bench.default_cpu_rows(synth.WORKLOADS["qwen06b"]) == 200
+    assert bench.default_cpu_rows(synth.WORKLOADS["openvocab"]) == 1024
