@@ -38,13 +38,18 @@
  *   afterwards).  A workspace may be reused across calls on one stream;
  *   calls that run concurrently need separate workspaces.
  * - Bounded waits: every device-side wait (grid barrier, mbarrier) gives up
- *   after a fixed number of polls and records BEAMDEC_ERR_TIMEOUT.  Two
+ *   after a fixed number of polls and records BEAMDEC_ERR_TIMEOUT.  Three
  *   uint32 words of a workspace are test hooks of those waits, zero in normal
- *   use (the library never writes them): bytes 12-15 replace the default
- *   poll count when nonzero; bytes 16-19 (beam_select workspaces) add that
- *   many arrivals to the grid barrier of the large-pool selection, which no
- *   block ever supplies, so its waits run out.  Tests use them to reach the
- *   timeout path without faulting or hanging a GPU.
+ *   use (the library never writes them): bytes 12-15 replace the grid
+ *   barrier's default poll count when nonzero; bytes 16-19 (beam_select
+ *   workspaces) add that many arrivals to the grid barrier of the
+ *   large-pool selection, which no block ever supplies, so its waits run
+ *   out; bytes 20-23 (beam_attn_decode and beam_lmhead_lse workspaces), when
+ *   nonzero, make each CTA of the tensor-core kernels first wait that many
+ *   polls on an mbarrier that nothing completes, before it issues any copy
+ *   or MMA, so the wait runs out and the CTA exits with the timeout status.
+ *   Tests use them to reach the timeout path without faulting or hanging a
+ *   GPU.
  */
 #ifndef BEAMDEC_H
 #define BEAMDEC_H
@@ -201,11 +206,12 @@ int beam_trie_export(const beamdec_trie* trie, int level, const int32_t** off,
  * Dense child masks for one level (the FlashRec announcement's fused SID trie
  * has a dense and a CSR form).  Bit c of node n's mask (ceil(C/32) 32-bit words
  * per node, device memory owned by the trie) is set when code c is one of n's
- * children.  While a level has masks, beam_select and beam_select_gumbel
- * called WITH lse_in enumerate that level's candidates from the mask (bit
+ * children.  While a level has masks, beam_select, beam_select_gumbel and
+ * beam_select_fixed_lse enumerate that level's candidates from the mask (bit
  * order = code order = child order) instead of the CSR code list; without
- * lse_in (the one-launch path) they keep the CSR list.  The selections are
- * identical either way.  beam_trie_make_dense
+ * lse_in that takes two launches (the rows' normalisers are streamed first,
+ * then the rows expanded) instead of one.  The selections are identical
+ * either way.  beam_trie_make_dense
  * builds them from the level's CSR (a host round trip on `stream`,
  * synchronised); beam_trie_drop_dense frees them; beam_trie_export_dense
  * returns the device pointer (NULL without masks) and words per node.

@@ -293,3 +293,30 @@ def test_all_prompts_empty(gpu_lib):
     want = oatt.attention_decode(inp, slot.numpy(), nl.numpy(), 2)
     _check(wl, out.double().cpu().numpy(), want, out_rounding=True)
     assert np.all(out[1, 10:].float().cpu().numpy() == 0)
+
+
+def test_mbarrier_timeout_is_reported(gpu_lib):
+    """A bounded mbarrier wait that runs out ends the tensor-core launch with
+    BEAMDEC_ERR_TIMEOUT instead of hanging: the workspace's probe hook makes
+    every CTA wait 1000 polls on a barrier nothing completes before it issues
+    any copy or MMA (a flag that nothing sets).  With the hook cleared the
+    same workspace matches the oracle."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl = synth.WORKLOADS["qwen06b"].scaled(name="probe", R=2, prompt_lens=[100, 128], W=40, T=3)
+    a = synth.attention_inputs(wl, 2, device=DEV)
+    slot = _slots(wl, 2, [40, 40])
+    nl = torch.tensor([40, 40], dtype=torch.int32)
+    ws = bd.workspace(bd.beam_attn_workspace_size(wl.R, wl.W, wl.Hq, wl.Hkv, wl.d, 128, wl.kv_dtype))
+    hooks = ws[:24].view(torch.int32)
+
+    def run():
+        return bd.beam_attn_decode(a["q"], a["shared_k"], a["shared_v"], a["prompt_offsets"], 128,
+                                   a["unshared_k"], a["unshared_v"], slot.to(DEV), nl.to(DEV), 2, ws=ws)
+    hooks[5] = 1000          # probe_polls
+    run()
+    assert bd.read_status(ws) == bd.ERR_TIMEOUT
+    hooks[5] = 0
+    out = run()
+    assert bd.read_status(ws) == 0
+    want = oatt.attention_decode(oracle_attn_inputs(a, a["q"], wl), slot.numpy(), nl.numpy(), 2)
+    _check(wl, out.double().cpu().numpy(), want)

@@ -99,3 +99,24 @@ def test_selection_from_lmhead_window(gpu_lib):
             break
         cum, node, n_live, slot = res["cum_out"], res["node_out"], res["n_live_out"], res["slot_out"]
         o_cum, o_node, o_nl, o_slot = ref["cum_out"], ref["node_out"], ref["n_live_out"], ref["slot_out"]
+
+
+def test_mbarrier_timeout_is_reported(gpu_lib):
+    """A bounded mbarrier wait that runs out ends the launch with
+    BEAMDEC_ERR_TIMEOUT instead of hanging: the workspace's probe hook makes
+    every CTA wait 1000 polls on a barrier nothing completes before it issues
+    any copy or MMA (a flag that nothing sets).  With the hook cleared the
+    same workspace gives the float64 result."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    rows, H, V = 200, 256, 5000
+    h, w = _inputs(rows, H, V, 11)
+    ws = bd.workspace(bd.beam_lmhead_workspace_size(rows, V))
+    hooks = ws[:24].view(torch.int32)
+    hooks[5] = 1000          # probe_polls
+    bd.beam_lmhead_lse(h, w, ws=ws)
+    assert bd.read_status(ws) == bd.ERR_TIMEOUT
+    hooks[5] = 0
+    lse, _ = bd.beam_lmhead_lse(h, w, ws=ws)
+    assert bd.read_status(ws) == 0
+    want_lse, _ = olm.lse_rows(h.double().cpu().numpy(), w.double().cpu().numpy())
+    assert np.abs(lse.cpu().numpy().astype(np.float64) - want_lse).max() < ATOL_LSE

@@ -578,26 +578,46 @@ def test_dense_masks_match_the_oracle_trie(gpu_lib):
 
 @pytest.mark.parametrize("mode", MODES)
 def test_dense_tiny_chain_bitexact(gpu_lib, mode):
-    """With masks on every level: the expansion kernel enumerates them, the
-    one-launch kernel keeps the CSR lists; both equal the oracle."""
+    """With masks on every level the candidates come from the masks both
+    with lse_in (the expansion kernel) and without it (the rows' normalisers
+    streamed first, then the same expansion); both equal the oracle."""
     wl = synth.WORKLOADS["tiny"]
     run_chain(wl, _catalog(wl), dense_levels=(0, 1, 2), mode=mode)
 
 
-def test_dense_qwen06b_chain_bitexact(gpu_lib):
+@pytest.mark.parametrize("mode", MODES)
+def test_dense_qwen06b_chain_bitexact(gpu_lib, mode):
     wl = synth.WORKLOADS["qwen06b"]
-    run_chain(wl, _catalog(wl), dense_levels=(0, 1))
+    run_chain(wl, _catalog(wl), dense_levels=(0, 1), mode=mode)
 
 
-def test_dense_onerec17b_bitexact_and_gumbel(gpu_lib):
+@pytest.mark.parametrize("mode", MODES)
+def test_dense_onerec17b_bitexact_and_gumbel(gpu_lib, mode):
     wl = synth.WORKLOADS["onerec17b"]
     items = _catalog(wl)
-    run_chain(wl, items, steps=2, dense_levels=(0, 1))
-    run_chain(wl, items, steps=2, dense_levels=(0, 1), temperature=0.9, seed=77)
+    run_chain(wl, items, steps=2, dense_levels=(0, 1), mode=mode)
+    run_chain(wl, items, steps=2, dense_levels=(0, 1), temperature=0.9, seed=77, mode=mode)
 
 
-def test_dense_masks_leave_the_one_launch_path_unchanged(gpu_lib):
-    """With masks on levels 0 and 1 the one-launch path (no lse_in) still
-    matches the oracle's chain: it enumerates the CSR lists."""
+def test_dense_masks_on_the_production_call(gpu_lib):
+    """With masks on levels 0 and 1 the production call (no lse_in) streams
+    the rows' normalisers and expands them from the masks (the expansion
+    kernel runs; without masks it does not), and matches the oracle's chain
+    at every step from the oracle's state."""
+    from wide_beam_generative_gb300 import beamdec as bd
     wl = synth.WORKLOADS["qwen06b"]
-    run_chain_own_lse(wl, items=_catalog(wl), dense_levels=(0, 1))
+    items = _catalog(wl)
+    run_chain_own_lse(wl, items=items, dense_levels=(0, 1))
+    gtrie = bd.beam_trie_build(items, [wl.C] * wl.levels, wl.token_base(), wl.V)
+    lg = synth.logits(wl, 0, device=DEV)
+    st = _init_state(wl.R, wl.W, wl.T)
+    counts = {}
+    for masks in (False, True):
+        if masks:
+            gtrie.make_dense(0)
+        bd.profile_enable(True)
+        bd.beam_select(lg, st["cum"], st["node"], st["n_live"], st["slot"], gtrie, 0, 0, wl.K)
+        torch.cuda.synchronize()
+        counts[masks] = bd.profile_read()["bd_expand_kernel"][1]
+        bd.profile_enable(False)
+    assert counts == {False: 0, True: 1}

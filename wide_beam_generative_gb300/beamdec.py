@@ -153,9 +153,9 @@ class Trie:
         return o, c
 
     def make_dense(self, level, stream=None):
-        """Build dense child masks for `level`; selections given ``lse_in``
-        then enumerate that level's candidates from them (the one-launch
-        path without ``lse_in`` keeps the CSR list; results are identical)."""
+        """Build dense child masks for `level`; selections then enumerate
+        that level's candidates from them (without ``lse_in`` in two
+        launches instead of one; results are identical)."""
         _check(lib().beam_trie_make_dense(self.handle, level, _stream(stream)), "beam_trie_make_dense")
 
     def drop_dense(self, level):

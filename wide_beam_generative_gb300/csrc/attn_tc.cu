@@ -113,6 +113,8 @@ struct Bars {
   uint64_t kv_full[kSlots], kv_empty[kSlots];
   uint64_t s_full[2], p_full[2];
   uint64_t done;
+  uint64_t probe;   // never completed: the timeout test hook waits on it
+  uint64_t drain;   // an aborting MMA thread's last commit
 };
 
 // One lane polls (bounded), the warp agrees, then every lane observes the
@@ -447,6 +449,8 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       mbar_init(&bars.p_full[t], 128);
     }
     mbar_init(&bars.done, 1);
+    mbar_init(&bars.probe, 1);
+    mbar_init(&bars.drain, 1);
     mbar_fence_init();
   }
   if (warp == 9) tmem_alloc(&tmem_base_sh, kTmemCols);
@@ -454,8 +458,15 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
+  const uint32_t probe = *reinterpret_cast<volatile uint32_t*>(&p.hdr->probe_polls);
+  if (probe != 0u) {   // test hook (block-uniform): a wait that runs out
+    if (threadIdx.x == 0 && !mbar_wait(&bars.probe, 0, probe)) abort_sh = 1;
+    __syncthreads();
+  }
 
-  if (warp == 8 && lane == 0) {
+  if (abort_sh) {
+    // nothing was issued: straight to the timeout exit
+  } else if (warp == 8 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     prefetch_tmap(&qmap);
     prefetch_tmap(&kmap);
@@ -539,8 +550,14 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
       }
       if (abort_sh) { ok = false; break; }
     }
-    if (ok) mma_commit(&bars.done);
-    else abort_sh = 1;
+    if (ok) {
+      mma_commit(&bars.done);
+    } else {
+      abort_sh = 1;
+      // the MMAs already issued complete before the CTA frees TMEM and exits
+      mma_commit(&bars.drain);
+      mbar_wait(&bars.drain, 0);
+    }
   } else if (warp == 10 && p.fuse) {
     // ------------------------------------------------------------ L2 prefetch
     // pulls this CTA's unshared K/V rows into L2 while the shared stage runs,

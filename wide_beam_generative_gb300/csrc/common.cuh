@@ -17,12 +17,17 @@ struct WsHeader {
   uint32_t bar_gen;      // grid barrier generation
   // Test hooks of the bounded waits, written by the caller (0 in normal use;
   // the zero-filled workspace starts that way and the library never sets
-  // them): poll_limit replaces the default poll count of every bounded wait;
+  // them): poll_limit replaces the grid barrier's default poll count;
   // bar_extra adds arrivals that no block ever supplies to the grid barrier,
-  // so each of its waits runs out and reports BEAMDEC_ERR_TIMEOUT.
+  // so each of its waits runs out and reports BEAMDEC_ERR_TIMEOUT;
+  // probe_polls makes each CTA of the tensor-core kernels (attention shared
+  // stage, LM head) first wait that many polls on an mbarrier that nothing
+  // completes, before it issues any copy or MMA, so the wait runs out and
+  // the CTA takes its timeout exit.
   uint32_t poll_limit;
   uint32_t bar_extra;
-  uint32_t pad[59];
+  uint32_t probe_polls;
+  uint32_t pad[58];
 };
 static_assert(sizeof(WsHeader) == kWsHeaderBytes, "header size");
 

@@ -58,6 +58,8 @@ struct LmParams {
 struct LmBars {
   uint64_t full[kStages], empty[kStages];
   uint64_t acc_full[2], acc_empty[2];
+  uint64_t probe;   // never completed: the timeout test hook waits on it
+  uint64_t drain;   // an aborting MMA thread's last commit
 };
 
 __device__ __forceinline__ bool warp_flag(volatile int* f) {
@@ -95,6 +97,8 @@ bd_lmhead_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant
       mbar_init(&bars.acc_full[a], 1);
       mbar_init(&bars.acc_empty[a], 128);
     }
+    mbar_init(&bars.probe, 1);
+    mbar_init(&bars.drain, 1);
     mbar_fence_init();
   }
   if (warp == 1) tmem_alloc(&tmem_base_sh, 2 * kBN);
@@ -102,8 +106,15 @@ bd_lmhead_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
+  const uint32_t probe = *reinterpret_cast<volatile uint32_t*>(&p.hdr->probe_polls);
+  if (probe != 0u) {   // test hook (block-uniform): a wait that runs out
+    if (threadIdx.x == 0 && !mbar_wait(&bars.probe, 0, probe)) abort_sh = 1;
+    __syncthreads();
+  }
 
-  if (warp == 0 && lane == 0) {
+  if (abort_sh) {
+    // nothing was issued: straight to the timeout exit
+  } else if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     prefetch_tmap(&amap);
     prefetch_tmap(&bmap);
@@ -151,7 +162,12 @@ bd_lmhead_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant
       mma_commit(&bars.acc_full[acc]);
       if (abort_sh) ok = false;
     }
-    if (!ok) abort_sh = 1;
+    if (!ok) {
+      abort_sh = 1;
+      // the MMAs already issued complete before the CTA frees TMEM and exits
+      mma_commit(&bars.drain);
+      mbar_wait(&bars.drain, 0);
+    }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // TMEM lane group of this warp

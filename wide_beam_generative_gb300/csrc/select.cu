@@ -1758,11 +1758,13 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
   const size_t dsm = fused ? kTailCap * sizeof(unsigned long long) : kKeyCache * sizeof(uint32_t);
   const bool gumbel = a.inv_tau > 0.f;
   const bool dense = a.has_trie && a.lvl.mask != nullptr;
-  // Open-vocabulary rows wider than the key cache: the one-launch kernel only
-  // streams each row for its normaliser (kept in the workspace), and the
-  // expansion kernel, whose register budget holds the two-pass wide-row
-  // select, expands the rows.
-  const bool two_phase = a.lse_in == nullptr && !a.has_trie && a.V > kKeyCache && a.K < a.V;
+  // Open-vocabulary rows wider than the key cache, and levels with dense
+  // child masks: the one-launch kernel only streams each row for its
+  // normaliser (kept in the workspace), and the expansion kernel, whose
+  // register budget holds the wide-row select and the mask enumeration,
+  // expands the rows.
+  const bool two_phase =
+      a.lse_in == nullptr && (dense || (!a.has_trie && a.V > kKeyCache && a.K < a.V));
   if (two_phase) {
     SelectArgs s1 = a2;
     s1.lse_only = 1;
