@@ -161,11 +161,11 @@ class Step:
         self.bd = bd
         self.wl = wl
         self.dev = dev
-        t0 = time.time()
         self.items = synth.catalog(wl)
+        t0 = time.time()
         self.trie = bd.beam_trie_build(self.items, [wl.C] * wl.levels, wl.token_base(), wl.V) \
             if wl.levels else None
-        self.t_setup_catalog = time.time() - t0
+        self.t_trie_build = time.time() - t0
         R, W, T = wl.R, wl.W, wl.T
         self.step = T - 1
         self.attn = synth.attention_inputs(wl, self.step, device=dev)
@@ -430,6 +430,7 @@ def gpu_arm(args, ws, rank, local):
 
     # end-to-end through the C ABI from pinned host buffers
     e2e = None if args.no_e2e else e2e_arm(step, args, ws, flush)
+    e2e_head = None if args.no_e2e else e2e_lmhead_arm(step, args, ws, flush)
     chain = None if args.no_chain else chain_arm(step, args, flush)
     gumbel = None if args.no_chain else gumbel_arm(step, args, flush)
     lmhead = None if args.no_chain else lmhead_arm(step, args, flush)
@@ -449,7 +450,10 @@ def gpu_arm(args, ws, rank, local):
         "roofline": roof, "step_roofline": step_roof, "kernels": kernels,
         "kernels_note": "per-kernel event times from a pass of the same steps just before the timed "
                         "region; inside it only the roofline kernel is bracketed by events",
-        "gpu_launches": launches, "clocks": clk, "e2e": e2e, "chain_graph": chain, "gumbel_select": gumbel,
+        "gpu_launches": launches, "clocks": clk, "e2e": e2e, "e2e_lmhead": e2e_head,
+        "setup": {"catalog_items": int(len(step.items)) if wl.levels else 0,
+                  "trie_build_s": round(step.t_trie_build, 3)},
+        "chain_graph": chain, "gumbel_select": gumbel,
         "lmhead_select": lmhead, "dense_trie": dense,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -458,25 +462,18 @@ def gpu_arm(args, ws, rank, local):
     return line
 
 
-def e2e_arm(step, args, ws, flush):
-    """Steps through the public API from pinned host buffers: every step
-    copies its inputs (logits, queries, beam state) to the device, runs the
-    selection and the attention, and reads the selection's outputs and the
-    attention output back.  Timed two ways: one step at a time (serial), and
-    as a serving loop that copies step i + 1's inputs on a second stream
-    into a second set of device buffers while step i computes (pipelined;
-    the value).  Every step's copies stay inside the timed region."""
-    wl, dev = step.wl, step.dev
-    s = step.state
-    host = {"logits": step.logits.cpu().pin_memory(), "q": step.attn["q"].cpu().pin_memory()}
-    for k in ("cum", "node", "n_live", "slot"):
-        host[k] = s[k].cpu().pin_memory()
+def _e2e_loop(step, args, ws, flush, host, compute, host_outs):
+    """Times a step through the public API from pinned host buffers: every
+    step copies `host` to the device, runs compute(device buffers), which
+    queues the device-to-host copies of the results into `host_outs`.  Timed
+    two ways: one step at a time (serial), and as a serving loop that copies
+    step i + 1's inputs on a second stream into a second set of device
+    buffers while step i computes (pipelined; the value).  Every step's
+    copies stay inside the timed region."""
+    dev = step.dev
     bufs = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
-    outs = ["tokens", "parents", "cum_out", "node_out", "n_live_out", "slot_out"]
-    host_out = {k: torch.empty_like(step.out_sel[k], device="cpu").pin_memory() for k in outs}
-    host_att = torch.empty_like(step.out_att, device="cpu").pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = sum(v.numel() * v.element_size() for v in host_out.values()) + host_att.numel() * host_att.element_size()
+    d2h = sum(v.numel() * v.element_size() for v in host_outs)
     stream = torch.cuda.current_stream()
     copy_stream = torch.cuda.Stream(device=dev)
 
@@ -484,17 +481,9 @@ def e2e_arm(step, args, ws, flush):
         for k, v in host.items():
             bufs[b][k].copy_(v, non_blocking=True)
 
-    def compute_from(b):
-        d = bufs[b]
-        st = dict(cum=d["cum"], node=d["node"], n_live=d["n_live"], slot=d["slot"])
-        step.run(logits=d["logits"], q=d["q"], state=st)
-        for k in outs:
-            host_out[k].copy_(step.out_sel[k], non_blocking=True)
-        host_att.copy_(step.out_att, non_blocking=True)
-
     def serial():
         h2d_into(0)
-        compute_from(0)
+        compute(bufs[0])
 
     def pipelined(n):
         copied = [torch.cuda.Event(), torch.cuda.Event()]
@@ -513,7 +502,7 @@ def e2e_arm(step, args, ws, flush):
                     h2d_into(nb)
                     copied[nb].record(copy_stream)
             stream.wait_event(copied[b])
-            compute_from(b)
+            compute(bufs[b])
             consumed[b].record(stream)
         stream.wait_stream(copy_stream)
 
@@ -546,6 +535,79 @@ def e2e_arm(step, args, ws, flush):
             "mode": f"pipelined over {n} steps (step i + 1's inputs copied while step i computes)",
             "serial_ms_per_step": round(ms_serial, 3),
             "serial_value": round(rows * ws / (ms_serial / 1e3), 1)}
+
+
+def e2e_arm(step, args, ws, flush):
+    """The benchmarked step end to end: each step copies its inputs (logits,
+    queries, beam state) to the device, runs the selection and the
+    attention, and reads the selection's outputs and the attention output
+    back."""
+    s = step.state
+    host = {"logits": step.logits.cpu().pin_memory(), "q": step.attn["q"].cpu().pin_memory()}
+    for k in ("cum", "node", "n_live", "slot"):
+        host[k] = s[k].cpu().pin_memory()
+    outs = ["tokens", "parents", "cum_out", "node_out", "n_live_out", "slot_out"]
+    host_out = {k: torch.empty_like(step.out_sel[k], device="cpu").pin_memory() for k in outs}
+    host_att = torch.empty_like(step.out_att, device="cpu").pin_memory()
+
+    def compute(d):
+        st = dict(cum=d["cum"], node=d["node"], n_live=d["n_live"], slot=d["slot"])
+        step.run(logits=d["logits"], q=d["q"], state=st)
+        for k in outs:
+            host_out[k].copy_(step.out_sel[k], non_blocking=True)
+        host_att.copy_(step.out_att, non_blocking=True)
+
+    return _e2e_loop(step, args, ws, flush, host, compute, list(host_out.values()) + [host_att])
+
+
+def e2e_lmhead_arm(step, args, ws, flush, H=2048):
+    """The step with the LM head in front (N2), end to end: each step copies
+    the beams' hidden states (bf16, hidden size H = 2048 as in Qwen3-1.7B),
+    the queries and the beam state to the device; the head GEMM reduces every
+    row to its log-sum-exp and writes only the level's window of logits (the
+    whole vocabulary without a trie), the selection takes the normalisers
+    (lse_in), the attention follows, and the selection's outputs and the
+    attention output are read back.  The head's weight [V, H] (random, bf16)
+    is resident, like any model weight.  This figure measures the library
+    rather than the host link: the per-step input is H x 2 bytes per beam
+    instead of V x 4."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl, dev, s = step.wl, step.dev, step.state
+    rows, V = wl.R * wl.W, wl.V
+    g = torch.Generator(device=dev).manual_seed(5)
+    hidden = torch.randn(rows, H, generator=g, device=dev).to(torch.bfloat16)
+    w = (torch.randn(V, H, generator=g, device=dev) * (2.0 / H ** 0.5)).to(torch.bfloat16)
+    lse = torch.empty(rows, dtype=torch.float32, device=dev)
+    logits = torch.empty((rows, V), dtype=torch.float32, device=dev)
+    ws_head = bd.workspace(bd.beam_lmhead_workspace_size(rows, V), dev)
+    tb = int(wl.token_base()[step.step]) if wl.levels else 0
+    win = wl.C if wl.levels else V
+    host = {"hidden": hidden.cpu().pin_memory(), "q": step.attn["q"].cpu().pin_memory()}
+    for k in ("cum", "node", "n_live", "slot"):
+        host[k] = s[k].cpu().pin_memory()
+    outs = ["tokens", "parents", "cum_out", "node_out", "n_live_out", "slot_out"]
+    host_out = {k: torch.empty_like(step.out_sel[k], device="cpu").pin_memory() for k in outs}
+    host_att = torch.empty_like(step.out_att, device="cpu").pin_memory()
+    a = step.attn
+
+    def compute(d):
+        bd.beam_lmhead_lse(d["hidden"], w, tb, win, lse_out=lse, logits_out=logits, ws=ws_head)
+        o = bd.beam_select(logits.view(wl.R, wl.W, V), d["cum"], d["node"], d["n_live"], d["slot"], step.trie,
+                           step.step, step.step, wl.K, lse_in=lse.view(wl.R, wl.W), out=step.out_sel,
+                           ws=step.ws_sel)
+        bd.beam_attn_decode(d["q"], a["shared_k"], a["shared_v"], a["prompt_offsets"], step.maxp,
+                            a["unshared_k"], a["unshared_v"], o["slot_out"], o["n_live_out"], step.step,
+                            k_scale=a["k_scale"], v_scale=a["v_scale"], out=step.out_att, ws=step.ws_att)
+        for k in outs:
+            host_out[k].copy_(step.out_sel[k], non_blocking=True)
+        host_att.copy_(step.out_att, non_blocking=True)
+
+    res = _e2e_loop(step, args, ws, flush, host, compute, list(host_out.values()) + [host_att])
+    assert bd.read_status(step.ws_sel) == 0 and bd.read_status(ws_head) == 0
+    res.update(hidden=H, window=win)
+    del w, logits, ws_head
+    torch.cuda.empty_cache()
+    return res
 
 
 def lmhead_arm(step, args, flush, H=2048):

@@ -5,8 +5,8 @@
 // a fused SID trie in CSR form keeps the illegal-SID rate at 0.
 //
 // The catalog is preprocessed once, not per decode step: items are sorted
-// lexicographically (packed into 64-bit keys when the code widths fit), de-
-// duplicated, and each level's CSR is read off the sorted order: sorted item
+// lexicographically (packed into 64-bit keys when the code widths fit, and
+// then sorted in slices on the host's cores and merged), de-duplicated, and each level's CSR is read off the sorted order: sorted item
 // i opens a new length-(t+1) prefix (an edge of level t) exactly when it
 // differs from item i-1 within its first t+1 codes.  The CSR arrays are then
 // uploaded to device memory owned by the handle.
@@ -16,6 +16,8 @@
 #include <cstring>
 #include <new>
 #include <numeric>
+#include <thread>
+#include <utility>
 #include <vector>
 
 #include "internal.h"
@@ -26,6 +28,41 @@ int bits_for(int32_t C) {
   int b = 0;
   while ((1ll << b) < (long long)C) ++b;
   return b;
+}
+
+// Ascending sort of (key, index) pairs: slices sorted on up to 16 threads,
+// then merged pairwise in rounds; the pairs are distinct (the index breaks
+// ties), so the result is the unique ascending order whatever the slicing.
+// Falls back to one thread when a thread cannot be started.
+void sort_pairs(std::vector<std::pair<uint64_t, int64_t>>& v) {
+  const int64_t n = (int64_t)v.size();
+  unsigned T = std::thread::hardware_concurrency();
+  T = T < 1 ? 1 : (T > 16 ? 16 : T);
+  if (n < (1 << 16) || T == 1) {
+    std::sort(v.begin(), v.end());
+    return;
+  }
+  std::vector<int64_t> b(T + 1);
+  for (unsigned i = 0; i <= T; ++i) b[i] = n * (int64_t)i / (int64_t)T;
+  auto run_all = [](std::vector<std::thread>& th) {
+    for (auto& t : th) t.join();
+  };
+  try {
+    std::vector<std::thread> th;
+    for (unsigned t = 0; t < T; ++t)
+      th.emplace_back([&v, &b, t] { std::sort(v.begin() + b[t], v.begin() + b[t + 1]); });
+    run_all(th);
+    for (unsigned w = 1; w < T; w *= 2) {
+      std::vector<std::thread> mt;
+      for (unsigned t = 0; t + w < T; t += 2 * w) {
+        const int64_t lo = b[t], mid = b[t + w], hi = b[std::min(t + 2 * w, T)];
+        mt.emplace_back([&v, lo, mid, hi] { std::inplace_merge(v.begin() + lo, v.begin() + mid, v.begin() + hi); });
+      }
+      run_all(mt);
+    }
+  } catch (...) {   // a thread could not be started (the joins above never throw)
+    std::sort(v.begin(), v.end());
+  }
 }
 
 }  // namespace
@@ -56,19 +93,18 @@ extern "C" int beam_trie_build(const int32_t* items, int64_t n_items, int levels
 
   // lexicographic order of the items
   std::vector<int64_t> order(n_items);
-  std::iota(order.begin(), order.end(), 0);
   if (total_bits <= 64) {
-    std::vector<uint64_t> key(n_items);
+    std::vector<std::pair<uint64_t, int64_t>> kp(n_items);
     for (int64_t i = 0; i < n_items; ++i) {
       uint64_t k = 0;
       for (int l = 0; l < levels; ++l)
         k = (total_bits ? (k << bits_for(codes_per_level[l])) : 0) | (uint64_t)items[i * levels + l];
-      key[i] = k;
+      kp[i] = {k, i};
     }
-    std::sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
-      return key[a] < key[b] || (key[a] == key[b] && a < b);
-    });
+    sort_pairs(kp);
+    for (int64_t i = 0; i < n_items; ++i) order[i] = kp[i].second;
   } else {
+    std::iota(order.begin(), order.end(), 0);
     std::sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
       const int32_t* x = items + a * levels;
       const int32_t* y = items + b * levels;
