@@ -78,26 +78,46 @@ def test_ragged_prompts_and_tails(gpu_lib):
             _check(wl, got, want)
 
 
+def _tile_beams(wl, n_live, extra=2, seed=0):
+    """The first and last live beam of every 256-row CTA tile (128 / G * 2
+    beams per tile) of every request, plus `extra` random live beams."""
+    per = 256 // wl.G
+    rng = np.random.default_rng(seed)
+    beams = []
+    for r, nl in enumerate(n_live):
+        js = set()
+        for j0 in range(0, nl, per):
+            js.update((j0, min(nl, j0 + per) - 1))
+        js.update(int(x) for x in rng.integers(0, nl, extra))
+        beams += [(r, j) for j in sorted(js)]
+    return beams
+
+
 def test_onerec17b_full_size_sampled(gpu_lib):
-    """The benchmarked shape: 4 requests x 512 beams x 16 heads, prompts 4096."""
+    """The benchmarked shape: 4 requests x 512 beams x 16 heads, prompts
+    4096; the first and last beam of every 256-row tile of every request."""
     wl = synth.WORKLOADS["onerec17b"]
-    beams = [(r, j) for r in range(wl.R) for j in (0, 1, 255, 510, 511)]
+    beams = _tile_beams(wl, [wl.W] * wl.R)
     got, want, _ = _run(wl, 2, [wl.W] * wl.R, beams=beams)
     _check(wl, got, want, beams)
 
 
 def test_fp8kv_full_size_sampled(gpu_lib):
+    """4 requests x 1000 beams, e4m3 KV, ragged prompts; every tile's first
+    and last live beam; dead beams zero."""
     wl = synth.WORKLOADS["fp8kv"]
-    beams = [(r, j) for r in range(wl.R) for j in (0, 333, 998)]
-    got, want, _ = _run(wl, 3, [wl.W, wl.W, 999, 500], beams=beams)
+    n_live = [wl.W, wl.W, 999, 500]
+    beams = _tile_beams(wl, n_live)
+    got, want, _ = _run(wl, 3, n_live, beams=beams)
     _check(wl, got, want, beams)
     assert np.all(got[2, 999:] == 0) and np.all(got[3, 500:] == 0)
 
 
 def test_openvocab_full_size_sampled(gpu_lib):
-    """2 requests x 5000 beams, 32 unshared tokens per beam at the last step."""
+    """2 requests x 5000 beams, 32 unshared tokens per beam at the last step
+    (the merge kernel); every tile's first and last beam."""
     wl = synth.WORKLOADS["openvocab"]
-    beams = [(r, j) for r in range(wl.R) for j in (0, 2500, 4999)]
+    beams = _tile_beams(wl, [wl.W] * wl.R)
     got, want, _ = _run(wl, 31, [wl.W] * wl.R, beams=beams)
     _check(wl, got, want, beams)
 
