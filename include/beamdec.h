@@ -132,7 +132,8 @@ int beam_lmhead_lse(const void* hidden, const void* weight, int rows, int hidden
  * 0 bd_expand_kernel (selection when lse_in is given), 1 bd_global_kernel,
  * 2 bd_attn_shared_simt_kernel, 3 bd_attn_shared_tc_kernel, 4 bd_attn_merge_kernel,
  * 5 bd_kv_e4m3_to_bf16_kernel, 6 bd_stream_select_kernel (the whole selection
- * step otherwise), 7 bd_lmhead_kernel, 8 bd_lmhead_lse_kernel.  Host-side state is process-wide; use from one host thread.
+ * step otherwise), 7 bd_lmhead_kernel, 8 bd_lmhead_lse_kernel, 9 bd_seed_kernel
+ * (open-vocabulary selection).  Host-side state is process-wide; use from one host thread.
  */
 int beamdec_profile_enable(int on);
 /* The same with a choice of kernels: bit k of kernel_mask brackets kernel id

@@ -84,6 +84,9 @@ struct SelectArgs {
   // one-launch kernel only: store each live row's scoring normaliser in the
   // workspace and stop (the expansion kernel then selects the rows)
   int lse_only;
+  // expansion kernel only: the workspace's seed histogram holds this call's
+  // seed of every request's cut (open-vocabulary rows)
+  int seeded;
 };
 int launch_select(const SelectArgs& a, cudaStream_t stream);
 
@@ -154,7 +157,7 @@ int sm_count();
 
 // ---- per-kernel event timing (off unless beamdec_profile_enable(1)) ---------
 enum KernelId { kKExpand = 0, kKGlobal = 1, kKAttnSimt = 2, kKAttnTc = 3, kKAttnMerge = 4,
-                kKKvConvert = 5, kKStream = 6, kKLmhead = 7, kKLmheadLse = 8, kKCount = 9 };
+                kKKvConvert = 5, kKStream = 6, kKLmhead = 7, kKLmheadLse = 8, kKSeed = 9, kKCount = 10 };
 void prof_begin(int kid, cudaStream_t s);
 void prof_end(int kid, cudaStream_t s);
 

@@ -25,7 +25,7 @@ int g_open[kKCount];
 const char* kNames[kKCount] = {"bd_expand_kernel", "bd_global_kernel", "bd_attn_shared_simt_kernel",
                                "bd_attn_shared_tc_kernel", "bd_attn_merge_kernel",
                                "bd_kv_e4m3_to_bf16_kernel", "bd_stream_select_kernel",
-                               "bd_lmhead_kernel", "bd_lmhead_lse_kernel"};
+                               "bd_lmhead_kernel", "bd_lmhead_lse_kernel", "bd_seed_kernel"};
 
 }  // namespace
 

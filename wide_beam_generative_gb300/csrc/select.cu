@@ -67,6 +67,7 @@ struct SelWs {
   uint32_t* hist;         // [R][kBins]
   uint32_t* cuthist;      // [R][kBins] score-bin counts of the pool when the
                           // cooperative kernel selects (the fused tail keeps them in hist)
+  uint32_t* seedhist;     // [R][kBins] score-bin counts of the cut seeds (open vocabulary)
   unsigned long long* pool;  // [R][W*Kp]
   unsigned long long* cand;  // [R][kSelectCap]
   float2* rowpart;        // [R][W][kMaxRowSplits] per-chunk (max, sum of exp)
@@ -83,6 +84,7 @@ __host__ __device__ inline SelWs carve(void* ws, int R, int W, int Kp) {
   s.rowtick = (int32_t*)p; p += align256((size_t)R * W * sizeof(int32_t));
   s.hist = (uint32_t*)p; p += align256((size_t)R * kBins * sizeof(uint32_t));
   s.cuthist = (uint32_t*)p; p += align256((size_t)R * kBins * sizeof(uint32_t));
+  s.seedhist = (uint32_t*)p; p += align256((size_t)R * kBins * sizeof(uint32_t));
   s.pool = (unsigned long long*)p; p += align256((size_t)R * W * Kp * 8);
   s.cand = (unsigned long long*)p; p += align256((size_t)R * kSelectCap * 8);
   s.rowpart = (float2*)p; p += align256((size_t)R * W * kMaxRowSplits * sizeof(float2));
@@ -347,9 +349,9 @@ __device__ __forceinline__ uint32_t cand_key(const SelectArgs& a, float cum, flo
 
 template <bool kG>
 __device__ __forceinline__ bool expand_wide(const SelectArgs& a, ExpandShared& sh, SelState* st,
-                                            unsigned long long* pool, uint32_t* gh, unsigned char* dyn,
-                                            const float* row, const int32_t* code, int tb, int n, int r,
-                                            int b, float cum, float lse, float ref);
+                                            unsigned long long* pool, uint32_t* gh, const uint32_t* seed,
+                                            unsigned char* dyn, const float* row, const int32_t* code,
+                                            int tb, int n, int r, int b, float cum, float lse, float ref);
 
 template <bool kPf, bool kG, bool kD>
 __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandShared& sh, const SelWs& ws,
@@ -492,8 +494,8 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
   // exact fallback for heavy ties
   if constexpr (!kPf) {
     if (!cached && kcache != nullptr && gh != nullptr &&
-        expand_wide<kG>(a, sh, st, pool, gh, reinterpret_cast<unsigned char*>(kcache), row, code, tb, n, r,
-                        b, cum, lse, ref))
+        expand_wide<kG>(a, sh, st, pool, gh, a.seeded ? ws.seedhist + (size_t)r * kBins : nullptr,
+                        reinterpret_cast<unsigned char*>(kcache), row, code, tb, n, r, b, cum, lse, ref))
       return;
   }
   auto kc = [&](int i) -> uint32_t { return cached ? kcache[i] : key_of(tok_of(i)); };
@@ -942,9 +944,9 @@ __device__ __forceinline__ void add_cut_hist(uint32_t* gh, const uint32_t* lh, i
 }
 template <bool kG>
 __device__ __forceinline__ bool expand_wide(const SelectArgs& a, ExpandShared& sh, SelState* st,
-                                            unsigned long long* pool, uint32_t* gh, unsigned char* dyn,
-                                            const float* row, const int32_t* code, int tb, int n, int r,
-                                            int b, float cum, float lse, float ref) {
+                                            unsigned long long* pool, uint32_t* gh, const uint32_t* seed,
+                                            unsigned char* dyn, const float* row, const int32_t* code,
+                                            int tb, int n, int r, int b, float cum, float lse, float ref) {
   static_assert(kTailBins * 4 + kWideBuf * 8 <= kTailCap * 8, "wide-row buffers");
   static_assert(kExpandThreads / 32 * 128 <= 2048, "64 staged pairs per warp in sh.hist");
   static_assert(kLadder <= 32, "ladder counts in sh.warp_cnt");
@@ -1048,9 +1050,14 @@ __device__ __forceinline__ bool expand_wide(const SelectArgs& a, ExpandShared& s
     queued = 0;
   };
 
-  // the request's cut (a snapshot: counts only grow, so it stays valid)
+  // the request's cut (a snapshot: counts only grow, so it stays valid);
+  // before its pool has W candidates, the cut its seed gives
   block_scan_bins(gh, lh, (uint32_t)a.W, sh);
   int bcut = (int)sh.digit;
+  if (seed != nullptr && bcut >= kTailBins - 1) {
+    block_scan_bins(seed, lh, (uint32_t)a.W, sh);
+    bcut = (int)sh.digit;
+  }
   // A logit below x_lo(bin) cannot reach that bin, and one at or above
   // x_hi(bin) reaches it or an earlier one: each bound lies one bin (1/64)
   // beyond the bin's edge, and near that edge the float32 roundings of the
@@ -1414,6 +1421,59 @@ bd_expand_kernel(SelectArgs a) {
   expand_and_select<kFused, false, kG, kD>(a, sh, ws, r, b, nl, lse, tail_smem);
 }
 
+// Seeds of the open-vocabulary requests' cuts, before their rows expand (the
+// rows that start while a request's pool holds fewer than W candidates
+// would otherwise have no cut).  Every thread takes the maximum of `span`
+// consecutive logits of one of a request's first kSeedRows live rows and
+// counts the score bin the expansion computes for that candidate in the
+// request's seed histogram.  Each maximum is a real candidate of its row,
+// and span >= V / K keeps a row's maxima at most K, so a row holding x of
+// them at or above a bin holds at least x of its top_k there: once W of them
+// lie at or above bin b*, a candidate in a later bin ranks below W pool
+// candidates, which is the request's cut.
+constexpr int kSeedRows = 16;
+inline int seed_span(int V, int K) {
+  int s = (V + K - 1) / K;
+  if (s < 16) s = 16;
+  return (s + 3) & ~3;   // whole float4 groups
+}
+__global__ void __launch_bounds__(kExpandThreads) bd_seed_kernel(SelectArgs a, int span) {
+  __shared__ uint32_t bins[kTailBins];   // the block's counts, added to the request's once per bin
+  const int r = blockIdx.z, b = blockIdx.y;
+  if (b >= a.n_live_in[r]) return;
+  for (int i = threadIdx.x; i < kTailBins; i += kExpandThreads) bins[i] = 0;
+  const SelWs ws = carve(a.ws, a.R, a.W, a.Kp);
+  const size_t rowi = (size_t)r * a.W + b;
+  const float* row = a.logits + rowi * (size_t)a.row_stride;
+  const long long i0 = ((long long)blockIdx.x * kExpandThreads + threadIdx.x) * span;
+  const bool on = i0 < a.V;
+  float m = -INFINITY;
+  if (on) {
+    const int n = (int)min((long long)span, (long long)a.V - i0);
+    const float* x = row + i0;
+    int j = 0;
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
+      const float4* x4 = reinterpret_cast<const float4*>(x);
+#pragma unroll 8
+      for (; j + 4 <= n; j += 4) {
+        const float4 v = __ldg(x4 + (j >> 2));
+        m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+      }
+    }
+    for (; j < n; ++j) m = fmaxf(m, __ldg(x + j));
+  }
+  const float lse = a.lse_in[rowi];   // the caller's, or the normaliser stream's in the workspace
+  const float cum = a.cum_in[rowi];
+  const float ref = bin_ref<false>(a, a.cum_in[(size_t)r * a.W]);
+  const uint32_t k = on ? cand_key<false>(a, cum, lse, m, r, b, 0) : 0u;
+  __syncthreads();   // the block's bins are zero
+  if (on) atomicAdd(bins + score_bin(ref, desc_key_value(k)), 1u);
+  __syncthreads();
+  uint32_t* sh = ws.seedhist + (size_t)r * kBins;
+  for (int i = threadIdx.x; i < kTailBins; i += kExpandThreads)
+    if (bins[i] != 0u) atomicAdd(sh + i, bins[i]);
+}
+
 // The whole selection step in one launch: S blocks per live logits row each
 // fold (max, sum of exp) of one chunk of the row (a1); the last of them (a
 // per-row ticket) combines the chunks into the row's log-sum-exp and goes on
@@ -1699,7 +1759,7 @@ size_t select_workspace_bytes(int R, int W, int K, int V) {
   const int Kp = K < V ? K : V;
   return kWsHeaderBytes + align256((size_t)R * sizeof(SelState)) +
          align256((size_t)R * W * sizeof(int32_t)) +
-         2 * align256((size_t)R * kBins * sizeof(uint32_t)) + align256((size_t)R * W * Kp * 8) +
+         3 * align256((size_t)R * kBins * sizeof(uint32_t)) + align256((size_t)R * W * Kp * 8) +
          align256((size_t)R * kSelectCap * 8) +
          align256((size_t)R * W * kMaxRowSplits * sizeof(float2)) + (size_t)R * W * sizeof(float);
 }
@@ -1777,6 +1837,17 @@ int launch_select(const SelectArgs& a, cudaStream_t stream) {
     a2.lse_in = ws.rowlse;   // the scoring normaliser of every live row
     a2.lse_out = nullptr;    // already written with the kernel's own value
     a2.score_lse = nullptr;
+  }
+  if (a2.lse_in != nullptr && !gumbel && !a.has_trie && a.V > kKeyCache && a.K < a.V) {
+    // seeds of the requests' cuts for the open-vocabulary expansion
+    const int span = seed_span(a.V, a.K);
+    const int per_block = kExpandThreads * span;
+    const dim3 gs((unsigned)((a.V + per_block - 1) / per_block), kSeedRows, (unsigned)a.R);
+    prof_begin(kKSeed, stream);
+    bd_seed_kernel<<<gs, kExpandThreads, 0, stream>>>(a2, span);
+    prof_end(kKSeed, stream);
+    if (cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
+    a2.seeded = 1;
   }
   if (a2.lse_in == nullptr) {
     dim3 g0(a.W * S, a.R);
