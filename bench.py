@@ -345,6 +345,8 @@ def gpu_arm(args, ws, rank, local):
     if args.requests:
         wl = wl.scaled(R=args.requests, prompt_lens=None if wl.prompt_lens is None else
                        list(wl.prompt_lens[:1]) * args.requests)
+    if args.beams:
+        wl = wl.scaled(W=args.beams, K=min(wl.K, args.beams))
     step = Step(wl, dev)
     rows = step.rows()
     flush = L2Flush(dev)
@@ -961,6 +963,8 @@ def main():
     ap.add_argument("--no-chain", action="store_true", help="skip the whole-chain CUDA-graph replay")
     ap.add_argument("--requests", type=int, default=None,
                     help="override the workload's request count (smaller cases for profiling)")
+    ap.add_argument("--beams", type=int, default=None,
+                    help="override the workload's beam width (top_k capped to it; smaller cases for profiling)")
     ap.add_argument("--lmhead-only", type=int, default=0, metavar="VOCAB",
                     help="profiling aid: run only the fused LM head (2048 rows, hidden 2048) over VOCAB "
                          "tokens, warm-up + 1 launch, and print its time")

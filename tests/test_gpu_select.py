@@ -207,6 +207,18 @@ def test_large_rows_with_ties(gpu_lib, mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
+def test_open_vocab_odd_vocab(gpu_lib, mode):
+    """An odd vocabulary above the key cache (12289 tokens): every row but
+    the first starts off a 16-byte boundary, so the normaliser stream, the
+    cut seeds and the wide-row select take their unaligned paths; few live
+    beams at step 0, then a top_k of 3 and of 2000."""
+    wl = synth.WORKLOADS["openvocab"].scaled(name="ov-odd", R=2, W=24, K=24, T=4, V=12289)
+    run_chain(wl, None, steps=3, mode=mode)
+    run_chain(wl, None, steps=2, K=3, mode=mode)
+    run_chain(wl, None, steps=2, K=2000, mode=mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
 def test_trie_node_above_key_cache(gpu_lib, mode):
     """A root with 16384 children (more than the 8192 keys a block caches):
     the large-row path enumerates the node's CSR code list."""
