@@ -56,7 +56,8 @@ struct SelState {
   int32_t tickets;            // expand blocks of the request that have finished
   int32_t bin_mode;           // 1: the pool is gathered by score bin (no radix passes)
   int32_t bin_cut;            // last score bin gathered in bin mode
-  int32_t pad[4];
+  uint32_t cutq;              // wide-row select: kTailBins - 1 - the tightest cut bin published (0: none)
+  int32_t pad[3];
 };
 static_assert(sizeof(SelState) == 64, "state size");
 
@@ -925,6 +926,7 @@ __device__ void smem_take_smallest(unsigned long long* keys, int nc, int nt, Exp
 // dyn: the 32 KB dynamic buffer (histogram in the lower 16 KB, candidates in
 // the upper 16 KB); sh.hist holds the warps' staged logits during a pass.
 constexpr int kWideBuf = 2048;   // (key << 32 | index) entries
+constexpr int kCutScanEvery = 16;  // rows between two scans of the pool's bin counts
 // Bins of the counting ladder, counted from the bin of the beam's own score:
 // 1.5 to 24 nats below it (64 bins per nat).
 constexpr int kLadder = 12;
@@ -1050,13 +1052,24 @@ __device__ __forceinline__ bool expand_wide(const SelectArgs& a, ExpandShared& s
     queued = 0;
   };
 
-  // the request's cut (a snapshot: counts only grow, so it stays valid);
-  // before its pool has W candidates, the cut its seed gives
-  block_scan_bins(gh, lh, (uint32_t)a.W, sh);
+  // the request's cut: the tightest one its rows have published (one load);
+  // while none is, and in every kCutScanEvery-th row, a snapshot of the
+  // pool's bin counts (counts only grow, so a snapshot stays valid) and,
+  // before the pool holds W candidates, the cut its seed gives, which the
+  // row publishes
+  if (tid == 0) sh.digit = (uint32_t)(kTailBins - 1) - __ldcg(&st->cutq);
+  __syncthreads();
   int bcut = (int)sh.digit;
-  if (seed != nullptr && bcut >= kTailBins - 1) {
-    block_scan_bins(seed, lh, (uint32_t)a.W, sh);
-    bcut = (int)sh.digit;
+  __syncthreads();   // read before the scan below rewrites sh.digit
+  if (bcut >= kTailBins - 1 || b % kCutScanEvery == 0) {
+    block_scan_bins(gh, lh, (uint32_t)a.W, sh);
+    int c = (int)sh.digit;
+    if (seed != nullptr && c >= kTailBins - 1) {
+      block_scan_bins(seed, lh, (uint32_t)a.W, sh);
+      c = (int)sh.digit;
+    }
+    bcut = c < bcut ? c : bcut;
+    if (tid == 0 && bcut < kTailBins - 1) atomicMax(&st->cutq, (uint32_t)(kTailBins - 1 - bcut));
   }
   // A logit below x_lo(bin) cannot reach that bin, and one at or above
   // x_hi(bin) reaches it or an earlier one: each bound lies one bin (1/64)
