@@ -524,17 +524,24 @@ def _e2e_loop(step, args, ws, flush, host, compute, host_outs):
     ms_serial = max_over_ranks(sum(times) / n, ws)
     pipelined(2)
     torch.cuda.synchronize()
-    flush()
-    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    pipelined(n)
-    e.record(stream)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(a.elapsed_time(e) / n, ws)
+    trials = []
+    for _ in range(3):   # the host link's rate varies between runs: the median of three loops
+        flush()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        pipelined(n)
+        e.record(stream)
+        torch.cuda.synchronize()
+        trials.append(a.elapsed_time(e) / n)
+    ms_pipe = max_over_ranks(sorted(trials)[1], ws)
     rows = step.rows()
+    # the serving loop runs whichever schedule is faster on this host
+    ms = min(ms_pipe, ms_serial)
+    mode = (f"pipelined over {n} steps (step i + 1's inputs copied while step i computes), median of 3"
+            if ms_pipe <= ms_serial else f"one step at a time over {n} steps (faster than the pipelined loop here)")
     return {"value": round(rows * ws / (ms / 1e3), 1), "unit": "beam-rows/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 3),
-            "mode": f"pipelined over {n} steps (step i + 1's inputs copied while step i computes)",
+            "mode": mode, "pipelined_ms_per_step": [round(x, 3) for x in trials],
             "serial_ms_per_step": round(ms_serial, 3),
             "serial_value": round(rows * ws / (ms_serial / 1e3), 1)}
 

@@ -405,6 +405,9 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
 
+  // the timeout test hook (0 in normal use), loaded with the CTA's first
+  // loads so that its latency hides behind theirs
+  const uint32_t probe = *reinterpret_cast<volatile uint32_t*>(&p.hdr->probe_polls);
   const int mt = blockIdx.x;
   const int g = blockIdx.y % p.Hkv;
   const int sp = blockIdx.y / p.Hkv;
@@ -458,7 +461,6 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t probe = *reinterpret_cast<volatile uint32_t*>(&p.hdr->probe_polls);
   if (probe != 0u) {   // test hook (block-uniform): a wait that runs out
     if (threadIdx.x == 0 && !mbar_wait(&bars.probe, 0, probe)) abort_sh = 1;
     __syncthreads();

@@ -84,6 +84,9 @@ bd_lmhead_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the timeout test hook (0 in normal use), loaded first so that its
+  // latency hides behind the set-up below
+  const uint32_t probe = *reinterpret_cast<volatile uint32_t*>(&p.hdr->probe_polls);
   const int nk = p.hidden / kBK;
   const int total = p.m_tiles * p.n_tiles;
 
@@ -106,7 +109,6 @@ bd_lmhead_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t probe = *reinterpret_cast<volatile uint32_t*>(&p.hdr->probe_polls);
   if (probe != 0u) {   // test hook (block-uniform): a wait that runs out
     if (threadIdx.x == 0 && !mbar_wait(&bars.probe, 0, probe)) abort_sh = 1;
     __syncthreads();
