@@ -108,6 +108,32 @@ struct TcParams {
   const float* v_scale;
 };
 
+// Low word of a 128-byte-swizzle shared-memory descriptor (start address and
+// leading byte offset, 16-byte units); the high word (stride byte offset,
+// version 1, swizzle mode) is the same for every operand of this kernel.  The
+// ring and Q lie below 256 KB, so a byte offset added to the address adds
+// offset >> 4 to the low word without a carry out of its 14-bit field.
+__device__ __forceinline__ uint32_t desc_lo(uint32_t addr, uint32_t lbo) {
+  return ((addr & 0x3FFFFu) >> 4) | (((lbo & 0x3FFFFu) >> 4) << 16);
+}
+constexpr uint32_t desc_hi(uint32_t sbo) { return ((sbo & 0x3FFFFu) >> 4) | (1u << 14) | (2u << 29); }
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 da, db;\n setp.ne.b32 p, %5, 0;\n"
+      " mov.b64 da, {%1, %3};\n mov.b64 db, {%2, %3};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 db;\n setp.ne.b32 p, %4, 0;\n"
+      " mov.b64 db, {%2, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(hi));
+}
+
 struct Bars {
   uint64_t q;
   uint64_t kv_full[kSlots], kv_empty[kSlots];
@@ -507,23 +533,24 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     auto wait_kv = [&](int i) -> bool {
       return mbar_wait(&bars.kv_full[i % kSlots], (uint32_t)(i / kSlots) & 1);
     };
+    const uint32_t hi = desc_hi(1024);   // Q, K and V: 8-row groups 1024 bytes apart
+    const uint32_t q_lo = desc_lo(qa, 16), k_lo = desc_lo(kvb, 16), v_lo = desc_lo(kvb, kVLbo);
     auto issue_s = [&](int t, int c) {   // S_t = Q_t K(c)^T
-      const uint32_t kb = kvb + ((2 * c) % kSlots) * kTileBytes;
-      const uint32_t qt = qa + t * kTileBytes;
+      const uint32_t kb = k_lo + (uint32_t)((2 * c) % kSlots) * (kTileBytes >> 4);
+      const uint32_t qt = q_lo + (uint32_t)t * (kTileBytes >> 4);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-        mma_bf16(tmem + t * 256, sdesc_sw128(qt + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                 idS, k > 0);
+        const uint32_t off = ((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4;
+        mma_ss(tmem + t * 256, qt + off, kb + off, hi, idS, k > 0);
       }
       mma_commit(&bars.s_full[t]);
     };
     auto issue_pv = [&](int t, int c) {   // O_t += P_t V(c), P_t read from TMEM
-      const uint32_t vb = kvb + ((2 * c + 1) % kSlots) * kTileBytes;
+      const uint32_t vb = v_lo + (uint32_t)((2 * c + 1) % kSlots) * (kTileBytes >> 4);
 #pragma unroll
       for (int k = 0; k < 8; ++k)   // 16 keys = 8 columns of packed bf16 pairs per step
-        mma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + k * 8,
-                    sdesc_sw128(vb + k * 16 * 128, kVLbo, kVSbo), idO, (c > 0 || k > 0) ? 1u : 0u);
+        mma_ts(tmem + t * 256 + 128, tmem + t * 256 + k * 8, vb + ((k * 16 * 128) >> 4), hi, idO,
+               (c > 0 || k > 0) ? 1u : 0u);
     };
     bool ok = mbar_wait(&bars.q, 0) && wait_kv(0);
     if (ok) {
