@@ -417,6 +417,24 @@ __device__ __forceinline__ void zero_rows(const TcParams& p, int r, int g, int r
   }
 }
 
+// CTAs are dispatched in block-index order with blockIdx.z slowest, so the
+// z-th plane of the grid takes the request with the z-th longest prompt
+// (ties by index): the longest requests start first and the short ones fill
+// the SMs behind them.  Up to 32 requests are ranked (one per lane, every
+// warp the same); more keep the index order.
+__device__ __forceinline__ int request_by_length(const int32_t* off, int R, int z) {
+  if (R > 32) return z;
+  const int lane = threadIdx.x & 31;
+  const int len = lane < R ? off[lane + 1] - off[lane] : -1;
+  int rank = 0;
+  for (int j = 0; j < R; ++j) {
+    const int lj = __shfl_sync(0xffffffffu, len, j);
+    rank += (lj > len || (lj == len && j < lane)) ? 1 : 0;
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, lane < R && rank == z);
+  return hit ? __ffs(hit) - 1 : z;
+}
+
 // Eleven warps: the register file is handed out in groups of four warps, so a
 // thread may hold at most 65536 / 384 -> 168 registers (a tenth or eleventh
 // warp costs no registers).
@@ -437,7 +455,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   const int mt = blockIdx.x;
   const int g = blockIdx.y % p.Hkv;
   const int sp = blockIdx.y / p.Hkv;
-  const int r = blockIdx.z;
+  const int r = request_by_length(p.prompt_offsets, p.R, blockIdx.z);
   const int row0 = mt * 256;
   const int G = p.G;
   if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 &&
