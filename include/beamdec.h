@@ -26,6 +26,16 @@
  * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *   Compute entry points only enqueue work: they never synchronise the host,
  *   never allocate, and return as soon as the kernels are launched.
+ * - Overlap between calls: beam_select's kernels let a kernel launched after
+ *   them with programmatic stream serialization begin while they drain; such
+ *   a kernel must execute griddepcontrol.wait before it reads any output of
+ *   the selection.  beam_attn_decode launches its kernels that way: they read
+ *   q and the prompt K/V (and, with E4M3 KV, nothing else) before waiting,
+ *   and slot_table, n_live and the unshared K/V only after the previous
+ *   kernel in the stream has completed.  A kernel the caller launches just
+ *   before beam_attn_decode that itself lets dependents begin early must have
+ *   finished writing q and the prompt K/V by then; kernels that do not (the
+ *   default) give the usual stream order.
  * - Return value: BEAMDEC_OK or a negative BEAMDEC_ERR_* code.  Argument
  *   errors are detected on the host before anything is launched.  Errors a
  *   kernel detects (a slot index out of range, a bounded wait that ran out)
@@ -426,10 +436,13 @@ int beam_attn_workspace_size(int R, int W, int Hq, int Hkv, int d, int max_promp
  * F32/F32/F32, BF16/BF16/BF16, BF16/E4M3/BF16.  BF16 queries with d = 128
  * and a group size dividing 128 take the tensor-core shared stage (fp8 KV is
  * first dequantised to bf16 in the workspace); other shapes run it on CUDA
- * cores.  When that stage covers every prompt in one split (bf16 KV, at most
- * 64 unshared tokens, q / unshared K, V / out 16-byte aligned), the unshared
- * stage and the merge run in its epilogue and the partials never leave the
- * kernel; otherwise a merge kernel reads them from the workspace.
+ * cores.  When that stage covers every prompt in one split (at most 6
+ * unshared tokens, q / unshared K, V / out 16-byte aligned, BF16 output),
+ * the unshared stage and the merge run in its epilogue and the partials
+ * never leave the kernel; otherwise a merge kernel reads them from the
+ * workspace.  The tensor-core stage (and the fp8 dequantisation) launch as
+ * programmatic dependents of the previous kernel in the stream (see the
+ * conventions above).
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  */
 int beam_attn_decode(const void* q, const void* shared_k, const void* shared_v,

@@ -47,6 +47,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <utility>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -83,6 +85,10 @@ constexpr uint32_t kVSbo = 1024;
 
 struct TcParams {
   int R, W, Hq, Hkv, G, rows, split_len;
+  // launched as a programmatic dependent of the previous kernel: wait for it
+  // before reading the slot table or the live counts (late: after the main
+  // loop; early: before everything, so dead tiles can skip the main loop)
+  int dep_wait_late;
   float scale_log2;   // sm_scale * log2(e)
   const float* k_scale;   // per kv head; fp8 KV only (nullptr otherwise)
   int64_t shared_rows;
@@ -417,6 +423,9 @@ __device__ __forceinline__ void zero_rows(const TcParams& p, int r, int g, int r
   }
 }
 
+// Wait for the grid this one depends on (returns at once when there is none).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // CTAs are dispatched in block-index order with blockIdx.z slowest, so the
 // z-th plane of the grid takes the request with the z-th longest prompt
 // (ties by index): the longest requests start first and the short ones fill
@@ -461,7 +470,8 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 &&
       (int64_t)p.prompt_offsets[p.R] != p.shared_rows)
     set_status(p.hdr, BEAMDEC_ERR_DEVICE_CHECK);   // the K/V maps end at shared_rows
-  if (row0 >= p.n_live[r] * G) {   // every row of the CTA is a dead beam
+  if (!p.dep_wait_late) grid_dep_wait();
+  if (!p.dep_wait_late && row0 >= p.n_live[r] * G) {   // every row of the CTA is a dead beam
     if (p.fuse) zero_rows(p, r, g, row0);
     return;
   }
@@ -474,6 +484,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     if (!p.fuse) {
       write_empty_partials(p, prow_base, row0);
     } else if (threadIdx.x < 256) {   // empty prompt: the unshared tokens alone
+      grid_dep_wait();
       const int t = threadIdx.x >> 7, rit = threadIdx.x & 127;
       float* ps = reinterpret_cast<float*>(sm + kOffKV + (uint32_t)t * (128u * 512u)) + rit;
       fused_row(p, r, g, row0 + threadIdx.x, nullptr, rit, 0u, false, -INFINITY, 0.f,
@@ -609,6 +620,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     // ------------------------------------------------------------ L2 prefetch
     // pulls this CTA's unshared K/V rows into L2 while the shared stage runs,
     // so the fused epilogue reads them from L2
+    grid_dep_wait();
     const int TW = p.T * p.W, nb = 256 / G, j0 = row0 / G, nl = p.n_live[r];
     for (int i = lane; i < nb * p.L; i += 32) {
       const int jj = i / p.L, u = i - jj * p.L;
@@ -708,6 +720,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
     if (!ok) abort_sh = 1;
     const int row = row0 + t * 128 + row_in_tile;
     if (p.fuse) {   // unshared stage + merge here; the K/V ring is idle now
+      grid_dep_wait();
       if (ok) {
         fence_after_sync();
         float* ps = reinterpret_cast<float*>(sm + kOffKV + (uint32_t)t * (128u * 512u)) + row_in_tile;
@@ -761,10 +774,15 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
 // value), rows [0, prompt_offsets[R]), for the tensor-core shared stage.  The
 // per-head scales are not applied here: K's scale multiplies the softmax
 // scale and V's scale the merged output.
+// It reads nothing the selection writes, so it is launched as a programmatic
+// dependent of the previous kernel and lets the shared stage launch the same
+// way; each thread waits for the previous grid before it exits, so that this
+// grid's completion (which the shared stage waits for) implies that one's.
 __global__ void __launch_bounds__(256)
 bd_kv_e4m3_to_bf16_kernel(const uint8_t* __restrict__ k8, const uint8_t* __restrict__ v8,
                           __nv_bfloat16* __restrict__ k16, __nv_bfloat16* __restrict__ v16,
                           const int32_t* prompt_offsets, int R, int64_t row_elems) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t n16 = (int64_t)prompt_offsets[R] * row_elems / 16;   // 16-element groups
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n16;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -787,9 +805,28 @@ bd_kv_e4m3_to_bf16_kernel(const uint8_t* __restrict__ k8, const uint8_t* __restr
     dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
   }
+  grid_dep_wait();
 }
 
 // ---- host side ------------------------------------------------------------------
+
+// Launch with programmatic stream serialization (the kernel may begin before
+// the previous kernel in the stream completes, when that kernel allows it).
+template <class... P, class... A>
+cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 }  // namespace
 
 bool attn_tc_supported(int q_dtype, int kv_dtype, int d, int G) {
@@ -837,11 +874,12 @@ int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t st
     if (blocks > 8 * sm_count()) blocks = 8 * sm_count();
     if (blocks < 1) blocks = 1;
     prof_begin(kKKvConvert, stream);
-    bd_kv_e4m3_to_bf16_kernel<<<blocks, 256, 0, stream>>>(
-        static_cast<const uint8_t*>(a.shared_k), static_cast<const uint8_t*>(a.shared_v), k16, v16,
-        a.prompt_offsets, a.R, (int64_t)a.Hkv * a.d);
+    const cudaError_t ce = launch_dependent(bd_kv_e4m3_to_bf16_kernel, dim3(blocks), dim3(256), 0, stream,
+                                            static_cast<const uint8_t*>(a.shared_k),
+                                            static_cast<const uint8_t*>(a.shared_v), k16, v16,
+                                            a.prompt_offsets, a.R, (int64_t)a.Hkv * a.d);
     prof_end(kKKvConvert, stream);
-    if (cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
+    if (ce != cudaSuccess || cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
     kbase = k16;
     vbase = v16;
   }
@@ -887,9 +925,18 @@ int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t st
   p.v_scale = a.kv_dtype == BEAMDEC_E4M3 ? a.v_scale : nullptr;
   dim3 grid((p.rows + 255) / 256, a.Hkv * pl.n_split, a.R);
   prof_begin(kKAttnTc, stream);
-  bd_attn_shared_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qm, km, vm, p);
+  // A programmatic dependent of the previous kernel in the stream: its CTAs
+  // may start while that kernel drains, if it allows it (the selection's
+  // kernels do).  The main loop reads only Q and the prompt K/V; the slot
+  // table and the live counts are read after the previous grid completes.
+  // At step 0 (one live beam per request) the CTAs wait first, so that
+  // dead tiles skip the main loop; the bf16 copy of e4m3 K/V is waited for
+  // before the main loop too.
+  p.dep_wait_late = (a.step > 0 && !(a.kv_dtype == BEAMDEC_E4M3 && a.shared_rows > 0)) ? 1 : 0;
+  const cudaError_t le = launch_dependent(bd_attn_shared_tc_kernel, grid, dim3(kThreads), kSmemBytes, stream,
+                                          qm, km, vm, p);
   prof_end(kKAttnTc, stream);
-  return cudaGetLastError() == cudaSuccess ? BEAMDEC_OK : BEAMDEC_ERR_CUDA;
+  return le == cudaSuccess && cudaGetLastError() == cudaSuccess ? BEAMDEC_OK : BEAMDEC_ERR_CUDA;
 }
 
 }  // namespace bd

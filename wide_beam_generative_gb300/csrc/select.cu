@@ -1423,6 +1423,7 @@ __device__ __forceinline__ void expand_and_select(const SelectArgs& a, ExpandSha
 template <bool kFused, bool kG, bool kD>
 __global__ void __launch_bounds__(kExpandThreads, kG ? 1 : 2)
 bd_expand_kernel(SelectArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // as in the stream kernel
   __shared__ ExpandShared sh;
   extern __shared__ __align__(16) unsigned char tail_smem[];
   const int r = blockIdx.x, b = blockIdx.y;   // the first rows of every request run first
@@ -1497,6 +1498,10 @@ __global__ void __launch_bounds__(kExpandThreads) bd_seed_kernel(SelectArgs a, i
 template <bool kFused, bool kG>
 __global__ void __launch_bounds__(kExpandThreads, 4)
 bd_stream_select_kernel(SelectArgs a) {
+  // a kernel launched after this one with programmatic stream serialization
+  // may start once every block of this grid has begun; it must wait for the
+  // grid's completion before reading any of its outputs
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ ExpandShared sh;
   extern __shared__ __align__(16) unsigned char tail_smem[];
   const int S = a.row_splits;
