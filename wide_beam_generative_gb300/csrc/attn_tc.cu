@@ -483,6 +483,7 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   if (k1 <= k0) {   // this split holds no key of the request
     if (!p.fuse) {
       write_empty_partials(p, prow_base, row0);
+      if (threadIdx.x == 0) grid_dep_wait();   // this grid ends after the previous one
     } else if (threadIdx.x < 256) {   // empty prompt: the unshared tokens alone
       grid_dep_wait();
       const int t = threadIdx.x >> 7, rit = threadIdx.x & 127;
@@ -764,6 +765,11 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   fence_before_sync();
   __syncthreads();
   if (abort_sh && threadIdx.x == 0) set_status(p.hdr, BEAMDEC_ERR_TIMEOUT);
+  // Whatever the path, one thread of every CTA waits for the previous grid
+  // before exiting, so this grid completes only after that one: the kernels
+  // after it in the stream (the merge kernel reads the slot table) keep the
+  // ordinary stream order.
+  if (threadIdx.x == 0) grid_dep_wait();
   if (warp == 9) {
     fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
