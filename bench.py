@@ -463,7 +463,10 @@ def gpu_arm(args, ws, rank, local):
                    "rows_per_step_per_gpu": rows, "l2": f"flushed before each step: a {L2_FLUSH_BYTES >> 20} MB write, then a "
                          f"{L2_FLUSH_BYTES >> 20} MB read so that no dirty line of the flush is left to "
                          f"write back inside the timed step",
-                   "parallelism": f"request-sharded replicas x{ws}"},
+                   "parallelism": f"request-sharded replicas x{ws}",
+                   "launch": "the attention's shared stage is a programmatic dependent of the selection "
+                             "(its main loop reads only the step's Q and prompt K/V; the slot table and "
+                             "live counts after the selection completes)"},
         "roofline": roof, "step_roofline": step_roof, "kernels": kernels,
         "kernels_note": "per-kernel event times from a pass of the same steps just before the timed "
                         "region (events between kernels stop the shared stage from starting while the "
