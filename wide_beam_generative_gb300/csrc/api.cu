@@ -37,11 +37,14 @@ AttnPlan attn_plan(int R, int W, int Hq, int Hkv, int d, int max_prompt_len, int
   const int chunk = 128;
   const int chunks = max_prompt_len > 0 ? (max_prompt_len + chunk - 1) / chunk : 1;
   // split count from a small time model (microseconds): each wave of CTAs
-  // costs its chunks (about 1.1 us per 128 keys for a 256-row tile on the
-  // tensor cores) plus a 2 us prologue, and every split's partial triples are
-  // read back by the merge at about 6 TB/s.
-  const double chunk_us = p.tensor_core ? 1.1 : 4.0;
-  const double part_us = (double)R * Hkv * rows * (d + 2) * 4 / 6.0e6;
+  // costs its chunks (about 1.75 us per 128 keys for a 256-row tile on the
+  // tensor cores, measured in a busy kernel) plus a 2 us prologue; every
+  // split's partial triples are read back by the merge at about 6 TB/s, and
+  // each split adds about 0.5 us of the merge's dependent reads (a 1 x 50
+  // beam, 2048-key step measured 50.0 / 46.0 / 47.8 / 54.3 us at 16 / 8 / 4
+  // / 2 splits).
+  const double chunk_us = p.tensor_core ? 1.75 : 4.0;
+  const double part_us = (double)R * Hkv * rows * (d + 2) * 4 / 6.0e6 + 0.5;
   int best = 1;
   double best_cost = 1e30;
   for (int s = 1; s <= 16 && s <= chunks; ++s) {
