@@ -165,3 +165,30 @@ def test_fixed_lse_select_validates_on_host(L):
         assert L.beam_select_fixed_lse(*head, FAKE, *rest, t, 0, *outs) == bd.ERR_INVALID_ARG, t
     for t in (0.0, 0.7):   # valid: reaches the same shape checks as beam_select
         assert L.beam_select_fixed_lse(*head, FAKE, *rest, t, 0, *outs) == bd.ERR_WORKSPACE
+
+
+def _splits_from_workspace(bd, R, W, Hq, Hkv, d, P):
+    """Prompt splits the attention planner chose, read back from the
+    workspace size (bf16 KV: header + per split and query row an (m, l)
+    pair and a d-float partial output, each array 256-byte padded)."""
+    rows1 = R * Hkv * W * (Hq // Hkv)
+    n = bd.beam_attn_workspace_size(R, W, Hq, Hkv, d, P, bd.BF16)
+    pad = lambda x: (x + 255) // 256 * 256
+    for s in range(1, 17):
+        if 256 + 2 * pad(rows1 * 4 * s) + pad(rows1 * d * 4 * s) == n:
+            return s
+    raise AssertionError(f"workspace size {n} matches no split count")
+
+
+def test_attention_planner_split_choices(L):
+    """The split model's choices on the benchmarked shapes: one split (the
+    merge fused in the shared stage) where the CTAs already fill the GPU,
+    eight for 1 x 50 beams over 2048 keys (measured 46.0 us per step against
+    50.0 at sixteen and 47.8 at four), and the CUDA-core stage's split of a
+    d = 64 prompt."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    assert _splits_from_workspace(bd, 4, 512, 16, 8, 128, 4096) == 1      # 4 x 512, prompts 4096
+    assert _splits_from_workspace(bd, 2, 5000, 16, 8, 128, 1024) == 1     # 2 x 5000, prompts 1024
+    assert _splits_from_workspace(bd, 1, 50, 16, 8, 128, 2048) == 8       # 1 x 50, prompt 2048
+    assert _splits_from_workspace(bd, 1, 8, 2, 1, 64, 256) == 2           # d = 64, CUDA cores
+    assert _splits_from_workspace(bd, 1, 50, 16, 8, 128, 128) == 1        # a single chunk
