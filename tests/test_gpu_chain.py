@@ -125,3 +125,37 @@ def test_graph_chain_matches_oracle(gpu_lib, name):
         dead = [(r, j) for r in range(R) for j in range(int(o_nl[r]), W)]
         for r, j in dead[:8]:
             assert not np.any(got[r, j]), (t, r, j)
+
+
+@pytest.mark.parametrize("prompt", [128, 1024])   # one prompt split (fused merge) / several (merge kernel)
+def test_eager_chain_with_dead_tiles_matches_oracle(gpu_lib, prompt):
+    """A catalog of 40 items leaves at most 40 of 300 beams alive after the
+    first steps, so whole 256-row tiles of the shared stage are dead while
+    the attention, launched right behind the selection that produced its
+    slot rows and live counts, reads them only after that selection has
+    completed.  Every step's attention, over the selection's own outputs,
+    matches the float64 oracle on live beams and is zero on dead ones."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl = synth.WORKLOADS["qwen06b"].scaled(name="deadtiles", W=300, K=300, n_items=40,
+                                           prompt_lens=[prompt], T=3)
+    trie, att, logits = _inputs(wl)
+    outs = _eager(wl, trie, att, logits)
+    torch.cuda.synchronize()
+    a0 = att[0]
+    R, W, T = wl.R, wl.W, wl.T
+    beams = _tile_beams(wl)
+    saw_dead_tile = False
+    for t in range(T):
+        o, y = outs[t]
+        nl = o["n_live_out"].cpu().numpy()
+        slot = o["slot_out"].cpu().numpy()
+        saw_dead_tile |= t > 0 and int(nl.min()) * wl.G <= 256 and W * wl.G > 512
+        inp = oracle_attn_inputs(a0, att[t]["q"], wl)
+        todo = [(r, j) for r in range(R) for j in beams + list(range(min(W, 4))) if j < int(nl[r])]
+        want = oatt.attention_decode(inp, slot, nl, t, beams=todo)
+        got = y.double().cpu().numpy()
+        err = max(float(np.abs(got[r, j] - want[r, j]).max()) for r, j in todo)
+        assert err < ATOL_ATTN[wl.kv_dtype], (t, err)
+        for r in range(R):
+            assert not np.any(got[r, int(nl[r]):]), (t, r)
+    assert saw_dead_tile
