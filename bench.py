@@ -173,6 +173,10 @@ class Step:
         self.ws_sel = bd.workspace(bd.beam_select_workspace_size(R, W, wl.K, wl.V), dev)
         self.ws_att = bd.workspace(bd.beam_attn_workspace_size(R, W, wl.Hq, wl.Hkv, wl.d, self.maxp,
                                                                wl.kv_dtype), dev)
+        # the request's prompt K/V is fixed for its decode: e4m3 is
+        # dequantised once, as a serving loop does at prefill (no-op otherwise)
+        bd.beam_attn_prepare_prompt(self.attn["shared_k"], self.attn["shared_v"], self.attn["prompt_offsets"],
+                                    self.maxp, W, wl.Hq, self.ws_att)
         # reach the last step's state with the real chain (untimed)
         st = dict(cum=torch.zeros((R, W), dtype=torch.float32, device=dev),
                   node=torch.zeros((R, W), dtype=torch.int32, device=dev),
@@ -208,7 +212,7 @@ class Step:
         bd.beam_attn_decode(a["q"] if q is None else q, a["shared_k"], a["shared_v"], a["prompt_offsets"],
                             self.maxp, a["unshared_k"], a["unshared_v"], o["slot_out"], o["n_live_out"],
                             self.step, k_scale=a["k_scale"], v_scale=a["v_scale"], out=self.out_att,
-                            ws=self.ws_att)
+                            ws=self.ws_att, prepared=True)
         return o
 
     def rows(self):
@@ -625,7 +629,8 @@ def e2e_lmhead_arm(step, args, ws, flush, H=2048):
                            ws=step.ws_sel)
         bd.beam_attn_decode(d["q"], a["shared_k"], a["shared_v"], a["prompt_offsets"], step.maxp,
                             a["unshared_k"], a["unshared_v"], o["slot_out"], o["n_live_out"], step.step,
-                            k_scale=a["k_scale"], v_scale=a["v_scale"], out=step.out_att, ws=step.ws_att)
+                            k_scale=a["k_scale"], v_scale=a["v_scale"], out=step.out_att, ws=step.ws_att,
+                            prepared=True)
         for k in outs:
             host_out[k].copy_(step.out_sel[k], non_blocking=True)
         host_att.copy_(step.out_att, non_blocking=True)

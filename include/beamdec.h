@@ -85,6 +85,9 @@ extern "C" {
 #define BEAMDEC_F32 0    /* IEEE binary32                                   */
 #define BEAMDEC_BF16 1   /* bfloat16                                         */
 #define BEAMDEC_E4M3 2   /* OCP fp8 E4M3FN, with a per-kv-head float scale   */
+/* kv_dtype of beam_attn_decode only: E4M3 KV whose prompt part the
+ * workspace already holds as bf16 (beam_attn_prepare_prompt). */
+#define BEAMDEC_E4M3_PREPARED 3
 
 /* ---- limits ------------------------------------------------------------ */
 #define BEAMDEC_MAX_BEAM_WIDTH 8192     /* W: beam index fits 13 bits        */
@@ -433,7 +436,8 @@ int beam_attn_workspace_size(int R, int W, int Hq, int Hkv, int d, int max_promp
  *   sm_scale        softmax scale (pass 0 for 1/sqrt(d)).
  *   out             [R][W][Hq][d] out_dtype (F32 or BF16).
  * Supported: d in {64, 128}; Hq % Hkv == 0; Hq/Hkv <= 16; q/kv/out dtypes
- * F32/F32/F32, BF16/BF16/BF16, BF16/E4M3/BF16.  BF16 queries with d = 128
+ * F32/F32/F32, BF16/BF16/BF16, BF16/E4M3/BF16 (and BF16/E4M3_PREPARED/BF16
+ * after beam_attn_prepare_prompt on the same workspace).  BF16 queries with d = 128
  * and a group size dividing 128 take the tensor-core shared stage (fp8 KV is
  * first dequantised to bf16 in the workspace); other shapes run it on CUDA
  * cores.  When that stage covers every prompt in one split (at most 6
@@ -453,6 +457,32 @@ int beam_attn_decode(const void* q, const void* shared_k, const void* shared_v,
                      int q_dtype, int kv_dtype, int out_dtype,
                      const float* k_scale, const float* v_scale, float sm_scale,
                      void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The prompt part of E4M3 KV, dequantised once into an attention workspace
+ * (the prompt KV of a request is fixed for all of its decode steps, while
+ * beam_attn_decode with BEAMDEC_E4M3 rewrites this bf16 copy on every call).
+ * Later beam_attn_decode calls on the same workspace pass kv_dtype
+ * BEAMDEC_E4M3_PREPARED with the same shared_k, shared_v and shared_rows:
+ * they read the copy and skip the dequantisation, so the shared stage can
+ * also start while the previous kernel drains (see the conventions above).
+ * The copy is exact (every e4m3 value is a bf16 value; the per-head scales
+ * are applied later, as without it).  The workspace records the two
+ * pointers and shared_rows; a PREPARED call with others sets
+ * BEAMDEC_ERR_DEVICE_CHECK in its status word.  A caller that rewrites the
+ * prompt KV in place must prepare again.
+ *
+ *   shared_k/v, prompt_offsets, max_prompt_len, shared_rows, R, W, Hq, Hkv, d:
+ *       as for beam_attn_decode (W and Hq size the workspace's layout).
+ *   kv_dtype  BEAMDEC_E4M3 (other types have nothing to prepare: the call
+ *             returns BEAMDEC_OK without launching anything; so do shapes
+ *             the tensor-core stage does not take, which read fp8 directly).
+ *   workspace as for beam_attn_decode (sized with BEAMDEC_E4M3).
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
+ */
+int beam_attn_prepare_prompt(const void* shared_k, const void* shared_v, const int32_t* prompt_offsets,
+                             int max_prompt_len, int64_t shared_rows, int R, int W, int Hq, int Hkv, int d,
+                             int kv_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

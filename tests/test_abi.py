@@ -192,3 +192,32 @@ def test_attention_planner_split_choices(L):
     assert _splits_from_workspace(bd, 1, 50, 16, 8, 128, 2048) == 8       # 1 x 50, prompt 2048
     assert _splits_from_workspace(bd, 1, 8, 2, 1, 64, 256) == 2           # d = 64, CUDA cores
     assert _splits_from_workspace(bd, 1, 50, 16, 8, 128, 128) == 1        # a single chunk
+
+
+def _prep(L, **kw):
+    args = dict(sk=FAKE, sv=FAKE, off=FAKE, maxp=256, rows=256, R=1, W=8, Hq=16, Hkv=8, d=128, kvd=2,
+                ws=FAKE, ws_bytes=0, stream=None)
+    args.update(kw)
+    return L.beam_attn_prepare_prompt(*args.values())
+
+
+def test_prepare_prompt_validation(L):
+    """beam_attn_prepare_prompt refuses bad arguments on the host and has
+    nothing to do for KV types without a bf16 copy (no launch either way);
+    the prepared kv type shares the e4m3 workspace layout."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    assert _prep(L, off=None) == bd.ERR_INVALID_ARG
+    assert _prep(L, ws=None) == bd.ERR_INVALID_ARG
+    assert _prep(L, kvd=3) == bd.ERR_INVALID_ARG                        # the prepared type is a decode type
+    assert _prep(L, kvd=-1) == bd.ERR_INVALID_ARG
+    assert _prep(L, d=96) == bd.ERR_UNSUPPORTED
+    assert _prep(L, rows=100) == bd.ERR_INVALID_ARG                     # fewer rows than a prompt
+    assert _prep(L, sk=None) == bd.ERR_INVALID_ARG
+    assert _prep(L, ws=ctypes.c_void_p(0x1010)) == bd.ERR_INVALID_ARG   # workspace not 256-byte aligned
+    assert _prep(L, kvd=1) == bd.OK                                     # bf16: nothing to prepare
+    assert _prep(L) == bd.ERR_WORKSPACE
+    for shape in ((4, 1000, 16, 8, 128, 5212), (1, 50, 16, 8, 128, 2048), (1, 8, 2, 1, 64, 256)):
+        assert bd.beam_attn_workspace_size(*shape, bd.E4M3_PREPARED) == \
+            bd.beam_attn_workspace_size(*shape, bd.E4M3)
+    assert _attn(L, qd=1, kvd=3, od=1) == bd.ERR_INVALID_ARG            # prepared e4m3 without scales
+    assert _attn(L, qd=1, kvd=4, od=1) == bd.ERR_INVALID_ARG

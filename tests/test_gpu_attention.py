@@ -340,3 +340,38 @@ def test_mbarrier_timeout_is_reported(gpu_lib):
     assert bd.read_status(ws) == 0
     want = oatt.attention_decode(oracle_attn_inputs(a, a["q"], wl), slot.numpy(), nl.numpy(), 2)
     _check(wl, out.double().cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("prompts,step", [([100, 0, 128], 2), ([300, 0, 517], 2), ([2048], 3)])
+def test_prepared_e4m3_equals_the_per_call_copy(gpu_lib, prompts, step):
+    """e4m3 prompt K/V dequantised once (beam_attn_prepare_prompt) and read by
+    prepared decode calls gives the same bits as the copy each plain call
+    makes, for a prompt in one split (merge in the shared stage) and split
+    prompts (merge kernel), at steps where the shared stage starts its main
+    loop before waiting; the copy persists across calls, and a prepared call
+    naming another prompt K/V is reported."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    wl = synth.WORKLOADS["fp8kv"].scaled(name="prep", R=len(prompts), prompt_lens=prompts, p_range=None,
+                                         W=200, T=4)
+    a = synth.attention_inputs(wl, step, device=DEV)
+    slot = _slots(wl, step, None).to(DEV)
+    nl = torch.tensor([wl.W] * (wl.R - 1) + [wl.W - 57], dtype=torch.int32, device=DEV)
+    maxp = int(synth.prompt_lens(wl).max())
+    size = bd.beam_attn_workspace_size(wl.R, wl.W, wl.Hq, wl.Hkv, wl.d, maxp, bd.E4M3)
+    ws_plain, ws_prep = bd.workspace(size, DEV), bd.workspace(size, DEV)
+
+    def call(ws, prepared, shared_k=None):
+        return bd.beam_attn_decode(a["q"], a["shared_k"] if shared_k is None else shared_k, a["shared_v"],
+                                   a["prompt_offsets"], maxp, a["unshared_k"], a["unshared_v"], slot, nl,
+                                   step, k_scale=a["k_scale"], v_scale=a["v_scale"], ws=ws,
+                                   prepared=prepared)
+    ref = call(ws_plain, False)
+    bd.beam_attn_prepare_prompt(a["shared_k"], a["shared_v"], a["prompt_offsets"], maxp, wl.W, wl.Hq, ws_prep)
+    got1 = call(ws_prep, True).clone()
+    got2 = call(ws_prep, True)
+    torch.cuda.synchronize()
+    assert bd.read_status(ws_plain) == 0 and bd.read_status(ws_prep) == 0
+    assert torch.equal(got1, ref) and torch.equal(got2, ref)
+    call(ws_prep, True, shared_k=a["shared_k"].clone())   # not the prompt K/V the copy is of
+    torch.cuda.synchronize()
+    assert bd.read_status(ws_prep) == bd.ERR_DEVICE_CHECK

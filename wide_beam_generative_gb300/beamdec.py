@@ -20,6 +20,7 @@ OK = 0
 ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_CHECK, ERR_ALLOC = \
     -1, -2, -3, -4, -5, -6, -7
 F32, BF16, E4M3 = 0, 1, 2
+E4M3_PREPARED = 3   # kv dtype of a decode call whose prompt K/V the workspace holds as bf16
 _DT = {torch.float32: F32, torch.bfloat16: BF16, torch.float8_e4m3fn: E4M3}
 
 _lib = None
@@ -64,6 +65,8 @@ _SIGS = {
     "beam_attn_decode": (c_int, [c_p, c_p, c_p, c_p, c_int, c_i64, c_p, c_p, c_p, c_p, c_int,
                                  c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                  c_p, c_p, c_f, c_p, c_p, c_sz, c_p]),
+    "beam_attn_prepare_prompt": (c_int, [c_p, c_p, c_p, c_int, c_i64, c_int, c_int, c_int, c_int, c_int,
+                                         c_int, c_p, c_sz, c_p]),
 }
 
 
@@ -324,11 +327,25 @@ def beam_select_static(logits, cum, node, n_live, slot_in, trie, level, step, K,
     return out
 
 
+def beam_attn_prepare_prompt(shared_k, shared_v, prompt_offsets, max_prompt_len, W, Hq, ws, stream=None):
+    """Writes the bf16 copy of e4m3 prompt K/V into the attention workspace
+    ``ws`` (sized for these shapes), for later ``beam_attn_decode(...,
+    prepared=True)`` calls on the same prompt; other KV types: nothing to do."""
+    R = prompt_offsets.shape[0] - 1
+    Hkv, d = shared_k.shape[1], shared_k.shape[2]
+    _need_cuda(shared_k, shared_v, prompt_offsets, ws)
+    rc = lib().beam_attn_prepare_prompt(_ptr(shared_k), _ptr(shared_v), _ptr(prompt_offsets),
+                                        int(max_prompt_len), int(shared_k.shape[0]), R, int(W), int(Hq),
+                                        Hkv, d, _DT[shared_k.dtype], _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "beam_attn_prepare_prompt")
+
+
 def beam_attn_decode(q, shared_k, shared_v, prompt_offsets, max_prompt_len, unshared_k, unshared_v,
                      slot_table, n_live, step, k_scale=None, v_scale=None, sm_scale=0.0,
-                     out=None, ws=None, stream=None):
+                     out=None, ws=None, stream=None, prepared=False):
     """Split-KV beam attention for one decode step; returns ``out``
-    [R, W, Hq, d] (fp32 for fp32 q, else bf16)."""
+    [R, W, Hq, d] (fp32 for fp32 q, else bf16).  ``prepared``: e4m3 KV whose
+    prompt part ``beam_attn_prepare_prompt`` already copied into ``ws``."""
     R, W, Hq, d = q.shape
     Hkv = unshared_k.shape[2]
     T = slot_table.shape[2]
@@ -336,6 +353,10 @@ def beam_attn_decode(q, shared_k, shared_v, prompt_offsets, max_prompt_len, unsh
                k_scale, v_scale)
     qd, kvd = _DT[q.dtype], _DT[unshared_k.dtype]
     od = F32 if qd == F32 else BF16
+    if prepared and kvd == E4M3:
+        if ws is None:
+            raise ValueError("prepared=True needs the workspace beam_attn_prepare_prompt wrote")
+        kvd = E4M3_PREPARED
     if out is None:
         out = torch.empty((R, W, Hq, d), dtype=torch.float32 if od == F32 else torch.bfloat16,
                           device=q.device)
@@ -395,6 +416,9 @@ class DecodeChain:
         self._ws_sel = workspace(beam_select_workspace_size(R, W, K, V), dev)
         self._ws_att = workspace(beam_attn_workspace_size(R, W, Hq, Hkv, d, max_prompt_len,
                                                           _DT[unshared_k.dtype]), dev)
+        # the prompt K/V is fixed for the chain: e4m3 is dequantised once here
+        # and every step reads the copy (other KV types: nothing to do)
+        beam_attn_prepare_prompt(shared_k, shared_v, prompt_offsets, max_prompt_len, W, Hq, self._ws_att)
 
         def chain():
             for k, v in self._state0.items():
@@ -406,7 +430,8 @@ class DecodeChain:
                                 score_lse=None if score_lse is None else score_lse[t])
                 beam_attn_decode(q[t], shared_k, shared_v, prompt_offsets, max_prompt_len, unshared_k,
                                  unshared_v, o["slot_out"], o["n_live_out"], t, k_scale=k_scale,
-                                 v_scale=v_scale, sm_scale=sm_scale, out=self.out[t], ws=self._ws_att)
+                                 v_scale=v_scale, sm_scale=sm_scale, out=self.out[t], ws=self._ws_att,
+                                 prepared=True)
                 st = dict(cum=o["cum_out"], node=o["node_out"], n_live=o["n_live_out"], slot=o["slot_out"])
 
         # one eager pass on a side stream (first-use setup such as kernel

@@ -262,7 +262,8 @@ extern "C" int beam_attn_workspace_size(int R, int W, int Hq, int Hkv, int d, in
   if (bytes == nullptr) return BEAMDEC_ERR_INVALID_ARG;
   const int s = attn_shape_check(R, W, Hq, Hkv, d, max_prompt_len);
   if (s != BEAMDEC_OK) return s;
-  if (kv_dtype < BEAMDEC_F32 || kv_dtype > BEAMDEC_E4M3) return BEAMDEC_ERR_INVALID_ARG;
+  if (kv_dtype < BEAMDEC_F32 || kv_dtype > BEAMDEC_E4M3_PREPARED) return BEAMDEC_ERR_INVALID_ARG;
+  if (kv_dtype == BEAMDEC_E4M3_PREPARED) kv_dtype = BEAMDEC_E4M3;   // the same layout
   const int q_dtype = kv_dtype == BEAMDEC_F32 ? BEAMDEC_F32 : BEAMDEC_BF16;
   AttnPlan p = attn_plan(R, W, Hq, Hkv, d, max_prompt_len, q_dtype, kv_dtype);
   *bytes = attn_workspace_bytes(R, W, Hq, Hkv, d, p);
@@ -289,6 +290,10 @@ extern "C" int beam_attn_decode(const void* q, const void* shared_k, const void*
   const int s = attn_shape_check(R, W, Hq, Hkv, d, max_prompt_len);
   if (s != BEAMDEC_OK) return s;
   if (T < 1 || step < 0 || step >= T) return BEAMDEC_ERR_INVALID_ARG;
+  // the prepared form of e4m3 KV: its prompt part is already in the
+  // workspace as bf16 (beam_attn_prepare_prompt)
+  const bool prepared = kv_dtype == BEAMDEC_E4M3_PREPARED;
+  if (prepared) kv_dtype = BEAMDEC_E4M3;
   if (!attn_types_ok(q_dtype, kv_dtype, out_dtype)) {
     const bool enums_ok = q_dtype >= 0 && q_dtype <= 2 && kv_dtype >= 0 && kv_dtype <= 2 &&
                           out_dtype >= 0 && out_dtype <= 2;
@@ -309,11 +314,41 @@ extern "C" int beam_attn_decode(const void* q, const void* shared_k, const void*
   a.k_scale = k_scale; a.v_scale = v_scale;
   a.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)d);
   a.out = out; a.ws = workspace;
+  a.kv_prepared = prepared && p.convert_kv;   // shapes without the bf16 copy read fp8 directly
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc = p.tensor_core ? launch_attn_shared_tc(a, p, st) : launch_attn_shared_simt(a, p, st);
   if (rc != BEAMDEC_OK) return rc;
   if (p.tensor_core && attn_tc_fused(a, p)) return BEAMDEC_OK;   // merged in the shared stage
   return launch_attn_merge(a, p, st);
+}
+
+extern "C" int beam_attn_prepare_prompt(const void* shared_k, const void* shared_v,
+                                        const int32_t* prompt_offsets, int max_prompt_len,
+                                        int64_t shared_rows, int R, int W, int Hq, int Hkv, int d,
+                                        int kv_dtype, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  if (prompt_offsets == nullptr || workspace == nullptr) return BEAMDEC_ERR_INVALID_ARG;
+  const int s = attn_shape_check(R, W, Hq, Hkv, d, max_prompt_len);
+  if (s != BEAMDEC_OK) return s;
+  if (kv_dtype < BEAMDEC_F32 || kv_dtype > BEAMDEC_E4M3) return BEAMDEC_ERR_INVALID_ARG;
+  if (shared_rows < 0 || (max_prompt_len > 0 && shared_rows < max_prompt_len) ||
+      shared_rows > (int64_t)R * max_prompt_len)
+    return BEAMDEC_ERR_INVALID_ARG;
+  if (shared_rows > 0 && (shared_k == nullptr || shared_v == nullptr)) return BEAMDEC_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BEAMDEC_ERR_INVALID_ARG;
+  if (kv_dtype != BEAMDEC_E4M3) return BEAMDEC_OK;   // nothing to prepare
+  AttnPlan p = attn_plan(R, W, Hq, Hkv, d, max_prompt_len, BEAMDEC_BF16, kv_dtype);
+  if (workspace_bytes < attn_workspace_bytes(R, W, Hq, Hkv, d, p)) return BEAMDEC_ERR_WORKSPACE;
+  if (!p.convert_kv || shared_rows == 0) return BEAMDEC_OK;   // no bf16 copy is read at this shape
+  if (((reinterpret_cast<uintptr_t>(shared_k) | reinterpret_cast<uintptr_t>(shared_v)) & 15u) != 0)
+    return BEAMDEC_ERR_INVALID_ARG;   // read in 16-byte groups, as beam_attn_decode does
+  AttnArgs a{};
+  a.shared_k = shared_k; a.shared_v = shared_v; a.prompt_offsets = prompt_offsets;
+  a.max_prompt_len = max_prompt_len; a.shared_rows = shared_rows;
+  a.R = R; a.W = W; a.Hq = Hq; a.Hkv = Hkv; a.d = d;
+  a.q_dtype = BEAMDEC_BF16; a.kv_dtype = kv_dtype; a.out_dtype = BEAMDEC_BF16;
+  a.ws = workspace;
+  return launch_kv_copy(a, p, static_cast<cudaStream_t>(stream), false);
 }
 
 // ---- LM head with fused log-sum-exp ---------------------------------------------

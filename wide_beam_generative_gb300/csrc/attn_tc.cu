@@ -89,6 +89,11 @@ struct TcParams {
   // before reading the slot table or the live counts (late: after the main
   // loop; early: before everything, so dead tiles can skip the main loop)
   int dep_wait_late;
+  // e4m3 KV prepared earlier: the workspace's record of the prompt K/V its
+  // bf16 copy came from must name these (else BEAMDEC_ERR_DEVICE_CHECK)
+  const void* prep_k;
+  const void* prep_v;
+  const void* prep_dst;   // where this call's maps read the copy
   float scale_log2;   // sm_scale * log2(e)
   const float* k_scale;   // per kv head; fp8 KV only (nullptr otherwise)
   int64_t shared_rows;
@@ -467,9 +472,16 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
   const int r = request_by_length(p.prompt_offsets, p.R, blockIdx.z);
   const int row0 = mt * 256;
   const int G = p.G;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 &&
-      (int64_t)p.prompt_offsets[p.R] != p.shared_rows)
-    set_status(p.hdr, BEAMDEC_ERR_DEVICE_CHECK);   // the K/V maps end at shared_rows
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) {
+    if ((int64_t)p.prompt_offsets[p.R] != p.shared_rows)
+      set_status(p.hdr, BEAMDEC_ERR_DEVICE_CHECK);   // the K/V maps end at shared_rows
+    if (p.prep_k != nullptr &&
+        (p.hdr->prep_k != reinterpret_cast<uintptr_t>(p.prep_k) ||
+         p.hdr->prep_v != reinterpret_cast<uintptr_t>(p.prep_v) ||
+         p.hdr->prep_rows != (unsigned long long)p.shared_rows ||
+         p.hdr->prep_dst != reinterpret_cast<uintptr_t>(p.prep_dst)))
+      set_status(p.hdr, BEAMDEC_ERR_DEVICE_CHECK);   // no copy of this prompt K/V at this place
+  }
   if (!p.dep_wait_late) grid_dep_wait();
   if (!p.dep_wait_late && row0 >= p.n_live[r] * G) {   // every row of the CTA is a dead beam
     if (p.fuse) zero_rows(p, r, g, row0);
@@ -781,14 +793,23 @@ bd_attn_shared_tc_kernel(const __grid_constant__ CUtensorMap qmap,
 // per-head scales are not applied here: K's scale multiplies the softmax
 // scale and V's scale the merged output.
 // It reads nothing the selection writes, so it is launched as a programmatic
-// dependent of the previous kernel and lets the shared stage launch the same
-// way; each thread waits for the previous grid before it exits, so that this
-// grid's completion (which the shared stage waits for) implies that one's.
+// dependent of the previous kernel; inside a decode call it lets the shared
+// stage launch the same way (that stage waits for this grid before its main
+// loop), while beam_attn_prepare_prompt's copy does not (a prepared call
+// reads the copy without waiting).  Each thread waits for the previous grid
+// before it exits, so that this grid's completion implies that one's.
 __global__ void __launch_bounds__(256)
 bd_kv_e4m3_to_bf16_kernel(const uint8_t* __restrict__ k8, const uint8_t* __restrict__ v8,
                           __nv_bfloat16* __restrict__ k16, __nv_bfloat16* __restrict__ v16,
-                          const int32_t* prompt_offsets, int R, int64_t row_elems) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+                          const int32_t* prompt_offsets, int R, int64_t row_elems, WsHeader* hdr,
+                          int64_t shared_rows, int early) {
+  if (early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x == 0 && threadIdx.x == 0) {   // what the copy holds, for prepared calls
+    hdr->prep_k = reinterpret_cast<uintptr_t>(k8);
+    hdr->prep_v = reinterpret_cast<uintptr_t>(v8);
+    hdr->prep_rows = (unsigned long long)shared_rows;
+    hdr->prep_dst = reinterpret_cast<uintptr_t>(k16);
+  }
   const int64_t n16 = (int64_t)prompt_offsets[R] * row_elems / 16;   // 16-element groups
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n16;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -853,6 +874,23 @@ bool attn_tc_fused(const AttnArgs& a, const AttnPlan& pl) {
          al16(a.out);
 }
 
+int launch_kv_copy(const AttnArgs& a, const AttnPlan& pl, cudaStream_t stream, bool early) {
+  __nv_bfloat16* k16 = attn_kv16(a.ws, a.R, a.W, a.Hq, a.Hkv, a.d, pl.n_split);
+  __nv_bfloat16* v16 = k16 + (size_t)a.R * a.max_prompt_len * a.Hkv * a.d;
+  const int64_t groups = a.shared_rows * a.Hkv * a.d / 16 * 2;
+  int blocks = (int)((groups + 255) / 256);
+  if (blocks > 8 * sm_count()) blocks = 8 * sm_count();
+  if (blocks < 1) blocks = 1;
+  prof_begin(kKKvConvert, stream);
+  const cudaError_t ce = launch_dependent(bd_kv_e4m3_to_bf16_kernel, dim3(blocks), dim3(256), 0, stream,
+                                          static_cast<const uint8_t*>(a.shared_k),
+                                          static_cast<const uint8_t*>(a.shared_v), k16, v16, a.prompt_offsets,
+                                          a.R, (int64_t)a.Hkv * a.d, reinterpret_cast<WsHeader*>(a.ws),
+                                          a.shared_rows, early ? 1 : 0);
+  prof_end(kKKvConvert, stream);
+  return (ce == cudaSuccess && cudaGetLastError() == cudaSuccess) ? BEAMDEC_OK : BEAMDEC_ERR_CUDA;
+}
+
 int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t stream) {
   const int G = a.Hq / a.Hkv;
   if (!attn_tc_supported(a.q_dtype, a.kv_dtype, a.d, G)) return BEAMDEC_ERR_UNSUPPORTED;
@@ -872,22 +910,15 @@ int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t st
   const void* kbase = a.shared_rows > 0 ? a.shared_k : a.q;
   const void* vbase = a.shared_rows > 0 ? a.shared_v : a.q;
   if (a.kv_dtype == BEAMDEC_E4M3 && a.shared_rows > 0) {
-    // dequantise the prompt KV once into the workspace (bf16, same layout)
+    // the prompt KV as bf16 in the workspace: made here, or earlier by
+    // beam_attn_prepare_prompt
+    if (!a.kv_prepared) {
+      const int rc = launch_kv_copy(a, pl, stream, true);
+      if (rc != BEAMDEC_OK) return rc;
+    }
     __nv_bfloat16* k16 = attn_kv16(a.ws, a.R, a.W, a.Hq, a.Hkv, a.d, pl.n_split);
-    __nv_bfloat16* v16 = k16 + (size_t)a.R * a.max_prompt_len * a.Hkv * a.d;
-    const int64_t groups = a.shared_rows * a.Hkv * a.d / 16 * 2;
-    int blocks = (int)((groups + 255) / 256);
-    if (blocks > 8 * sm_count()) blocks = 8 * sm_count();
-    if (blocks < 1) blocks = 1;
-    prof_begin(kKKvConvert, stream);
-    const cudaError_t ce = launch_dependent(bd_kv_e4m3_to_bf16_kernel, dim3(blocks), dim3(256), 0, stream,
-                                            static_cast<const uint8_t*>(a.shared_k),
-                                            static_cast<const uint8_t*>(a.shared_v), k16, v16,
-                                            a.prompt_offsets, a.R, (int64_t)a.Hkv * a.d);
-    prof_end(kKKvConvert, stream);
-    if (ce != cudaSuccess || cudaGetLastError() != cudaSuccess) return BEAMDEC_ERR_CUDA;
     kbase = k16;
-    vbase = v16;
+    vbase = k16 + (size_t)a.R * a.max_prompt_len * a.Hkv * a.d;
   }
   CUtensorMap qm, km, vm;
   {
@@ -938,7 +969,10 @@ int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& pl, cudaStream_t st
   // At step 0 (one live beam per request) the CTAs wait first, so that
   // dead tiles skip the main loop; the bf16 copy of e4m3 K/V is waited for
   // before the main loop too.
-  p.dep_wait_late = (a.step > 0 && !(a.kv_dtype == BEAMDEC_E4M3 && a.shared_rows > 0)) ? 1 : 0;
+  p.dep_wait_late = (a.step > 0 && !(a.kv_dtype == BEAMDEC_E4M3 && a.shared_rows > 0 && !a.kv_prepared)) ? 1 : 0;
+  p.prep_k = (a.kv_prepared && a.shared_rows > 0) ? a.shared_k : nullptr;
+  p.prep_v = a.shared_v;
+  p.prep_dst = kbase;
   const cudaError_t le = launch_dependent(bd_attn_shared_tc_kernel, grid, dim3(kThreads), kSmemBytes, stream,
                                           qm, km, vm, p);
   prof_end(kKAttnTc, stream);

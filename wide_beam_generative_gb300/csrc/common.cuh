@@ -27,7 +27,10 @@ struct WsHeader {
   uint32_t poll_limit;
   uint32_t bar_extra;
   uint32_t probe_polls;
-  uint32_t pad[58];
+  // attention workspaces: the prompt K/V (and its row count) whose bf16 copy
+  // the workspace holds, written by the dequantisation kernel
+  unsigned long long prep_k, prep_v, prep_rows, prep_dst;
+  uint32_t pad[50];
 };
 static_assert(sizeof(WsHeader) == kWsHeaderBytes, "header size");
 

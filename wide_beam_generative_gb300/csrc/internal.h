@@ -115,6 +115,9 @@ struct AttnArgs {
   int q_dtype, kv_dtype, out_dtype;
   const float* k_scale; const float* v_scale; float sm_scale;
   void* out; void* ws;
+  // e4m3 KV whose prompt part the workspace already holds as bf16
+  // (beam_attn_prepare_prompt): the shared stage reads it, no copy is made
+  bool kv_prepared;
 };
 // Split plan of the shared stage over the prompt.
 struct AttnPlan {
@@ -129,6 +132,10 @@ AttnPlan attn_plan(int R, int W, int Hq, int Hkv, int d, int max_prompt_len, int
 size_t attn_workspace_bytes(int R, int W, int Hq, int Hkv, int d, const AttnPlan& p);
 int launch_attn_shared_simt(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 int launch_attn_shared_tc(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
+// The bf16 copy of e4m3 prompt K/V in the workspace (and its record of
+// shared_k, shared_v, shared_rows and where the copy lies), launched as a
+// programmatic dependent; early: the kernel after it may start before it ends.
+int launch_kv_copy(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream, bool early);
 bool attn_tc_supported(int q_dtype, int kv_dtype, int d, int G);
 bool attn_tc_fused(const AttnArgs& a, const AttnPlan& p);   // merge inside the shared stage
 
