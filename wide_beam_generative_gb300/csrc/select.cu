@@ -125,6 +125,59 @@ __device__ void warp_find_digit(const volatile uint32_t* hist, int nbins, uint32
   __syncwarp();
 }
 
+// The digit holding the need-th smallest key (need >= 1) of a shared-memory
+// histogram of nb digits (a power of two, at most 4 * kExpandThreads),
+// searched by the whole block: thread t sums its nb / kExpandThreads
+// consecutive digits (one digit, or none, when nb is smaller), one block
+// prefix sum places them, and the thread whose digits hold the need-th key
+// walks them again and writes sh.digit = that digit and sh.below = keys in lower digits.  A
+// histogram of fewer than need keys is searched for its last key (none: digit
+// 0, below 0).  Every thread of a kExpandThreads block calls it; it ends with
+// a block barrier.  (One warp scanning 2048 digits alone is a serial chain of
+// 64 shared loads per lane: about 2 us per radix pass.)  Not inlined: inside
+// the 32-register stream kernels it would crowd the callers' registers.
+template <class Smem>
+__device__ __noinline__ void block_find_digit(const uint32_t* h, int nb, uint32_t need, Smem& sh) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int per = nb > kExpandThreads ? nb / kExpandThreads : 1;
+  const int d0 = t * per;
+  const bool mine = d0 < nb;   // digits d0 .. d0 + per - 1 are this thread's
+  uint32_t sum = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sum += (i < per && mine) ? h[d0 + i] : 0u;
+  uint32_t inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) sh.warp_cnt[warp] = (int)inc;
+  __syncthreads();
+  uint32_t run = inc - sum, tot = 0;
+  for (int w = 0; w < kExpandThreads / 32; ++w) {
+    const uint32_t c = (uint32_t)sh.warp_cnt[w];
+    if (w < warp) run += c;
+    tot += c;
+  }
+  if (need > tot) need = tot;
+  if (t == 0 && tot == 0) {
+    sh.digit = 0;
+    sh.below = 0;
+  }
+  if (mine && run < need && need <= run + sum) {   // the need-th key is in this thread's digits
+    for (int j = 0; j < per; ++j) {
+      const uint32_t c = h[d0 + j];
+      if (need <= run + c) {
+        sh.digit = (uint32_t)(d0 + j);
+        sh.below = run;
+        break;
+      }
+      run += c;
+    }
+  }
+  __syncthreads();
+}
+
 // Block-wide exclusive rank of `flag` among the block's threads, and the total.
 __device__ __forceinline__ int block_rank(int flag, int* warp_cnt, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -535,8 +588,7 @@ __device__ __forceinline__ void expand_candidates(const SelectArgs& a, ExpandSha
       }
     }
     __syncthreads();
-    if (tid < 32) warp_find_digit(sh.hist, nb, need, &sh.digit, &sh.below);
-    __syncthreads();
+    block_find_digit(sh.hist, nb, need, sh);
     prefix |= sh.digit << sh_next;
     need -= sh.below;
     shift = sh_next;
@@ -769,8 +821,7 @@ __device__ uint32_t narrow_pass(const unsigned long long* keys, int n, unsigned 
     warp_hist_add(sh.hist, (uint32_t)(k >> nshift) & mask, on);
   }
   __syncthreads();
-  if (threadIdx.x < 32) warp_find_digit(sh.hist, nb, need, &sh.digit, &sh.below);
-  __syncthreads();
+  block_find_digit(sh.hist, nb, need, sh);
   const uint32_t D = sh.digit, below = sh.below, in_bin = sh.hist[D];
   __syncthreads();
   sure += below;
