@@ -324,11 +324,14 @@ def read_traffic(kernel, workload):
     if not os.path.exists(path):
         return None
     src_for = {"bd_expand_kernel": "select.cu", "bd_global_kernel": "select.cu", "bd_stream_select_kernel": "select.cu",
+               "bd_seed_kernel": "select.cu",
                "bd_kv_e4m3_to_bf16_kernel": "attn_tc.cu",
                "bd_attn_shared_simt_kernel": "attn_simt.cu", "bd_attn_shared_tc_kernel": "attn_tc.cu",
                "bd_attn_merge_kernel": "attn_merge.cu"}
-    src = os.path.join(ROOT, "wide_beam_generative_gb300", "csrc", src_for.get(kernel, ""))
-    if not os.path.exists(src):
+    if kernel not in src_for:
+        return None
+    src = os.path.join(ROOT, "wide_beam_generative_gb300", "csrc", src_for[kernel])
+    if not os.path.isfile(src):
         return None
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:12]
     for line in open(path):

@@ -74,6 +74,12 @@ def test_traffic_rows_count_only_for_their_workload_and_source(tmp_path, monkeyp
     assert bench.read_traffic("bd_stream_select_kernel", "onerec17b") == 1234.0
     assert bench.read_traffic("bd_stream_select_kernel", "openvocab") is None   # no row for it
     assert bench.read_traffic("bd_stream_select_kernel", "fp8kv") is None       # taken on other source
+    (tmp_path / "profiles" / "ncu_traffic.md").write_text(
+        "| kernel | workload | bytes per launch | source sha256[:12] | capture |\n|---|---|---|---|---|\n"
+        f"| bd_seed_kernel | openvocab | 77 | {sha} | x |\n"
+        f"| bd_unknown_kernel | openvocab | 88 | {sha} | x |\n")
+    assert bench.read_traffic("bd_seed_kernel", "openvocab") == 77.0
+    assert bench.read_traffic("bd_unknown_kernel", "openvocab") is None         # no source file known
 
 
 def test_cpu_sample_is_bounded():
