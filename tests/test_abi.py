@@ -221,3 +221,44 @@ def test_prepare_prompt_validation(L):
             bd.beam_attn_workspace_size(*shape, bd.E4M3)
     assert _attn(L, qd=1, kvd=3, od=1) == bd.ERR_INVALID_ARG            # prepared e4m3 without scales
     assert _attn(L, qd=1, kvd=4, od=1) == bd.ERR_INVALID_ARG
+
+
+def _lmh(L, **kw):
+    args = dict(hidden=FAKE, weight=FAKE, rows=2048, hidden_dim=2048, V=151936, w0=8192, wlen=8192,
+                lse=FAKE, logits=FAKE, stride=8192 * 2, ws=FAKE, ws_bytes=0, stream=None)
+    args.update(kw)
+    return L.beam_lmhead_lse(*args.values())
+
+
+def test_lmhead_validation_on_host(L):
+    """beam_lmhead_lse checks its pointers, shapes, window, alignment and
+    workspace size before any device call (every case here fails one of
+    those checks, so nothing is launched); its workspace size grows with
+    the rows and the vocabulary."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    for k in ("hidden", "weight", "lse", "ws"):
+        assert _lmh(L, **{k: None}) == bd.ERR_INVALID_ARG, k
+    assert _lmh(L, rows=0) == bd.ERR_INVALID_ARG
+    assert _lmh(L, V=0) == bd.ERR_INVALID_ARG
+    assert _lmh(L, hidden_dim=32) == bd.ERR_INVALID_ARG                     # below one 64-wide slice
+    assert _lmh(L, w0=-1) == bd.ERR_INVALID_ARG
+    assert _lmh(L, wlen=-1) == bd.ERR_INVALID_ARG
+    assert _lmh(L, w0=151936 - 100, wlen=101) == bd.ERR_INVALID_ARG          # window past the vocabulary
+    assert _lmh(L, hidden_dim=2048 + 32) == bd.ERR_UNSUPPORTED               # not a multiple of 64
+    assert _lmh(L, V=(1 << 18) + 1) == bd.ERR_UNSUPPORTED                    # above the largest vocabulary
+    assert _lmh(L, logits=None) == bd.ERR_INVALID_ARG                        # a window needs its buffer
+    assert _lmh(L, stride=8192 + 8191) == bd.ERR_INVALID_ARG                 # row shorter than the window's end
+    assert _lmh(L, hidden=ctypes.c_void_p(0x1008)) == bd.ERR_INVALID_ARG     # not 16-byte aligned
+    assert _lmh(L, weight=ctypes.c_void_p(0x1008)) == bd.ERR_INVALID_ARG
+    assert _lmh(L, ws=ctypes.c_void_p(0x1010)) == bd.ERR_INVALID_ARG         # not 256-byte aligned
+    assert _lmh(L) == bd.ERR_WORKSPACE                                       # zero workspace bytes
+    assert _lmh(L, wlen=0, logits=None) == bd.ERR_WORKSPACE                  # lse only: no window buffer needed
+    size = ctypes.c_size_t()
+    assert L.beam_lmhead_workspace_size(0, 151936, ctypes.byref(size)) == bd.ERR_INVALID_ARG
+    assert L.beam_lmhead_workspace_size(2048, 0, ctypes.byref(size)) == bd.ERR_INVALID_ARG
+    assert L.beam_lmhead_workspace_size(2048, 151936, None) == bd.ERR_INVALID_ARG
+    sizes = []
+    for rows, V in ((128, 512), (2048, 512), (2048, 151936)):
+        assert L.beam_lmhead_workspace_size(rows, V, ctypes.byref(size)) == bd.OK
+        sizes.append(size.value)
+    assert 0 < sizes[0] <= sizes[1] <= sizes[2]
