@@ -262,3 +262,33 @@ def test_lmhead_validation_on_host(L):
         assert L.beam_lmhead_workspace_size(rows, V, ctypes.byref(size)) == bd.OK
         sizes.append(size.value)
     assert 0 < sizes[0] <= sizes[1] <= sizes[2]
+
+
+def test_profile_and_status_calls_on_host(L):
+    """The profiling, status and trie-info entry points refuse bad arguments
+    without touching a device; kernel ids name the kernels in the order the
+    header documents; with nothing recorded a read returns zero launches
+    (no event is created while recording is off)."""
+    from wide_beam_generative_gb300 import beamdec as bd
+    names = ["bd_expand_kernel", "bd_global_kernel", "bd_attn_shared_simt_kernel",
+             "bd_attn_shared_tc_kernel", "bd_attn_merge_kernel", "bd_kv_e4m3_to_bf16_kernel",
+             "bd_stream_select_kernel", "bd_lmhead_kernel", "bd_lmhead_lse_kernel", "bd_seed_kernel"]
+    assert [L.beamdec_kernel_name(i).decode() for i in range(len(names))] == names
+    assert L.beamdec_kernel_name(-1) == b"" and L.beamdec_kernel_name(len(names)) == b""
+    assert L.beamdec_profile_enable(0) == bd.OK                   # off: creates nothing
+    ms, n = ctypes.c_float(-1.0), ctypes.c_int(-1)
+    for kid in range(len(names)):
+        assert L.beamdec_profile_read(kid, ctypes.byref(ms), ctypes.byref(n)) == bd.OK
+        assert (ms.value, n.value) == (0.0, 0)
+    assert L.beamdec_profile_read(-1, ctypes.byref(ms), ctypes.byref(n)) == bd.ERR_INVALID_ARG
+    assert L.beamdec_profile_read(len(names), ctypes.byref(ms), ctypes.byref(n)) == bd.ERR_INVALID_ARG
+    assert L.beamdec_profile_read(0, None, ctypes.byref(n)) == bd.ERR_INVALID_ARG
+    assert L.beamdec_profile_read(0, ctypes.byref(ms), None) == bd.ERR_INVALID_ARG
+    st = ctypes.c_int32(7)
+    assert L.beamdec_read_status(None, None, ctypes.byref(st)) == bd.ERR_INVALID_ARG
+    assert L.beamdec_read_status(FAKE, None, None) == bd.ERR_INVALID_ARG
+    assert st.value == 7                                          # untouched on refusal
+    lv = ctypes.c_int(-1)
+    assert L.beam_trie_info(None, ctypes.byref(lv), None, None, None, None, None) == bd.ERR_INVALID_ARG
+    assert lv.value == -1
+    L.beam_trie_free(None)                                        # a null handle is a no-op
